@@ -1,0 +1,317 @@
+"""Pins for the CPU oracle: each test ties it to something other than itself.
+
+The pages print no labels or centroids for a worked example, so the oracle is
+pinned by exact arithmetic on tiny inputs, independent library routines,
+closed forms, invariants and planted structure.  Each test names the plausible
+mistake it would catch.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+from scipy.spatial.distance import cdist
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# Philox4x32-10 (the k-means++ draws)
+# --------------------------------------------------------------------------
+def _kat_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            v = [int(t, 16) for t in line.split()]
+            rows.append((v[0:4], v[4:6], v[6:10]))
+    return rows
+
+
+@pytest.mark.parametrize("ctr,key,want", _kat_rows())
+def test_philox_known_answers(ctr, key, want):
+    # catches: a wrong multiplier, Weyl constant, round count or word order
+    got = oracle.philox4x32_10(ctr, key)
+    assert [int(x) for x in got] == want
+
+
+def test_uniform_is_uniform():
+    # catches: a bit-assembly mistake that skews or truncates the 53-bit uniform
+    u = np.array([oracle.uniform(7, i) for i in range(20000)])
+    assert u.min() >= 0.0 and u.max() < 1.0
+    assert stats.kstest(u, "uniform").pvalue > 1e-3
+    # different seeds give different streams
+    assert oracle.uniform(7, 0) != oracle.uniform(8, 0)
+
+
+# --------------------------------------------------------------------------
+# Assignment
+# --------------------------------------------------------------------------
+def _exact_assign(Xi, Ci):
+    """Brute force in exact integer arithmetic (inputs are small integers)."""
+    labels, best, second = [], [], []
+    for x in Xi:
+        ds = [sum((int(a) - int(b)) ** 2 for a, b in zip(x, c)) for c in Ci]
+        m = min(ds)
+        j = ds.index(m)  # first (lowest) index attaining the minimum
+        labels.append(j)
+        best.append(m)
+        rest = ds[:j] + ds[j + 1:]
+        second.append(min(rest) if rest else math.inf)
+    return labels, best, second
+
+
+def test_assign_exact_integers_with_ties():
+    # catches: a dropped term, wrong sign, '<=' tie-break, wrong runner-up
+    rng = np.random.default_rng(3)
+    Xi = rng.integers(-3, 4, size=(40, 5))
+    Ci = rng.integers(-3, 4, size=(9, 5))
+    Ci[6] = Ci[2]  # duplicate centroid: exact ties must go to index 2
+    labels, best, second, inertia = oracle.assign(Xi.astype(np.float32), Ci.astype(np.float32))
+    want_l, want_b, want_s = _exact_assign(Xi, Ci)
+    assert labels.tolist() == want_l
+    assert best.tolist() == [float(v) for v in want_b]
+    assert second.tolist() == [float(v) for v in want_s]
+    assert inertia == float(sum(want_b))
+    assert 6 not in set(labels.tolist())
+
+
+def test_assign_matches_scipy_cdist_on_the_probe_check_shape():
+    # n=512, k=17, d=64: the separate float32 problem the fusion-probe page
+    # uses to check its running-loop labels.  scipy's cdist is an independent
+    # implementation of the squared Euclidean distance.
+    X = synth.gaussian((512, 64), seed=11)
+    C = synth.gaussian((17, 64), seed=12)
+    labels, best, second, _ = oracle.assign(X, C)
+    D = cdist(X.astype(np.float64), C.astype(np.float64), metric="sqeuclidean")
+    np.testing.assert_allclose(best, D.min(axis=1), rtol=1e-12)
+    srt = np.sort(D, axis=1)
+    np.testing.assert_allclose(second, srt[:, 1], rtol=1e-12)
+    gap = srt[:, 1] - srt[:, 0]
+    clear = gap > 1e-9 * srt[:, 0]
+    assert clear.all()
+    np.testing.assert_array_equal(labels, D.argmin(axis=1))
+
+
+def test_assign_gram_identity():
+    # ||x - c||^2 = ||x||^2 + ||c||^2 - 2 x.c (the Gram form of the
+    # "Gram assignment" section), evaluated by a matmul in float64.
+    X = synth.gaussian((300, 96), seed=21, scale=2.0)
+    C = synth.gaussian((23, 96), seed=22, scale=2.0)
+    labels, best, _, _ = oracle.assign(X, C)
+    X64, C64 = X.astype(np.float64), C.astype(np.float64)
+    G = (X64 ** 2).sum(1)[:, None] + (C64 ** 2).sum(1)[None, :] - 2.0 * X64 @ C64.T
+    np.testing.assert_allclose(best, G[np.arange(300), labels], rtol=1e-10, atol=1e-9)
+    assert np.all(G.min(axis=1) >= best - 1e-9 * (1 + np.abs(best)))
+
+
+def test_assign_recovers_planted_blobs():
+    # with C = the planted centers the nearest center is the sample's own blob
+    # (gap ~ 2d against noise sigma = 0.5); catches any transposed operand
+    X, centers, blob = synth.planted_blobs(2048, 128, 64, seed=5)
+    labels, best, second, _ = oracle.assign(X, centers)
+    np.testing.assert_array_equal(labels, blob)
+    assert np.all(second - best > 50.0)
+
+
+def test_assign_single_centroid():
+    X = synth.gaussian((100, 7), seed=31)
+    C = synth.gaussian((1, 7), seed=32)
+    labels, best, second, inertia = oracle.assign(X, C)
+    assert (labels == 0).all()
+    assert np.isinf(second).all()
+    np.testing.assert_allclose(best, ((X.astype(np.float64) - C[0]) ** 2).sum(1), rtol=1e-13)
+    assert inertia == pytest.approx(best.sum(), rel=1e-14)
+
+
+def test_assign_one_feature_matches_sorted_search():
+    # d = 1: nearest neighbour on a line by binary search over sorted centroids
+    x = synth.gaussian((1000, 1), seed=41)[:, 0]
+    c = synth.gaussian((37, 1), seed=42)[:, 0]
+    labels, _, _, _ = oracle.assign(x[:, None], c[:, None])
+    order = np.argsort(c, kind="stable")
+    cs = c[order].astype(np.float64)
+    pos = np.searchsorted(cs, x.astype(np.float64))
+    want = []
+    for xi, p in zip(x.astype(np.float64), pos):
+        cands = [q for q in (p - 1, p) if 0 <= q < len(cs)]
+        dist = [(xi - cs[q]) ** 2 for q in cands]
+        m = min(dist)
+        want.append(min(order[q] for q, dq in zip(cands, dist) if dq == m))
+    np.testing.assert_array_equal(labels, want)
+
+
+def test_assign_permutation_and_translation():
+    # relabelling centroids relabels the answer; a common shift changes nothing
+    X = synth.gaussian((400, 33), seed=51)
+    C = synth.gaussian((29, 33), seed=52)
+    labels, best, _, _ = oracle.assign(X, C)
+    perm = np.random.default_rng(1).permutation(29)
+    l2, b2, _, _ = oracle.assign(X, C[perm])
+    np.testing.assert_array_equal(perm[l2], labels)
+    np.testing.assert_array_equal(b2, best)
+    shift = np.float32(0.25)  # exact in binary32 for these magnitudes: small
+    l3, b3, _, _ = oracle.assign(X + shift, C + shift)
+    np.testing.assert_array_equal(l3, labels)
+    np.testing.assert_allclose(b3, best, rtol=1e-5)
+
+
+# --------------------------------------------------------------------------
+# Update
+# --------------------------------------------------------------------------
+def test_update_single_cluster_is_global_mean():
+    X = synth.gaussian((5000, 20), seed=61, scale=3.0)
+    C_old = np.zeros((1, 20), np.float32)
+    C_new, counts = oracle.update(X, np.zeros(5000, np.int64), C_old)
+    assert counts.tolist() == [5000]
+    want = X.astype(np.float64).mean(axis=0)
+    np.testing.assert_allclose(C_new[0], want, rtol=2e-7, atol=1e-9)
+
+
+def test_update_matches_unbuffered_scatter_add():
+    # np.add.at accumulates each member into its cluster in sample order
+    X = synth.gaussian((3000, 17), seed=71)
+    labels = np.random.default_rng(2).integers(0, 40, size=3000)
+    C_old = synth.gaussian((41, 17), seed=72)  # cluster 40 stays empty
+    C_new, counts = oracle.update(X, labels, C_old)
+    sums = np.zeros((41, 17), np.float64)
+    np.add.at(sums, labels, X.astype(np.float64))
+    cnt = np.bincount(labels, minlength=41)
+    np.testing.assert_array_equal(counts, cnt)
+    nz = cnt > 0
+    np.testing.assert_array_equal(C_new[nz], (sums[nz] / cnt[nz, None]).astype(np.float32))
+    assert cnt[40] == 0
+    np.testing.assert_array_equal(C_new[40], C_old[40])  # bit-for-bit kept
+
+
+def test_update_far_centroid_stays_empty_and_unchanged():
+    X, centers, _ = synth.planted_blobs(1024, 16, 8, seed=81)
+    C = centers.copy()
+    C[3] += np.float32(1e3)
+    labels, _, _, _ = oracle.assign(X, C)
+    C_new, counts = oracle.update(X, labels, C)
+    assert counts[3] == 0
+    assert C_new[3].tobytes() == C[3].tobytes()
+    # centroid * count = member sum for the others
+    for j in range(8):
+        if counts[j]:
+            s = X[labels == j].astype(np.float64).sum(0)
+            np.testing.assert_allclose(C_new[j].astype(np.float64) * counts[j], s,
+                                       rtol=1e-6, atol=1e-4)
+
+
+def test_update_rejects_bad_labels():
+    X = synth.gaussian((10, 3), seed=1)
+    with pytest.raises(ValueError):
+        oracle.update(X, np.full(10, 5, np.int64), np.zeros((5, 3), np.float32))
+
+
+def test_random_rows_init_never_empties_first_iteration():
+    X, C0, _ = synth.workload_inputs(synth.Workload("t", 4096, 64, 32, 64, 1, 9, 19, ""))
+    labels, best, _, _ = oracle.assign(X, C0)
+    _, counts = oracle.update(X, labels, C0)
+    assert (counts > 0).all()
+
+
+def test_lloyd_inertia_never_increases():
+    X, C, _ = synth.workload_inputs(synth.Workload("t", 2048, 32, 24, 32, 1, 13, 23, ""))
+    prev = math.inf
+    for _ in range(10):
+        C, labels, best, _, inertia, counts = oracle.lloyd_iter(X, C)
+        assert inertia <= prev * (1 + 1e-12)
+        prev = inertia
+
+
+def test_oracle_thread_count_does_not_change_bits():
+    X = synth.gaussian((777, 45), seed=91)
+    C = synth.gaussian((31, 45), seed=92)
+    a = oracle.lloyd_iter(X, C, nthreads=1)
+    b = oracle.lloyd_iter(X, C, nthreads=4)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(np.asarray(u), np.asarray(v))
+
+
+# --------------------------------------------------------------------------
+# k-means++
+# --------------------------------------------------------------------------
+def test_kmeanspp_trial_count():
+    # "2 + log(n_clusters)", natural log, floored
+    assert oracle.n_trials_for(1) == 2
+    assert oracle.n_trials_for(1024) == 8
+    assert oracle.n_trials_for(2) == 2
+    assert oracle.n_trials_for(3) == 3
+
+
+def test_kmeanspp_first_center_is_uniform_draw():
+    X = synth.gaussian((1000, 4), seed=3)
+    for seed in (0, 1, 99):
+        idx, _, _ = oracle.kmeanspp(X, 1, seed)
+        assert idx[0] == int(math.floor(oracle.uniform(seed, 0) * 1000))
+
+
+def test_kmeanspp_second_draw_follows_d2_law():
+    # with one trial, center 1 is sampled with probability D^2_i / sum D^2
+    pts = np.array([[0.0], [1.0], [2.0], [4.0], [7.0], [11.0]], np.float32)
+    n = len(pts)
+    expected = np.zeros(n)
+    observed = np.zeros(n)
+    for seed in range(3000):
+        idx, _, _ = oracle.kmeanspp(pts, 2, seed, n_trials=1)
+        d2 = (pts[:, 0].astype(np.float64) - pts[idx[0], 0]) ** 2
+        expected += d2 / d2.sum()
+        observed[idx[1]] += 1
+    assert observed[expected == 0].sum() == 0
+    keep = expected > 0
+    chi = stats.chisquare(observed[keep], expected[keep] * observed.sum() / expected[keep].sum())
+    assert chi.pvalue > 1e-3
+
+
+def test_kmeanspp_distinct_points_never_repeat():
+    # a chosen point has D^2 = 0, so with the strict '>' search it is never
+    # drawn again: k = n gives a permutation
+    X = synth.gaussian((40, 3), seed=5)
+    idx, margins, pots = oracle.kmeanspp(X, 40, 7, n_trials=3)
+    assert sorted(idx.tolist()) == list(range(40))
+    assert pots[-1] == 0.0
+    assert np.all(np.diff(pots) <= 1e-12)  # potential never increases
+
+
+def test_kmeanspp_identical_points_take_last_index():
+    # sum D^2 = 0: no running sum exceeds the target, the draw clips to n - 1
+    X = np.ones((10, 4), np.float32)
+    idx, _, _ = oracle.kmeanspp(X, 3, 1, n_trials=2)
+    assert idx[1] == 9 and idx[2] == 9
+
+
+def test_kmeanspp_hits_every_separated_blob():
+    # 16 blobs, centers 100 apart: greedy D^2 seeding with 4 trials puts one
+    # center in each blob
+    centers = np.arange(16, dtype=np.float32)[:, None] * 100.0 * np.ones((1, 8), np.float32)
+    X = np.repeat(centers, 30, axis=0) + synth.gaussian((480, 8), seed=8, scale=0.5)
+    idx, _, _ = oracle.kmeanspp(X, 16, 2024, n_trials=4)
+    assert sorted((idx // 30).tolist()) == list(range(16))
+
+
+def test_kmeanspp_margins_are_fractions():
+    X = synth.gaussian((500, 6), seed=9)
+    idx, margins, _ = oracle.kmeanspp(X, 20, 3)
+    assert len(margins) == 1 + 19 * oracle.n_trials_for(20)
+    assert np.all(margins >= 0) and np.all(margins <= 0.5)
+
+
+# --------------------------------------------------------------------------
+# Input generator
+# --------------------------------------------------------------------------
+def test_blob_generator_statistics_and_determinism():
+    X, centers, blob = synth.planted_blobs(4096, 64, 16, seed=3, threads=3)
+    X2, _, _ = synth.planted_blobs(4096, 64, 16, seed=3, threads=1)
+    assert X.tobytes() == X2.tobytes()  # thread count does not change bytes
+    noise = X - centers[blob]
+    assert abs(noise.std() - 0.5) < 0.01
+    assert abs(centers.std() - 1.0) < 0.05
+    assert (blob == np.arange(4096) % 16).all()
