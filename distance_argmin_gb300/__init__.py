@@ -1,0 +1,271 @@
+"""Python binding of the GB300 k-means library (``include/kmeans_gb300.h``).
+
+Argument marshalling only: every function checks tensor types, shapes and
+devices, passes raw device pointers, sizes and the current CUDA stream to the
+C ABI of ``libkmeans_gb300.so``, and raises ``KMeansError`` on a non-zero
+status.  All arithmetic runs in the library's CUDA kernels.  PyTorch supplies
+device memory (outputs and the workspace when the caller passes none) and
+streams.  There is no CPU path: without the built library every call fails.
+
+Names follow the C ABI: ``kmeans_assign``, ``kmeans_assign_ffma``,
+``kmeans_update``, ``kmeans_lloyd_iter``, ``kmeanspp_init``,
+``kmeans_workspace_bytes``, ``kmeans_device_status``, ``kmeans_status_string``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkmeans_gb300.so")
+
+KMEANS_OK = 0
+KMEANS_ERR_INVALID_ARG = 1
+KMEANS_ERR_UNSUPPORTED = 2
+KMEANS_ERR_WORKSPACE = 3
+KMEANS_ERR_CUDA = 4
+KMEANS_ERR_DEVICE_TIMEOUT = 5
+KMEANS_ERR_DEVICE_LABEL = 6
+
+OP_ASSIGN = 0
+OP_ASSIGN_FFMA = 1
+OP_UPDATE = 2
+OP_LLOYD = 3
+OP_KMEANSPP = 4
+
+# Every symbol the header declares (the ABI test checks the library exports them).
+EXPORTS = (
+    "kmeans_workspace_bytes", "kmeans_assign", "kmeans_assign_ffma", "kmeans_update",
+    "kmeans_lloyd_iter", "kmeanspp_init", "kmeans_device_status", "kmeans_status_string",
+    "kmeans_build_info",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KMeansError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {kmeans_status_string(status)} (status {status})")
+
+
+def load(path: str | None = None):
+    """Load the library once; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with `python -m distance_argmin_gb300.build`"
+                               " (the library has no CPU fallback)")
+        lib = ctypes.CDLL(p)
+        P, I64, U64, SZ, INT = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t,
+                                ctypes.c_int)
+        lib.kmeans_workspace_bytes.argtypes = [INT, I64, I64, I64]
+        lib.kmeans_workspace_bytes.restype = SZ
+        assign_sig = [P, P, I64, I64, I64, P, P, P, P, SZ, U64, P]
+        lib.kmeans_assign.argtypes = assign_sig
+        lib.kmeans_assign.restype = INT
+        lib.kmeans_assign_ffma.argtypes = assign_sig
+        lib.kmeans_assign_ffma.restype = INT
+        lib.kmeans_update.argtypes = [P, P, P, P, P, I64, I64, I64, P, SZ, U64, P]
+        lib.kmeans_update.restype = INT
+        lib.kmeans_lloyd_iter.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, P, SZ, U64, P]
+        lib.kmeans_lloyd_iter.restype = INT
+        lib.kmeanspp_init.argtypes = [P, I64, I64, I64, INT, U64, P, P, P, SZ, P]
+        lib.kmeanspp_init.restype = INT
+        lib.kmeans_device_status.argtypes = [P, P]
+        lib.kmeans_device_status.restype = INT
+        lib.kmeans_status_string.argtypes = [INT]
+        lib.kmeans_status_string.restype = ctypes.c_char_p
+        lib.kmeans_build_info.argtypes = []
+        lib.kmeans_build_info.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def kmeans_status_string(status: int) -> str:
+    return load().kmeans_status_string(int(status)).decode()
+
+
+def kmeans_build_info() -> str:
+    return load().kmeans_build_info().decode()
+
+
+def kmeans_workspace_bytes(op: int, n: int, k: int, d: int) -> int:
+    return int(load().kmeans_workspace_bytes(op, n, k, d))
+
+
+def n_trials_for(k: int) -> int:
+    """2 + floor(ln k): the default k-means++ trial count."""
+    return 2 + int(math.floor(math.log(k)))
+
+
+# ----------------------------------------------------------------- helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    torch = _torch()
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(t, name, dtype, shape=None, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def workspace(op: int, n: int, k: int, d: int, device=None):
+    """A device workspace big enough for ``op`` on these sizes (uint8 tensor)."""
+    torch = _torch()
+    nbytes = kmeans_workspace_bytes(op, n, k, d)
+    if nbytes == 0:
+        raise KMeansError(KMEANS_ERR_INVALID_ARG, "kmeans_workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(ws, op, n, k, d, device):
+    if ws is None:
+        return workspace(op, n, k, d, device)
+    _check(ws, "ws", _torch().uint8, device=device)
+    return ws
+
+
+def _raise(status, what):
+    if status != KMEANS_OK:
+        raise KMeansError(status, what)
+
+
+# ------------------------------------------------------------- entry points
+def _assign(fn_name, op, X, C, labels, best_dist, inertia, ws, seed, stream):
+    torch = _torch()
+    _check(X, "X", torch.float32)
+    n, d = X.shape
+    _check(C, "C", torch.float32, device=X.device)
+    k = C.shape[0]
+    if C.dim() != 2 or C.shape[1] != d:
+        raise ValueError("C must be (k, d) with the same d as X")
+    if labels is None:
+        labels = torch.empty(n, dtype=torch.int64, device=X.device)
+    if best_dist is None:
+        best_dist = torch.empty(n, dtype=torch.float32, device=X.device)
+    if inertia is None:
+        inertia = torch.empty(1, dtype=torch.float64, device=X.device)
+    _check(labels, "labels", torch.int64, (n,), X.device)
+    _check(best_dist, "best_dist", torch.float32, (n,), X.device)
+    _check(inertia, "inertia", torch.float64, (1,), X.device)
+    ws = _ws(ws, op, n, k, d, X.device)
+    st = getattr(load(), fn_name)(_ptr(X), _ptr(C), n, k, d, _ptr(labels), _ptr(best_dist), _ptr(inertia),
+                                  _ptr(ws), ws.numel(), seed & (2**64 - 1), _stream_handle(stream))
+    _raise(st, fn_name)
+    return labels, best_dist, inertia
+
+
+def kmeans_assign(X, C, labels=None, best_dist=None, inertia=None, ws=None, seed=0, stream=None):
+    """Nearest centroid on the tensor cores -> ``(labels, best_dist, inertia)``."""
+    return _assign("kmeans_assign", OP_ASSIGN, X, C, labels, best_dist, inertia, ws, seed, stream)
+
+
+def kmeans_assign_ffma(X, C, labels=None, best_dist=None, inertia=None, ws=None, seed=0, stream=None):
+    """The same assignment with float32 FMA on the CUDA cores (comparator)."""
+    return _assign("kmeans_assign_ffma", OP_ASSIGN_FFMA, X, C, labels, best_dist, inertia, ws, seed, stream)
+
+
+def kmeans_update(X, labels, C_old, C_new=None, counts=None, ws=None, seed=0, stream=None):
+    """Mean of members, empty clusters keep ``C_old`` -> ``(C_new, counts)``."""
+    torch = _torch()
+    _check(X, "X", torch.float32)
+    n, d = X.shape
+    _check(labels, "labels", torch.int64, (n,), X.device)
+    _check(C_old, "C_old", torch.float32, device=X.device)
+    k = C_old.shape[0]
+    if C_new is None:
+        C_new = torch.empty_like(C_old)
+    if counts is None:
+        counts = torch.empty(k, dtype=torch.int32, device=X.device)
+    _check(C_new, "C_new", torch.float32, (k, d), X.device)
+    _check(counts, "counts", torch.int32, (k,), X.device)
+    ws = _ws(ws, OP_UPDATE, n, k, d, X.device)
+    st = load().kmeans_update(_ptr(X), _ptr(labels), _ptr(C_old), _ptr(C_new), _ptr(counts), n, k, d,
+                              _ptr(ws), ws.numel(), seed & (2**64 - 1), _stream_handle(stream))
+    _raise(st, "kmeans_update")
+    return C_new, counts
+
+
+def kmeans_lloyd_iter(X, C_old, C_new=None, labels=None, best_dist=None, inertia=None, counts=None, ws=None,
+                      seed=0, stream=None):
+    """One Lloyd iteration -> ``(C_new, labels, best_dist, inertia, counts)``."""
+    torch = _torch()
+    _check(X, "X", torch.float32)
+    n, d = X.shape
+    _check(C_old, "C_old", torch.float32, device=X.device)
+    k = C_old.shape[0]
+    if C_new is None:
+        C_new = torch.empty_like(C_old)
+    if labels is None:
+        labels = torch.empty(n, dtype=torch.int64, device=X.device)
+    if best_dist is None:
+        best_dist = torch.empty(n, dtype=torch.float32, device=X.device)
+    if inertia is None:
+        inertia = torch.empty(1, dtype=torch.float64, device=X.device)
+    if counts is None:
+        counts = torch.empty(k, dtype=torch.int32, device=X.device)
+    _check(C_new, "C_new", torch.float32, (k, d), X.device)
+    _check(labels, "labels", torch.int64, (n,), X.device)
+    _check(best_dist, "best_dist", torch.float32, (n,), X.device)
+    _check(inertia, "inertia", torch.float64, (1,), X.device)
+    _check(counts, "counts", torch.int32, (k,), X.device)
+    ws = _ws(ws, OP_LLOYD, n, k, d, X.device)
+    st = load().kmeans_lloyd_iter(_ptr(X), _ptr(C_old), _ptr(C_new), _ptr(labels), _ptr(best_dist),
+                                  _ptr(inertia), _ptr(counts), n, k, d, _ptr(ws), ws.numel(),
+                                  seed & (2**64 - 1), _stream_handle(stream))
+    _raise(st, "kmeans_lloyd_iter")
+    return C_new, labels, best_dist, inertia, counts
+
+
+def kmeanspp_init(X, k: int, seed: int, n_trials: int = 0, centers=None, indices=None, ws=None, stream=None):
+    """Greedy D^2 seeding -> ``(indices, centers)``."""
+    torch = _torch()
+    _check(X, "X", torch.float32)
+    n, d = X.shape
+    if indices is None:
+        indices = torch.empty(k, dtype=torch.int64, device=X.device)
+    if centers is None:
+        centers = torch.empty((k, d), dtype=torch.float32, device=X.device)
+    _check(indices, "indices", torch.int64, (k,), X.device)
+    _check(centers, "centers", torch.float32, (k, d), X.device)
+    ws = _ws(ws, OP_KMEANSPP, n, k, d, X.device)
+    st = load().kmeanspp_init(_ptr(X), n, d, k, int(n_trials), seed & (2**64 - 1), _ptr(centers), _ptr(indices),
+                              _ptr(ws), ws.numel(), _stream_handle(stream))
+    _raise(st, "kmeanspp_init")
+    return indices, centers
+
+
+def kmeans_device_status(ws, stream=None) -> int:
+    """Synchronise the stream; status of the last call that used ``ws``."""
+    return int(load().kmeans_device_status(_ptr(ws), _stream_handle(stream)))

@@ -1,0 +1,190 @@
+// C ABI of the library (declared in include/kmeans_gb300.h): argument
+// validation, workspace sizing and the order of kernel launches on the
+// caller's stream.  Nothing here allocates memory or synchronises, except
+// kmeans_device_status, whose job is to wait for the stream.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/kmeans_gb300.h"
+#include "assign_common.cuh"
+#include "common.cuh"
+#include "kmeanspp.cuh"
+#include "update.cuh"
+
+using namespace km;
+
+namespace {
+
+constexpr int64_t kMaxIndex = 0x7fffffffLL;  // labels and member lists use 32-bit indices
+
+bool sizes_ok(int64_t n, int64_t k, int64_t d) {
+    return n >= 1 && k >= 1 && k <= n && d >= 1 && n <= kMaxIndex && k <= kMaxIndex && d <= kMaxIndex;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int check_ws(const void *ws, size_t ws_bytes, size_t need) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KMEANS_ERR_WORKSPACE;
+    if (ws_bytes < need) return KMEANS_ERR_WORKSPACE;
+    return KMEANS_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? KMEANS_OK : KMEANS_ERR_CUDA; }
+
+int tc_path_ok(const float *X, const float *C, int64_t d) {
+    return (d % 4 == 0 && aligned16(X) && aligned16(C)) ? KMEANS_OK : KMEANS_ERR_UNSUPPORTED;
+}
+
+int default_trials(int64_t k) { return 2 + (int)floor(log((double)k)); }
+
+int run_assign(bool tensor_cores, const float *X, const float *C, int64_t n, int64_t k, int64_t d, int64_t *labels,
+               float *best_dist, double *inertia, void *ws, size_t ws_bytes, cudaStream_t s) {
+    if (!X || !C || !labels || !best_dist) return KMEANS_ERR_INVALID_ARG;
+    if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    if (!aligned4(X) || !aligned4(C)) return KMEANS_ERR_INVALID_ARG;
+    if (tensor_cores) {
+        const int st = tc_path_ok(X, C, d);
+        if (st != KMEANS_OK) return st;
+    } else if ((k + 127) / 128 > 65535) {
+        return KMEANS_ERR_UNSUPPORTED;
+    }
+    const AssignLayout L = assign_layout(n, k, d, tensor_cores);
+    const int wst = check_ws(ws, ws_bytes, (size_t)L.bytes);
+    if (wst != KMEANS_OK) return wst;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    cudaError_t e;
+    if (tensor_cores) {
+        e = launch_prep_split(C, n, k, d, L, w, s);
+        if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, L, w, s);
+    } else {
+        e = launch_prep_norms(C, n, k, d, L, w, s);
+        if (e == cudaSuccess) e = launch_assign_ffma(X, C, n, k, d, L, w, s);
+    }
+    if (e == cudaSuccess) e = launch_finalize(n, L, w, labels, best_dist, inertia, s);
+    return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
+    if (!sizes_ok(n, k, d)) return 0;
+    switch (op) {
+        case KMEANS_OP_ASSIGN:
+            return (size_t)assign_layout(n, k, d, true).bytes;
+        case KMEANS_OP_ASSIGN_FFMA:
+            return (size_t)assign_layout(n, k, d, false).bytes;
+        case KMEANS_OP_UPDATE:
+            return (size_t)update_layout(n, k, d).bytes;
+        case KMEANS_OP_LLOYD: {
+            const int64_t a = assign_layout(n, k, d, true).bytes;
+            const int64_t u = update_layout(n, k, d).bytes;
+            return (size_t)(a > u ? a : u);
+        }
+        case KMEANS_OP_KMEANSPP:
+            return (size_t)kpp_layout(n, k, kKppMaxTrials).bytes;
+        default:
+            return 0;
+    }
+}
+
+int kmeans_assign(const float *X, const float *C, int64_t n, int64_t k, int64_t d, int64_t *labels,
+                  float *best_dist, double *inertia, void *ws, size_t ws_bytes, uint64_t seed, void *stream) {
+    (void)seed;
+    return run_assign(true, X, C, n, k, d, labels, best_dist, inertia, ws, ws_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int kmeans_assign_ffma(const float *X, const float *C, int64_t n, int64_t k, int64_t d, int64_t *labels,
+                       float *best_dist, double *inertia, void *ws, size_t ws_bytes, uint64_t seed, void *stream) {
+    (void)seed;
+    return run_assign(false, X, C, n, k, d, labels, best_dist, inertia, ws, ws_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int kmeans_update(const float *X, const int64_t *labels, const float *C_old, float *C_new, int32_t *counts,
+                  int64_t n, int64_t k, int64_t d, void *ws, size_t ws_bytes, uint64_t seed, void *stream) {
+    (void)seed;
+    if (!X || !labels || !C_old || !C_new) return KMEANS_ERR_INVALID_ARG;
+    if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    if (!aligned4(X) || !aligned4(C_old) || !aligned4(C_new) || (reinterpret_cast<uintptr_t>(labels) & 7u))
+        return KMEANS_ERR_INVALID_ARG;
+    const UpdateLayout L = update_layout(n, k, d);
+    const int wst = check_ws(ws, ws_bytes, (size_t)L.bytes);
+    if (wst != KMEANS_OK) return wst;
+    return cuda_status(launch_update(X, labels, C_old, C_new, counts, n, k, d, L, static_cast<uint8_t *>(ws), true,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int kmeans_lloyd_iter(const float *X, const float *C_old, float *C_new, int64_t *labels, float *best_dist,
+                      double *inertia, int32_t *counts, int64_t n, int64_t k, int64_t d, void *ws, size_t ws_bytes,
+                      uint64_t seed, void *stream) {
+    (void)seed;
+    if (!X || !C_old || !C_new || !labels || !best_dist) return KMEANS_ERR_INVALID_ARG;
+    if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    if (!aligned4(C_new) || (reinterpret_cast<uintptr_t>(labels) & 7u)) return KMEANS_ERR_INVALID_ARG;
+    const int st = tc_path_ok(X, C_old, d);
+    if (st != KMEANS_OK) return st;
+    const size_t need = kmeans_workspace_bytes(KMEANS_OP_LLOYD, n, k, d);
+    const int wst = check_ws(ws, ws_bytes, need);
+    if (wst != KMEANS_OK) return wst;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    const AssignLayout A = assign_layout(n, k, d, true);
+    cudaError_t e = launch_prep_split(C_old, n, k, d, A, w, s);
+    if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, A, w, s);
+    if (e == cudaSuccess) e = launch_finalize(n, A, w, labels, best_dist, inertia, s);
+    // the update reuses the same workspace: the assignment's scratch is dead
+    // once its labels are written
+    if (e == cudaSuccess) e = launch_update(X, labels, C_old, C_new, counts, n, k, d, update_layout(n, k, d), w, false, s);
+    return cuda_status(e);
+}
+
+int kmeanspp_init(const float *X, int64_t n, int64_t d, int64_t k, int n_trials, uint64_t seed, float *centers,
+                  int64_t *indices, void *ws, size_t ws_bytes, void *stream) {
+    if (!X || !indices) return KMEANS_ERR_INVALID_ARG;
+    if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    if (!aligned4(X) || (centers && !aligned4(centers)) || (reinterpret_cast<uintptr_t>(indices) & 7u))
+        return KMEANS_ERR_INVALID_ARG;
+    const int T = n_trials > 0 ? n_trials : default_trials(k);
+    if (T > kKppMaxTrials) return KMEANS_ERR_UNSUPPORTED;
+    const KppLayout L = kpp_layout(n, k, T);
+    const int wst = check_ws(ws, ws_bytes, (size_t)L.bytes);
+    if (wst != KMEANS_OK) return wst;
+    return cuda_status(launch_kmeanspp(X, n, d, k, T, seed, centers, indices, L, static_cast<uint8_t *>(ws),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int kmeans_device_status(const void *ws, void *stream) {
+    if (ws == nullptr) return KMEANS_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KMEANS_ERR_CUDA;
+    uint32_t st = 0;
+    if (cudaMemcpy(&st, ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return KMEANS_ERR_CUDA;
+    if (st & kFlagTimeout) return KMEANS_ERR_DEVICE_TIMEOUT;
+    if (st & kFlagBadLabel) return KMEANS_ERR_DEVICE_LABEL;
+    return KMEANS_OK;
+}
+
+const char *kmeans_status_string(int status) {
+    switch (status) {
+        case KMEANS_OK: return "ok";
+        case KMEANS_ERR_INVALID_ARG: return "invalid argument";
+        case KMEANS_ERR_UNSUPPORTED: return "unsupported by this build (see the header's requirements)";
+        case KMEANS_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+        case KMEANS_ERR_CUDA: return "CUDA runtime error";
+        case KMEANS_ERR_DEVICE_TIMEOUT: return "a device pipeline wait ran out of time";
+        case KMEANS_ERR_DEVICE_LABEL: return "a label outside [0, k) reached the update";
+        default: return "unknown status";
+    }
+}
+
+const char *kmeans_build_info(void) {
+    return "kmeans_gb300 sm_103a: assign = tcgen05 bf16x3 split, 128x256 tile, BK 32, 3 stages, "
+           "persistent 1 CTA/SM; comparator = FFMA 128x128; update = LSD radix member list + "
+           "compensated segmented mean; k-means++ = Philox4x32-10 greedy D^2";
+}
+
+}  // extern "C"

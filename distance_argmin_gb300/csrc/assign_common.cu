@@ -1,0 +1,197 @@
+// Assignment prologue (centroid norms and bf16 split) and epilogue (labels,
+// distances, inertia).
+//
+// ||c_j||^2 is computed once per call and reused by every sample tile
+// ("004 — tile sizes, a Cython Lloyd step, and k-means++", section "Schedules
+// added").  The reported distance adds ||x_i||^2 back to the winning score
+// ||c||^2 - 2 x.c ("Three shapes that fit an eager Gram assignment", section
+// "Gram assignment"), clamped at zero, and the result per sample is an int64
+// label plus a float32 distance (same page, section "Running argmin, one
+// centroid").
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "assign_common.cuh"
+#include "common.cuh"
+
+namespace km {
+
+__device__ __forceinline__ void kahan_add(float &sum, float &comp, float v) {
+    const float y = v - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 h) {
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// One warp per centroid row.  d % 4 == 0 and C 16-byte aligned (checked on
+// the host for this path); columns d .. d_pad-1 of the copies are zeroed.
+__global__ void prep_split_kernel(const float *__restrict__ C, int k, int d, int d_pad,
+                                  __nv_bfloat16 *__restrict__ chi, __nv_bfloat16 *__restrict__ clo,
+                                  float *__restrict__ cnorm, unsigned long long *__restrict__ keys, int n,
+                                  WsHeader *hdr) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr->status = 0u;
+        hdr->done_blocks = 0u;
+    }
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    for (int j = gw; j < k; j += nw) {
+        const float *row = C + (size_t)j * d;
+        float sum = 0.f, comp = 0.f;
+        for (int f = lane * 4; f < d_pad; f += 128) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (f < d) v = __ldg(reinterpret_cast<const float4 *>(row + f));
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+            const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+            const float2 f01 = __bfloat1622float2(h01);
+            const float2 f23 = __bfloat1622float2(h23);
+            const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+            const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+            const size_t o = (size_t)j * d_pad + f;
+            *reinterpret_cast<uint2 *>(chi + o) = make_uint2(bf16x2_bits(h01), bf16x2_bits(h23));
+            *reinterpret_cast<uint2 *>(clo + o) = make_uint2(bf16x2_bits(l01), bf16x2_bits(l23));
+            float q = v.x * v.x;
+            q = fmaf(v.y, v.y, q);
+            q = fmaf(v.z, v.z, q);
+            q = fmaf(v.w, v.w, q);
+            kahan_add(sum, comp, q);
+        }
+        const float tot = warp_sum(sum - comp);
+        if (lane == 0) cnorm[j] = tot;
+    }
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        keys[i] = kEmptyKey;
+}
+
+// Norms only (any d, any 4-byte alignment).
+__global__ void prep_norms_kernel(const float *__restrict__ C, int k, int d, float *__restrict__ cnorm,
+                                  unsigned long long *__restrict__ keys, int n, WsHeader *hdr) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr->status = 0u;
+        hdr->done_blocks = 0u;
+    }
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    for (int j = gw; j < k; j += nw) {
+        const float *row = C + (size_t)j * d;
+        float sum = 0.f, comp = 0.f;
+        for (int f = lane; f < d; f += 32) {
+            const float v = __ldg(row + f);
+            kahan_add(sum, comp, v * v);
+        }
+        const float tot = warp_sum(sum - comp);
+        if (lane == 0) cnorm[j] = tot;
+    }
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        keys[i] = kEmptyKey;
+}
+
+constexpr int kFinThreads = 256;
+
+// Rows are split into gridDim.x contiguous ranges (fixed by n), each summed in
+// a fixed order; the last block to finish adds the block sums in index order.
+__global__ void finalize_kernel(const unsigned long long *__restrict__ keys, const float *__restrict__ xnorm,
+                                int n, int64_t *__restrict__ labels, float *__restrict__ best,
+                                double *inertia, double *partial, WsHeader *hdr) {
+    __shared__ double red[kFinThreads];
+    __shared__ int is_last;
+    const int nb = gridDim.x;
+    const int per = (n + nb - 1) / nb;
+    const int r0 = blockIdx.x * per;
+    const int r1 = min(n, r0 + per);
+    double s = 0.0;
+    for (int r = r0 + threadIdx.x; r < r1; r += kFinThreads) {
+        const unsigned long long key = keys[r];
+        if (key == kEmptyKey) {  // only for non-finite inputs
+            labels[r] = -1;
+            best[r] = __int_as_float(0x7fc00000);
+            continue;
+        }
+        const float score = ord_to_float(static_cast<uint32_t>(key >> 32));
+        const float b = fmaxf(0.f, xnorm[r] + score);
+        labels[r] = static_cast<int64_t>(static_cast<uint32_t>(key & 0xffffffffu));
+        best[r] = b;
+        s += static_cast<double>(b);
+    }
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = kFinThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (inertia == nullptr) return;
+    if (threadIdx.x == 0) {
+        partial[blockIdx.x] = red[0];
+        __threadfence();
+        const unsigned t = atomicAdd(&hdr->done_blocks, 1u);
+        is_last = (t == (unsigned)nb - 1u);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    double v = 0.0;
+    for (int b = threadIdx.x; b < nb; b += kFinThreads) v += __ldcg(partial + b);
+    red[threadIdx.x] = v;
+    __syncthreads();
+    for (int w = kFinThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        *inertia = red[0];
+        hdr->done_blocks = 0u;
+    }
+}
+
+static int prep_grid(int64_t k, int64_t n) {
+    const int64_t by_rows = (k + 7) / 8;  // 8 warps per block, one row each
+    const int64_t by_keys = (n + 255) / 256;
+    int64_t g = by_rows > by_keys ? by_rows : by_keys;
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    if (g > cap) g = cap;
+    return (int)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_prep_split(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
+                              uint8_t *ws, cudaStream_t s) {
+    prep_split_kernel<<<prep_grid(k, n), 256, 0, s>>>(
+        C, (int)k, (int)d, (int)L.d_pad, reinterpret_cast<__nv_bfloat16 *>(ws + L.off_chi),
+        reinterpret_cast<__nv_bfloat16 *>(ws + L.off_clo), reinterpret_cast<float *>(ws + L.off_cnorm),
+        reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_norms(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
+                              uint8_t *ws, cudaStream_t s) {
+    prep_norms_kernel<<<prep_grid(k, n), 256, 0, s>>>(C, (int)k, (int)d,
+                                                      reinterpret_cast<float *>(ws + L.off_cnorm),
+                                                      reinterpret_cast<unsigned long long *>(ws + L.off_keys),
+                                                      (int)n, reinterpret_cast<WsHeader *>(ws));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(int64_t n, const AssignLayout &L, uint8_t *ws, int64_t *labels, float *best,
+                            double *inertia, cudaStream_t s) {
+    int64_t nb = (n + kFinThreads - 1) / kFinThreads;
+    if (nb > kMaxReduceBlocks) nb = kMaxReduceBlocks;
+    finalize_kernel<<<(int)nb, kFinThreads, 0, s>>>(
+        reinterpret_cast<const unsigned long long *>(ws + L.off_keys),
+        reinterpret_cast<const float *>(ws + L.off_xnorm), (int)n, labels, best, inertia,
+        reinterpret_cast<double *>(ws + L.off_partial), reinterpret_cast<WsHeader *>(ws));
+    return cudaGetLastError();
+}
+
+}  // namespace km

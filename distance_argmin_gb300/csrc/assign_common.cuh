@@ -1,0 +1,34 @@
+// Host-side launchers shared by the assignment entry points.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace km {
+
+int device_sm_count();
+int assign_tc_smem_bytes();
+
+// Clears the status word, splits C into bf16 hi / lo copies (row pitch
+// L.d_pad), computes ||c_j||^2 and resets the per-sample keys.
+cudaError_t launch_prep_split(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
+                              uint8_t *ws, cudaStream_t s);
+
+// Clears the status word, computes ||c_j||^2 and resets the keys (no split).
+cudaError_t launch_prep_norms(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
+                              uint8_t *ws, cudaStream_t s);
+
+cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
+                             uint8_t *ws, cudaStream_t s);
+
+cudaError_t launch_assign_ffma(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
+                               const AssignLayout &L, uint8_t *ws, cudaStream_t s);
+
+// Keys -> int64 labels, float32 distances (+ ||x||^2, clamped at 0) and the
+// float64 inertia in a fixed reduction order.
+cudaError_t launch_finalize(int64_t n, const AssignLayout &L, uint8_t *ws, int64_t *labels, float *best,
+                            double *inertia, cudaStream_t s);
+
+}  // namespace km

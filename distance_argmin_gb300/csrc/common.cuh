@@ -1,0 +1,192 @@
+// Shared device helpers of the GB300 k-means library: status word, bounded
+// waits, order-preserving keys for the fused argmin, workspace layout.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kmeans_gb300.h"
+
+namespace km {
+
+// ---------------------------------------------------------------------------
+// Device status word.  Lives in the first bytes of the caller's workspace and
+// is cleared by every entry point before its first kernel.  Kernels OR flags
+// into it; the host maps them to kmeans_status codes.
+// ---------------------------------------------------------------------------
+enum : uint32_t {
+    kFlagTimeout = 1u,   // a pipeline wait ran out of time
+    kFlagBadLabel = 2u,  // update saw a label outside [0, k)
+};
+
+struct WsHeader {
+    uint32_t status;          // device status flags
+    uint32_t done_blocks;     // "last block" counter of the inertia reduction
+    uint32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// Wall-clock limit of one pipeline wait.  A wait that legitimately takes this
+// long does not exist (the slowest stage waits for one k-block of a tile).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void flag_error(uint32_t *status, uint32_t flag) {
+    atomicOr(status, flag);
+}
+
+__device__ __forceinline__ bool error_raised(const uint32_t *status) {
+    return *reinterpret_cast<const volatile uint32_t *>(status) != 0u;
+}
+
+// ---------------------------------------------------------------------------
+// Order-preserving 32-bit image of a float: a < b (as finite floats) iff
+// ord(a) < ord(b) (as unsigned).  The fused argmin packs ord(score) above the
+// centroid index into one 64-bit key, so an unsigned 64-bit minimum picks the
+// smallest score and, among equal scores, the lowest index.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t float_to_ord(float f) {
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float ord_to_float(uint32_t o) {
+    uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+    return __uint_as_float(u);
+}
+
+__device__ __forceinline__ uint64_t make_key(float score, uint32_t j) {
+    return (static_cast<uint64_t>(float_to_ord(score)) << 32) | j;
+}
+
+constexpr uint64_t kEmptyKey = ~0ull;
+
+// ---------------------------------------------------------------------------
+// Workspace layout.  Every region is 1 KiB aligned.  Sizes depend on n, on
+// k*d (the split centroids) and on n/4096 (sort tiles); never on n*k.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+struct AssignLayout {
+    int64_t d_pad;       // row pitch (elements) of the split centroid copies
+    int64_t off_keys;    // n x u64 packed (score, index) keys
+    int64_t off_xnorm;   // n x f32 ||x_i||^2
+    int64_t off_cnorm;   // k x f32 ||c_j||^2
+    int64_t off_chi;     // k x d_pad bf16 hi part of C
+    int64_t off_clo;     // k x d_pad bf16 lo part of C
+    int64_t off_partial; // kMaxReduceBlocks x f64 inertia partial sums
+    int64_t bytes;
+};
+
+constexpr int kMaxReduceBlocks = 1024;
+
+inline AssignLayout assign_layout(int64_t n, int64_t k, int64_t d, bool split) {
+    AssignLayout L{};
+    L.d_pad = align_up(d, 64);
+    int64_t o = sizeof(WsHeader);
+    o = align_up(o, 1024); L.off_keys = o; o += n * 8;
+    o = align_up(o, 1024); L.off_xnorm = o; o += n * 4;
+    o = align_up(o, 1024); L.off_cnorm = o; o += k * 4;
+    if (split) {
+        o = align_up(o, 1024); L.off_chi = o; o += k * L.d_pad * 2;
+        o = align_up(o, 1024); L.off_clo = o; o += k * L.d_pad * 2;
+    } else {
+        L.off_chi = L.off_clo = 0;
+    }
+    o = align_up(o, 1024); L.off_partial = o; o += kMaxReduceBlocks * 8;
+    L.bytes = align_up(o, 1024);
+    return L;
+}
+
+// Update: LSD radix sort of the labels (8-bit digits) into a member list,
+// then a segmented mean over fixed chunks of that list.
+constexpr int kSortTile = 4096;      // labels per radix tile
+constexpr int kSortThreads = 256;
+constexpr int kRadixBins = 256;
+
+struct UpdateLayout {
+    int64_t n_tiles;     // radix tiles
+    int64_t chunk;       // members per segmented-mean chunk
+    int64_t n_chunks;
+    int64_t off_counts;  // k x i32 member counts
+    int64_t off_offsets; // (k + 1) x i32 exclusive scan of counts
+    int64_t off_hist;    // 256 x n_tiles x i32 digit histograms (scanned in place)
+    int64_t off_keys_a;  // n x u32 sort keys (ping)
+    int64_t off_vals_a;  // n x i32 sort values (ping)
+    int64_t off_keys_b;  // n x u32 (pong)
+    int64_t off_vals_b;  // n x i32 (pong)
+    int64_t off_head;    // n_chunks x d f32 partial sums, cluster entering a chunk
+    int64_t off_tail;    // n_chunks x d f32 partial sums, cluster leaving a chunk
+    int64_t bytes;
+};
+
+inline int64_t update_chunk(int64_t n, int64_t d) {
+    // members per chunk: enough chunks to fill the machine several times over
+    // with 512-column slices, at least 64 members per chunk
+    int64_t slices = (d + 511) / 512;
+    int64_t target_ctas = 152 * 8;
+    int64_t chunks = (target_ctas + slices - 1) / slices;
+    int64_t c = (n + chunks - 1) / chunks;
+    if (c < 64) c = 64;
+    c = align_up(c, 32);
+    return c > 4096 ? 4096 : c;  // the chunk's member list is staged in shared memory
+}
+
+inline UpdateLayout update_layout(int64_t n, int64_t k, int64_t d) {
+    UpdateLayout L{};
+    L.n_tiles = (n + kSortTile - 1) / kSortTile;
+    L.chunk = update_chunk(n, d);
+    L.n_chunks = (n + L.chunk - 1) / L.chunk;
+    int64_t o = sizeof(WsHeader);
+    o = align_up(o, 1024); L.off_counts = o; o += k * 4;
+    o = align_up(o, 1024); L.off_offsets = o; o += (k + 1) * 4;
+    o = align_up(o, 1024); L.off_hist = o; o += kRadixBins * L.n_tiles * 4;
+    o = align_up(o, 1024); L.off_keys_a = o; o += n * 4;
+    o = align_up(o, 1024); L.off_vals_a = o; o += n * 4;
+    o = align_up(o, 1024); L.off_keys_b = o; o += n * 4;
+    o = align_up(o, 1024); L.off_vals_b = o; o += n * 4;
+    o = align_up(o, 1024); L.off_head = o; o += L.n_chunks * d * 4;
+    o = align_up(o, 1024); L.off_tail = o; o += L.n_chunks * d * 4;
+    L.bytes = align_up(o, 1024);
+    return L;
+}
+
+// k-means++: D^2, running sums, per-trial distances and potentials.
+struct KppLayout {
+    int T;
+    int64_t n_blocks;     // blocks of the scan / potential reductions
+    int64_t off_d2;       // n x f64 current D^2
+    int64_t off_dist;     // T x n x f64 distances to the trial candidates
+    int64_t off_bsum;     // n_blocks x f64 block sums of D^2
+    int64_t off_bpot;     // T x kKppMaxCtas x f64 per-CTA potentials
+    int64_t off_cand;     // T x i64 candidates of the current center
+    int64_t off_chosen;   // i32 winning trial of the previous center
+    int64_t bytes;
+};
+
+constexpr int kKppScanBlock = 1024;   // samples per scan block
+constexpr int kKppMaxCtas = 1024;     // CTAs of the distance pass (fixed per n)
+constexpr int kKppMaxTrials = 32;
+
+inline KppLayout kpp_layout(int64_t n, int64_t k, int T) {
+    KppLayout L{};
+    L.T = T;
+    L.n_blocks = (n + kKppScanBlock - 1) / kKppScanBlock;
+    int64_t o = sizeof(WsHeader);
+    o = align_up(o, 1024); L.off_d2 = o; o += n * 8;
+    o = align_up(o, 1024); L.off_dist = o; o += (int64_t)T * n * 8;
+    o = align_up(o, 1024); L.off_bsum = o; o += L.n_blocks * 8;
+    o = align_up(o, 1024); L.off_bpot = o; o += (int64_t)T * kKppMaxCtas * 8;
+    o = align_up(o, 1024); L.off_cand = o; o += (int64_t)T * 8;
+    o = align_up(o, 1024); L.off_chosen = o; o += 8;
+    L.bytes = align_up(o, 1024);
+    (void)k;
+    return L;
+}
+
+}  // namespace km

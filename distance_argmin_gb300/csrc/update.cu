@@ -1,0 +1,344 @@
+// Mean update of the Lloyd iteration ("Three shapes that fit an eager Gram
+// assignment", section "Full Lloyd step": every centroid becomes the mean of
+// its members).  No (n, k) one-hot matrix: the labels are sorted into a member
+// list and each centroid's members are summed as one contiguous segment.
+//
+//   1. count members per cluster and clear the digit histograms
+//   2. stable LSD radix sort of (label, sample index), 8-bit digits
+//      (ceil(bits(k-1) / 8) passes: hist -> scan -> stable scatter)
+//   3. exclusive scan of the counts -> segment offsets
+//   4. segmented sum over fixed chunks of the member list: a CTA owns one
+//      chunk x one 512-column slice, sums each segment in member order with
+//      compensated float32 additions and writes the mean when the segment is
+//      inside its chunk, or a partial sum when it crosses the chunk boundary
+//   5. fix-up: segments that crossed chunks add their partials in chunk order;
+//      empty clusters keep their old row bit for bit
+// Every step has a fixed order, so C_new is bitwise reproducible.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "update.cuh"
+
+namespace km {
+
+__device__ __forceinline__ uint32_t clamp_label(int64_t lab, int k, uint32_t *status) {
+    if (lab < 0 || lab >= k) {
+        flag_error(status, kFlagBadLabel);
+        return (uint32_t)(k - 1);
+    }
+    return (uint32_t)lab;
+}
+
+// counts[] = 0 (and header cleared when this call owns it)
+__global__ void update_clear_kernel(int32_t *counts, int k, WsHeader *hdr, int clear_header) {
+    if (clear_header && blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr->status = 0u;
+        hdr->done_blocks = 0u;
+    }
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < k; j += gridDim.x * blockDim.x) counts[j] = 0;
+}
+
+// Per-tile digit histogram of pass `shift`; the first pass reads the int64
+// labels directly (and counts members per cluster), later passes read the
+// keys the previous pass wrote.
+__global__ void __launch_bounds__(kSortThreads)
+    radix_hist_kernel(const int64_t *__restrict__ labels, const uint32_t *__restrict__ keys_in, int n, int k,
+                      int shift, int n_tiles, int32_t *__restrict__ hist, int32_t *__restrict__ counts,
+                      uint32_t *status) {
+    __shared__ int32_t h[kRadixBins];
+    for (int b = threadIdx.x; b < kRadixBins; b += kSortThreads) h[b] = 0;
+    __syncthreads();
+    const int tile = blockIdx.x;
+    const int base = tile * kSortTile;
+    const int end = min(n, base + kSortTile);
+    for (int i = base + threadIdx.x; i < end; i += kSortThreads) {
+        uint32_t key;
+        if (labels) {
+            key = clamp_label(labels[i], k, status);
+            // warp-aggregated member count
+            const uint32_t active = __activemask();
+            const uint32_t peers = __match_any_sync(active, key);
+            const int leader = __ffs(peers) - 1;
+            if ((int)(threadIdx.x & 31) == leader) atomicAdd(counts + key, __popc(peers));
+        } else {
+            key = keys_in[i];
+        }
+        atomicAdd(&h[(key >> shift) & 0xffu], 1);
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < kRadixBins; b += kSortThreads) hist[b * n_tiles + tile] = h[b];
+}
+
+// Exclusive scan of `len` int32 values, out[i] = sum of in[0..i-1] (one CTA,
+// 1024 threads; `in` may equal `out`).  The total goes to *total_out if given.
+__global__ void __launch_bounds__(1024) exclusive_scan_kernel(const int32_t *in, int32_t *out, int64_t len,
+                                                              int32_t *total_out) {
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int64_t base = 0; base < len; base += 1024) {
+        const int64_t i = base + threadIdx.x;
+        const int32_t v = i < len ? in[i] : 0;
+        int32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) warp_tot[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int32_t w = warp_tot[lane];
+            int32_t wi = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t t = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += t;
+            }
+            warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+        }
+        __syncthreads();
+        const int32_t c = carry;
+        if (i < len) out[i] = c + warp_tot[wid] + incl - v;
+        __syncthreads();
+        if (threadIdx.x == 1023) carry = c + warp_tot[wid] + incl;
+        __syncthreads();
+    }
+    if (total_out && threadIdx.x == 0) *total_out = carry;
+}
+
+// Stable scatter of one radix pass.  The tile is walked in rounds of 256
+// elements in index order; inside a round an element's rank among equal
+// digits comes from its warp (match_any) and the warps before it.
+__global__ void __launch_bounds__(kSortThreads)
+    radix_scatter_kernel(const int64_t *__restrict__ labels, const uint32_t *__restrict__ keys_in,
+                         const int32_t *__restrict__ vals_in, int n, int k, int shift, int n_tiles,
+                         const int32_t *__restrict__ hist_scanned, uint32_t *__restrict__ keys_out,
+                         int32_t *__restrict__ vals_out, uint32_t *status) {
+    constexpr int W = kSortThreads / 32;
+    __shared__ int32_t base_off[kRadixBins];
+    __shared__ int32_t wcount[W][kRadixBins];
+    const int tile = blockIdx.x;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int b = threadIdx.x; b < kRadixBins; b += kSortThreads) base_off[b] = hist_scanned[b * n_tiles + tile];
+    const int tbase = tile * kSortTile;
+    const int tend = min(n, tbase + kSortTile);
+    for (int r0 = tbase; r0 < tend; r0 += kSortThreads) {
+        for (int b = threadIdx.x; b < W * kRadixBins; b += kSortThreads) (&wcount[0][0])[b] = 0;
+        __syncthreads();
+        const int i = r0 + threadIdx.x;
+        const bool valid = i < tend;
+        uint32_t key = 0u;
+        int32_t val = 0;
+        if (valid) {
+            if (labels) {
+                key = clamp_label(labels[i], k, status);
+                val = i;
+            } else {
+                key = keys_in[i];
+                val = vals_in[i];
+            }
+        }
+        const uint32_t digit = valid ? ((key >> shift) & 0xffu) : 0xffffffffu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+        const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+        if (valid && rank_in_warp == 0) wcount[wid][digit] = __popc(peers);
+        __syncthreads();
+        if (valid) {
+            int32_t off = base_off[digit] + rank_in_warp;
+            for (int w = 0; w < wid; ++w) off += wcount[w][digit];
+            keys_out[off] = key;
+            vals_out[off] = val;
+        }
+        __syncthreads();
+        for (int b = threadIdx.x; b < kRadixBins; b += kSortThreads) {
+            int32_t add = 0;
+#pragma unroll
+            for (int w = 0; w < W; ++w) add += wcount[w][b];
+            base_off[b] += add;
+        }
+        __syncthreads();
+    }
+}
+
+__device__ __forceinline__ void kahan4(float4 &s, float4 &c, const float4 v) {
+    float y, t;
+    y = v.x - c.x; t = s.x + y; c.x = (t - s.x) - y; s.x = t;
+    y = v.y - c.y; t = s.y + y; c.y = (t - s.y) - y; s.y = t;
+    y = v.z - c.z; t = s.z + y; c.z = (t - s.z) - y; s.z = t;
+    y = v.w - c.w; t = s.w + y; c.w = (t - s.w) - y; s.w = t;
+}
+
+constexpr int kMeanThreads = 128;
+constexpr int kMaxChunk = 4096;
+
+// One CTA = one chunk of the member list x one slice of columns.
+// VEC: 4 columns per thread with 16-byte loads (d % 4 == 0, X aligned).
+template <bool VEC>
+__global__ void __launch_bounds__(kMeanThreads)
+    segmented_mean_kernel(const float *__restrict__ X, const int32_t *__restrict__ perm,
+                          const uint32_t *__restrict__ sorted_labels, const int32_t *__restrict__ offsets,
+                          int n, int d, int chunk, float *__restrict__ C_new, float *__restrict__ head,
+                          float *__restrict__ tail) {
+    __shared__ int32_t s_perm[kMaxChunk];
+    __shared__ uint32_t s_lab[kMaxChunk];
+    const int c = blockIdx.x;
+    const int p0 = c * chunk;
+    const int p1 = min(n, p0 + chunk);
+    for (int p = p0 + threadIdx.x; p < p1; p += kMeanThreads) {
+        s_perm[p - p0] = perm[p];
+        s_lab[p - p0] = sorted_labels[p];
+    }
+    __syncthreads();
+    constexpr int CPT = VEC ? 4 : 1;  // columns per thread
+    const int col = (blockIdx.y * kMeanThreads + threadIdx.x) * CPT;
+    if (col >= d) return;
+    int p = p0;
+    while (p < p1) {
+        const uint32_t j = s_lab[p - p0];
+        const int seg0 = offsets[j];
+        const int seg1 = offsets[j + 1];
+        int q = min(seg1, p1);
+        if (q <= p) q = p + 1;  // only reachable with inconsistent (invalid) labels
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f), cmp = make_float4(0.f, 0.f, 0.f, 0.f);
+        int r = p;
+        if (VEC) {
+            for (; r + 4 <= q; r += 4) {
+                const float4 v0 = __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r - p0] * d + col));
+                const float4 v1 = __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r + 1 - p0] * d + col));
+                const float4 v2 = __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r + 2 - p0] * d + col));
+                const float4 v3 = __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r + 3 - p0] * d + col));
+                kahan4(s, cmp, v0);
+                kahan4(s, cmp, v1);
+                kahan4(s, cmp, v2);
+                kahan4(s, cmp, v3);
+            }
+            for (; r < q; ++r)
+                kahan4(s, cmp, __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r - p0] * d + col)));
+        } else {
+            for (; r < q; ++r) {
+                const float v = __ldg(X + (size_t)s_perm[r - p0] * d + col);
+                const float y = v - cmp.x;
+                const float t = s.x + y;
+                cmp.x = (t - s.x) - y;
+                s.x = t;
+            }
+        }
+        const float4 tot = make_float4(s.x - cmp.x, s.y - cmp.y, s.z - cmp.z, s.w - cmp.w);
+        float *dst;
+        bool mean = false;
+        if (seg0 >= p0 && seg1 <= p1) {
+            dst = C_new + (size_t)j * d + col;
+            mean = true;
+        } else if (seg0 < p0) {
+            dst = head + (size_t)c * d + col;
+        } else {
+            dst = tail + (size_t)c * d + col;
+        }
+        if (mean) {
+            const float cnt = (float)(seg1 - seg0);
+            if (VEC) *reinterpret_cast<float4 *>(dst) = make_float4(tot.x / cnt, tot.y / cnt, tot.z / cnt, tot.w / cnt);
+            else *dst = tot.x / cnt;
+        } else {
+            if (VEC) *reinterpret_cast<float4 *>(dst) = tot;
+            else *dst = tot.x;
+        }
+        p = q;
+    }
+}
+
+// Segments that crossed chunk boundaries, empty clusters, and the counts.
+__global__ void __launch_bounds__(kMeanThreads)
+    mean_fixup_kernel(const int32_t *__restrict__ offsets, const float *__restrict__ head,
+                      const float *__restrict__ tail, const float *__restrict__ C_old, float *__restrict__ C_new,
+                      int32_t *__restrict__ counts_out, int k, int d, int chunk) {
+    for (int j = blockIdx.x; j < k; j += gridDim.x) {
+        const int seg0 = offsets[j];
+        const int seg1 = offsets[j + 1];
+        const int cnt = seg1 - seg0;
+        if (counts_out && threadIdx.x == 0) counts_out[j] = cnt;
+        if (cnt == 0) {
+            if (C_new != C_old)
+                for (int f = threadIdx.x; f < d; f += kMeanThreads) C_new[(size_t)j * d + f] = C_old[(size_t)j * d + f];
+            continue;
+        }
+        const int cs = seg0 / chunk;
+        const int ce = (seg1 - 1) / chunk;
+        if (cs == ce) continue;
+        for (int f = threadIdx.x; f < d; f += kMeanThreads) {
+            float s = tail[(size_t)cs * d + f], cmp = 0.f;
+            for (int c = cs + 1; c <= ce; ++c) {
+                const float v = head[(size_t)c * d + f];
+                const float y = v - cmp;
+                const float t = s + y;
+                cmp = (t - s) - y;
+                s = t;
+            }
+            C_new[(size_t)j * d + f] = (s - cmp) / (float)cnt;
+        }
+    }
+}
+
+static int radix_passes(int64_t k) {
+    int bits = 0;
+    while (bits < 32 && ((int64_t)1 << bits) < k) ++bits;  // labels 0..k-1 need `bits` bits
+    const int p = (bits + 7) / 8;
+    return p < 1 ? 1 : p;
+}
+
+cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_old, float *C_new,
+                          int32_t *counts_out, int64_t n, int64_t k, int64_t d, const UpdateLayout &L,
+                          uint8_t *ws, bool clear_header, cudaStream_t s) {
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.off_counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.off_offsets);
+    int32_t *hist = reinterpret_cast<int32_t *>(ws + L.off_hist);
+    uint32_t *ka = reinterpret_cast<uint32_t *>(ws + L.off_keys_a);
+    int32_t *va = reinterpret_cast<int32_t *>(ws + L.off_vals_a);
+    uint32_t *kb = reinterpret_cast<uint32_t *>(ws + L.off_keys_b);
+    int32_t *vb = reinterpret_cast<int32_t *>(ws + L.off_vals_b);
+    float *head = reinterpret_cast<float *>(ws + L.off_head);
+    float *tail = reinterpret_cast<float *>(ws + L.off_tail);
+    uint32_t *status = &hdr->status;
+    const int tiles = (int)L.n_tiles;
+
+    update_clear_kernel<<<(int)((k + 255) / 256 < 1024 ? (k + 255) / 256 : 1024), 256, 0, s>>>(
+        counts, (int)k, hdr, clear_header ? 1 : 0);
+    const int passes = radix_passes(k);
+    uint32_t *kin = nullptr, *kout = ka;
+    int32_t *vin = nullptr, *vout = va;
+    for (int ps = 0; ps < passes; ++ps) {
+        const int shift = 8 * ps;
+        const int64_t *lab = ps == 0 ? labels : nullptr;
+        radix_hist_kernel<<<tiles, kSortThreads, 0, s>>>(lab, kin, (int)n, (int)k, shift, tiles, hist, counts,
+                                                          status);
+        exclusive_scan_kernel<<<1, 1024, 0, s>>>(hist, hist, (int64_t)kRadixBins * tiles, nullptr);
+        radix_scatter_kernel<<<tiles, kSortThreads, 0, s>>>(lab, kin, vin, (int)n, (int)k, shift, tiles, hist,
+                                                             kout, vout, status);
+        kin = kout;
+        vin = vout;
+        kout = (kout == ka) ? kb : ka;
+        vout = (vout == va) ? vb : va;
+    }
+    // counts -> offsets (k + 1 entries: the scan writes the total at [k])
+    exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, offsets, k, offsets + k);
+
+    const bool vec = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(C_new)) & 15) == 0;
+    const int cols_per_cta = kMeanThreads * (vec ? 4 : 1);
+    const dim3 grid((unsigned)L.n_chunks, (unsigned)((d + cols_per_cta - 1) / cols_per_cta));
+    if (vec)
+        segmented_mean_kernel<true><<<grid, kMeanThreads, 0, s>>>(X, vin, kin, offsets, (int)n, (int)d,
+                                                                   (int)L.chunk, C_new, head, tail);
+    else
+        segmented_mean_kernel<false><<<grid, kMeanThreads, 0, s>>>(X, vin, kin, offsets, (int)n, (int)d,
+                                                                    (int)L.chunk, C_new, head, tail);
+    const int fix_grid = (int)(k < 4096 ? k : 4096);
+    mean_fixup_kernel<<<fix_grid, kMeanThreads, 0, s>>>(offsets, head, tail, C_old, C_new, counts_out, (int)k,
+                                                       (int)d, (int)L.chunk);
+    return cudaGetLastError();
+}
+
+}  // namespace km

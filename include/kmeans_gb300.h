@@ -1,0 +1,156 @@
+/*
+ * kmeans_gb300.h -- C ABI of the GB300 (sm_103a) k-means library.
+ *
+ * The library computes one Lloyd iteration of k-means and greedy k-means++
+ * seeding on one GPU.  Every entry point takes caller-owned DEVICE pointers,
+ * the sizes n (samples), k (centroids), d (features), a caller-owned device
+ * workspace, a seed and a CUDA stream, enqueues its kernels on that stream and
+ * returns without synchronising.  The library allocates no memory.
+ *
+ * Sources for what is computed (three pages of one benchmarking journal):
+ *  [G] "Three shapes that fit an eager Gram assignment", section "Gram
+ *      assignment": nearest centroid = argmin_c ||x - c||^2, evaluated through
+ *      ||x||^2 + ||c||^2 - 2 x.c.
+ *  [R] same page, section "Running argmin, one centroid": the assignment
+ *      result is an int64 label and a float32 winning distance per sample
+ *      (n * 12 bytes); no (n, k) distance matrix is ever stored.
+ *  [U] same page, section "Full Lloyd step": each centroid becomes the mean of
+ *      its members.
+ *  [S] "004 — tile sizes, a Cython Lloyd step, and k-means++", section
+ *      "Schedules added": ||x||^2 does not change the argmin and is left out of
+ *      the comparison; ||c||^2 is computed once per centroid and reused.
+ *  [K] same page, section "k-means++": greedy D^2 seeding with
+ *      2 + log(n_clusters) candidate trials per new center.
+ *
+ * Conventions shared by every entry point
+ *  - Layout: X is (n, d) float32 row-major, C is (k, d) float32 row-major,
+ *    both contiguous.  labels are int64 (n), distances float32 (n).
+ *  - Sizes: 1 <= k <= n, d >= 1, n < 2^31, k < 2^31.
+ *  - Precision: inputs must be finite.  The assignment contraction runs on the
+ *    tensor cores as three bf16 products of an error-compensated split of
+ *    each float32 operand (hi = bf16(v), lo = bf16(v - hi)) with float32
+ *    accumulation; the reported distance is within 1e-4 * (||x||^2 + ||c||^2)
+ *    of the exact one.  Ties between centroids go to the lowest index.
+ *  - Workspace: `ws` is a device buffer of at least
+ *    kmeans_workspace_bytes(op, n, k, d) bytes, 256-byte aligned, owned by the
+ *    caller.  Its size has no n*k term: no (n, k) buffer exists anywhere.
+ *    One workspace must not be used by two calls that may run concurrently.
+ *  - Errors: the return value reports argument validation
+ *    (KMEANS_ERR_INVALID_ARG, KMEANS_ERR_UNSUPPORTED, KMEANS_ERR_WORKSPACE)
+ *    and launch failures (KMEANS_ERR_CUDA).  Nothing is enqueued when a call
+ *    returns an error.  Faults found on the device (a pipeline wait that ran
+ *    out of time, a label outside [0, k)) are recorded in a status word in
+ *    the workspace, which each call clears when it starts; read it with
+ *    kmeans_device_status().
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *    default stream).
+ */
+#ifndef KMEANS_GB300_H
+#define KMEANS_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KMEANS_OK = 0,
+    KMEANS_ERR_INVALID_ARG = 1,     /* null pointer, bad size, k > n, ...       */
+    KMEANS_ERR_UNSUPPORTED = 2,     /* valid but outside this build's limits     */
+    KMEANS_ERR_WORKSPACE = 3,       /* ws too small or misaligned                */
+    KMEANS_ERR_CUDA = 4,            /* a CUDA runtime call failed                */
+    KMEANS_ERR_DEVICE_TIMEOUT = 5,  /* a device pipeline wait ran out of time    */
+    KMEANS_ERR_DEVICE_LABEL = 6     /* kmeans_update saw a label outside [0, k)  */
+} kmeans_status;
+
+/* Operation codes for kmeans_workspace_bytes. */
+enum {
+    KMEANS_OP_ASSIGN = 0,
+    KMEANS_OP_ASSIGN_FFMA = 1,
+    KMEANS_OP_UPDATE = 2,
+    KMEANS_OP_LLOYD = 3,
+    KMEANS_OP_KMEANSPP = 4
+};
+
+/* Bytes of device workspace the operation needs for these sizes (0 when the
+ * sizes are invalid).  Linear in n, in k*d and in n/4096; never in n*k. */
+size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d);
+
+/* Assignment [G][R][S].
+ * For every sample i: labels[i] = the lowest j minimising ||x_i - c_j||^2,
+ * best_dist[i] = max(0, ||x_i||^2 + ||c_j||^2 - 2 x_i.c_j) for that j, and
+ * *inertia = sum_i best_dist[i] accumulated in float64 in a fixed order.
+ * X, C: inputs (device).  labels, best_dist: outputs (device).
+ * inertia: output (device, one double), may be NULL.
+ * Extra requirement of this tensor-core path: d % 4 == 0 and X, C 16-byte
+ * aligned (KMEANS_ERR_UNSUPPORTED otherwise; kmeans_assign_ffma has none).
+ * seed: unused (kept for a uniform signature). */
+int kmeans_assign(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
+                  int64_t *labels, float *best_dist, double *inertia,
+                  void *ws, size_t ws_bytes, uint64_t seed, void *stream);
+
+/* The same assignment [G][R][S] computed with plain float32 FMA on the CUDA
+ * cores (register-blocked tiles, the argmin fused into the same kernel).  It
+ * exists to be measured against kmeans_assign; any d and any 4-byte alignment
+ * are accepted. */
+int kmeans_assign_ffma(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
+                       int64_t *labels, float *best_dist, double *inertia,
+                       void *ws, size_t ws_bytes, uint64_t seed, void *stream);
+
+/* Mean update [U].
+ * C_new[j] = mean of the rows X[i] with labels[i] == j, summed in float32 with
+ * compensation in a fixed order (bitwise reproducible run to run); a cluster
+ * with no members keeps C_old[j] bit for bit.  counts (device int32, k) may
+ * be NULL; it receives the member counts.  C_new may alias C_old.
+ * labels must lie in [0, k); a label outside that range leaves C_new
+ * unspecified and sets KMEANS_ERR_DEVICE_LABEL in the status word.
+ * seed: unused. */
+int kmeans_update(const float *X, const int64_t *labels, const float *C_old, float *C_new,
+                  int32_t *counts, int64_t n, int64_t k, int64_t d,
+                  void *ws, size_t ws_bytes, uint64_t seed, void *stream);
+
+/* One Lloyd iteration [U]: kmeans_assign of X against C_old, then
+ * kmeans_update into C_new with those labels.  labels, best_dist and
+ * *inertia (device, may be NULL) receive the assignment; counts (device,
+ * may be NULL) the member counts.  C_new must not alias C_old.
+ * Same requirements as kmeans_assign. */
+int kmeans_lloyd_iter(const float *X, const float *C_old, float *C_new, int64_t *labels,
+                      float *best_dist, double *inertia, int32_t *counts,
+                      int64_t n, int64_t k, int64_t d,
+                      void *ws, size_t ws_bytes, uint64_t seed, void *stream);
+
+/* Greedy k-means++ seeding [K].
+ * indices (device int64, k) receives the chosen sample indices, centers
+ * (device float32 (k, d), may be NULL) the chosen rows of X.
+ * n_trials <= 0 selects 2 + floor(ln k).  The draws come from Philox4x32-10
+ * (Salmon et al., SC'11) keyed by `seed`: counter (draw, 0, 0, 0), uniform =
+ * top 53 bits of the first two output words; draw 0 picks the first center
+ * uniformly, draw 1 + (c-1)*n_trials + t is trial t of center c.  A trial
+ * takes the first sample whose running sum of D^2 exceeds uniform * sum(D^2)
+ * (the last sample if none does); the trial with the lowest potential
+ * sum_i min(D^2_i, ||x_i - cand||^2) wins (lowest trial on ties).
+ * Distances are float32 differences squared with compensated summation;
+ * running sums and potentials are float64. */
+int kmeanspp_init(const float *X, int64_t n, int64_t d, int64_t k, int n_trials,
+                  uint64_t seed, float *centers, int64_t *indices,
+                  void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream` and returns the device status word of the last call
+ * that used `ws` (KMEANS_OK, KMEANS_ERR_DEVICE_TIMEOUT or
+ * KMEANS_ERR_DEVICE_LABEL), or KMEANS_ERR_CUDA if the stream reports an error. */
+int kmeans_device_status(const void *ws, void *stream);
+
+/* Human-readable text for a kmeans_status value (static storage). */
+const char *kmeans_status_string(int status);
+
+/* Build identification of the library: target architecture, tile shapes and
+ * pipeline depth (static storage). */
+const char *kmeans_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KMEANS_GB300_H */

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header
+declares, validates arguments before touching the GPU, and sizes workspaces
+with no n*k term.  No kernel runs here (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kmeans_gb300.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "probe_byte_counts.txt")
+
+
+@pytest.fixture(scope="module")
+def km():
+    from distance_argmin_gb300 import build as b
+    b.build()
+    import distance_argmin_gb300 as km
+    km.load()
+    return km
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol(km):
+    declared = _declared_functions()
+    assert "kmeans_assign" in declared and "kmeanspp_init" in declared
+    lib = ctypes.CDLL(km.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in the header but not exported"
+    assert set(km.EXPORTS) == set(declared)
+
+
+def test_status_strings(km):
+    for st in range(7):
+        s = km.kmeans_status_string(st)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert km.kmeans_status_string(99) == "unknown status"
+    assert "sm_103a" in km.kmeans_build_info()
+
+
+def _lib(km):
+    return km.load()
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
+FAKE_WS = ctypes.c_void_p(0x100000)  # 256-byte aligned
+
+
+def test_invalid_arguments_are_rejected_on_the_host(km):
+    lib = _lib(km)
+    n, k, d = 100, 10, 16
+    ws_need = km.kmeans_workspace_bytes(km.OP_ASSIGN, n, k, d)
+    args = lambda X, C, n, k, d, ws=FAKE_WS, wsb=ws_need: (X, C, n, k, d, FAKE, FAKE, None, ws, wsb, 0, None)
+    assert lib.kmeans_assign(*args(None, FAKE, n, k, d)) == km.KMEANS_ERR_INVALID_ARG
+    assert lib.kmeans_assign(*args(FAKE, FAKE, n, n + 1, d)) == km.KMEANS_ERR_INVALID_ARG  # k > n
+    assert lib.kmeans_assign(*args(FAKE, FAKE, 0, 0, d)) == km.KMEANS_ERR_INVALID_ARG
+    assert lib.kmeans_assign(*args(FAKE, FAKE, n, k, 0)) == km.KMEANS_ERR_INVALID_ARG
+    assert lib.kmeans_assign(*args(FAKE, FAKE, n, k, 18)) == km.KMEANS_ERR_UNSUPPORTED    # d % 4
+    assert lib.kmeans_assign(*args(FAKE, FAKE, n, k, d, wsb=ws_need - 1)) == km.KMEANS_ERR_WORKSPACE
+    assert lib.kmeans_assign(*args(FAKE, FAKE, n, k, d, ws=ctypes.c_void_p(0x100010))) == \
+        km.KMEANS_ERR_WORKSPACE  # misaligned
+    assert lib.kmeans_assign(*args(FAKE, FAKE, 2**31, 10, d)) == km.KMEANS_ERR_INVALID_ARG
+    # the FFMA comparator accepts any d, but still checks the workspace
+    assert lib.kmeans_assign_ffma(*args(FAKE, FAKE, n, k, 18, wsb=1)) == km.KMEANS_ERR_WORKSPACE
+    upd = lambda labels, ws, wsb: lib.kmeans_update(FAKE, labels, FAKE, FAKE, None, n, k, d, ws, wsb, 0, None)
+    assert upd(None, FAKE_WS, 1 << 30) == km.KMEANS_ERR_INVALID_ARG
+    assert upd(FAKE, FAKE_WS, 16) == km.KMEANS_ERR_WORKSPACE
+    assert lib.kmeans_lloyd_iter(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, n, k, 6, FAKE_WS, 1 << 30, 0,
+                                 None) == km.KMEANS_ERR_UNSUPPORTED
+    assert lib.kmeanspp_init(FAKE, n, d, k, 33, 0, None, FAKE, FAKE_WS, 1 << 30, None) == \
+        km.KMEANS_ERR_UNSUPPORTED  # more than 32 trials
+    assert lib.kmeanspp_init(FAKE, n, d, k, 0, 0, None, None, FAKE_WS, 1 << 30, None) == \
+        km.KMEANS_ERR_INVALID_ARG
+    assert lib.kmeans_device_status(None, None) == km.KMEANS_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("op", [0, 1, 2, 3, 4])
+def test_workspace_has_no_n_times_k_term(km, op):
+    f = lambda n, k: km.kmeans_workspace_bytes(op, n, k, 512)
+    n, k = 1 << 16, 1 << 12
+    mixed = f(2 * n, 2 * k) - f(2 * n, k) - f(n, 2 * k) + f(n, k)
+    assert abs(mixed) <= 16 * 1024  # only region alignment remains
+    assert km.kmeans_workspace_bytes(op, 10, 11, 4) == 0  # k > n is invalid
+
+
+def test_workspace_far_below_the_distance_matrix_at_every_workload(km):
+    import synth
+    for w in list(synth.WORKLOADS.values()) + [synth.KMEANSPP]:
+        for op in (km.OP_ASSIGN, km.OP_LLOYD, km.OP_KMEANSPP):
+            ws = km.kmeans_workspace_bytes(op, w.n, w.k, w.d)
+            assert 0 < ws < w.n * w.k * 4, (w.name, op, ws)
+
+
+def test_probe_byte_counts_from_the_page(km):
+    # the fusion-probe page prints the sizes of the buffers a fused assignment
+    # must avoid; check them against the shapes, and the workspace against them
+    vals = {}
+    for line in open(GOLDEN):
+        if line.startswith("#") or not line.strip():
+            continue
+        name, v = line.split()
+        vals[name] = float(v)
+    n, k, d = 4096, 256, 512
+    MiB = 1024 * 1024
+    assert vals["distance_nk"] * MiB == n * k * 4
+    assert vals["broadcast_nkd"] * MiB == n * k * d * 4
+    assert vals["one_centroid_difference_nd"] * MiB == n * d * 4
+    assert round(n * 8 / MiB, 3) == vals["labels_n_int64"]
+    assert km.kmeans_workspace_bytes(km.OP_ASSIGN, n, k, d) < vals["distance_nk"] * MiB

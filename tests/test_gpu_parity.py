@@ -1,0 +1,271 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.  Small shapes are compared on every row; full-size
+workloads on a seeded sample of rows (assignment) and on every row (update,
+with the GPU's own labels so near-tie flips do not cascade)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import check_assign, check_centroids
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def dev_tensor(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+SMALL = [
+    # (n, k, d): the fusion-probe page's separate check shape first, then
+    # tails in every tile dimension (128 samples, 256 centroids, 32 features)
+    (512, 17, 64),
+    (1000, 300, 100),
+    (777, 1, 36),
+    (300, 300, 8),
+    (2000, 513, 132),
+    (130, 257, 4),
+    (4096, 256, 512),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("impl", ["tc", "ffma"])
+@pytest.mark.parametrize("data", ["blobs", "gauss"])
+def test_assign_matches_oracle(gpu_lib, shape, impl, data):
+    n, k, d = shape
+    if data == "blobs":
+        X, _, _ = synth.planted_blobs(n, d, max(1, k), seed=n + k + d)
+        C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=d)])
+    else:
+        X = synth.gaussian((n, d), seed=n * 3 + 1, scale=2.0)
+        C = synth.gaussian((k, d), seed=k * 7 + 2, scale=2.0)
+    fn = gpu_lib.kmeans_assign if impl == "tc" else gpu_lib.kmeans_assign_ffma
+    labels, best, inertia = fn(dev_tensor(X), dev_tensor(C))
+    o_l, o_b, o_s, o_in = oracle.assign(X, C)
+    check_assign(X, C, host(labels), host(best), o_l, o_b, o_s, what=f"{impl} {shape}")
+    assert abs(float(inertia.item()) - o_in) <= 1e-4 * max(o_in, 1e-30) + 1e-6
+
+
+@pytest.mark.parametrize("impl", ["tc", "ffma"])
+def test_duplicate_centroids_resolve_to_lowest_index(gpu_lib, impl):
+    X = synth.gaussian((1500, 96), seed=5)
+    C = synth.gaussian((600, 96), seed=6)
+    C[517] = C[3]      # across centroid tiles
+    C[40] = C[39]      # inside one tile
+    C[299] = C[260]
+    fn = gpu_lib.kmeans_assign if impl == "tc" else gpu_lib.kmeans_assign_ffma
+    labels, best, _ = fn(dev_tensor(X), dev_tensor(C))
+    lab = host(labels)
+    assert not np.isin(lab, [517, 40, 299]).any()
+    o_l, o_b, o_s, _ = oracle.assign(X, C)
+    check_assign(X, C, lab, host(best), o_l, o_b, o_s, what=impl)
+
+
+def test_planted_centers_are_recovered_exactly(gpu_lib):
+    X, centers, blob = synth.planted_blobs(8192, 256, 300, seed=9)
+    labels, _, _ = gpu_lib.kmeans_assign(dev_tensor(X), dev_tensor(centers))
+    assert np.array_equal(host(labels), blob)
+
+
+def test_single_sample_single_centroid(gpu_lib):
+    X = synth.gaussian((1, 12), seed=1)
+    labels, best, inertia = gpu_lib.kmeans_assign(dev_tensor(X), dev_tensor(X))
+    assert host(labels).tolist() == [0]
+    assert float(host(best)[0]) == 0.0
+
+
+@pytest.mark.parametrize("shape", [(512, 17, 64), (2000, 513, 132), (5000, 40, 7), (4096, 256, 512),
+                                   (70000, 3, 20)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_update_matches_oracle(gpu_lib, shape):
+    n, k, d = shape
+    X = synth.gaussian((n, d), seed=n + 5, scale=1.5)
+    C_old = synth.gaussian((k, d), seed=k + 6)
+    labels = np.random.default_rng(n).integers(0, k, size=n).astype(np.int64)
+    if k > 2:
+        labels[labels == 1] = 0  # cluster 1 empty: keeps its row bit for bit
+    C_new, counts = gpu_lib.kmeans_update(dev_tensor(X), dev_tensor(labels), dev_tensor(C_old))
+    o_C, o_cnt = oracle.update(X, labels, C_old)
+    assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+    got = host(C_new)
+    check_centroids(got, o_C, what=str(shape))
+    empty = o_cnt == 0
+    assert got[empty].tobytes() == C_old[empty].tobytes()
+
+
+def test_update_single_cluster_and_skewed_sizes(gpu_lib):
+    # one huge cluster spanning many chunks plus tiny ones
+    n, k, d = 100000, 9, 36
+    X = synth.gaussian((n, d), seed=3)
+    labels = np.zeros(n, np.int64)
+    labels[::1000] = np.arange(100) % 8 + 1
+    C_old = synth.gaussian((k, d), seed=4)
+    C_new, counts = gpu_lib.kmeans_update(dev_tensor(X), dev_tensor(labels), dev_tensor(C_old))
+    o_C, o_cnt = oracle.update(X, labels, C_old)
+    assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+    check_centroids(host(C_new), o_C, what="skewed")
+
+
+def test_update_in_place(gpu_lib):
+    n, k, d = 3000, 50, 64
+    X = synth.gaussian((n, d), seed=8)
+    C = synth.gaussian((k, d), seed=9)
+    labels = np.random.default_rng(1).integers(0, k - 1, size=n).astype(np.int64)  # k-1 empty
+    Cd = dev_tensor(C)
+    gpu_lib.kmeans_update(dev_tensor(X), dev_tensor(labels), Cd, C_new=Cd)
+    o_C, _ = oracle.update(X, labels, C)
+    check_centroids(host(Cd), o_C, what="in place")
+
+
+def test_lloyd_probe_workload(gpu_lib):
+    w = synth.WORKLOADS["probe"]
+    X, C0, _ = synth.workload_inputs(w)
+    C1, labels, best, inertia, counts = gpu_lib.kmeans_lloyd_iter(dev_tensor(X), dev_tensor(C0))
+    o_l, o_b, o_s, o_in = oracle.assign(X, C0)
+    lab = host(labels)
+    check_assign(X, C0, lab, host(best), o_l, o_b, o_s, what="probe")
+    o_C1, o_cnt = oracle.update(X, lab, C0)
+    check_centroids(host(C1), o_C1, what="probe update")
+    assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+    assert (o_cnt > 0).all()  # random-row initialisation never empties a cluster at step 1
+
+
+def test_bitwise_reproducible(gpu_lib):
+    X, C0, _ = synth.workload_inputs(synth.Workload("t", 20000, 700, 200, 700, 1, 31, 32, ""))
+    Xd, Cd = dev_tensor(X), dev_tensor(C0)
+    a = [host(t) for t in gpu_lib.kmeans_lloyd_iter(Xd, Cd)]
+    b = [host(t) for t in gpu_lib.kmeans_lloyd_iter(Xd, Cd)]
+    for u, v in zip(a, b):
+        assert u.tobytes() == v.tobytes()
+
+
+def test_library_allocates_no_device_memory(gpu_lib):
+    X, C0, _ = synth.workload_inputs(synth.Workload("t", 16384, 512, 256, 512, 1, 41, 42, ""))
+    Xd, Cd = dev_tensor(X), dev_tensor(C0)
+    outs = [torch.empty_like(Cd), torch.empty(16384, dtype=torch.int64, device="cuda"),
+            torch.empty(16384, device="cuda"), torch.empty(1, dtype=torch.float64, device="cuda"),
+            torch.empty(512, dtype=torch.int32, device="cuda")]
+    ws = gpu_lib.workspace(gpu_lib.OP_LLOYD, 16384, 512, 256)
+    gpu_lib.kmeans_lloyd_iter(Xd, Cd, *outs, ws=ws)  # first call loads the kernels
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        gpu_lib.kmeans_lloyd_iter(Xd, Cd, *outs, ws=ws)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert ws.numel() < 16384 * 512 * 4  # smaller than the (n, k) matrix it replaces
+
+
+def test_bad_label_is_reported_not_faulted(gpu_lib):
+    n, k, d = 5000, 20, 16
+    X = synth.gaussian((n, d), seed=2)
+    C = synth.gaussian((k, d), seed=3)
+    labels = np.random.default_rng(0).integers(0, k, size=n).astype(np.int64)
+    labels[1234] = k + 7
+    ws = gpu_lib.workspace(gpu_lib.OP_UPDATE, n, k, d)
+    gpu_lib.kmeans_update(dev_tensor(X), dev_tensor(labels), dev_tensor(C), ws=ws)
+    assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_ERR_DEVICE_LABEL
+    labels[1234] = 0
+    gpu_lib.kmeans_update(dev_tensor(X), dev_tensor(labels), dev_tensor(C), ws=ws)
+    assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_OK
+
+
+def test_status_ok_after_assign(gpu_lib):
+    X = synth.gaussian((3000, 64), seed=2)
+    C = synth.gaussian((100, 64), seed=3)
+    ws = gpu_lib.workspace(gpu_lib.OP_ASSIGN, 3000, 100, 64)
+    gpu_lib.kmeans_assign(dev_tensor(X), dev_tensor(C), ws=ws)
+    assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_OK
+
+
+# ------------------------------------------------------------- k-means++
+@pytest.mark.parametrize("case", [(3000, 64, 40, 0, 42), (3000, 64, 40, 1, 7), (500, 33, 60, 3, 123),
+                                  (2048, 128, 32, 8, 2024), (1000, 4, 1000, 2, 5)],
+                         ids=lambda c: "n%d_d%d_k%d_T%d_s%d" % c)
+def test_kmeanspp_indices_match_oracle(gpu_lib, case):
+    n, d, k, T, seed = case
+    X, _, _ = synth.planted_blobs(n, d, max(1, k // 2), seed=n + d)
+    idx, centers = gpu_lib.kmeanspp_init(dev_tensor(X), k, seed, n_trials=T)
+    o_idx, margins, _ = oracle.kmeanspp(X, k, seed, n_trials=T)
+    got = host(idx)
+    assert np.array_equal(got, o_idx), f"first mismatch at {np.argmax(got != o_idx)}"
+    assert host(centers).tobytes() == np.ascontiguousarray(X[o_idx]).tobytes()
+
+
+def test_kmeanspp_identical_points(gpu_lib):
+    X = np.ones((100, 8), np.float32)
+    idx, _ = gpu_lib.kmeanspp_init(dev_tensor(X), 5, 3, n_trials=2)
+    o_idx, _, _ = oracle.kmeanspp(X, 5, 3, n_trials=2)
+    assert np.array_equal(host(idx), o_idx)
+
+
+# ------------------------------------------------------ full-size workloads
+def _sample_rows(n, m, seed):
+    return np.sort(np.random.default_rng(seed).choice(n, size=min(n, m), replace=False))
+
+
+@pytest.mark.slow
+def test_lloyd10_workload_ten_iterations(gpu_lib):
+    w = synth.WORKLOADS["lloyd10"]
+    X, C0, _ = synth.workload_inputs(w)
+    Xd = dev_tensor(X)
+    C = C0
+    prev = np.inf
+    ws = gpu_lib.workspace(gpu_lib.OP_LLOYD, w.n, w.k, w.d)
+    flips = 0
+    for it in range(w.iters):
+        Cd = dev_tensor(C)
+        C1, labels, best, inertia, counts = gpu_lib.kmeans_lloyd_iter(Xd, Cd, ws=ws)
+        lab = host(labels)
+        rows = _sample_rows(w.n, 512, it)
+        o_l, o_b, o_s, _ = oracle.assign(X[rows], C)
+        flips += check_assign(X[rows], C, lab, host(best), o_l, o_b, o_s, rows=rows, what=f"iter {it}")
+        o_C1, o_cnt = oracle.update(X, lab, C)
+        check_centroids(host(C1), o_C1, what=f"iter {it} update")
+        assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+        val = float(inertia.item())
+        assert val <= prev * (1 + 1e-6), f"inertia rose at iteration {it}"
+        prev = val
+        C = host(C1)
+    print(f"near-tie flips over 10 x 512 sampled rows: {flips}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["sample_heavy", "centroid_heavy", "feature_heavy"])
+def test_large_workload_one_iteration(gpu_lib, name):
+    w = synth.WORKLOADS[name]
+    X, C0, _ = synth.workload_inputs(w)
+    Xd, Cd = dev_tensor(X), dev_tensor(C0)
+    C1, labels, best, inertia, counts = gpu_lib.kmeans_lloyd_iter(Xd, Cd)
+    lab, bd = host(labels), host(best)
+    del Xd
+    torch.cuda.empty_cache()
+    rows = _sample_rows(w.n, 128, 17)
+    o_l, o_b, o_s, _ = oracle.assign(X[rows], C0)
+    check_assign(X[rows], C0, lab, bd, o_l, o_b, o_s, rows=rows, what=name)
+    o_C1, o_cnt = oracle.update(X, lab, C0)
+    check_centroids(host(C1), o_C1, what=name + " update")
+    assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+    # every label is a valid index and every distance finite and non-negative
+    assert lab.min() >= 0 and lab.max() < w.k
+    assert np.isfinite(bd).all() and (bd >= 0).all()
+
+
+@pytest.mark.slow
+def test_kmeanspp_workload_prefix(gpu_lib):
+    w = synth.KMEANSPP
+    X, _, _ = synth.planted_blobs(w.n, w.d, w.blobs, w.data_seed)
+    T = oracle.n_trials_for(w.k)
+    idx, _ = gpu_lib.kmeanspp_init(dev_tensor(X), w.k, w.init_seed, n_trials=T)
+    got = host(idx)
+    assert len(np.unique(got)) == w.k  # D^2 sampling never repeats a chosen sample
+    o_idx, margins, _ = oracle.kmeanspp(X, 12, w.init_seed, n_trials=T)
+    assert np.array_equal(got[:12], o_idx), f"first mismatch at {np.argmax(got[:12] != o_idx)}"
