@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Benchmark: one k-means Lloyd iteration (assign + mean update) per step.
+
+Workload (default ``lloyd10``): n = 65536 samples, k = 1024 centroids,
+d = 2048 features, float32 planted Gaussian blobs (1024 centers ~ N(0, 1),
+noise sigma 0.5), initial centroids = seeded random rows of X.  Each step is
+one Lloyd iteration whose output centroids feed the next step.
+
+Printed JSON line (rank 0):
+* ``value``: whole-job throughput in TFLOP/s, 2 n k d per Lloyd iteration
+  over the device time of the K timed iterations (inputs resident in HBM);
+* ``ms_per_step``: the Lloyd iteration time;
+* ``assign``: the assignment call alone (2 n k d over its time) and its
+  fraction of the fp32-accurate tensor roofline; ``roofline`` describes it;
+* ``e2e``: the same metric through the public API with the step's inputs
+  copied from pinned host memory and its results copied back, every step;
+* ``cpu_baseline``: the CPU oracle on a bounded sample of the same workload.
+
+``--impl reference`` times the CPU oracle alone (the reference arm).
+Under torchrun every rank runs its own replica of the workload (the update
+needs every sample's label, so one problem does not shard without an
+all-reduce; replicas only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "assign_tc_kernel_lloyd10.md")
+KERNEL_SOURCE = os.path.join(ROOT, "distance_argmin_gb300", "csrc", "assign_tc.cu")
+METRIC = "Lloyd iter time & assign TFLOP/s (2nkd/t) at 1 GB300, % of fp32-accurate roofline"
+SPLIT_PRODUCTS = 3  # bf16x3: hi*hi + hi*lo + lo*hi per fp32 product
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="lloyd10")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    if os.path.exists(MEASURED_PEAKS):
+        with open(MEASURED_PEAKS) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the assign kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    sha = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    rec_sha, traffic = None, None
+    for line in open(PROFILE_SUMMARY):
+        line = line.strip().strip("`")
+        if line.startswith("source_sha256:"):
+            rec_sha = line.split(":", 1)[1].strip()
+        elif line.startswith("traffic_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if (rec_sha == sha and traffic is not None) else None
+
+
+def launches_per_lloyd_step(k: int) -> int:
+    bits = 0
+    while (1 << bits) < k:
+        bits += 1
+    passes = max(1, (bits + 7) // 8)
+    # prep + assign + finalize | clear + passes x (hist, scan, scatter) + scan + mean + fixup
+    return 3 + 1 + 3 * passes + 3
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_index, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        pmax = max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded), "power_w_max": pmax}
+
+
+# ---------------------------------------------------------------- helpers
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def oracle_sample_step(oracle, X, C, rows):
+    """One bounded-sample Lloyd step of the oracle: assign the sampled rows,
+    then the mean update over those rows.  Returns seconds."""
+    t0 = time.perf_counter()
+    labels, _, _, _ = oracle.assign(X[rows], C)
+    oracle.update(X[rows], labels, C)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(oracle, w, X, C0, budget_s=20.0):
+    """Time the oracle (as it stands, all host cores) on seeded row samples
+    of the workload; TFLOP/s = 2 * rows * k * d / time (the per-row cost of
+    the full iteration is the same for every row)."""
+    import numpy as np
+    rng = np.random.default_rng(7)
+    rows = np.sort(rng.choice(w.n, size=min(w.n, 256), replace=False))
+    t = oracle_sample_step(oracle, X, C0, rows)  # calibrate
+    m = int(min(w.n, max(256, 256 * budget_s / max(t, 1e-3) * 0.8)))
+    rows = np.sort(rng.choice(w.n, size=m, replace=False))
+    t = oracle_sample_step(oracle, X, C0, rows)
+    return {"value": 2.0 * m * w.k * w.d / t / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "sample": f"{m} of {w.n} seeded rows: binary64 brute-force assign of the rows "
+                                        f"against all {w.k} centroids + mean update of those rows; {t:.1f} s",
+            "seconds": t}
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    w = synth.WORKLOADS[args.workload]
+    X, C0, _ = synth.workload_inputs(w)
+    rng = np.random.default_rng(11)
+    rows_per_step = 256
+    samples = [np.sort(rng.choice(w.n, size=rows_per_step, replace=False)) for _ in range(args.warmup + args.steps)]
+    for i in range(args.warmup):
+        oracle_sample_step(oracle, X, C0, samples[i])
+    t = 0.0
+    for i in range(args.steps):
+        t += oracle_sample_step(oracle, X, C0, samples[args.warmup + i])
+    ms_per_step = 1e3 * t / args.steps
+    value = 2.0 * rows_per_step * w.k * w.d / (t / args.steps) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "n": w.n, "k": w.k, "d": w.d, "blobs": w.blobs,
+                   "step": f"oracle Lloyd step on {rows_per_step} seeded rows"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": f"{rows_per_step} seeded rows of {w.n} per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------- GB300 arm
+def run_gb300(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import distance_argmin_gb300 as km
+    import synth
+
+    rank, world, local = env_rank()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from distance_argmin_gb300 import build as kb
+    kb.build()
+    km.load()
+
+    w = synth.WORKLOADS[args.workload]
+    X, C0, _ = synth.workload_inputs(w)
+    n, k, d = w.n, w.k, w.d
+    flop = 2.0 * n * k * d
+    Xd = torch.from_numpy(X).to(dev)
+    C0d = torch.from_numpy(C0).to(dev)
+    Cbuf = [C0d.clone(), torch.empty_like(C0d)]
+    labels = torch.empty(n, dtype=torch.int64, device=dev)
+    best = torch.empty(n, dtype=torch.float32, device=dev)
+    counts = torch.empty(k, dtype=torch.int32, device=dev)
+    steps, warm = args.steps, args.warmup
+    inertia = torch.zeros(max(steps, warm, 1), dtype=torch.float64, device=dev)
+    ws = km.workspace(km.OP_LLOYD, n, k, d, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def lloyd(i, slot):
+        src, dst = Cbuf[i % 2], Cbuf[(i + 1) % 2]
+        km.kmeans_lloyd_iter(Xd, src, dst, labels, best, inertia[slot:slot + 1], counts, ws=ws, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+    sampler = ClockSampler(gpu_index)
+
+    # warm-up Lloyd iterations from C0, then restart from C0 for the timed run
+    for i in range(warm):
+        lloyd(i, i)
+    Cbuf[0].copy_(C0d)
+    barrier()
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    for i in range(steps):
+        lloyd(i, i)
+    ev1.record(stream)
+    barrier()
+    t_lloyd = ev0.elapsed_time(ev1) / 1e3 / steps
+    inertia_hist = inertia[:steps].cpu().numpy()
+    final_C = Cbuf[steps % 2]
+
+    # the assignment alone (prep + tensor-core kernel + finalize), same stream
+    ws_a = km.workspace(km.OP_ASSIGN, n, k, d, dev)
+    inertia_a = torch.empty(1, dtype=torch.float64, device=dev)
+    for _ in range(warm):
+        km.kmeans_assign(Xd, C0d, labels, best, inertia_a, ws=ws_a, stream=stream)
+    barrier()
+    ev0.record(stream)
+    for _ in range(steps):
+        km.kmeans_assign(Xd, C0d, labels, best, inertia_a, ws=ws_a, stream=stream)
+    ev1.record(stream)
+    barrier()
+    t_assign = ev0.elapsed_time(ev1) / 1e3 / steps
+
+    # the update alone (labels from the assignment above)
+    C_upd = torch.empty_like(C0d)
+    ws_u = km.workspace(km.OP_UPDATE, n, k, d, dev)
+    for _ in range(warm):
+        km.kmeans_update(Xd, labels, C0d, C_upd, counts, ws=ws_u, stream=stream)
+    barrier()
+    ev0.record(stream)
+    for _ in range(steps):
+        km.kmeans_update(Xd, labels, C0d, C_upd, counts, ws=ws_u, stream=stream)
+    ev1.record(stream)
+    barrier()
+    t_update = ev0.elapsed_time(ev1) / 1e3 / steps
+    clocks = sampler.stop()
+
+    # end to end: pinned host inputs in, results out, every step
+    e2e = None
+    if not args.no_e2e:
+        Xh = torch.from_numpy(X).pin_memory()
+        Ch = torch.from_numpy(C0).pin_memory()
+        C_out_h = torch.empty((k, d), dtype=torch.float32).pin_memory()
+        lab_h = torch.empty(n, dtype=torch.int64).pin_memory()
+        in_h = torch.empty(1, dtype=torch.float64).pin_memory()
+        Xe = torch.empty_like(Xd)
+        Ce = torch.empty_like(C0d)
+        Cn = torch.empty_like(C0d)
+        e2e_steps = max(1, min(steps, 50))
+
+        def e2e_step():
+            Xe.copy_(Xh, non_blocking=True)
+            Ce.copy_(Ch, non_blocking=True)
+            km.kmeans_lloyd_iter(Xe, Ce, Cn, labels, best, inertia_a, counts, ws=ws, stream=stream)
+            C_out_h.copy_(Cn, non_blocking=True)
+            lab_h.copy_(labels, non_blocking=True)
+            in_h.copy_(inertia_a, non_blocking=True)
+
+        for _ in range(min(warm, 3)):
+            e2e_step()
+        barrier()
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ev1.record(stream)
+        barrier()
+        t_e2e = ev0.elapsed_time(ev1) / 1e3 / e2e_steps
+        e2e = {"value": flop / t_e2e / 1e12, "unit": "TFLOP/s", "ms_per_step": 1e3 * t_e2e,
+               "steps": e2e_steps,
+               "h2d_bytes_per_step": int(Xh.numel() * 4 + Ch.numel() * 4),
+               "d2h_bytes_per_step": int(C_out_h.numel() * 4 + lab_h.numel() * 8 + 8)}
+
+    # max over ranks
+    times = torch.tensor([t_lloyd, t_assign, t_update, e2e["ms_per_step"] / 1e3 if e2e else 0.0],
+                         dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    t_lloyd, t_assign, t_update, t_e2e_max = [float(v) for v in times.cpu()]
+    if e2e and world > 1:
+        e2e["value"] = world * flop / t_e2e_max / 1e12
+
+    peaks, peaks_src = load_peaks()
+    r_peak = peaks["bf16_tflops"] / SPLIT_PRODUCTS
+    assign_tflops = flop / t_assign / 1e12
+    upd_bytes = 4.0 * n * d + 8.0 * n + 4.0 * k * d
+    line = {
+        "metric": METRIC,
+        "value": world * flop / t_lloyd / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": 1e3 * t_lloyd,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "n": n, "k": k, "d": d, "blobs": w.blobs,
+                   "init": "seeded random rows of X", "l2": "inputs larger than L2 (X 512 MiB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "assign": {"ms": 1e3 * t_assign, "tflops": assign_tflops, "frac_of_R": assign_tflops / r_peak,
+                   "R_tflops": r_peak, "R": f"fp32-accurate roofline = bf16 dense peak ({peaks_src}, burst) / 3 "
+                                             "(bf16x3 split: 3 MMAs per fp32 product)"},
+        "update": {"ms": 1e3 * t_update, "gbs": upd_bytes / t_update / 1e9,
+                   "frac_of_hbm": upd_bytes / t_update / 1e9 / peaks["hbm_gbs"]},
+        "lloyd_frac_of_roofline": (flop / (r_peak * 1e12) + upd_bytes / (peaks["hbm_gbs"] * 1e9)) / t_lloyd,
+        "roofline": {"bound": "tensor", "achieved": assign_tflops, "peak": r_peak, "unit": "TFLOP/s",
+                     "frac": assign_tflops / r_peak, "traffic": recorded_traffic(),
+                     "kernel": "assign_tc_kernel (timed as the kmeans_assign call: prep + kernel + finalize)",
+                     "peak_source": f"{peaks_src} bf16 burst {peaks['bf16_tflops']} / 3"},
+        "inertia_first10": [float(v) for v in inertia_hist[:10]],
+        "gpu_launches": steps * launches_per_lloyd_step(k),
+        "clocks": clocks,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        line["cpu_baseline"] = cpu_baseline(oracle, w, X, C0)
+        line["cpu_baseline"].pop("seconds", None)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

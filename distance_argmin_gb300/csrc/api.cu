@@ -182,9 +182,10 @@ const char *kmeans_status_string(int status) {
 }
 
 const char *kmeans_build_info(void) {
-    return "kmeans_gb300 sm_103a: assign = tcgen05 bf16x3 split, 128x256 tile, BK 32, 3 stages, "
-           "persistent 1 CTA/SM; comparator = FFMA 128x128; update = LSD radix member list + "
-           "compensated segmented mean; k-means++ = Philox4x32-10 greedy D^2";
+    return "kmeans_gb300 sm_103a: assign = tcgen05 cta_group::2 CTA pairs, 256x256 tile, bf16x3 split "
+           "(hi.hi and corrections in separate f32 accumulators), BK 32, X/C ring 4, split ring 6, "
+           "8 split warps; comparator = FFMA 128x128; update = LSD radix member list + compensated "
+           "segmented mean; k-means++ = Philox4x32-10 greedy D^2";
 }
 
 }  // extern "C"

@@ -11,20 +11,36 @@
 //
 // Precision: the pages run float32 with TF32 disabled.  Here each float32
 // operand v is split as hi = bf16(v), lo = bf16(v - hi) (v = hi + lo to about
-// 2^-16 relative) and x.c is accumulated in float32 tensor memory as
-// hi_x.hi_c + hi_x.lo_c + lo_x.hi_c.  The dropped lo_x.lo_c term and the
-// split residuals are below 3 * 2^-16 |x_f c_f| per feature.
+// 2^-16 relative) and x.c = hi_x.hi_c + (lo_x.hi_c + hi_x.lo_c), dropping the
+// lo_x.lo_c term.  The tensor cores add each 16-wide partial product into the
+// float32 accumulator with a truncating add, so every MMA into an accumulator
+// of magnitude |x.c| costs up to one unit in its last place, always in the
+// same direction.  The large product hi.hi therefore gets an accumulator of
+// its own and the two small correction products another: only d/16 truncating
+// adds act at the magnitude of x.c (not 3 d/16), and the correction
+// accumulator stays about 2^8 times smaller.  The two are added in float32 in
+// the epilogue.
 //
-// Structure (one CTA per SM, persistent over a grouped tile order):
-//   warp 8      TMA producer: X (fp32) tile, C hi / C lo (bf16) tiles
-//   warps 0-3   split X into bf16 hi / lo in the UMMA shared-memory layout,
-//               accumulate ||x_i||^2 on the way
-//   warp 9      allocates tensor memory, issues tcgen05.mma (3 products per
-//               16-wide K step) into one of two 128 x 256 f32 accumulators
-//   warps 4-7   epilogue: tcgen05.ld the accumulator, score = ||c||^2 - 2 acc,
-//               row min / argmin, atomicMin into the per-sample key
-// Every wait is bounded; a timeout raises a flag in the status word and the
-// whole CTA winds down without hanging.
+// Structure: CTA pairs (clusters of 2, tcgen05 cta_group::2), persistent over
+// a grouped tile order.  A pair owns a 256-sample x 256-centroid tile: each
+// CTA holds 128 samples (its half of A, the rows of its tensor memory) and
+// 128 centroids (its half of B); the even CTA issues the M = 256 MMAs for both.
+//   warp 16      TMA producer (each CTA): its X rows (fp32) and its C rows
+//                (bf16 hi / lo), 4-deep ring
+//   warps 0-7    split X into bf16 hi / lo in the UMMA shared-memory layout
+//                (6-deep ring), accumulate ||x_i||^2 on a sample block's first
+//                centroid tile, then signal the even CTA that this k-block of
+//                A (and B) is ready
+//   warp 17      allocates the pair's tensor memory (both CTAs); in the even
+//                CTA issues tcgen05.mma: per 16-wide K step hi.hi into the
+//                main accumulator, lo.hi and hi.lo into the correction
+//                accumulator; completions are multicast to both CTAs
+//   warps 8-15   epilogue (each CTA, its 128 rows): tcgen05.ld both
+//                accumulators (two warps per lane quarter, 128 columns each),
+//                score = ||c||^2 - 2 (main + corr), row min / argmin,
+//                atomicMin into the per-sample key
+// Every wait is bounded; a timeout raises a flag in the status word and both
+// CTAs wind down without hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -40,29 +56,49 @@
 namespace km {
 
 namespace tc {
-constexpr int BM = 128;                       // samples per tile (UMMA M)
-constexpr int BN = 256;                       // centroids per tile (UMMA N)
-constexpr int BK = 32;                        // features per pipeline stage
-constexpr int STAGES = 3;
-constexpr int THREADS = 320;
-constexpr int X_BYTES = BM * BK * 4;          // fp32 X tile, 128-byte swizzle
-constexpr int A_BYTES = BM * BK * 2;          // one bf16 X part, 64-byte swizzle
-constexpr int B_BYTES = BN * BK * 2;          // one bf16 C part, 64-byte swizzle
-constexpr int STAGE_BYTES = X_BYTES + 2 * A_BYTES + 2 * B_BYTES;
-constexpr int TX_BYTES = X_BYTES + 2 * B_BYTES;
+constexpr int BM = 128;                        // samples per CTA (the pair's MMA has M = 256)
+constexpr int BN = 256;                        // centroids per pair tile (UMMA N)
+constexpr int BN_CTA = BN / 2;                 // centroid rows each CTA loads
+constexpr int BK = 32;                         // features per pipeline stage
+constexpr int SXB = 4;                         // X + C stages (TMA ring)
+constexpr int SA = 6;                          // split-X stages
+constexpr int SPLIT_WARPS = 8;                 // warps converting X to bf16 hi / lo
+constexpr int EPI_WARPS = 8;
+constexpr int WARP_EPI = SPLIT_WARPS;
+constexpr int WARP_TMA = SPLIT_WARPS + EPI_WARPS;
+constexpr int WARP_MMA = WARP_TMA + 1;
+constexpr int THREADS = (WARP_MMA + 1) * 32;
+constexpr int SPLIT_THREADS = SPLIT_WARPS * 32;
+constexpr int ROWS_PER_SPLIT_THREAD = BM * 8 / SPLIT_THREADS;  // 8 threads per 32-float row
+constexpr int SPLIT_ROW_STRIDE = SPLIT_THREADS / 8;
+constexpr int X_BYTES = BM * BK * 4;           // fp32 X tile, 128-byte swizzle
+constexpr int B_BYTES = BN_CTA * BK * 2;       // one bf16 C part, 64-byte swizzle
+constexpr int A_BYTES = BM * BK * 2;           // one bf16 X part, 64-byte swizzle
+constexpr int XB_STAGE = X_BYTES + 2 * B_BYTES;
+constexpr int A_STAGE = 2 * A_BYTES;
+constexpr int A_BASE = SXB * XB_STAGE;
+constexpr int BAR_BASE = A_BASE + SA * A_STAGE;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
-constexpr int ACC_COLS = BN;                  // f32 columns per accumulator
-constexpr int TMEM_COLS = 2 * ACC_COLS;       // double-buffered
-constexpr int GROUP_M = 16;                   // sample blocks per raster band
-constexpr uint32_t SBO_64B = 8 * 64;          // 8 rows x 64 bytes per swizzle atom
-static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1 KiB aligned");
+constexpr int SMEM_BYTES = BAR_BASE + BAR_BYTES + 1024;  // + alignment slack
+constexpr int TX_BYTES = XB_STAGE;
+constexpr int ACC_MAIN = 0;                    // tensor-memory columns
+constexpr int ACC_CORR = BN;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int GROUP_M = 8;                     // pair sample blocks per raster band
+constexpr uint32_t SBO_64B = 8 * 64;           // 8 rows x 64 bytes per swizzle atom
+constexpr uint16_t PAIR_MASK = 0x3;
+static_assert(XB_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages stay 1 KiB aligned");
+static_assert(SPLIT_WARPS % 4 == 0 && WARP_EPI % 4 == 0, "epilogue warps start on a lane-quarter boundary");
 static_assert(SMEM_BYTES <= 232448, "fits the 227 KiB opt-in limit");
+// barrier slots
+constexpr int XB_FULL = 0, XB_EMPTY = SXB, A_FULL = 2 * SXB, A_EMPTY = 2 * SXB + SA;
+constexpr int T_FULL = 2 * SXB + 2 * SA, T_EMPTY = T_FULL + 1, DRAIN = T_FULL + 2, NUM_BARS = T_FULL + 3;
+static_assert(NUM_BARS * 8 + 16 <= BAR_BYTES, "barriers fit");
 }  // namespace tc
 
 struct TcParams {
     int n, k, d;
-    int num_m, num_n, num_kb, num_tiles;
+    int num_m, num_n, num_kb, num_tiles;  // num_m counts 256-sample pair blocks
     const float *cnorm;
     float *xnorm;
     unsigned long long *keys;
@@ -82,7 +118,44 @@ __device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 h) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__global__ void __launch_bounds__(tc::THREADS, 1)
+// One k-block of the X split: 128 rows x 32 fp32 (128-byte swizzled TMA
+// tile) -> bf16 hi and lo tiles in the 64-byte-swizzled K-major layout the
+// tensor cores read.  Thread t handles 16-byte chunk (t & 7) of rows
+// (t >> 3) + SPLIT_ROW_STRIDE * i.  With NORM it also adds the squares of its
+// values into a compensated running sum per row.
+template <bool NORM>
+__device__ __forceinline__ void split_kblock(const uint8_t *xs, uint8_t *ahi, int t,
+                                             float (&acc)[tc::ROWS_PER_SPLIT_THREAD],
+                                             float (&comp)[tc::ROWS_PER_SPLIT_THREAD]) {
+    uint8_t *alo = ahi + tc::A_BYTES;
+    const int c = t & 7;
+#pragma unroll
+    for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) {
+        const int r = tc::SPLIT_ROW_STRIDE * i + (t >> 3);
+        const float4 v = *reinterpret_cast<const float4 *>(xs + r * 128 + ((c ^ (r & 7)) << 4));
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+        const float2 f01 = __bfloat1622float2(h01);
+        const float2 f23 = __bfloat1622float2(h23);
+        const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+        const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+        const uint32_t off = r * 64 + ((((c >> 1) ^ ((r >> 1) & 3)) << 4) | ((c & 1) << 3));
+        *reinterpret_cast<uint2 *>(ahi + off) = make_uint2(bf162_bits(h01), bf162_bits(h23));
+        *reinterpret_cast<uint2 *>(alo + off) = make_uint2(bf162_bits(l01), bf162_bits(l23));
+        if (NORM) {
+            float q = v.x * v.x;
+            q = fmaf(v.y, v.y, q);
+            q = fmaf(v.z, v.z, q);
+            q = fmaf(v.w, v.w, q);
+            const float y = q - comp[i];
+            const float tsum = acc[i] + y;
+            comp[i] = (tsum - acc[i]) - y;
+            acc[i] = tsum;
+        }
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     assign_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmChi,
                      const __grid_constant__ CUtensorMap tmClo, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -90,129 +163,116 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = smem_addr(smem);
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + tc::STAGES * tc::STAGE_BYTES);
-    // barrier slots: full[3] afull[3] empty[3] tfull[2] tempty[2] drain[1]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + tc::BAR_BASE);
     auto bar = [&](int i) { return smem_addr(bars + i); };
-    const int FULL = 0, AFULL = 3, EMPTY = 6, TFULL = 9, TEMPTY = 11, DRAIN = 13;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 16);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + tc::NUM_BARS);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0 = the CTA that issues the MMAs
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < tc::STAGES; ++s) {
-            mbar_init(bar(FULL + s), 1);
-            mbar_init(bar(AFULL + s), 4);
-            mbar_init(bar(EMPTY + s), 1);
+        for (int s = 0; s < tc::SXB; ++s) {
+            mbar_init(bar(tc::XB_FULL + s), 1);
+            mbar_init(bar(tc::XB_EMPTY + s), tc::SPLIT_WARPS + 1);  // split warps + the MMA commit
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(bar(TFULL + a), 1);
-            mbar_init(bar(TEMPTY + a), 4);
+        for (int s = 0; s < tc::SA; ++s) {
+            mbar_init(bar(tc::A_FULL + s), 2 * tc::SPLIT_WARPS);  // split warps of both CTAs (even CTA's copy)
+            mbar_init(bar(tc::A_EMPTY + s), 1);
         }
-        mbar_init(bar(DRAIN), 1);
+        mbar_init(bar(tc::T_FULL), 1);
+        mbar_init(bar(tc::T_EMPTY), 2 * tc::EPI_WARPS);  // epilogue warps of both CTAs (even CTA's copy)
+        mbar_init(bar(tc::DRAIN), 1);
         fence_barrier_init();
     }
-    if (warp == 9) {
-        tmem_alloc(smem_addr(tmem_holder), tc::TMEM_COLS);
-        tmem_relinquish();
+    if (warp == tc::WARP_MMA) {
+        tmem_alloc_pair(smem_addr(tmem_holder), tc::TMEM_COLS);
+        tmem_relinquish_pair();
         tc_fence_before();
     }
-    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before anyone arrives remotely
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    if (warp < 4) {
+    if (warp < tc::SPLIT_WARPS) {
         // ------------------------------------------------ split X into hi / lo
-        const int t = threadIdx.x;  // 0..127
+        const int t = threadIdx.x;  // 0 .. SPLIT_THREADS-1
         const int c = t & 7;        // 16-byte chunk (4 floats) of a 128-byte fp32 row
         int it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        for (int tile = pair; tile < p.num_tiles && ok; tile += num_pairs) {
             int mb, nb;
             tile_coords(tile, p.num_m, p.num_n, mb, nb);
-            float acc[8], comp[8];
+            const int m0 = mb * (2 * tc::BM) + (int)rank * tc::BM;
+            float acc[tc::ROWS_PER_SPLIT_THREAD], comp[tc::ROWS_PER_SPLIT_THREAD];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = comp[i] = 0.f;
+            for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) acc[i] = comp[i] = 0.f;
             for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                const int s = it % tc::STAGES;
-                const uint32_t ph = (it / tc::STAGES) & 1;
-                if (!mbar_wait_warp(bar(FULL + s), ph, p.status)) {
+                const int s = it % tc::SXB;
+                const int as = it % tc::SA;
+                if (!mbar_wait_warp(bar(tc::XB_FULL + s), (it / tc::SXB) & 1, p.status) ||
+                    !mbar_wait_warp(bar(tc::A_EMPTY + as), ((it / tc::SA) & 1) ^ 1, p.status)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *xs = smem + s * tc::STAGE_BYTES;
-                uint8_t *ahi = smem + s * tc::STAGE_BYTES + tc::X_BYTES;
-                uint8_t *alo = ahi + tc::A_BYTES;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = 16 * i + (t >> 3);
-                    const float4 v =
-                        *reinterpret_cast<const float4 *>(xs + r * 128 + ((c ^ (r & 7)) << 4));
-                    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
-                    const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
-                    const float2 f01 = __bfloat1622float2(h01);
-                    const float2 f23 = __bfloat1622float2(h23);
-                    const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
-                    const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
-                    const uint32_t off =
-                        r * 64 + ((((c >> 1) ^ ((r >> 1) & 3)) << 4) | ((c & 1) << 3));
-                    *reinterpret_cast<uint2 *>(ahi + off) = make_uint2(bf162_bits(h01), bf162_bits(h23));
-                    *reinterpret_cast<uint2 *>(alo + off) = make_uint2(bf162_bits(l01), bf162_bits(l23));
-                    float q = v.x * v.x;
-                    q = fmaf(v.y, v.y, q);
-                    q = fmaf(v.z, v.z, q);
-                    q = fmaf(v.w, v.w, q);
-                    const float y = q - comp[i];
-                    const float tsum = acc[i] + y;
-                    comp[i] = (tsum - acc[i]) - y;
-                    acc[i] = tsum;
-                }
+                const uint8_t *xs = smem + s * tc::XB_STAGE;
+                uint8_t *ahi = smem + tc::A_BASE + as * tc::A_STAGE;
+                if (nb == 0)
+                    split_kblock<true>(xs, ahi, t, acc, comp);  // this tile also reports ||x||^2
+                else
+                    split_kblock<false>(xs, ahi, t, acc, comp);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(AFULL + s));
+                if (lane == 0) {
+                    mbar_arrive_cluster(map_to_cta(bar(tc::A_FULL + as), 0));
+                    mbar_arrive(bar(tc::XB_EMPTY + s));  // the fp32 X tile has been read
+                }
             }
             if (!ok) break;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) {
                 float v = acc[i] - comp[i];
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
-                const int row = mb * tc::BM + 16 * i + (t >> 3);
+                const int row = m0 + tc::SPLIT_ROW_STRIDE * i + (t >> 3);
                 if (nb == 0 && c == 0 && row < p.n) p.xnorm[row] = v;
             }
         }
-    } else if (warp < 8) {
+    } else if (warp < tc::WARP_EPI + tc::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+        const int q = warp & 3;              // tensor-memory lane quarter this warp may read
+        const int half = (warp - tc::WARP_EPI) >> 2;  // which 128 of the tile's 256 columns
+        const uint32_t t_empty = map_to_cta(bar(tc::T_EMPTY), 0);
         int tile_iter = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++tile_iter) {
+        for (int tile = pair; tile < p.num_tiles; tile += num_pairs, ++tile_iter) {
             int mb, nb;
             tile_coords(tile, p.num_m, p.num_n, mb, nb);
-            const int a = tile_iter & 1;
-            const uint32_t ph = (tile_iter >> 1) & 1;
-            if (!mbar_wait_warp(bar(TFULL + a), ph, p.status)) break;
+            if (!mbar_wait_warp(bar(tc::T_FULL), tile_iter & 1, p.status)) break;
             tc_fence_after();
-            const int n0 = nb * tc::BN;
+            const int n0 = nb * tc::BN + half * (tc::BN / 2);
             float best = __int_as_float(0x7f800000);  // +inf
             int arg = -1;
 #pragma unroll 1
-            for (int ch = 0; ch < tc::BN / 32; ++ch) {
+            for (int ch = 0; ch < tc::BN / 64; ++ch) {
                 const int j0 = n0 + ch * 32;
                 if (j0 >= p.k) break;
-                float v[32];
-                tmem_ld_32x32b_x32(tmem_base + (uint32_t)(a * tc::ACC_COLS + ch * 32) +
-                                       ((uint32_t)(q * 32) << 16),
-                                   v);
+                const uint32_t col = (uint32_t)(half * (tc::BN / 2) + ch * 32);
+                const uint32_t lanes = (uint32_t)(q * 32) << 16;
+                float vm[32], vc[32];
+                tmem_ld_2x_32x32b_x32(tmem_base + lanes + tc::ACC_MAIN + col,
+                                      tmem_base + lanes + tc::ACC_CORR + col, vm, vc);
                 const float4 *cn4 = reinterpret_cast<const float4 *>(p.cnorm + j0);
                 if (j0 + 32 <= p.k) {
 #pragma unroll
                     for (int u4 = 0; u4 < 8; ++u4) {
                         const float4 cn = __ldg(cn4 + u4);
-                        const float s0 = fmaf(-2.f, v[4 * u4 + 0], cn.x);
-                        const float s1 = fmaf(-2.f, v[4 * u4 + 1], cn.y);
-                        const float s2 = fmaf(-2.f, v[4 * u4 + 2], cn.z);
-                        const float s3 = fmaf(-2.f, v[4 * u4 + 3], cn.w);
+                        const float s0 = fmaf(-2.f, vm[4 * u4 + 0] + vc[4 * u4 + 0], cn.x);
+                        const float s1 = fmaf(-2.f, vm[4 * u4 + 1] + vc[4 * u4 + 1], cn.y);
+                        const float s2 = fmaf(-2.f, vm[4 * u4 + 2] + vc[4 * u4 + 2], cn.z);
+                        const float s3 = fmaf(-2.f, vm[4 * u4 + 3] + vc[4 * u4 + 3], cn.w);
                         if (s0 < best) { best = s0; arg = j0 + 4 * u4 + 0; }
                         if (s1 < best) { best = s1; arg = j0 + 4 * u4 + 1; }
                         if (s2 < best) { best = s2; arg = j0 + 4 * u4 + 2; }
@@ -222,7 +282,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         if (j0 + u < p.k) {
-                            const float s = fmaf(-2.f, v[u], __ldg(p.cnorm + j0 + u));
+                            const float s = fmaf(-2.f, vm[u] + vc[u], __ldg(p.cnorm + j0 + u));
                             if (s < best) { best = s; arg = j0 + u; }
                         }
                     }
@@ -230,11 +290,11 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(TEMPTY + a));
-            const int row = mb * tc::BM + q * 32 + lane;
+            if (lane == 0) mbar_arrive_cluster(t_empty);
+            const int row = mb * (2 * tc::BM) + (int)rank * tc::BM + q * 32 + lane;
             if (row < p.n && arg >= 0) atomicMin(p.keys + row, make_key(best, (uint32_t)arg));
         }
-    } else if (warp == 8) {
+    } else if (warp == tc::WARP_TMA) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tmX);
@@ -242,80 +302,82 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             tma_prefetch_desc(&tmClo);
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            for (int tile = pair; tile < p.num_tiles && ok; tile += num_pairs) {
                 int mb, nb;
                 tile_coords(tile, p.num_m, p.num_n, mb, nb);
+                const int m0 = mb * (2 * tc::BM) + (int)rank * tc::BM;
+                const int c0 = nb * tc::BN + (int)rank * tc::BN_CTA;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const int s = it % tc::STAGES;
-                    const uint32_t ph = (it / tc::STAGES) & 1;
-                    if (!mbar_wait(bar(EMPTY + s), ph ^ 1, p.status)) {
+                    const int s = it % tc::SXB;
+                    if (!mbar_wait(bar(tc::XB_EMPTY + s), ((it / tc::SXB) & 1) ^ 1, p.status)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t st = sbase + s * tc::STAGE_BYTES;
-                    mbar_arrive_expect_tx(bar(FULL + s), tc::TX_BYTES);
-                    tma_load_2d(st, &tmX, bar(FULL + s), kb * tc::BK, mb * tc::BM);
-                    tma_load_2d(st + tc::X_BYTES + 2 * tc::A_BYTES, &tmChi, bar(FULL + s), kb * tc::BK,
-                                nb * tc::BN);
-                    tma_load_2d(st + tc::X_BYTES + 2 * tc::A_BYTES + tc::B_BYTES, &tmClo, bar(FULL + s),
-                                kb * tc::BK, nb * tc::BN);
+                    const uint32_t st = sbase + s * tc::XB_STAGE;
+                    mbar_arrive_expect_tx(bar(tc::XB_FULL + s), tc::TX_BYTES);
+                    tma_load_2d(st, &tmX, bar(tc::XB_FULL + s), kb * tc::BK, m0);
+                    tma_load_2d(st + tc::X_BYTES, &tmChi, bar(tc::XB_FULL + s), kb * tc::BK, c0);
+                    tma_load_2d(st + tc::X_BYTES + tc::B_BYTES, &tmClo, bar(tc::XB_FULL + s), kb * tc::BK, c0);
                 }
             }
             if (!ok) {
                 // let copies already in flight land before the CTA exits
-                const int issued = it;
-                for (int j = max(0, issued - tc::STAGES); j < issued; ++j)
-                    mbar_wait_drain(bar(FULL + (j % tc::STAGES)), (j / tc::STAGES) & 1);
+                for (int j = max(0, it - tc::SXB); j < it; ++j)
+                    mbar_wait_drain(bar(tc::XB_FULL + (j % tc::SXB)), (j / tc::SXB) & 1);
             }
         }
     } else {
         // ---------------------------------------------------------- MMA issue
-        if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16_f32(tc::BM, tc::BN);
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16_f32(2 * tc::BM, tc::BN);
+            const uint32_t d_main = tmem_base + tc::ACC_MAIN;
+            const uint32_t d_corr = tmem_base + tc::ACC_CORR;
             int it = 0, tile_iter = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++tile_iter) {
-                const int a = tile_iter & 1;
-                if (!mbar_wait(bar(TEMPTY + a), ((tile_iter >> 1) & 1) ^ 1, p.status)) break;
+            for (int tile = pair; tile < p.num_tiles && ok; tile += num_pairs, ++tile_iter) {
+                if (!mbar_wait_cluster(bar(tc::T_EMPTY), (tile_iter & 1) ^ 1, p.status)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(a * tc::ACC_COLS);
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const int s = it % tc::STAGES;
-                    const uint32_t ph = (it / tc::STAGES) & 1;
-                    if (!mbar_wait(bar(FULL + s), ph, p.status) || !mbar_wait(bar(AFULL + s), ph, p.status)) {
+                    const int s = it % tc::SXB;
+                    const int as = it % tc::SA;
+                    // both CTAs' split warps have seen their X and C stage land
+                    if (!mbar_wait_cluster(bar(tc::A_FULL + as), (it / tc::SA) & 1, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t ahi = sbase + s * tc::STAGE_BYTES + tc::X_BYTES;
-                    const uint32_t alo = ahi + tc::A_BYTES;
-                    const uint32_t bhi = alo + tc::A_BYTES;
+                    const uint32_t bhi = sbase + s * tc::XB_STAGE + tc::X_BYTES;
                     const uint32_t blo = bhi + tc::B_BYTES;
+                    const uint32_t ahi = sbase + tc::A_BASE + as * tc::A_STAGE;
+                    const uint32_t alo = ahi + tc::A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < tc::BK / 16; ++kk) {
                         const uint64_t dah = umma_smem_desc(ahi + kk * 32, tc::SBO_64B, kLayoutSW64);
                         const uint64_t dal = umma_smem_desc(alo + kk * 32, tc::SBO_64B, kLayoutSW64);
                         const uint64_t dbh = umma_smem_desc(bhi + kk * 32, tc::SBO_64B, kLayoutSW64);
                         const uint64_t dbl = umma_smem_desc(blo + kk * 32, tc::SBO_64B, kLayoutSW64);
-                        mma_bf16_ss(d_tmem, dal, dbh, idesc, (kb | kk) != 0 ? 1u : 0u);
-                        mma_bf16_ss(d_tmem, dah, dbl, idesc, 1u);
-                        mma_bf16_ss(d_tmem, dah, dbh, idesc, 1u);
+                        const uint32_t first = (kb | kk) != 0 ? 1u : 0u;
+                        mma_bf16_ss_pair(d_main, dah, dbh, idesc, first);
+                        mma_bf16_ss_pair(d_corr, dal, dbh, idesc, first);
+                        mma_bf16_ss_pair(d_corr, dah, dbl, idesc, 1u);
                     }
-                    mma_commit(bar(EMPTY + s));
+                    mma_commit_pair_multicast(bar(tc::XB_EMPTY + s), tc::PAIR_MASK);
+                    mma_commit_pair_multicast(bar(tc::A_EMPTY + as), tc::PAIR_MASK);
                 }
                 if (!ok) break;
-                mma_commit(bar(TFULL + a));
+                mma_commit_pair_multicast(bar(tc::T_FULL), tc::PAIR_MASK);
             }
             // no MMA may still be writing tensor memory when it is released
-            mma_commit(bar(DRAIN));
-            mbar_wait_drain(bar(DRAIN), 0);
+            mma_commit_pair(bar(tc::DRAIN));
+            mbar_wait_drain(bar(tc::DRAIN), 0);
         }
     }
 
-    __syncthreads();
-    if (warp == 9) {
+    __syncwarp();
+    cluster_sync();  // no CTA leaves while its peer may still signal it
+    if (warp == tc::WARP_MMA) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, tc::TMEM_COLS);
+        tmem_dealloc_pair(tmem_base, tc::TMEM_COLS);
     }
 }
 
@@ -365,6 +427,35 @@ int device_sm_count() {
 
 int assign_tc_smem_bytes() { return tc::SMEM_BYTES; }
 
+// CTA pairs that can be resident at once (the persistent grid never exceeds
+// it, so no pair waits for another to finish).
+static int resident_pairs() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (cached[dev] == 0) {
+        int clusters = 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
+        cfg.blockDim = dim3(tc::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&clusters, assign_tc_kernel, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();  // clear
+            clusters = device_sm_count() / 2;
+        }
+        cached[dev] = clusters < 1 ? 1 : clusters;
+    }
+    return cached[dev];
+}
+
 cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
                              uint8_t *ws, cudaStream_t stream) {
     static std::once_flag attr_once;
@@ -381,16 +472,16 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, X, (uint64_t)d, (uint64_t)n, (uint64_t)d,
                    tc::BK, tc::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmChi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, chi, (uint64_t)L.d_pad, (uint64_t)k,
-                   (uint64_t)L.d_pad, tc::BK, tc::BN, CU_TENSOR_MAP_SWIZZLE_64B) ||
+                   (uint64_t)L.d_pad, tc::BK, tc::BN_CTA, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !encode_2d(&tmClo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, clo, (uint64_t)L.d_pad, (uint64_t)k,
-                   (uint64_t)L.d_pad, tc::BK, tc::BN, CU_TENSOR_MAP_SWIZZLE_64B))
+                   (uint64_t)L.d_pad, tc::BK, tc::BN_CTA, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
 
     TcParams p{};
     p.n = (int)n;
     p.k = (int)k;
     p.d = (int)d;
-    p.num_m = (int)((n + tc::BM - 1) / tc::BM);
+    p.num_m = (int)((n + 2 * tc::BM - 1) / (2 * tc::BM));
     p.num_n = (int)((k + tc::BN - 1) / tc::BN);
     p.num_kb = (int)((d + tc::BK - 1) / tc::BK);
     p.num_tiles = p.num_m * p.num_n;
@@ -398,7 +489,9 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     p.xnorm = reinterpret_cast<float *>(ws + L.off_xnorm);
     p.keys = reinterpret_cast<unsigned long long *>(ws + L.off_keys);
     p.status = &reinterpret_cast<WsHeader *>(ws)->status;
-    const int grid = p.num_tiles < device_sm_count() ? p.num_tiles : device_sm_count();
+    const int max_pairs = resident_pairs();
+    const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
+    const int grid = 2 * (pairs > 0 ? pairs : 1);
     assign_tc_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, stream>>>(tmX, tmChi, tmClo, p);
     return cudaGetLastError();
 }

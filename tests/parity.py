@@ -28,7 +28,7 @@ def check_assign(X, C, labels, best, o_labels, o_best, o_second, rows=None, what
 
     ``X`` holds the sample rows the oracle saw (already subset when ``rows``
     is given); ``labels``/``best`` are the GPU's full outputs.  Returns the
-    number of near-tie label flips.
+    number of near-tie label flips and the worst relative distance error.
     """
     labels = np.asarray(labels)
     best = np.asarray(best, dtype=np.float64)
@@ -50,7 +50,7 @@ def check_assign(X, C, labels, best, o_labels, o_best, o_second, rows=None, what
         dj = oracle.sqdist(X[i], C[labels[i]])
         assert dj - o_best[i] <= DIST_RTOL * scale[i], f"{what}: flip at {i} is not a near tie"
     assert labels.min() >= 0 and labels.max() < C.shape[0]
-    return int(len(flips))
+    return int(len(flips)), float((err / scale).max())
 
 
 def check_centroids(got, want, what=""):

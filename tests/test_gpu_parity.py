@@ -230,7 +230,8 @@ def test_lloyd10_workload_ten_iterations(gpu_lib):
         lab = host(labels)
         rows = _sample_rows(w.n, 512, it)
         o_l, o_b, o_s, _ = oracle.assign(X[rows], C)
-        flips += check_assign(X[rows], C, lab, host(best), o_l, o_b, o_s, rows=rows, what=f"iter {it}")
+        f, worst = check_assign(X[rows], C, lab, host(best), o_l, o_b, o_s, rows=rows, what=f"iter {it}")
+        flips += f
         o_C1, o_cnt = oracle.update(X, lab, C)
         check_centroids(host(C1), o_C1, what=f"iter {it} update")
         assert np.array_equal(host(counts).astype(np.int64), o_cnt)
@@ -251,9 +252,10 @@ def test_large_workload_one_iteration(gpu_lib, name):
     lab, bd = host(labels), host(best)
     del Xd
     torch.cuda.empty_cache()
-    rows = _sample_rows(w.n, 128, 17)
+    rows = _sample_rows(w.n, 512, 17)
     o_l, o_b, o_s, _ = oracle.assign(X[rows], C0)
-    check_assign(X[rows], C0, lab, bd, o_l, o_b, o_s, rows=rows, what=name)
+    flips, worst = check_assign(X[rows], C0, lab, bd, o_l, o_b, o_s, rows=rows, what=name)
+    print(f"{name}: worst relative distance error {worst:.3e}, near-tie flips {flips} of {len(rows)}")
     o_C1, o_cnt = oracle.update(X, lab, C0)
     check_centroids(host(C1), o_C1, what=name + " update")
     assert np.array_equal(host(counts).astype(np.int64), o_cnt)
