@@ -28,6 +28,8 @@ KMEANS_ERR_WORKSPACE = 3
 KMEANS_ERR_CUDA = 4
 KMEANS_ERR_DEVICE_TIMEOUT = 5
 KMEANS_ERR_DEVICE_LABEL = 6
+KMEANS_ERR_SCRATCH_LIMIT = 7
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 OP_ASSIGN = 0
 OP_ASSIGN_FFMA = 1
@@ -39,7 +41,7 @@ OP_KMEANSPP = 4
 EXPORTS = (
     "kmeans_workspace_bytes", "kmeans_assign", "kmeans_assign_ffma", "kmeans_update",
     "kmeans_lloyd_iter", "kmeanspp_init", "kmeans_device_status", "kmeans_status_string",
-    "kmeans_build_info",
+    "kmeans_build_info", "kmeans_assign_noalloc",
 )
 
 _lock = threading.Lock()
@@ -72,6 +74,8 @@ def load(path: str | None = None):
         lib.kmeans_assign.restype = INT
         lib.kmeans_assign_ffma.argtypes = assign_sig
         lib.kmeans_assign_ffma.restype = INT
+        lib.kmeans_assign_noalloc.argtypes = [P, P, I64, I64, I64, P, P, P, U64, P]
+        lib.kmeans_assign_noalloc.restype = INT
         lib.kmeans_update.argtypes = [P, P, P, P, P, I64, I64, I64, P, SZ, U64, P]
         lib.kmeans_update.restype = INT
         lib.kmeans_lloyd_iter.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, P, SZ, U64, P]
@@ -194,6 +198,26 @@ def kmeans_assign(X, C, labels=None, best_dist=None, inertia=None, ws=None, seed
 def kmeans_assign_ffma(X, C, labels=None, best_dist=None, inertia=None, ws=None, seed=0, stream=None):
     """The same assignment with float32 FMA on the CUDA cores (comparator)."""
     return _assign("kmeans_assign_ffma", OP_ASSIGN_FFMA, X, C, labels, best_dist, inertia, ws, seed, stream)
+
+
+def kmeans_assign_noalloc(X, C, labels, best_dist, inertia=None, seed=0, stream=None):
+    """``kmeans_assign`` for callers that cannot allocate device memory: the
+    library's built-in scratch replaces the workspace, and the caller passes
+    the outputs.  Problems needing more than NOALLOC_SCRATCH_BYTES of scratch
+    raise KMeansError(KMEANS_ERR_SCRATCH_LIMIT)."""
+    torch = _torch()
+    _check(X, "X", torch.float32)
+    n, d = X.shape
+    _check(C, "C", torch.float32, device=X.device)
+    k = C.shape[0]
+    _check(labels, "labels", torch.int64, (n,), X.device)
+    _check(best_dist, "best_dist", torch.float32, (n,), X.device)
+    if inertia is not None:
+        _check(inertia, "inertia", torch.float64, (1,), X.device)
+    st = load().kmeans_assign_noalloc(_ptr(X), _ptr(C), n, k, d, _ptr(labels), _ptr(best_dist), _ptr(inertia),
+                                      seed & (2**64 - 1), _stream_handle(stream))
+    _raise(st, "kmeans_assign_noalloc")
+    return labels, best_dist, inertia
 
 
 def kmeans_update(X, labels, C_old, C_new=None, counts=None, ws=None, seed=0, stream=None):

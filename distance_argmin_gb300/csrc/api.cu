@@ -177,6 +177,9 @@ const char *kmeans_status_string(int status) {
         case KMEANS_ERR_CUDA: return "CUDA runtime error";
         case KMEANS_ERR_DEVICE_TIMEOUT: return "a device pipeline wait ran out of time";
         case KMEANS_ERR_DEVICE_LABEL: return "a label outside [0, k) reached the update";
+        case KMEANS_ERR_SCRATCH_LIMIT:
+            return "problem too large for the built-in scratch of kmeans_assign_noalloc "
+                   "(use kmeans_assign with a workspace)";
         default: return "unknown status";
     }
 }

@@ -62,7 +62,9 @@ typedef enum {
     KMEANS_ERR_WORKSPACE = 3,       /* ws too small or misaligned                */
     KMEANS_ERR_CUDA = 4,            /* a CUDA runtime call failed                */
     KMEANS_ERR_DEVICE_TIMEOUT = 5,  /* a device pipeline wait ran out of time    */
-    KMEANS_ERR_DEVICE_LABEL = 6     /* kmeans_update saw a label outside [0, k)  */
+    KMEANS_ERR_DEVICE_LABEL = 6,    /* kmeans_update saw a label outside [0, k)  */
+    KMEANS_ERR_SCRATCH_LIMIT = 7    /* kmeans_assign_noalloc: the problem needs more
+                                       than KMEANS_NOALLOC_SCRATCH_BYTES of scratch */
 } kmeans_status;
 
 /* Operation codes for kmeans_workspace_bytes. */
@@ -144,6 +146,35 @@ int kmeans_device_status(const void *ws, void *stream);
 
 /* Human-readable text for a kmeans_status value (static storage). */
 const char *kmeans_status_string(int status);
+
+/* Size of the device array that kmeans_assign_noalloc uses as its scratch.
+ * Every GPU that loads this library holds it until the process exits. */
+#define KMEANS_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* kmeans_assign without a workspace argument (the pages have no counterpart:
+ * it exists for callers, not for the method).  Some callers cannot call
+ * cudaMalloc when they need an assignment: code running under an allocator
+ * that forbids new device allocations, plugins that are handed only their
+ * input and output buffers, or real-time loops where an allocation and the
+ * synchronisation it can imply are not allowed.  They pass only X, C and the
+ * outputs; the scratch comes from one device array of
+ * KMEANS_NOALLOC_SCRATCH_BYTES built into the library (16 MiB: enough for
+ * 12 n + 4 k + 4 k ceil(d/64)*64 bytes plus 11 KiB, e.g. n = 65536, k = 1024,
+ * d = 2048).  Larger problems are rejected with KMEANS_ERR_SCRATCH_LIMIT
+ * before anything is enqueued; use kmeans_assign with a workspace for them.
+ * Same inputs, outputs, requirements and results as kmeans_assign.  The
+ * entry point allocates nothing and calls no allocating routine.
+ * The first call on each device looks up the array's device address (one
+ * cudaGetSymbolAddress): make that first call before any stream capture.
+ * Every call, on every stream, shares the one array and leaves its contents
+ * behind (each call resets what must start fresh); calls that can overlap on
+ * the GPU race with each other and must be serialised by the caller.
+ * Device-side timeouts are recorded in the array's status word, which
+ * kmeans_device_status cannot reach; a call that returned KMEANS_OK and was
+ * synchronised produced complete outputs unless labels hold -1. */
+int kmeans_assign_noalloc(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
+                          int64_t *labels, float *best_dist, double *inertia, uint64_t seed,
+                          void *stream);
 
 /* Build identification of the library: target architecture, tile shapes and
  * pipeline depth (static storage). */

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(km):
 
 
 def test_status_strings(km):
-    for st in range(7):
+    for st in range(8):
         s = km.kmeans_status_string(st)
         assert isinstance(s, str) and s and s != "unknown status"
     assert km.kmeans_status_string(99) == "unknown status"
