@@ -54,6 +54,7 @@ def parse_args():
     ap.add_argument("--workload", default="lloyd10")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kmeanspp", action="store_true")
     return ap.parse_args()
 
 
@@ -210,6 +211,30 @@ def run_reference(args):
 
 
 # -------------------------------------------------------------- GB300 arm
+def time_kmeanspp(km, synth, dev, stream, barrier):
+    """Greedy k-means++ on its own workload (65536 x 8192, 1024 centers,
+    8 trials): one timed call after a short warm-up call."""
+    import torch
+    w = synth.KMEANSPP
+    X, _, _ = synth.planted_blobs(w.n, w.d, w.blobs, w.data_seed)
+    Xd = torch.from_numpy(X).to(dev)
+    T = km.n_trials_for(w.k)
+    ws = km.workspace(km.OP_KMEANSPP, w.n, w.k, w.d, dev)
+    idx = torch.empty(w.k, dtype=torch.int64, device=dev)
+    cen = torch.empty((w.k, w.d), dtype=torch.float32, device=dev)
+    km.kmeanspp_init(Xd, 8, w.init_seed, n_trials=T, ws=ws, stream=stream)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    km.kmeanspp_init(Xd, w.k, w.init_seed, n_trials=T, centers=cen, indices=idx, ws=ws, stream=stream)
+    e1.record(stream)
+    barrier()
+    t = e0.elapsed_time(e1) / 1e3
+    moved = 4.0 * w.n * w.d * w.k  # one read of X per center
+    return {"workload": f"n={w.n} d={w.d} k={w.k} trials={T}", "ms": 1e3 * t, "gbs": moved / t / 1e9,
+            "ms_per_center": 1e3 * t / w.k}
+
+
 def run_gb300(args):
     import numpy as np
     import torch
@@ -296,7 +321,24 @@ def run_gb300(args):
     ev1.record(stream)
     barrier()
     t_update = ev0.elapsed_time(ev1) / 1e3 / steps
+
+    # the FFMA comparator on the same workload (fewer calls: it is ~10x slower)
+    ws_f = km.workspace(km.OP_ASSIGN_FFMA, n, k, d, dev)
+    f_steps = max(1, min(steps, 20))
+    km.kmeans_assign_ffma(Xd, C0d, labels, best, inertia_a, ws=ws_f, stream=stream)
+    barrier()
+    ev0.record(stream)
+    for _ in range(f_steps):
+        km.kmeans_assign_ffma(Xd, C0d, labels, best, inertia_a, ws=ws_f, stream=stream)
+    ev1.record(stream)
+    barrier()
+    t_ffma = ev0.elapsed_time(ev1) / 1e3 / f_steps
+    del ws_f
     clocks = sampler.stop()
+
+    kpp = None
+    if not args.no_kmeanspp:
+        kpp = time_kmeanspp(km, synth, dev, stream, barrier)
 
     # end to end: pinned host inputs in, results out, every step
     e2e = None
@@ -367,6 +409,8 @@ def run_gb300(args):
                                              "(bf16x3 split: 3 MMAs per fp32 product)"},
         "update": {"ms": 1e3 * t_update, "gbs": upd_bytes / t_update / 1e9,
                    "frac_of_hbm": upd_bytes / t_update / 1e9 / peaks["hbm_gbs"]},
+        "assign_ffma": {"ms": 1e3 * t_ffma, "tflops": flop / t_ffma / 1e12,
+                        "speedup_of_tensor_path": t_ffma / t_assign},
         "lloyd_frac_of_roofline": (flop / (r_peak * 1e12) + upd_bytes / (peaks["hbm_gbs"] * 1e9)) / t_lloyd,
         "roofline": {"bound": "tensor", "achieved": assign_tflops, "peak": r_peak, "unit": "TFLOP/s",
                      "frac": assign_tflops / r_peak, "traffic": recorded_traffic(),
@@ -378,6 +422,9 @@ def run_gb300(args):
     }
     if e2e:
         line["e2e"] = e2e
+    if kpp:
+        kpp["frac_of_hbm"] = kpp["gbs"] / peaks["hbm_gbs"]
+        line["kmeanspp"] = kpp
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

@@ -47,6 +47,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "assign_common.cuh"
@@ -103,6 +104,7 @@ struct TcParams {
     float *xnorm;
     unsigned long long *keys;
     uint32_t *status;
+    int test_starve;  // test hook: the producer issues no loads, so the pipeline waits run out
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb) {
@@ -296,7 +298,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
         }
     } else if (warp == tc::WARP_TMA) {
         // ------------------------------------------------------- TMA producer
-        if (lane == 0) {
+        if (lane == 0 && !p.test_starve) {
             tma_prefetch_desc(&tmX);
             tma_prefetch_desc(&tmChi);
             tma_prefetch_desc(&tmClo);
@@ -489,6 +491,11 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     p.xnorm = reinterpret_cast<float *>(ws + L.off_xnorm);
     p.keys = reinterpret_cast<unsigned long long *>(ws + L.off_keys);
     p.status = &reinterpret_cast<WsHeader *>(ws)->status;
+    // Test-only fault injection (no trap, no fault): with this variable set the
+    // producer issues nothing, every consumer's bounded wait runs out, the
+    // status word reports KMEANS_ERR_DEVICE_TIMEOUT and the outputs hold -1.
+    const char *starve = getenv("KMEANS_GB300_TEST_STARVE_PIPELINE");
+    p.test_starve = (starve != nullptr && starve[0] == '1') ? 1 : 0;
     const int max_pairs = resident_pairs();
     const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
     const int grid = 2 * (pairs > 0 ? pairs : 1);

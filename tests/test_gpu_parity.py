@@ -274,3 +274,22 @@ def test_kmeanspp_workload_prefix(gpu_lib):
     assert len(np.unique(got)) == w.k  # D^2 sampling never repeats a chosen sample
     o_idx, margins, _ = oracle.kmeanspp(X, 12, w.init_seed, n_trials=T)
     assert np.array_equal(got[:12], o_idx), f"first mismatch at {np.argmax(got[:12] != o_idx)}"
+
+
+def test_starved_pipeline_times_out_and_reports(gpu_lib, monkeypatch):
+    # Fault injection on the host side: the producer issues no loads, every
+    # bounded pipeline wait runs out (2 s), the kernel winds down and the
+    # status word says so; the context stays usable for the next call.
+    X = synth.gaussian((1000, 64), seed=1)
+    C = synth.gaussian((50, 64), seed=2)
+    Xd, Cd = dev_tensor(X), dev_tensor(C)
+    ws = gpu_lib.workspace(gpu_lib.OP_ASSIGN, 1000, 50, 64)
+    monkeypatch.setenv("KMEANS_GB300_TEST_STARVE_PIPELINE", "1")
+    labels, best, _ = gpu_lib.kmeans_assign(Xd, Cd, ws=ws)
+    assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_ERR_DEVICE_TIMEOUT
+    assert (host(labels) == -1).all()
+    monkeypatch.delenv("KMEANS_GB300_TEST_STARVE_PIPELINE")
+    labels, best, _ = gpu_lib.kmeans_assign(Xd, Cd, ws=ws)
+    assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_OK
+    o_l, o_b, o_s, _ = oracle.assign(X, C)
+    check_assign(X, C, host(labels), host(best), o_l, o_b, o_s, what="after timeout")
