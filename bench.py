@@ -83,12 +83,15 @@ def recorded_traffic():
 
 
 def launches_per_lloyd_step(k: int) -> int:
+    """Kernels one kmeans_lloyd_iter call launches (the library's own)."""
+    assign = 3  # prep_split, assign_tc, finalize
+    if k <= 32768:
+        return assign + 6  # tile_count, col_prefix, scan, tile_scatter, segmented_mean, fixup
     bits = 0
     while (1 << bits) < k:
         bits += 1
     passes = max(1, (bits + 7) // 8)
-    # prep + assign + finalize | clear + passes x (hist, scan, scatter) + scan + mean + fixup
-    return 3 + 1 + 3 * passes + 3
+    return assign + 1 + 3 * passes + 3  # clear, passes x (hist, scan, scatter), scan, mean, fixup
 
 
 # ---------------------------------------------------------------- clocks

@@ -122,8 +122,16 @@ struct UpdateLayout {
     int64_t off_vals_b;  // n x i32 (pong)
     int64_t off_head;    // n_chunks x d f32 partial sums, cluster entering a chunk
     int64_t off_tail;    // n_chunks x d f32 partial sums, cluster leaving a chunk
+    int64_t off_tailc;   // n_chunks x i32 cluster that leaves each chunk (-1: none)
+    int64_t n_utiles;    // tiles of the counting scatter (a constant cap, not n-proportional)
+    int64_t utile;       // samples per counting tile
+    int64_t off_table;   // n_utiles x k x i32 per-tile cluster counts, then column prefixes
+    bool counting;       // counting scatter (k <= kCountingMaxK) instead of the radix sort
     int64_t bytes;
 };
+
+constexpr int64_t kCountingMaxK = 32768;  // per-tile counters fit in shared memory
+constexpr int64_t kCountingTiles = 256;
 
 inline int64_t update_chunk(int64_t n, int64_t d) {
     // members per chunk: enough chunks to fill the machine several times over
@@ -152,6 +160,14 @@ inline UpdateLayout update_layout(int64_t n, int64_t k, int64_t d) {
     o = align_up(o, 1024); L.off_vals_b = o; o += n * 4;
     o = align_up(o, 1024); L.off_head = o; o += L.n_chunks * d * 4;
     o = align_up(o, 1024); L.off_tail = o; o += L.n_chunks * d * 4;
+    o = align_up(o, 1024); L.off_tailc = o; o += L.n_chunks * 4;
+    L.counting = k <= kCountingMaxK;
+    L.n_utiles = kCountingTiles;  // fixed, so the table is O(k) for every n
+    L.utile = (n + L.n_utiles - 1) / L.n_utiles;
+    L.off_table = 0;
+    if (L.counting) {
+        o = align_up(o, 1024); L.off_table = o; o += L.n_utiles * k * 4;
+    }
     L.bytes = align_up(o, 1024);
     return L;
 }

@@ -164,6 +164,82 @@ __global__ void __launch_bounds__(kSortThreads)
     }
 }
 
+// ------------------------------------------- counting scatter (k <= 32768)
+// The member list is the samples sorted by (label, index).  With per-tile
+// cluster counts the position of sample i is
+//   offsets[label_i] + (members of label_i in earlier tiles)
+//                    + (members of label_i earlier in i's own tile),
+// which three small kernels produce without a full sort.
+
+// table[t][j] = members of cluster j among tile t's samples.
+__global__ void __launch_bounds__(256)
+    upd_tile_count_kernel(const int64_t *__restrict__ labels, int n, int k, int tile, int32_t *__restrict__ table,
+                          uint32_t *status, WsHeader *hdr, int clear_header) {
+    extern __shared__ int32_t cnt[];
+    if (clear_header && blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr->status = 0u;
+        hdr->done_blocks = 0u;
+    }
+    for (int j = threadIdx.x; j < k; j += blockDim.x) cnt[j] = 0;
+    __syncthreads();
+    const int i0 = blockIdx.x * tile;
+    const int i1 = min(n, i0 + tile);
+    for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+        const uint32_t lab = clamp_label(labels[i], k, status);
+        const uint32_t peers = __match_any_sync(__activemask(), lab);
+        if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&cnt[lab], __popc(peers));
+    }
+    __syncthreads();
+    int32_t *row = table + (size_t)blockIdx.x * k;
+    for (int j = threadIdx.x; j < k; j += blockDim.x) row[j] = cnt[j];
+}
+
+// Per cluster: table[t][j] <- members of j in tiles before t; totals[j].
+__global__ void __launch_bounds__(256)
+    upd_col_prefix_kernel(int32_t *__restrict__ table, int tiles, int k, int32_t *__restrict__ totals) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= k) return;
+    int32_t run = 0;
+    for (int t = 0; t < tiles; ++t) {
+        const int32_t c = table[(size_t)t * k + j];
+        table[(size_t)t * k + j] = run;
+        run += c;
+    }
+    totals[j] = run;
+}
+
+// One warp walks its tile in index order, 32 samples at a time; the cursor of
+// each cluster (in shared memory) gives the member-list position.
+__global__ void __launch_bounds__(256)
+    upd_tile_scatter_kernel(const int64_t *__restrict__ labels, int n, int k, int tile,
+                            const int32_t *__restrict__ table, const int32_t *__restrict__ offsets,
+                            int32_t *__restrict__ perm, uint32_t *__restrict__ sorted_labels, uint32_t *status) {
+    extern __shared__ int32_t cur[];
+    const int32_t *row = table + (size_t)blockIdx.x * k;
+    for (int j = threadIdx.x; j < k; j += blockDim.x) cur[j] = offsets[j] + row[j];
+    __syncthreads();
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    const int i0 = blockIdx.x * tile;
+    const int i1 = min(n, i0 + tile);
+    for (int b = i0; b < i1; b += 32) {
+        const int i = b + lane;
+        const bool valid = i < i1;
+        const uint32_t lab = valid ? clamp_label(labels[i], k, status) : 0xffffffffu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, lab);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        int32_t pos = 0;
+        if (valid) pos = cur[lab] + rank;
+        __syncwarp();
+        if (valid && rank == 0) cur[lab] += __popc(peers);
+        __syncwarp();
+        if (valid) {
+            perm[pos] = i;
+            sorted_labels[pos] = lab;
+        }
+    }
+}
+
 __device__ __forceinline__ void kahan4(float4 &s, float4 &c, const float4 v) {
     float y, t;
     y = v.x - c.x; t = s.x + y; c.x = (t - s.x) - y; s.x = t;
@@ -173,7 +249,6 @@ __device__ __forceinline__ void kahan4(float4 &s, float4 &c, const float4 v) {
 }
 
 constexpr int kMeanThreads = 128;
-constexpr int kMaxChunk = 4096;
 
 // One CTA = one chunk of the member list x one slice of columns.
 // VEC: 4 columns per thread with 16-byte loads (d % 4 == 0, X aligned).
@@ -182,10 +257,12 @@ __global__ void __launch_bounds__(kMeanThreads)
     segmented_mean_kernel(const float *__restrict__ X, const int32_t *__restrict__ perm,
                           const uint32_t *__restrict__ sorted_labels, const int32_t *__restrict__ offsets,
                           int n, int d, int chunk, float *__restrict__ C_new, float *__restrict__ head,
-                          float *__restrict__ tail) {
-    __shared__ int32_t s_perm[kMaxChunk];
-    __shared__ uint32_t s_lab[kMaxChunk];
+                          float *__restrict__ tail, int32_t *__restrict__ tailc) {
+    extern __shared__ int32_t s_members[];  // [chunk] sample indices, then [chunk] labels
+    int32_t *s_perm = s_members;
+    uint32_t *s_lab = reinterpret_cast<uint32_t *>(s_members + chunk);
     const int c = blockIdx.x;
+    if (tailc && blockIdx.y == 0 && threadIdx.x == 0) tailc[c] = -1;
     const int p0 = c * chunk;
     const int p1 = min(n, p0 + chunk);
     for (int p = p0 + threadIdx.x; p < p1; p += kMeanThreads) {
@@ -206,6 +283,14 @@ __global__ void __launch_bounds__(kMeanThreads)
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f), cmp = make_float4(0.f, 0.f, 0.f, 0.f);
         int r = p;
         if (VEC) {
+            for (; r + 8 <= q; r += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    v[u] = __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r + u - p0] * d + col));
+#pragma unroll
+                for (int u = 0; u < 8; ++u) kahan4(s, cmp, v[u]);
+            }
             for (; r + 4 <= q; r += 4) {
                 const float4 v0 = __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r - p0] * d + col));
                 const float4 v1 = __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r + 1 - p0] * d + col));
@@ -237,6 +322,7 @@ __global__ void __launch_bounds__(kMeanThreads)
             dst = head + (size_t)c * d + col;
         } else {
             dst = tail + (size_t)c * d + col;
+            if (tailc && blockIdx.y == 0 && threadIdx.x == 0) tailc[c] = (int32_t)j;
         }
         if (mean) {
             const float cnt = (float)(seg1 - seg0);
@@ -282,6 +368,42 @@ __global__ void __launch_bounds__(kMeanThreads)
     }
 }
 
+// Fix-up of the counting path: block c finishes the cluster that leaves
+// chunk c (its tail partial plus the head partials of the chunks it covers, in
+// chunk order); every block then copies the old row of empty clusters in its
+// stride and writes the counts.
+__global__ void __launch_bounds__(kMeanThreads)
+    mean_fixup_chunks_kernel(const int32_t *__restrict__ offsets, const int32_t *__restrict__ totals,
+                             const float *__restrict__ head, const float *__restrict__ tail,
+                             const int32_t *__restrict__ tailc, int n_chunks, const float *__restrict__ C_old,
+                             float *__restrict__ C_new, int32_t *__restrict__ counts_out, int k, int d, int chunk) {
+    for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+        const int j = tailc[c];
+        if (j < 0) continue;
+        const int seg0 = offsets[j];
+        const int seg1 = offsets[j + 1];
+        const int ce = (seg1 - 1) / chunk;
+        const float cnt = (float)(seg1 - seg0);
+        for (int f = threadIdx.x; f < d; f += kMeanThreads) {
+            float s = tail[(size_t)c * d + f], cmp = 0.f;
+            for (int cc = c + 1; cc <= ce; ++cc) {
+                const float v = head[(size_t)cc * d + f];
+                const float y = v - cmp;
+                const float t = s + y;
+                cmp = (t - s) - y;
+                s = t;
+            }
+            C_new[(size_t)j * d + f] = (s - cmp) / cnt;
+        }
+    }
+    for (int j = blockIdx.x; j < k; j += gridDim.x) {
+        const int cnt = totals[j];
+        if (counts_out && threadIdx.x == 0) counts_out[j] = cnt;
+        if (cnt == 0 && C_new != C_old)
+            for (int f = threadIdx.x; f < d; f += kMeanThreads) C_new[(size_t)j * d + f] = C_old[(size_t)j * d + f];
+    }
+}
+
 static int radix_passes(int64_t k) {
     int bits = 0;
     while (bits < 32 && ((int64_t)1 << bits) < k) ++bits;  // labels 0..k-1 need `bits` bits
@@ -304,6 +426,49 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
     float *tail = reinterpret_cast<float *>(ws + L.off_tail);
     uint32_t *status = &hdr->status;
     const int tiles = (int)L.n_tiles;
+    const bool vec = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(C_new)) & 15) == 0;
+    const int cols_per_cta = kMeanThreads * (vec ? 4 : 1);
+    const dim3 mgrid((unsigned)L.n_chunks, (unsigned)((d + cols_per_cta - 1) / cols_per_cta));
+    const size_t msmem = (size_t)L.chunk * 8;
+
+    if (L.counting) {
+        int32_t *table = reinterpret_cast<int32_t *>(ws + L.off_table);
+        int32_t *perm = va;
+        uint32_t *slab = ka;
+        int32_t *tailc = reinterpret_cast<int32_t *>(ws + L.off_tailc);
+        const int ut = (int)L.n_utiles;
+        const size_t csmem = (size_t)k * 4;
+        if (csmem > 48 * 1024) {
+            // per device, once: allow the per-cluster counters above the 48 KiB default
+            static bool attr_set[64] = {false};
+            int dev = 0;
+            cudaGetDevice(&dev);
+            if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+                cudaFuncSetAttribute(upd_tile_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kCountingMaxK * 4));
+                cudaFuncSetAttribute(upd_tile_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kCountingMaxK * 4));
+                attr_set[dev] = true;
+            }
+        }
+        upd_tile_count_kernel<<<ut, 256, csmem, s>>>(labels, (int)n, (int)k, (int)L.utile, table, status, hdr,
+                                                     clear_header ? 1 : 0);
+        upd_col_prefix_kernel<<<(int)((k + 255) / 256), 256, 0, s>>>(table, ut, (int)k, counts);
+        exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, offsets, k, offsets + k);
+        upd_tile_scatter_kernel<<<ut, 256, csmem, s>>>(labels, (int)n, (int)k, (int)L.utile, table, offsets, perm,
+                                                       slab, status);
+        if (vec)
+            segmented_mean_kernel<true><<<mgrid, kMeanThreads, msmem, s>>>(X, perm, slab, offsets, (int)n, (int)d,
+                                                                           (int)L.chunk, C_new, head, tail, tailc);
+        else
+            segmented_mean_kernel<false><<<mgrid, kMeanThreads, msmem, s>>>(X, perm, slab, offsets, (int)n, (int)d,
+                                                                            (int)L.chunk, C_new, head, tail, tailc);
+        const int fgrid = (int)(L.n_chunks > 256 ? L.n_chunks : 256);
+        mean_fixup_chunks_kernel<<<fgrid, kMeanThreads, 0, s>>>(offsets, counts, head, tail, tailc, (int)L.n_chunks,
+                                                               C_old, C_new, counts_out, (int)k, (int)d,
+                                                               (int)L.chunk);
+        return cudaGetLastError();
+    }
 
     update_clear_kernel<<<(int)((k + 255) / 256 < 1024 ? (k + 255) / 256 : 1024), 256, 0, s>>>(
         counts, (int)k, hdr, clear_header ? 1 : 0);
@@ -326,15 +491,12 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
     // counts -> offsets (k + 1 entries: the scan writes the total at [k])
     exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, offsets, k, offsets + k);
 
-    const bool vec = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(C_new)) & 15) == 0;
-    const int cols_per_cta = kMeanThreads * (vec ? 4 : 1);
-    const dim3 grid((unsigned)L.n_chunks, (unsigned)((d + cols_per_cta - 1) / cols_per_cta));
     if (vec)
-        segmented_mean_kernel<true><<<grid, kMeanThreads, 0, s>>>(X, vin, kin, offsets, (int)n, (int)d,
-                                                                   (int)L.chunk, C_new, head, tail);
+        segmented_mean_kernel<true><<<mgrid, kMeanThreads, msmem, s>>>(X, vin, kin, offsets, (int)n, (int)d,
+                                                                       (int)L.chunk, C_new, head, tail, nullptr);
     else
-        segmented_mean_kernel<false><<<grid, kMeanThreads, 0, s>>>(X, vin, kin, offsets, (int)n, (int)d,
-                                                                    (int)L.chunk, C_new, head, tail);
+        segmented_mean_kernel<false><<<mgrid, kMeanThreads, msmem, s>>>(X, vin, kin, offsets, (int)n, (int)d,
+                                                                        (int)L.chunk, C_new, head, tail, nullptr);
     const int fix_grid = (int)(k < 4096 ? k : 4096);
     mean_fixup_kernel<<<fix_grid, kMeanThreads, 0, s>>>(offsets, head, tail, C_old, C_new, counts_out, (int)k,
                                                        (int)d, (int)L.chunk);

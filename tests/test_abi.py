@@ -80,13 +80,21 @@ def test_invalid_arguments_are_rejected_on_the_host(km):
     assert lib.kmeans_device_status(None, None) == km.KMEANS_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("op", [0, 1, 2, 3, 4])
-def test_workspace_has_no_n_times_k_term(km, op):
+@pytest.mark.parametrize("op", [0, 1, 2, 4])
+@pytest.mark.parametrize("n", [1 << 12, 1 << 16])
+def test_workspace_has_no_n_times_k_term(km, op, n):
     f = lambda n, k: km.kmeans_workspace_bytes(op, n, k, 512)
-    n, k = 1 << 16, 1 << 12
+    k = n >> 4
     mixed = f(2 * n, 2 * k) - f(2 * n, k) - f(n, 2 * k) + f(n, k)
     assert abs(mixed) <= 16 * 1024  # only region alignment remains
     assert km.kmeans_workspace_bytes(op, 10, 11, 4) == 0  # k > n is invalid
+
+
+def test_lloyd_workspace_is_the_larger_of_its_steps(km):
+    for n, k, d in [(4096, 256, 512), (65536, 1024, 2048), (131072, 8192, 8192)]:
+        a = km.kmeans_workspace_bytes(km.OP_ASSIGN, n, k, d)
+        u = km.kmeans_workspace_bytes(km.OP_UPDATE, n, k, d)
+        assert km.kmeans_workspace_bytes(km.OP_LLOYD, n, k, d) == max(a, u)
 
 
 def test_workspace_far_below_the_distance_matrix_at_every_workload(km):

@@ -85,7 +85,7 @@ def test_single_sample_single_centroid(gpu_lib):
 
 
 @pytest.mark.parametrize("shape", [(512, 17, 64), (2000, 513, 132), (5000, 40, 7), (4096, 256, 512),
-                                   (70000, 3, 20)],
+                                   (70000, 3, 20), (100000, 20000, 12), (40000, 33000, 8)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_update_matches_oracle(gpu_lib, shape):
     n, k, d = shape
