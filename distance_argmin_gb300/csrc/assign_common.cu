@@ -34,42 +34,62 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 h) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// One warp per centroid row.  d % 4 == 0 and C 16-byte aligned (checked on
-// the host for this path); columns d .. d_pad-1 of the copies are zeroed.
-__global__ void prep_split_kernel(const float *__restrict__ C, int k, int d, int d_pad,
-                                  __nv_bfloat16 *__restrict__ chi, __nv_bfloat16 *__restrict__ clo,
-                                  float *__restrict__ cnorm, unsigned long long *__restrict__ keys, int n,
-                                  WsHeader *hdr) {
+// One 128-thread block per centroid row (grid-stride over rows); each thread
+// converts up to 4 float4 groups per pass with its loads issued together.
+// d % 4 == 0 and C 16-byte aligned (checked on the host for this path);
+// columns d .. d_pad-1 of the copies are zeroed.
+constexpr int kPrepThreads = 128;
+
+__global__ void __launch_bounds__(kPrepThreads)
+    prep_split_kernel(const float *__restrict__ C, int k, int d, int d_pad, __nv_bfloat16 *__restrict__ chi,
+                      __nv_bfloat16 *__restrict__ clo, float *__restrict__ cnorm,
+                      unsigned long long *__restrict__ keys, int n, WsHeader *hdr) {
+    __shared__ float red[kPrepThreads / 32];
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         hdr->status = 0u;
         hdr->done_blocks = 0u;
     }
-    const int lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int nw = gridDim.x * (blockDim.x >> 5);
-    for (int j = gw; j < k; j += nw) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int j = blockIdx.x; j < k; j += gridDim.x) {
         const float *row = C + (size_t)j * d;
         float sum = 0.f, comp = 0.f;
-        for (int f = lane * 4; f < d_pad; f += 128) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (f < d) v = __ldg(reinterpret_cast<const float4 *>(row + f));
-            const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
-            const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
-            const float2 f01 = __bfloat1622float2(h01);
-            const float2 f23 = __bfloat1622float2(h23);
-            const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
-            const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
-            const size_t o = (size_t)j * d_pad + f;
-            *reinterpret_cast<uint2 *>(chi + o) = make_uint2(bf16x2_bits(h01), bf16x2_bits(h23));
-            *reinterpret_cast<uint2 *>(clo + o) = make_uint2(bf16x2_bits(l01), bf16x2_bits(l23));
-            float q = v.x * v.x;
-            q = fmaf(v.y, v.y, q);
-            q = fmaf(v.z, v.z, q);
-            q = fmaf(v.w, v.w, q);
-            kahan_add(sum, comp, q);
+        for (int f0 = threadIdx.x * 4; f0 < d_pad; f0 += kPrepThreads * 16) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int f = f0 + u * kPrepThreads * 4;
+                v[u] = f < d ? __ldg(reinterpret_cast<const float4 *>(row + f)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int f = f0 + u * kPrepThreads * 4;
+                if (f >= d_pad) break;
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(v[u].x, v[u].y);
+                const __nv_bfloat162 h23 = __floats2bfloat162_rn(v[u].z, v[u].w);
+                const float2 f01 = __bfloat1622float2(h01);
+                const float2 f23 = __bfloat1622float2(h23);
+                const __nv_bfloat162 l01 = __floats2bfloat162_rn(v[u].x - f01.x, v[u].y - f01.y);
+                const __nv_bfloat162 l23 = __floats2bfloat162_rn(v[u].z - f23.x, v[u].w - f23.y);
+                const size_t o = (size_t)j * d_pad + f;
+                *reinterpret_cast<uint2 *>(chi + o) = make_uint2(bf16x2_bits(h01), bf16x2_bits(h23));
+                *reinterpret_cast<uint2 *>(clo + o) = make_uint2(bf16x2_bits(l01), bf16x2_bits(l23));
+                float q = v[u].x * v[u].x;
+                q = fmaf(v[u].y, v[u].y, q);
+                q = fmaf(v[u].z, v[u].z, q);
+                q = fmaf(v[u].w, v[u].w, q);
+                kahan_add(sum, comp, q);
+            }
         }
-        const float tot = warp_sum(sum - comp);
-        if (lane == 0) cnorm[j] = tot;
+        const float part = warp_sum(sum - comp);
+        if (lane == 0) red[wid] = part;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kPrepThreads / 32; ++w) tot += red[w];
+            cnorm[j] = tot;
+        }
+        __syncthreads();
     }
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
         keys[i] = kEmptyKey;
@@ -157,9 +177,8 @@ __global__ void finalize_kernel(const unsigned long long *__restrict__ keys, con
 }
 
 static int prep_grid(int64_t k, int64_t n) {
-    const int64_t by_rows = (k + 7) / 8;  // 8 warps per block, one row each
-    const int64_t by_keys = (n + 255) / 256;
-    int64_t g = by_rows > by_keys ? by_rows : by_keys;
+    const int64_t by_keys = (n + 1023) / 1024;
+    int64_t g = k > by_keys ? k : by_keys;
     const int64_t cap = (int64_t)device_sm_count() * 16;
     if (g > cap) g = cap;
     return (int)(g < 1 ? 1 : g);
@@ -167,7 +186,7 @@ static int prep_grid(int64_t k, int64_t n) {
 
 cudaError_t launch_prep_split(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
                               uint8_t *ws, cudaStream_t s) {
-    prep_split_kernel<<<prep_grid(k, n), 256, 0, s>>>(
+    prep_split_kernel<<<prep_grid(k, n), kPrepThreads, 0, s>>>(
         C, (int)k, (int)d, (int)L.d_pad, reinterpret_cast<__nv_bfloat16 *>(ws + L.off_chi),
         reinterpret_cast<__nv_bfloat16 *>(ws + L.off_clo), reinterpret_cast<float *>(ws + L.off_cnorm),
         reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws));

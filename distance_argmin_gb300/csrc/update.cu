@@ -195,17 +195,44 @@ __global__ void __launch_bounds__(256)
 }
 
 // Per cluster: table[t][j] <- members of j in tiles before t; totals[j].
-__global__ void __launch_bounds__(256)
-    upd_col_prefix_kernel(int32_t *__restrict__ table, int tiles, int k, int32_t *__restrict__ totals) {
-    const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= k) return;
-    int32_t run = 0;
-    for (int t = 0; t < tiles; ++t) {
-        const int32_t c = table[(size_t)t * k + j];
-        table[(size_t)t * k + j] = run;
-        run += c;
+// One block covers kPrefixCols clusters; thread t holds tile t (the tile
+// count equals the block size) and the tiles are scanned across the block.
+constexpr int kPrefixCols = 8;
+__global__ void __launch_bounds__(kCountingTiles)
+    upd_col_prefix_kernel(int32_t *__restrict__ table, int k, int32_t *__restrict__ totals) {
+    __shared__ int32_t wsum[kCountingTiles / 32][kPrefixCols];
+    const int t = threadIdx.x;
+    const int lane = t & 31, wid = t >> 5;
+    const int j0 = blockIdx.x * kPrefixCols;
+    int32_t v[kPrefixCols], incl[kPrefixCols];
+#pragma unroll
+    for (int u = 0; u < kPrefixCols; ++u) v[u] = (j0 + u < k) ? table[(size_t)t * k + j0 + u] : 0;
+#pragma unroll
+    for (int u = 0; u < kPrefixCols; ++u) {
+        int32_t x = v[u];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        incl[u] = x;
+        if (lane == 31) wsum[wid][u] = x;
     }
-    totals[j] = run;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kPrefixCols; ++u) {
+        int32_t before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kCountingTiles / 32; ++w) {
+            const int32_t ws = wsum[w][u];
+            if (w < wid) before += ws;
+            total += ws;
+        }
+        if (j0 + u < k) {
+            table[(size_t)t * k + j0 + u] = before + incl[u] - v[u];
+            if (t == kCountingTiles - 1) totals[j0 + u] = total;
+        }
+    }
 }
 
 // One warp walks its tile in index order, 32 samples at a time; the cursor of
@@ -384,16 +411,26 @@ __global__ void __launch_bounds__(kMeanThreads)
         const int seg1 = offsets[j + 1];
         const int ce = (seg1 - 1) / chunk;
         const float cnt = (float)(seg1 - seg0);
-        for (int f = threadIdx.x; f < d; f += kMeanThreads) {
-            float s = tail[(size_t)c * d + f], cmp = 0.f;
+        // columns in groups of 4 per thread, each group's partials loaded before the adds
+        for (int f0 = threadIdx.x * 4; f0 < d; f0 += kMeanThreads * 4) {
+            float s[4], cmp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s[u] = f0 + u < d ? tail[(size_t)c * d + f0 + u] : 0.f;
             for (int cc = c + 1; cc <= ce; ++cc) {
-                const float v = head[(size_t)cc * d + f];
-                const float y = v - cmp;
-                const float t = s + y;
-                cmp = (t - s) - y;
-                s = t;
+                float v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = f0 + u < d ? head[(size_t)cc * d + f0 + u] : 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float y = v[u] - cmp[u];
+                    const float t = s[u] + y;
+                    cmp[u] = (t - s[u]) - y;
+                    s[u] = t;
+                }
             }
-            C_new[(size_t)j * d + f] = (s - cmp) / cnt;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (f0 + u < d) C_new[(size_t)j * d + f0 + u] = (s[u] - cmp[u]) / cnt;
         }
     }
     for (int j = blockIdx.x; j < k; j += gridDim.x) {
@@ -453,7 +490,8 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
         }
         upd_tile_count_kernel<<<ut, 256, csmem, s>>>(labels, (int)n, (int)k, (int)L.utile, table, status, hdr,
                                                      clear_header ? 1 : 0);
-        upd_col_prefix_kernel<<<(int)((k + 255) / 256), 256, 0, s>>>(table, ut, (int)k, counts);
+        upd_col_prefix_kernel<<<(int)((k + kPrefixCols - 1) / kPrefixCols), kCountingTiles, 0, s>>>(table, (int)k,
+                                                                                                   counts);
         exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, offsets, k, offsets + k);
         upd_tile_scatter_kernel<<<ut, 256, csmem, s>>>(labels, (int)n, (int)k, (int)L.utile, table, offsets, perm,
                                                        slab, status);
