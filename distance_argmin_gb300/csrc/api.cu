@@ -85,7 +85,7 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
             return (size_t)(a > u ? a : u);
         }
         case KMEANS_OP_KMEANSPP:
-            return (size_t)kpp_layout(n, k, kKppMaxTrials).bytes;
+            return (size_t)kpp_layout(n, d, kKppMaxTrials).bytes;
         default:
             return 0;
     }
@@ -151,7 +151,7 @@ int kmeanspp_init(const float *X, int64_t n, int64_t d, int64_t k, int n_trials,
         return KMEANS_ERR_INVALID_ARG;
     const int T = n_trials > 0 ? n_trials : default_trials(k);
     if (T > kKppMaxTrials) return KMEANS_ERR_UNSUPPORTED;
-    const KppLayout L = kpp_layout(n, k, T);
+    const KppLayout L = kpp_layout(n, d, T);
     const int wst = check_ws(ws, ws_bytes, (size_t)L.bytes);
     if (wst != KMEANS_OK) return wst;
     return cuda_status(launch_kmeanspp(X, n, d, k, T, seed, centers, indices, L, static_cast<uint8_t *>(ws),

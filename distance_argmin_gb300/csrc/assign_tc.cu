@@ -64,7 +64,9 @@ constexpr int BK = 32;                         // features per pipeline stage
 constexpr int SXB = 4;                         // X + C stages (TMA ring)
 constexpr int SA = 6;                          // split-X stages
 constexpr int SPLIT_WARPS = 8;                 // warps converting X to bf16 hi / lo
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 8;                   // 4 or 8: one or two warps per tensor-memory lane quarter
+constexpr int EPI_COLS = BN * 4 / EPI_WARPS;   // accumulator columns each epilogue warp reads
+constexpr int EPI_CHUNK = 32;                  // columns per tensor-memory load (16 or 32)
 constexpr int WARP_EPI = SPLIT_WARPS;
 constexpr int WARP_TMA = SPLIT_WARPS + EPI_WARPS;
 constexpr int WARP_MMA = WARP_TMA + 1;
@@ -246,7 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     } else if (warp < tc::WARP_EPI + tc::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;              // tensor-memory lane quarter this warp may read
-        const int half = (warp - tc::WARP_EPI) >> 2;  // which 128 of the tile's 256 columns
+        const int part = (warp - tc::WARP_EPI) >> 2;  // which EPI_COLS of the tile's 256 columns
         const uint32_t t_empty = map_to_cta(bar(tc::T_EMPTY), 0);
         int tile_iter = 0;
         for (int tile = pair; tile < p.num_tiles; tile += num_pairs, ++tile_iter) {
@@ -254,22 +256,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             tile_coords(tile, p.num_m, p.num_n, mb, nb);
             if (!mbar_wait_warp(bar(tc::T_FULL), tile_iter & 1, p.status)) break;
             tc_fence_after();
-            const int n0 = nb * tc::BN + half * (tc::BN / 2);
+            const int n0 = nb * tc::BN + part * tc::EPI_COLS;
             float best = __int_as_float(0x7f800000);  // +inf
             int arg = -1;
 #pragma unroll 1
-            for (int ch = 0; ch < tc::BN / 64; ++ch) {
-                const int j0 = n0 + ch * 32;
+            for (int ch = 0; ch < tc::EPI_COLS / tc::EPI_CHUNK; ++ch) {
+                const int j0 = n0 + ch * tc::EPI_CHUNK;
                 if (j0 >= p.k) break;
-                const uint32_t col = (uint32_t)(half * (tc::BN / 2) + ch * 32);
+                const uint32_t col = (uint32_t)(part * tc::EPI_COLS + ch * tc::EPI_CHUNK);
                 const uint32_t lanes = (uint32_t)(q * 32) << 16;
-                float vm[32], vc[32];
-                tmem_ld_2x_32x32b_x32(tmem_base + lanes + tc::ACC_MAIN + col,
-                                      tmem_base + lanes + tc::ACC_CORR + col, vm, vc);
+                float vm[tc::EPI_CHUNK], vc[tc::EPI_CHUNK];
+                tmem_ld_pair<tc::EPI_CHUNK>(tmem_base + lanes + tc::ACC_MAIN + col,
+                                            tmem_base + lanes + tc::ACC_CORR + col, vm, vc);
                 const float4 *cn4 = reinterpret_cast<const float4 *>(p.cnorm + j0);
-                if (j0 + 32 <= p.k) {
+                if (j0 + tc::EPI_CHUNK <= p.k) {
 #pragma unroll
-                    for (int u4 = 0; u4 < 8; ++u4) {
+                    for (int u4 = 0; u4 < tc::EPI_CHUNK / 4; ++u4) {
                         const float4 cn = __ldg(cn4 + u4);
                         const float s0 = fmaf(-2.f, vm[4 * u4 + 0] + vc[4 * u4 + 0], cn.x);
                         const float s1 = fmaf(-2.f, vm[4 * u4 + 1] + vc[4 * u4 + 1], cn.y);
@@ -282,7 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                     }
                 } else {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
+                    for (int u = 0; u < tc::EPI_CHUNK; ++u) {
                         if (j0 + u < p.k) {
                             const float s = fmaf(-2.f, vm[u] + vc[u], __ldg(p.cnorm + j0 + u));
                             if (s < best) { best = s; arg = j0 + u; }

@@ -173,35 +173,41 @@ inline UpdateLayout update_layout(int64_t n, int64_t k, int64_t d) {
 }
 
 // k-means++: D^2, running sums, per-trial distances and potentials.
+constexpr int kKppScanBlock = 1024;   // samples per scan / potential block
+constexpr int kKppMaxTrials = 32;
+constexpr int kKppGroupTrials = 8;    // trial candidates per pass over X
+constexpr int kKppSliceFloats = 2048; // features of the 8 candidates a CTA keeps in shared memory (64 KiB)
+
 struct KppLayout {
     int T;
-    int64_t n_blocks;     // blocks of the scan / potential reductions
+    int64_t n_blocks;     // 1024-sample blocks of the scan / potential reductions
+    int S;                // feature slices (the distance pass splits d so a slice of the candidates stays resident)
+    int W;                // features per slice (multiple of 8)
     int64_t off_d2;       // n x f64 current D^2
     int64_t off_dist;     // T x n x f64 distances to the trial candidates
+    int64_t off_dpart;    // S x 8 x n x f64 per-slice partial distances of one pass
     int64_t off_bsum;     // n_blocks x f64 block sums of D^2
-    int64_t off_bpot;     // T x kKppMaxCtas x f64 per-CTA potentials
+    int64_t off_bpot;     // T x n_blocks x f64 block potentials
     int64_t off_cand;     // T x i64 candidates of the current center
-    int64_t off_chosen;   // i32 winning trial of the previous center
+    int64_t off_chosen;   // spare
     int64_t bytes;
 };
 
-constexpr int kKppScanBlock = 1024;   // samples per scan block
-constexpr int kKppMaxCtas = 1024;     // CTAs of the distance pass (fixed per n)
-constexpr int kKppMaxTrials = 32;
-
-inline KppLayout kpp_layout(int64_t n, int64_t k, int T) {
+inline KppLayout kpp_layout(int64_t n, int64_t d, int T) {
     KppLayout L{};
     L.T = T;
     L.n_blocks = (n + kKppScanBlock - 1) / kKppScanBlock;
+    L.S = (int)((d + kKppSliceFloats - 1) / kKppSliceFloats);
+    L.W = (int)align_up((d + L.S - 1) / L.S, 8);
     int64_t o = sizeof(WsHeader);
     o = align_up(o, 1024); L.off_d2 = o; o += n * 8;
     o = align_up(o, 1024); L.off_dist = o; o += (int64_t)T * n * 8;
+    o = align_up(o, 1024); L.off_dpart = o; o += (int64_t)L.S * kKppGroupTrials * n * 8;
     o = align_up(o, 1024); L.off_bsum = o; o += L.n_blocks * 8;
-    o = align_up(o, 1024); L.off_bpot = o; o += (int64_t)T * kKppMaxCtas * 8;
+    o = align_up(o, 1024); L.off_bpot = o; o += (int64_t)T * L.n_blocks * 8;
     o = align_up(o, 1024); L.off_cand = o; o += (int64_t)T * 8;
     o = align_up(o, 1024); L.off_chosen = o; o += 8;
     L.bytes = align_up(o, 1024);
-    (void)k;
     return L;
 }
 

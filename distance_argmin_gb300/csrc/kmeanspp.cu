@@ -2,18 +2,20 @@
 // k-means++", section "k-means++": 2 + log(n_clusters) candidate trials per new
 // center).  The centers are chosen one after the other; each round is:
 //
-//   K1 blocksum  D^2 <- min(D^2, distances to the previous winner); per-block
-//                sums of D^2 (fixed order)
-//   K2 pick      per trial: uniform from Philox4x32-10, target = u * sum D^2,
-//                candidate = first sample whose running sum exceeds the target
-//   K3 dist      one pass over X: squared distance of every sample to every
-//                trial candidate; per-CTA partial potentials
-//                sum_i min(D^2_i, dist_ti)
-//   K4 select    potential per trial, lowest wins (lowest trial on ties)
+//   update   the winner of the previous round is the trial with the lowest
+//            potential (lowest trial on ties); D^2 <- min(D^2, its distances);
+//            per-block sums of D^2 (fixed order)
+//   pick     per trial: uniform from Philox4x32-10, target = u * sum D^2,
+//            candidate = first sample whose running sum exceeds the target
+//   dist     one pass over X per 8 trials: each block keeps one feature slice
+//            of the candidates in shared memory and streams its samples once,
+//            writing per-slice partial squared distances
+//   combine  distances = slice partials added in slice order; per-block
+//            potentials sum_i min(D^2_i, dist_ti)
 //
 // Distances: float32 differences, squared and summed in runs of 8 features,
-// runs added with compensation, lanes combined in float64.  Running sums and
-// potentials are float64.  Every reduction has a fixed order.
+// runs added with compensation, lanes and slices combined in float64.  Running
+// sums and potentials are float64.  Every reduction has a fixed order.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -63,34 +65,7 @@ __global__ void kpp_first_kernel(int64_t n, uint64_t seed, int64_t *cand, int64_
     indices[0] = idx;
 }
 
-// --------------------------------------------------------------- K1 blocksum
 constexpr int kBsThreads = 256;
-
-__global__ void __launch_bounds__(kBsThreads)
-    kpp_blocksum_kernel(const double *__restrict__ dist, const int32_t *__restrict__ sel_t, int64_t n, int init,
-                        double *__restrict__ D2, double *__restrict__ bsum) {
-    __shared__ double red[kBsThreads];
-    const double *db = dist + (init ? 0 : (int64_t)(*sel_t) * n);
-    const int64_t base = (int64_t)blockIdx.x * kKppScanBlock;
-    double s = 0.0;
-#pragma unroll
-    for (int q = 0; q < kKppScanBlock / kBsThreads; ++q) {
-        const int64_t i = base + threadIdx.x + (int64_t)q * kBsThreads;
-        if (i < n) {
-            const double v = db[i];
-            const double nd = init ? v : fmin(D2[i], v);
-            D2[i] = nd;
-            s += nd;
-        }
-    }
-    red[threadIdx.x] = s;
-    __syncthreads();
-    for (int w = kBsThreads / 2; w > 0; w >>= 1) {
-        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) bsum[blockIdx.x] = red[0];
-}
 
 // ------------------------------------------------------------------ K2 pick
 __device__ __forceinline__ double warp_incl_scan(double v, int lane) {
@@ -135,31 +110,48 @@ __global__ void kpp_pick_kernel(const double *__restrict__ bsum, int64_t n_block
     }
     int64_t pick = n - 1;
     // scan samples from that block on (later blocks only matter if rounding
-    // put the target between the block's own running sum and its block sum)
-    if (blk >= 0) {
-        double run = blk_before;
-        bool found = false;
-        for (int64_t i0 = blk * kKppScanBlock; i0 < n && !found; i0 += 32) {
-            const double v = (i0 + lane < n) ? D2[i0 + lane] : 0.0;
-            const double incl = run + warp_incl_scan(v, lane);
-            const uint32_t hit = __ballot_sync(0xffffffffu, (i0 + lane < n) && incl > target);
-            if (hit) {
-                pick = i0 + (__ffs(hit) - 1);
-                found = true;
+    // put the target between the block's own running sum and its block sum):
+    // lane l sums samples [32 l, 32 l + 32) of the 1024-sample block, one
+    // warp scan of those totals finds the lane, which then walks its 32
+    double run = blk_before;
+    for (int64_t b = blk; b >= 0 && b < n_blocks; ++b) {
+        const int64_t i0 = b * kKppScanBlock + lane * 32;
+        double v[32];
+        double tot = 0.0;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = (i0 + e < n) ? D2[i0 + e] : 0.0;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) tot += v[e];
+        const double incl = run + warp_incl_scan(tot, lane);
+        const uint32_t hit = __ballot_sync(0xffffffffu, incl > target);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            if (lane == l) {
+                double acc = incl - tot;
+                int64_t found = i0 + 31;
+                for (int e = 0; e < 32; ++e) {
+                    acc += v[e];
+                    if (acc > target) {
+                        found = i0 + e;
+                        break;
+                    }
+                }
+                pick = found < n ? found : n - 1;
             }
-            run = __shfl_sync(0xffffffffu, incl, 31);
+            pick = __shfl_sync(0xffffffffu, pick, l);
+            break;
         }
+        run = __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) cand[t] = pick;
 }
 
 // ------------------------------------------------------------------ K3 dist
 namespace kd {
-constexpr int KT = 8;        // trial candidates per pass over X
-constexpr int ROWS = 2;      // samples per warp at a time
+constexpr int KT = kKppGroupTrials;  // trial candidates per pass over X
+constexpr int ROWS = 2;              // samples per warp at a time
 constexpr int WARPS = 8;
 constexpr int THREADS = WARPS * 32;
-constexpr int SL = 1024;     // features of the candidates staged per slice
 constexpr int GROUP = WARPS * ROWS;
 }  // namespace kd
 
@@ -170,34 +162,69 @@ __device__ __forceinline__ void kahan(float &s, float &c, float v) {
     s = t;
 }
 
-template <bool VEC>
-__device__ __forceinline__ void load8(const float *__restrict__ p, int avail, float (&v)[8]) {
-    if (VEC && avail >= 8) {
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(p + 4));
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
+// Error-free sum: s + e == a + b exactly (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// Warp sum of double-float values (hi + lo) with a butterfly: every level
+// adds exactly with TwoSum and renormalises, so the result keeps about 44 bits
+// and is the same on every lane (each step is symmetric in its operands).
+__device__ __forceinline__ void lane_sum_double_float(float &hi, float &lo) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = e < avail ? __ldg(p + e) : 0.f;
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ohi = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float olo = __shfl_xor_sync(0xffffffffu, lo, o);
+        float s, e;
+        two_sum(hi, ohi, s, e);
+        e += lo + olo;
+        hi = s + e;
+        lo = e - (hi - s);
     }
 }
 
-// dist[t][i] = ||x_i - x_cand[t]||^2 for t in [t0, min(T, t0 + KT)), and
-// bpot[t][blockIdx.x] = sum over this CTA's samples of min(D2_i, dist[t][i])
-// (skipped when D2 is null).
 template <bool VEC>
-__global__ void __launch_bounds__(kd::THREADS, 2)
-    kpp_dist_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand, int T, int t0,
-                    const double *__restrict__ D2, double *__restrict__ dist, double *__restrict__ bpot) {
-    __shared__ __align__(16) float cs[kd::KT][kd::SL];
-    __shared__ double wpot[kd::WARPS][kd::KT];
+__device__ __forceinline__ void load8(const float *__restrict__ p, int avail, float2 (&v)[4]) {
+    if (VEC && avail >= 8) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p + 4));
+        v[0] = make_float2(a.x, a.y);
+        v[1] = make_float2(a.z, a.w);
+        v[2] = make_float2(b.x, b.y);
+        v[3] = make_float2(b.z, b.w);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            v[e] = make_float2(2 * e < avail ? __ldg(p + 2 * e) : 0.f, 2 * e + 1 < avail ? __ldg(p + 2 * e + 1) : 0.f);
+    }
+}
+
+// Partial distances over one feature slice (blockIdx.y) to trials
+// [t0, t0 + nt): dpart[slice][t][i] = sum over the slice of (x_if - cand_tf)^2.
+// The block stages its slice of the candidates (negated) in shared memory once
+// and then streams its share of the samples, each sample read exactly once.
+// Differences and squares use the packed two-float instructions; each run of
+// 8 features is added to a compensated per-lane sum.
+template <bool VEC>
+__global__ void __launch_bounds__(kd::THREADS, 3)
+    kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand, int T,
+                         int t0, int W, double *__restrict__ dpart) {
+    extern __shared__ __align__(16) float cs[];  // [KT][W], negated
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nt = min(kd::KT, T - t0);
-    double pot[kd::KT];
-#pragma unroll
-    for (int t = 0; t < kd::KT; ++t) pot[t] = 0.0;
+    const int slice = blockIdx.y;
+    const int fb = slice * W;
+    const int width = min(W, d - fb);
+    for (int e = threadIdx.x; e < kd::KT * W; e += kd::THREADS) {
+        const int t = e / W, f = e - t * W;
+        float v = 0.f;
+        if (t < nt && f < width) v = -__ldg(X + cand[t0 + t] * (int64_t)d + fb + f);
+        cs[e] = v;
+    }
+    __syncthreads();
 
     const int64_t n_groups = (n + kd::GROUP - 1) / kd::GROUP;
     for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x) {
@@ -207,98 +234,155 @@ __global__ void __launch_bounds__(kd::THREADS, 2)
         for (int r = 0; r < kd::ROWS; ++r)
 #pragma unroll
             for (int t = 0; t < kd::KT; ++t) s[r][t] = c[r][t] = 0.f;
-
-        for (int f0 = 0; f0 < d; f0 += kd::SL) {
-            const int width = min(kd::SL, d - f0);
-            __syncthreads();
-            for (int e = threadIdx.x; e < kd::KT * kd::SL; e += kd::THREADS) {
-                const int t = e / kd::SL, f = e % kd::SL;
-                float v = 0.f;
-                if (t < nt && f < width) v = __ldg(X + cand[t0 + t] * (int64_t)d + f0 + f);
-                cs[t][f] = v;
+        // the next step's samples are loaded before this step's arithmetic
+        float2 x[kd::ROWS][4], xn[kd::ROWS][4];
+        auto fetch = [&](int f, float2 (&dst)[kd::ROWS][4]) {
+#pragma unroll
+            for (int r = 0; r < kd::ROWS; ++r) {
+                if (r0 + r < n && f < width) {
+                    load8<VEC>(X + (r0 + r) * (int64_t)d + fb + f, width - f, dst[r]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[r][e] = make_float2(0.f, 0.f);
+                }
             }
-            __syncthreads();
-            for (int f = lane * 8; f < width; f += 256) {
-                const int avail = width - f;
-                float x[kd::ROWS][8];
+        };
+        fetch(lane * 8, x);
+        for (int f = lane * 8; f < width; f += 256) {
+            fetch(f + 256, xn);
+#pragma unroll
+            for (int t = 0; t < kd::KT; ++t) {
+                const float4 ca = *reinterpret_cast<const float4 *>(&cs[t * W + f]);
+                const float4 cb = *reinterpret_cast<const float4 *>(&cs[t * W + f + 4]);
+                const float2 nc[4] = {make_float2(ca.x, ca.y), make_float2(ca.z, ca.w), make_float2(cb.x, cb.y),
+                                      make_float2(cb.z, cb.w)};
 #pragma unroll
                 for (int r = 0; r < kd::ROWS; ++r) {
-                    if (r0 + r < n) {
-                        load8<VEC>(X + (r0 + r) * (int64_t)d + f0 + f, avail, x[r]);
-                    } else {
+                    const float2 e0 = __fadd2_rn(x[r][0], nc[0]);
+                    float2 run = __fmul2_rn(e0, e0);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[r][e] = 0.f;
+                    for (int e = 1; e < 4; ++e) {
+                        const float2 de = __fadd2_rn(x[r][e], nc[e]);
+                        run = __ffma2_rn(de, de, run);
                     }
-                }
-#pragma unroll
-                for (int t = 0; t < kd::KT; ++t) {
-                    const float4 ca = *reinterpret_cast<const float4 *>(&cs[t][f]);
-                    const float4 cb = *reinterpret_cast<const float4 *>(&cs[t][f + 4]);
-                    const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-#pragma unroll
-                    for (int r = 0; r < kd::ROWS; ++r) {
-                        float e0 = x[r][0] - cv[0];
-                        float run = e0 * e0;
-#pragma unroll
-                        for (int e = 1; e < 8; ++e) {
-                            const float de = x[r][e] - cv[e];
-                            run = fmaf(de, de, run);
-                        }
-                        kahan(s[r][t], c[r][t], run);
-                    }
+                    kahan(s[r][t], c[r][t], run.x + run.y);
                 }
             }
+#pragma unroll
+            for (int r = 0; r < kd::ROWS; ++r)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[r][e] = xn[r][e];
         }
-        // lanes -> one float64 distance per (row, trial), fixed tree order
+        // lanes -> one partial per (row, trial): a double-float butterfly in
+        // float32 (the float64 pipe of this part is far too slow for it)
 #pragma unroll
         for (int r = 0; r < kd::ROWS; ++r) {
             const int64_t row = r0 + r;
 #pragma unroll
             for (int t = 0; t < kd::KT; ++t) {
-                double v = static_cast<double>(s[r][t]) - static_cast<double>(c[r][t]);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (t < nt && row < n) {
-                    if (lane == 0) dist[(int64_t)(t0 + t) * n + row] = v;
-                    if (D2) pot[t] += fmin(D2[row], v);
-                }
+                float hi = s[r][t], lo = -c[r][t];
+                lane_sum_double_float(hi, lo);
+                if (lane == 0 && t < nt && row < n)
+                    dpart[((int64_t)slice * kd::KT + t) * n + row] = static_cast<double>(hi) + static_cast<double>(lo);
             }
         }
     }
-    if (D2 == nullptr) return;
-    if (lane == 0)
-#pragma unroll
-        for (int t = 0; t < kd::KT; ++t) wpot[warp][t] = pot[t];
-    __syncthreads();
-    if (threadIdx.x < nt) {
-        double v = 0.0;
-        for (int w = 0; w < kd::WARPS; ++w) v += wpot[w][threadIdx.x];
-        bpot[(int64_t)(t0 + threadIdx.x) * gridDim.x + blockIdx.x] = v;
-    }
 }
 
-// ----------------------------------------------------------------- K4 select
-__global__ void kpp_select_kernel(const double *__restrict__ bpot, int n_cta, int T, const int64_t *__restrict__ cand,
-                                  int64_t c, int64_t *__restrict__ indices, int32_t *__restrict__ sel_t) {
-    __shared__ double pot[64];
-    const int lane = threadIdx.x & 31;
-    const int t = threadIdx.x >> 5;
-    if (t < T) {
-        double v = 0.0;
-        for (int b0 = 0; b0 < n_cta; b0 += 32) {
-            const double x = (b0 + lane < n_cta) ? bpot[(int64_t)t * n_cta + b0 + lane] : 0.0;
-            v += __shfl_sync(0xffffffffu, warp_incl_scan(x, lane), 31);
+// dist[t0 + t][i] = sum of the S slice partials (slice order); with D2, the
+// block potentials bpot[t0 + t][block] = sum over the block's samples of
+// min(D2_i, dist) in a fixed order.  Grid: (sample blocks, trials).
+__global__ void __launch_bounds__(kBsThreads)
+    kpp_combine_kernel(const double *__restrict__ dpart, int S, int64_t n, int t0, const double *__restrict__ D2,
+                       double *__restrict__ dist, double *__restrict__ bpot, int64_t n_blocks) {
+    __shared__ double red[kBsThreads];
+    const int t = blockIdx.y;
+    const int64_t base = (int64_t)blockIdx.x * kKppScanBlock;
+    double pot = 0.0;
+#pragma unroll
+    for (int q = 0; q < kKppScanBlock / kBsThreads; ++q) {
+        const int64_t i = base + threadIdx.x + (int64_t)q * kBsThreads;
+        if (i < n) {
+            double v = 0.0;
+            for (int sl = 0; sl < S; ++sl) v += dpart[((int64_t)sl * kd::KT + t) * n + i];
+            dist[(int64_t)(t0 + t) * n + i] = v;
+            if (D2) pot += fmin(D2[i], v);
         }
-        if (lane == 0) pot[t] = v;
+    }
+    if (D2 == nullptr) return;
+    red[threadIdx.x] = pot;
+    __syncthreads();
+    for (int w = kBsThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) bpot[(int64_t)(t0 + t) * n_blocks + blockIdx.x] = red[0];
+}
+
+// The winning trial of the previous center: lowest total potential (lowest
+// trial on ties), every block computing the same sums in the same order.
+__device__ int select_best_trial(const double *__restrict__ bpot, int T, int64_t n_blocks) {
+    __shared__ int best_s;
+    __shared__ double pot_s[kKppMaxTrials];
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    for (int t = w; t < T; t += blockDim.x / 32) {
+        double v = 0.0;
+        for (int64_t b = lane; b < n_blocks; b += 32) v += bpot[(int64_t)t * n_blocks + b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) pot_s[t] = v;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         int best = 0;
         for (int q = 1; q < T; ++q)
-            if (pot[q] < pot[best]) best = q;
-        *sel_t = best;
-        indices[c] = cand[best];
+            if (pot_s[q] < pot_s[best]) best = q;
+        best_s = best;
     }
+    __syncthreads();
+    return best_s;
+}
+
+// K1 of center c: choose the winner of center c-1 (from c = 2 on), lower D^2
+// by its distances, and the per-block sums of D^2 for the draws of center c.
+__global__ void __launch_bounds__(kBsThreads)
+    kpp_update_kernel(const double *__restrict__ dist, const double *__restrict__ bpot, int T, int64_t n,
+                      int64_t n_blocks, const int64_t *__restrict__ cand, int64_t *__restrict__ indices,
+                      int64_t prev, int init, double *__restrict__ D2, double *__restrict__ bsum) {
+    __shared__ double red[kBsThreads];
+    int best = 0;
+    if (!init) {
+        best = select_best_trial(bpot, T, n_blocks);
+        if (blockIdx.x == 0 && threadIdx.x == 0) indices[prev] = cand[best];
+    }
+    const double *db = dist + (int64_t)best * n;
+    const int64_t base = (int64_t)blockIdx.x * kKppScanBlock;
+    double s = 0.0;
+#pragma unroll
+    for (int q = 0; q < kKppScanBlock / kBsThreads; ++q) {
+        const int64_t i = base + threadIdx.x + (int64_t)q * kBsThreads;
+        if (i < n) {
+            const double v = db[i];
+            const double nd = init ? v : fmin(D2[i], v);
+            D2[i] = nd;
+            s += nd;
+        }
+    }
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = kBsThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) bsum[blockIdx.x] = red[0];
+}
+
+// Winner of the last center.
+__global__ void kpp_select_last_kernel(const double *__restrict__ bpot, int T, int64_t n_blocks,
+                                       const int64_t *__restrict__ cand, int64_t *__restrict__ indices, int64_t c) {
+    const int best = select_best_trial(bpot, T, n_blocks);
+    if (threadIdx.x == 0) indices[c] = cand[best];
 }
 
 __global__ void gather_rows_kernel(const float *__restrict__ X, const int64_t *__restrict__ idx, int64_t k, int d,
@@ -309,45 +393,59 @@ __global__ void gather_rows_kernel(const float *__restrict__ X, const int64_t *_
     }
 }
 
-static int dist_grid(int64_t n) {
-    const int64_t groups = (n + kd::GROUP - 1) / kd::GROUP;
-    int64_t g = groups < (int64_t)kKppMaxCtas ? groups : (int64_t)kKppMaxCtas;
-    return (int)(g < 1 ? 1 : g);
-}
-
-template <bool VEC>
-static void launch_dist(const float *X, int64_t n, int d, const int64_t *cand, int T, const double *D2, double *dist,
-                        double *bpot, cudaStream_t s) {
-    const int grid = dist_grid(n);
-    for (int t0 = 0; t0 < T; t0 += kd::KT)
-        kpp_dist_kernel<VEC><<<grid, kd::THREADS, 0, s>>>(X, n, d, cand, T, t0, D2, dist, bpot);
-}
-
 cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int T, uint64_t seed, float *centers,
                             int64_t *indices, const KppLayout &L, uint8_t *ws, cudaStream_t s) {
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
     double *D2 = reinterpret_cast<double *>(ws + L.off_d2);
     double *dist = reinterpret_cast<double *>(ws + L.off_dist);
+    double *dpart = reinterpret_cast<double *>(ws + L.off_dpart);
     double *bsum = reinterpret_cast<double *>(ws + L.off_bsum);
     double *bpot = reinterpret_cast<double *>(ws + L.off_bpot);
     int64_t *cand = reinterpret_cast<int64_t *>(ws + L.off_cand);
-    int32_t *sel_t = reinterpret_cast<int32_t *>(ws + L.off_chosen);
     const bool vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(X) & 15) == 0;
+    const size_t smem = (size_t)kd::KT * L.W * sizeof(float);
+    {
+        static bool attr_set[64] = {false};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+            cudaFuncSetAttribute(kpp_dist_part_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(kd::KT * kKppSliceFloats * sizeof(float)));
+            cudaFuncSetAttribute(kpp_dist_part_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(kd::KT * kKppSliceFloats * sizeof(float)));
+            attr_set[dev] = true;
+        }
+    }
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t groups = (n + kd::GROUP - 1) / kd::GROUP;
+    int64_t gx = (3 * (int64_t)(sms > 0 ? sms : 1) + L.S - 1) / L.S;  // about three blocks per SM in total
+    if (gx > groups) gx = groups;
+    const dim3 dgrid((unsigned)(gx < 1 ? 1 : gx), (unsigned)L.S);
+
     auto dist_pass = [&](int Tn, const double *d2) {
-        if (vec) launch_dist<true>(X, n, (int)d, cand, Tn, d2, dist, bpot, s);
-        else launch_dist<false>(X, n, (int)d, cand, Tn, d2, dist, bpot, s);
+        for (int t0 = 0; t0 < Tn; t0 += kd::KT) {
+            if (vec)
+                kpp_dist_part_kernel<true><<<dgrid, kd::THREADS, smem, s>>>(X, n, (int)d, cand, Tn, t0, L.W, dpart);
+            else
+                kpp_dist_part_kernel<false><<<dgrid, kd::THREADS, smem, s>>>(X, n, (int)d, cand, Tn, t0, L.W, dpart);
+            const int nt = Tn - t0 < kd::KT ? Tn - t0 : kd::KT;
+            kpp_combine_kernel<<<dim3((unsigned)L.n_blocks, (unsigned)nt), kBsThreads, 0, s>>>(dpart, L.S, n, t0, d2,
+                                                                                              dist, bpot, L.n_blocks);
+        }
     };
-    const int n_cta = dist_grid(n);
 
     kpp_first_kernel<<<1, 1, 0, s>>>(n, seed, cand, indices, hdr);
     dist_pass(1, nullptr);  // distances to the first center
     for (int64_t c = 1; c < k; ++c) {
-        kpp_blocksum_kernel<<<(int)L.n_blocks, kBsThreads, 0, s>>>(dist, sel_t, n, c == 1 ? 1 : 0, D2, bsum);
+        kpp_update_kernel<<<(int)L.n_blocks, kBsThreads, 0, s>>>(dist, bpot, T, n, L.n_blocks, cand, indices, c - 1,
+                                                                 c == 1 ? 1 : 0, D2, bsum);
         kpp_pick_kernel<<<1, 32 * T, 0, s>>>(bsum, L.n_blocks, D2, n, seed, 1 + (uint64_t)(c - 1) * (uint64_t)T, T,
                                              cand);
         dist_pass(T, D2);
-        kpp_select_kernel<<<1, 32 * T, 0, s>>>(bpot, n_cta, T, cand, c, indices, sel_t);
     }
+    if (k > 1) kpp_select_last_kernel<<<1, 256, 0, s>>>(bpot, T, L.n_blocks, cand, indices, k - 1);
     if (centers) {
         const int g = (int)(k < 4096 ? k : 4096);
         gather_rows_kernel<<<g, 256, 0, s>>>(X, indices, k, (int)d, centers);

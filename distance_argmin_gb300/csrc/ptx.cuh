@@ -271,6 +271,36 @@ __device__ __forceinline__ void tmem_ld_2x_32x32b_x32(uint32_t ta, uint32_t tb, 
     }
 }
 
+// Two 16-column loads (two accumulators of the same rows) and one wait.
+__device__ __forceinline__ void tmem_ld_2x_32x32b_x16(uint32_t ta, uint32_t tb, float (&a)[16], float (&b)[16]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        a[i] = __uint_as_float(r[i]);
+        b[i] = __uint_as_float(r[16 + i]);
+    }
+}
+
+// Width-generic front end used by the epilogue.
+template <int W>
+__device__ __forceinline__ void tmem_ld_pair(uint32_t ta, uint32_t tb, float (&a)[W], float (&b)[W]) {
+    static_assert(W == 16 || W == 32, "16 or 32 columns");
+    if constexpr (W == 32) tmem_ld_2x_32x32b_x32(ta, tb, a, b);
+    else tmem_ld_2x_32x32b_x16(ta, tb, a, b);
+}
+
 // ------------------------------------------- tcgen05, CTA pair (cta_group::2)
 // Allocation, relinquish and deallocation are collective: one warp in each
 // CTA of the pair executes them with the same column count.
