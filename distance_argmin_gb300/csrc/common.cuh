@@ -185,7 +185,7 @@ struct KppLayout {
     int W;                // features per slice (multiple of 8)
     int64_t off_d2;       // n x f64 current D^2
     int64_t off_dist;     // T x n x f64 distances to the trial candidates
-    int64_t off_dpart;    // S x 8 x n x f64 per-slice partial distances of one pass
+    int64_t off_dpart;    // S x 8 x n x (f32 hi, f32 lo) per-slice partial distances of one pass
     int64_t off_bsum;     // n_blocks x f64 block sums of D^2
     int64_t off_bpot;     // T x n_blocks x f64 block potentials
     int64_t off_cand;     // T x i64 candidates of the current center

@@ -210,7 +210,7 @@ __device__ __forceinline__ void load8(const float *__restrict__ p, int avail, fl
 template <bool VEC>
 __global__ void __launch_bounds__(kd::THREADS, 3)
     kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand, int T,
-                         int t0, int W, double *__restrict__ dpart) {
+                         int t0, int W, float2 *__restrict__ dpart) {
     extern __shared__ __align__(16) float cs[];  // [KT][W], negated
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -282,18 +282,17 @@ __global__ void __launch_bounds__(kd::THREADS, 3)
             for (int t = 0; t < kd::KT; ++t) {
                 float hi = s[r][t], lo = -c[r][t];
                 lane_sum_double_float(hi, lo);
-                if (lane == 0 && t < nt && row < n)
-                    dpart[((int64_t)slice * kd::KT + t) * n + row] = static_cast<double>(hi) + static_cast<double>(lo);
+                if (lane == 0 && t < nt && row < n) dpart[((int64_t)slice * kd::KT + t) * n + row] = make_float2(hi, lo);
             }
         }
     }
 }
 
-// dist[t0 + t][i] = sum of the S slice partials (slice order); with D2, the
+// dist[t0 + t][i] = sum of the S slice partials (slice order, double-float); with D2, the
 // block potentials bpot[t0 + t][block] = sum over the block's samples of
 // min(D2_i, dist) in a fixed order.  Grid: (sample blocks, trials).
 __global__ void __launch_bounds__(kBsThreads)
-    kpp_combine_kernel(const double *__restrict__ dpart, int S, int64_t n, int t0, const double *__restrict__ D2,
+    kpp_combine_kernel(const float2 *__restrict__ dpart, int S, int64_t n, int t0, const double *__restrict__ D2,
                        double *__restrict__ dist, double *__restrict__ bpot, int64_t n_blocks) {
     __shared__ double red[kBsThreads];
     const int t = blockIdx.y;
@@ -303,8 +302,17 @@ __global__ void __launch_bounds__(kBsThreads)
     for (int q = 0; q < kKppScanBlock / kBsThreads; ++q) {
         const int64_t i = base + threadIdx.x + (int64_t)q * kBsThreads;
         if (i < n) {
-            double v = 0.0;
-            for (int sl = 0; sl < S; ++sl) v += dpart[((int64_t)sl * kd::KT + t) * n + i];
+            // slice partials added as double-float values, one conversion at the end
+            float hi = 0.f, lo = 0.f;
+            for (int sl = 0; sl < S; ++sl) {
+                const float2 pv = dpart[((int64_t)sl * kd::KT + t) * n + i];
+                float s2, e;
+                two_sum(hi, pv.x, s2, e);
+                e += lo + pv.y;
+                hi = s2 + e;
+                lo = e - (hi - s2);
+            }
+            const double v = static_cast<double>(hi) + static_cast<double>(lo);
             dist[(int64_t)(t0 + t) * n + i] = v;
             if (D2) pot += fmin(D2[i], v);
         }
@@ -398,7 +406,7 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
     double *D2 = reinterpret_cast<double *>(ws + L.off_d2);
     double *dist = reinterpret_cast<double *>(ws + L.off_dist);
-    double *dpart = reinterpret_cast<double *>(ws + L.off_dpart);
+    float2 *dpart = reinterpret_cast<float2 *>(ws + L.off_dpart);
     double *bsum = reinterpret_cast<double *>(ws + L.off_bsum);
     double *bpot = reinterpret_cast<double *>(ws + L.off_bpot);
     int64_t *cand = reinterpret_cast<int64_t *>(ws + L.off_cand);
