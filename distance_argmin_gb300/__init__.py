@@ -293,3 +293,53 @@ def kmeanspp_init(X, k: int, seed: int, n_trials: int = 0, centers=None, indices
 def kmeans_device_status(ws, stream=None) -> int:
     """Synchronise the stream; status of the last call that used ``ws``."""
     return int(load().kmeans_device_status(_ptr(ws), _stream_handle(stream)))
+
+
+def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_out_h, labels_h, inertia_h,
+                           chunks: int = 4, ws=None, inertia_parts=None, copy_stream=None, stream=None):
+    """One Lloyd iteration on inputs that live in pinned host memory.
+
+    The samples are copied to the device in ``chunks`` row slices on
+    ``copy_stream``; each slice is assigned on ``stream`` as soon as it has
+    landed (kmeans_assign on the slice), overlapping the copy of the next.
+    The mean update then runs on the whole device copy, and C_new, the labels
+    and the per-slice inertias come back to host memory.  Returns the events
+    the caller can wait on; ``inertia_h`` holds the per-slice inertias, whose
+    sum (in slice order) is the iteration's inertia.
+    Xh, Ch, C_out_h, labels_h, inertia_h: pinned host tensors.
+    Xd, Cd, C_new, labels, best_dist, counts: device tensors (preallocated).
+    """
+    torch = _torch()
+    n, d = Xh.shape
+    k = Ch.shape[0]
+    stream = stream or torch.cuda.current_stream()
+    copy_stream = copy_stream or torch.cuda.Stream()
+    if inertia_parts is None:
+        inertia_parts = torch.empty(chunks, dtype=torch.float64, device=Xd.device)
+    if ws is None:
+        ws = workspace(OP_LLOYD, n, k, d, Xd.device)
+    bounds = [(n * i) // chunks for i in range(chunks + 1)]
+    start = torch.cuda.Event()
+    start.record(stream)
+    copy_stream.wait_event(start)
+    landed = []
+    with torch.cuda.stream(copy_stream):
+        Cd.copy_(Ch, non_blocking=True)
+        for i in range(chunks):
+            r0, r1 = bounds[i], bounds[i + 1]
+            Xd[r0:r1].copy_(Xh[r0:r1], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy_stream)
+            landed.append(ev)
+    for i in range(chunks):
+        r0, r1 = bounds[i], bounds[i + 1]
+        stream.wait_event(landed[i])
+        kmeans_assign(Xd[r0:r1], Cd, labels[r0:r1], best_dist[r0:r1], inertia_parts[i:i + 1], ws=ws, stream=stream)
+    kmeans_update(Xd, labels, Cd, C_new, counts, ws=ws, stream=stream)
+    with torch.cuda.stream(stream):
+        C_out_h.copy_(C_new, non_blocking=True)
+        labels_h.copy_(labels, non_blocking=True)
+        inertia_h.copy_(inertia_parts, non_blocking=True)
+    done = torch.cuda.Event()
+    done.record(stream)
+    return done

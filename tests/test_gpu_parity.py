@@ -293,3 +293,29 @@ def test_starved_pipeline_times_out_and_reports(gpu_lib, monkeypatch):
     assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_OK
     o_l, o_b, o_s, _ = oracle.assign(X, C)
     check_assign(X, C, host(labels), host(best), o_l, o_b, o_s, what="after timeout")
+
+
+def test_lloyd_iteration_from_host_buffers_matches_device_call(gpu_lib):
+    # the pipelined host-input iteration (row slices assigned as they land)
+    # gives the same labels, centroids and inertia as the device-resident call
+    w = synth.Workload("t", 30000, 300, 132, 300, 1, 51, 52, "")
+    X, C0, _ = synth.workload_inputs(w)
+    n, k, d = w.n, w.k, w.d
+    ref = gpu_lib.kmeans_lloyd_iter(dev_tensor(X), dev_tensor(C0))
+    Xh = torch.from_numpy(X).pin_memory()
+    Ch = torch.from_numpy(C0).pin_memory()
+    Xd, Cd = torch.empty_like(Xh, device="cuda"), torch.empty_like(Ch, device="cuda")
+    C_new = torch.empty_like(Cd)
+    labels = torch.empty(n, dtype=torch.int64, device="cuda")
+    best = torch.empty(n, device="cuda")
+    counts = torch.empty(k, dtype=torch.int32, device="cuda")
+    C_out_h = torch.empty((k, d), dtype=torch.float32).pin_memory()
+    lab_h = torch.empty(n, dtype=torch.int64).pin_memory()
+    parts_h = torch.empty(3, dtype=torch.float64).pin_memory()
+    done = gpu_lib.kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best, counts, C_out_h, lab_h, parts_h,
+                                          chunks=3)
+    done.synchronize()
+    np.testing.assert_array_equal(lab_h.numpy(), host(ref[1]))
+    assert C_out_h.numpy().tobytes() == host(ref[0]).tobytes()
+    scale = (sq_norms(X) + sq_norms(C0)[lab_h.numpy()]).sum()
+    assert abs(float(parts_h.numpy().sum()) - float(ref[3].item())) <= 1e-6 * scale
