@@ -72,8 +72,9 @@ constexpr int WARP_TMA = SPLIT_WARPS + EPI_WARPS;
 constexpr int WARP_MMA = WARP_TMA + 1;
 constexpr int THREADS = (WARP_MMA + 1) * 32;
 constexpr int SPLIT_THREADS = SPLIT_WARPS * 32;
-constexpr int ROWS_PER_SPLIT_THREAD = BM * 8 / SPLIT_THREADS;  // 8 threads per 32-float row
-constexpr int SPLIT_ROW_STRIDE = SPLIT_THREADS / 8;
+constexpr int SPLIT_GROUPS = BK / 8;                            // 8-feature groups per row of a k-block
+constexpr int ROWS_PER_SPLIT_THREAD = BM * SPLIT_GROUPS / SPLIT_THREADS;
+constexpr int SPLIT_ROW_STRIDE = SPLIT_THREADS / SPLIT_GROUPS;
 constexpr int X_BYTES = BM * BK * 4;           // fp32 X tile, 128-byte swizzle
 constexpr int B_BYTES = BN_CTA * BK * 2;       // one bf16 C part, 64-byte swizzle
 constexpr int A_BYTES = BM * BK * 2;           // one bf16 X part, 64-byte swizzle
@@ -122,35 +123,50 @@ __device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 h) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// hi = bf16(a), lo = bf16(a - hi) for a pair of floats, packed two per word
+// (the first float in the low half).  a - hi is exact; one packed fma forms
+// both differences.
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint32_t &lo) {
+    hi = bf162_bits(__floats2bfloat162_rn(a, b));
+    const float2 hf = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+    const float2 d = __ffma2_rn(hf, make_float2(-1.f, -1.f), make_float2(a, b));
+    lo = bf162_bits(__floats2bfloat162_rn(d.x, d.y));
+}
+
 // One k-block of the X split: 128 rows x 32 fp32 (128-byte swizzled TMA
 // tile) -> bf16 hi and lo tiles in the 64-byte-swizzled K-major layout the
-// tensor cores read.  Thread t handles 16-byte chunk (t & 7) of rows
-// (t >> 3) + SPLIT_ROW_STRIDE * i.  With NORM it also adds the squares of its
-// values into a compensated running sum per row.
+// tensor cores read.  Thread t handles the 8-feature group (t & 3) of rows
+// (t >> 2) + SPLIT_ROW_STRIDE * i: two 16-byte loads, two 16-byte stores.
+// With NORM it also adds the squares of its values into a compensated
+// running sum per row.
 template <bool NORM>
 __device__ __forceinline__ void split_kblock(const uint8_t *xs, uint8_t *ahi, int t,
                                              float (&acc)[tc::ROWS_PER_SPLIT_THREAD],
                                              float (&comp)[tc::ROWS_PER_SPLIT_THREAD]) {
     uint8_t *alo = ahi + tc::A_BYTES;
-    const int c = t & 7;
+    const int g = t & (tc::SPLIT_GROUPS - 1);
 #pragma unroll
     for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) {
-        const int r = tc::SPLIT_ROW_STRIDE * i + (t >> 3);
-        const float4 v = *reinterpret_cast<const float4 *>(xs + r * 128 + ((c ^ (r & 7)) << 4));
-        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
-        const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
-        const float2 f01 = __bfloat1622float2(h01);
-        const float2 f23 = __bfloat1622float2(h23);
-        const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
-        const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
-        const uint32_t off = r * 64 + ((((c >> 1) ^ ((r >> 1) & 3)) << 4) | ((c & 1) << 3));
-        *reinterpret_cast<uint2 *>(ahi + off) = make_uint2(bf162_bits(h01), bf162_bits(h23));
-        *reinterpret_cast<uint2 *>(alo + off) = make_uint2(bf162_bits(l01), bf162_bits(l23));
+        const int r = tc::SPLIT_ROW_STRIDE * i + t / tc::SPLIT_GROUPS;
+        const float4 v0 = *reinterpret_cast<const float4 *>(xs + r * 128 + (((2 * g) ^ (r & 7)) << 4));
+        const float4 v1 = *reinterpret_cast<const float4 *>(xs + r * 128 + (((2 * g + 1) ^ (r & 7)) << 4));
+        uint4 h, l;
+        split_pair(v0.x, v0.y, h.x, l.x);
+        split_pair(v0.z, v0.w, h.y, l.y);
+        split_pair(v1.x, v1.y, h.z, l.z);
+        split_pair(v1.z, v1.w, h.w, l.w);
+        const uint32_t off = r * 64 + ((g ^ ((r >> 1) & 3)) << 4);
+        *reinterpret_cast<uint4 *>(ahi + off) = h;
+        *reinterpret_cast<uint4 *>(alo + off) = l;
         if (NORM) {
-            float q = v.x * v.x;
-            q = fmaf(v.y, v.y, q);
-            q = fmaf(v.z, v.z, q);
-            q = fmaf(v.w, v.w, q);
+            float q = v0.x * v0.x;
+            q = fmaf(v0.y, v0.y, q);
+            q = fmaf(v0.z, v0.z, q);
+            q = fmaf(v0.w, v0.w, q);
+            q = fmaf(v1.x, v1.x, q);
+            q = fmaf(v1.y, v1.y, q);
+            q = fmaf(v1.z, v1.z, q);
+            q = fmaf(v1.w, v1.w, q);
             const float y = q - comp[i];
             const float tsum = acc[i] + y;
             comp[i] = (tsum - acc[i]) - y;
@@ -203,7 +219,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     if (warp < tc::SPLIT_WARPS) {
         // ------------------------------------------------ split X into hi / lo
         const int t = threadIdx.x;  // 0 .. SPLIT_THREADS-1
-        const int c = t & 7;        // 16-byte chunk (4 floats) of a 128-byte fp32 row
         int it = 0;
         bool ok = true;
         for (int tile = pair; tile < p.num_tiles && ok; tile += num_pairs) {
@@ -240,9 +255,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 float v = acc[i] - comp[i];
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
-                v += __shfl_xor_sync(0xffffffffu, v, 4);
-                const int row = m0 + tc::SPLIT_ROW_STRIDE * i + (t >> 3);
-                if (nb == 0 && c == 0 && row < p.n) p.xnorm[row] = v;
+                const int row = m0 + tc::SPLIT_ROW_STRIDE * i + t / tc::SPLIT_GROUPS;
+                if (nb == 0 && (t & (tc::SPLIT_GROUPS - 1)) == 0 && row < p.n) p.xnorm[row] = v;
             }
         }
     } else if (warp < tc::WARP_EPI + tc::EPI_WARPS) {
