@@ -86,7 +86,9 @@ def launches_per_lloyd_step(k: int) -> int:
     """Kernels one kmeans_lloyd_iter call launches (the library's own)."""
     assign = 3  # prep_split, assign_tc, finalize
     if k <= 32768:
-        return assign + 6  # tile_count, col_prefix, scan, tile_scatter, segmented_mean, fixup
+        # finalize also counts the members per tile; then col_prefix, scan,
+        # tile_scatter, segmented_mean, fixup
+        return assign + 5
     bits = 0
     while (1 << bits) < k:
         bits += 1

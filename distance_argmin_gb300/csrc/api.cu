@@ -136,10 +136,16 @@ int kmeans_lloyd_iter(const float *X, const float *C_old, float *C_new, int64_t 
     const AssignLayout A = assign_layout(n, k, d, true);
     cudaError_t e = launch_prep_split(C_old, n, k, d, A, w, s);
     if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, A, w, s);
-    if (e == cudaSuccess) e = launch_finalize(n, A, w, labels, best_dist, inertia, s);
     // the update reuses the same workspace: the assignment's scratch is dead
-    // once its labels are written
-    if (e == cudaSuccess) e = launch_update(X, labels, C_old, C_new, counts, n, k, d, update_layout(n, k, d), w, false, s);
+    // once its labels are written.  On the counting path the finalize step
+    // also counts members per tile; the count table and its block sums lie
+    // above the keys and norms it reads.
+    const UpdateLayout U = update_layout(n, k, d);
+    const bool fused = U.counting && U.off_table >= A.off_xnorm + n * 4 && U.off_table >= A.off_keys + n * 8;
+    if (e == cudaSuccess)
+        e = fused ? launch_finalize_counting(n, k, A, U, w, labels, best_dist, inertia, s)
+                  : launch_finalize(n, A, w, labels, best_dist, inertia, s);
+    if (e == cudaSuccess) e = launch_update(X, labels, C_old, C_new, counts, n, k, d, U, w, false, s, fused);
     return cuda_status(e);
 }
 

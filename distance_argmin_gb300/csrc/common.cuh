@@ -126,6 +126,7 @@ struct UpdateLayout {
     int64_t n_utiles;    // tiles of the counting scatter (a constant cap, not n-proportional)
     int64_t utile;       // samples per counting tile
     int64_t off_table;   // n_utiles x k x i32 per-tile cluster counts, then column prefixes
+    int64_t off_fin_partial;  // n_utiles x f64 inertia block sums of the Lloyd iteration's finalize
     bool counting;       // counting scatter (k <= kCountingMaxK) instead of the radix sort
     int64_t bytes;
 };
@@ -165,8 +166,12 @@ inline UpdateLayout update_layout(int64_t n, int64_t k, int64_t d) {
     L.n_utiles = kCountingTiles;  // fixed, so the table is O(k) for every n
     L.utile = (n + L.n_utiles - 1) / L.n_utiles;
     L.off_table = 0;
+    L.off_fin_partial = 0;
     if (L.counting) {
         o = align_up(o, 1024); L.off_table = o; o += L.n_utiles * k * 4;
+        // last: the Lloyd iteration writes it while the assignment's keys and
+        // norms (which lie below the member lists) are still being read
+        o = align_up(o, 1024); L.off_fin_partial = o; o += L.n_utiles * 8;
     }
     L.bytes = align_up(o, 1024);
     return L;

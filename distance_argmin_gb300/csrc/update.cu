@@ -194,6 +194,70 @@ __global__ void __launch_bounds__(256)
     for (int j = threadIdx.x; j < k; j += blockDim.x) row[j] = cnt[j];
 }
 
+// The assignment's finalize step fused with the count above, for the Lloyd
+// iteration: block t turns the packed keys of counting tile t into labels and
+// distances (||x||^2 added back, clamped at 0), counts the tile's members per
+// cluster, and adds its distances into a float64 block sum; the last block to
+// finish adds the block sums in tile order.
+constexpr int kFinCountThreads = 256;
+
+__global__ void __launch_bounds__(kFinCountThreads)
+    fin_tile_count_kernel(const unsigned long long *__restrict__ keys, const float *__restrict__ xnorm, int n, int k,
+                          int tile, int64_t *__restrict__ labels, float *__restrict__ best, double *inertia,
+                          double *partial, int32_t *__restrict__ table, WsHeader *hdr) {
+    extern __shared__ int32_t cnt[];
+    __shared__ double red[kFinCountThreads / 32];
+    __shared__ int is_last;
+    for (int j = threadIdx.x; j < k; j += blockDim.x) cnt[j] = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int i0 = blockIdx.x * tile;
+    const int i1 = min(n, i0 + tile);
+    double s = 0.0;
+    for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+        const unsigned long long key = keys[i];
+        uint32_t lab;
+        if (key == kEmptyKey) {  // only for non-finite inputs
+            labels[i] = -1;
+            best[i] = __int_as_float(0x7fc00000);
+            flag_error(&hdr->status, kFlagBadLabel);
+            lab = (uint32_t)(k - 1);
+        } else {
+            lab = static_cast<uint32_t>(key & 0xffffffffu);
+            const float b = fmaxf(0.f, xnorm[i] + ord_to_float(static_cast<uint32_t>(key >> 32)));
+            labels[i] = static_cast<int64_t>(lab);
+            best[i] = b;
+            s += static_cast<double>(b);
+        }
+        const uint32_t peers = __match_any_sync(__activemask(), lab);
+        if (lane == __ffs(peers) - 1) atomicAdd(&cnt[lab], __popc(peers));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+    if (lane == 0) red[wid] = s;
+    __syncthreads();
+    int32_t *row = table + (size_t)blockIdx.x * k;
+    for (int j = threadIdx.x; j < k; j += blockDim.x) row[j] = cnt[j];
+    if (inertia == nullptr) return;
+    if (threadIdx.x == 0) {
+        double b = 0.0;
+        for (int w = 0; w < kFinCountThreads / 32; ++w) b += red[w];
+        partial[blockIdx.x] = b;
+        __threadfence();
+        const unsigned t = atomicAdd(&hdr->done_blocks, 1u);
+        is_last = (t == gridDim.x - 1u);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) {
+        double v = 0.0;
+        for (int b = 0; b < (int)gridDim.x; ++b) v += __ldcg(partial + b);
+        *inertia = v;
+        hdr->done_blocks = 0u;
+    }
+}
+
 // Per cluster: table[t][j] <- members of j in tiles before t; totals[j].
 // One block covers kPrefixCols clusters; thread t holds tile t (the tile
 // count equals the block size) and the tiles are scanned across the block.
@@ -236,33 +300,43 @@ __global__ void __launch_bounds__(kCountingTiles)
 }
 
 // One warp walks its tile in index order, 32 samples at a time; the cursor of
-// each cluster (in shared memory) gives the member-list position.
+// each cluster (in shared memory) gives the member-list position.  The whole
+// block first stages the tile's labels in shared memory.
+constexpr int kMaxCountingTile = 2048;  // samples per tile staged at once
+
 __global__ void __launch_bounds__(256)
     upd_tile_scatter_kernel(const int64_t *__restrict__ labels, int n, int k, int tile,
                             const int32_t *__restrict__ table, const int32_t *__restrict__ offsets,
                             int32_t *__restrict__ perm, uint32_t *__restrict__ sorted_labels, uint32_t *status) {
     extern __shared__ int32_t cur[];
+    __shared__ uint32_t lab_s[kMaxCountingTile];
     const int32_t *row = table + (size_t)blockIdx.x * k;
     for (int j = threadIdx.x; j < k; j += blockDim.x) cur[j] = offsets[j] + row[j];
-    __syncthreads();
-    if (threadIdx.x >= 32) return;
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     const int i0 = blockIdx.x * tile;
     const int i1 = min(n, i0 + tile);
-    for (int b = i0; b < i1; b += 32) {
-        const int i = b + lane;
-        const bool valid = i < i1;
-        const uint32_t lab = valid ? clamp_label(labels[i], k, status) : 0xffffffffu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, lab);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        int32_t pos = 0;
-        if (valid) pos = cur[lab] + rank;
-        __syncwarp();
-        if (valid && rank == 0) cur[lab] += __popc(peers);
-        __syncwarp();
-        if (valid) {
-            perm[pos] = i;
-            sorted_labels[pos] = lab;
+    for (int c0 = i0; c0 < i1; c0 += kMaxCountingTile) {
+        const int c1 = min(i1, c0 + kMaxCountingTile);
+        __syncthreads();
+        for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) lab_s[i - c0] = clamp_label(labels[i], k, status);
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            for (int b = c0; b < c1; b += 32) {
+                const int i = b + lane;
+                const bool valid = i < c1;
+                const uint32_t lab = valid ? lab_s[i - c0] : 0xffffffffu;
+                const uint32_t peers = __match_any_sync(0xffffffffu, lab);
+                const int rank = __popc(peers & ((1u << lane) - 1u));
+                int32_t pos = 0;
+                if (valid) pos = cur[lab] + rank;
+                __syncwarp();
+                if (valid && rank == 0) cur[lab] += __popc(peers);
+                __syncwarp();
+                if (valid) {
+                    perm[pos] = i;
+                    sorted_labels[pos] = lab;
+                }
+            }
         }
     }
 }
@@ -441,6 +515,21 @@ __global__ void __launch_bounds__(kMeanThreads)
     }
 }
 
+// Per device, once: allow the per-cluster shared-memory counters of the
+// counting path above the 48 KiB default.
+static void set_counting_smem_limits(int64_t k) {
+    if (k * 4 <= 48 * 1024) return;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || attr_set[dev]) return;
+    cudaFuncSetAttribute(upd_tile_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kCountingMaxK * 4));
+    cudaFuncSetAttribute(fin_tile_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kCountingMaxK * 4));
+    cudaFuncSetAttribute(upd_tile_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)(kCountingMaxK * 4));
+    attr_set[dev] = true;
+}
+
 static int radix_passes(int64_t k) {
     int bits = 0;
     while (bits < 32 && ((int64_t)1 << bits) < k) ++bits;  // labels 0..k-1 need `bits` bits
@@ -450,7 +539,7 @@ static int radix_passes(int64_t k) {
 
 cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_old, float *C_new,
                           int32_t *counts_out, int64_t n, int64_t k, int64_t d, const UpdateLayout &L,
-                          uint8_t *ws, bool clear_header, cudaStream_t s) {
+                          uint8_t *ws, bool clear_header, cudaStream_t s, bool tile_counts_ready) {
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
     int32_t *counts = reinterpret_cast<int32_t *>(ws + L.off_counts);
     int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.off_offsets);
@@ -475,21 +564,10 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
         int32_t *tailc = reinterpret_cast<int32_t *>(ws + L.off_tailc);
         const int ut = (int)L.n_utiles;
         const size_t csmem = (size_t)k * 4;
-        if (csmem > 48 * 1024) {
-            // per device, once: allow the per-cluster counters above the 48 KiB default
-            static bool attr_set[64] = {false};
-            int dev = 0;
-            cudaGetDevice(&dev);
-            if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-                cudaFuncSetAttribute(upd_tile_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)(kCountingMaxK * 4));
-                cudaFuncSetAttribute(upd_tile_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)(kCountingMaxK * 4));
-                attr_set[dev] = true;
-            }
-        }
-        upd_tile_count_kernel<<<ut, 256, csmem, s>>>(labels, (int)n, (int)k, (int)L.utile, table, status, hdr,
-                                                     clear_header ? 1 : 0);
+        set_counting_smem_limits(k);
+        if (!tile_counts_ready)
+            upd_tile_count_kernel<<<ut, 256, csmem, s>>>(labels, (int)n, (int)k, (int)L.utile, table, status, hdr,
+                                                         clear_header ? 1 : 0);
         upd_col_prefix_kernel<<<(int)((k + kPrefixCols - 1) / kPrefixCols), kCountingTiles, 0, s>>>(table, (int)k,
                                                                                                    counts);
         exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, offsets, k, offsets + k);
@@ -538,6 +616,16 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
     const int fix_grid = (int)(k < 4096 ? k : 4096);
     mean_fixup_kernel<<<fix_grid, kMeanThreads, 0, s>>>(offsets, head, tail, C_old, C_new, counts_out, (int)k,
                                                        (int)d, (int)L.chunk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_counting(int64_t n, int64_t k, const AssignLayout &A, const UpdateLayout &U,
+                                     uint8_t *ws, int64_t *labels, float *best, double *inertia, cudaStream_t s) {
+    set_counting_smem_limits(k);
+    fin_tile_count_kernel<<<(int)U.n_utiles, kFinCountThreads, (size_t)k * 4, s>>>(
+        reinterpret_cast<const unsigned long long *>(ws + A.off_keys), reinterpret_cast<const float *>(ws + A.off_xnorm),
+        (int)n, (int)k, (int)U.utile, labels, best, inertia, reinterpret_cast<double *>(ws + U.off_fin_partial),
+        reinterpret_cast<int32_t *>(ws + U.off_table), reinterpret_cast<WsHeader *>(ws));
     return cudaGetLastError();
 }
 

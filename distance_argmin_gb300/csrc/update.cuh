@@ -10,6 +10,12 @@ namespace km {
 
 cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_old, float *C_new,
                           int32_t *counts_out, int64_t n, int64_t k, int64_t d, const UpdateLayout &L,
-                          uint8_t *ws, bool clear_header, cudaStream_t s);
+                          uint8_t *ws, bool clear_header, cudaStream_t s, bool tile_counts_ready = false);
+
+// Assignment finalize fused with the update's per-tile cluster counts (one
+// block per counting tile); used by the Lloyd iteration when the counting
+// path applies.
+cudaError_t launch_finalize_counting(int64_t n, int64_t k, const AssignLayout &A, const UpdateLayout &U,
+                                     uint8_t *ws, int64_t *labels, float *best, double *inertia, cudaStream_t s);
 
 }  // namespace km
