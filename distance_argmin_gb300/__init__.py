@@ -37,11 +37,17 @@ OP_UPDATE = 2
 OP_LLOYD = 3
 OP_KMEANSPP = 4
 
+KERNEL_ASSIGN_TC = 0
+KERNEL_UPDATE_MEAN = 1
+KERNEL_KMEANSPP_DIST = 2
+TRACE_MAX_CAPACITY = 65536
+
 # Every symbol the header declares (the ABI test checks the library exports them).
 EXPORTS = (
     "kmeans_workspace_bytes", "kmeans_assign", "kmeans_assign_ffma", "kmeans_update",
     "kmeans_lloyd_iter", "kmeanspp_init", "kmeans_device_status", "kmeans_status_string",
-    "kmeans_build_info", "kmeans_assign_noalloc",
+    "kmeans_build_info", "kmeans_assign_noalloc", "kmeans_trace_start", "kmeans_trace_read",
+    "kmeans_trace_stop",
 )
 
 _lock = threading.Lock()
@@ -88,6 +94,12 @@ def load(path: str | None = None):
         lib.kmeans_status_string.restype = ctypes.c_char_p
         lib.kmeans_build_info.argtypes = []
         lib.kmeans_build_info.restype = ctypes.c_char_p
+        lib.kmeans_trace_start.argtypes = [INT]
+        lib.kmeans_trace_start.restype = INT
+        lib.kmeans_trace_read.argtypes = [INT, P, P, P]
+        lib.kmeans_trace_read.restype = INT
+        lib.kmeans_trace_stop.argtypes = []
+        lib.kmeans_trace_stop.restype = INT
         _lib = lib
         return lib
 
@@ -293,6 +305,28 @@ def kmeanspp_init(X, k: int, seed: int, n_trials: int = 0, centers=None, indices
 def kmeans_device_status(ws, stream=None) -> int:
     """Synchronise the stream; status of the last call that used ``ws``."""
     return int(load().kmeans_device_status(_ptr(ws), _stream_handle(stream)))
+
+
+def kmeans_trace_start(capacity: int = 1024) -> None:
+    """Time each call's dominant kernel with CUDA events (up to ``capacity``
+    launches per kernel kind) until kmeans_trace_stop."""
+    _raise(load().kmeans_trace_start(int(capacity)), "kmeans_trace_start")
+
+
+def kmeans_trace_read(kernel: int):
+    """``(ms_total, timed_launches, launches)`` of one traced kernel kind
+    (KERNEL_ASSIGN_TC, KERNEL_UPDATE_MEAN, KERNEL_KMEANSPP_DIST); waits for
+    the recorded events."""
+    ms = ctypes.c_double(0.0)
+    timed, seen = ctypes.c_int64(0), ctypes.c_int64(0)
+    _raise(load().kmeans_trace_read(int(kernel), ctypes.byref(ms), ctypes.byref(timed), ctypes.byref(seen)),
+           "kmeans_trace_read")
+    return ms.value, timed.value, seen.value
+
+
+def kmeans_trace_stop() -> None:
+    """Turn tracing off and release its events."""
+    _raise(load().kmeans_trace_stop(), "kmeans_trace_stop")
 
 
 def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_out_h, labels_h, inertia_h,

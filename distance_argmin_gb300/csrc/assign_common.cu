@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                       __nv_bfloat16 *__restrict__ clo, float *__restrict__ cnorm,
                       unsigned long long *__restrict__ keys, int n, WsHeader *hdr) {
     __shared__ float red[kPrepThreads / 32];
+    griddep_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         hdr->status = 0u;
         hdr->done_blocks = 0u;
@@ -128,6 +129,7 @@ __global__ void finalize_kernel(const unsigned long long *__restrict__ keys, con
                                 double *inertia, double *partial, WsHeader *hdr) {
     __shared__ double red[kFinThreads];
     __shared__ int is_last;
+    griddep_wait();
     const int nb = gridDim.x;
     const int per = (n + nb - 1) / nb;
     const int r0 = blockIdx.x * per;
@@ -206,11 +208,10 @@ cudaError_t launch_finalize(int64_t n, const AssignLayout &L, uint8_t *ws, int64
                             double *inertia, cudaStream_t s) {
     int64_t nb = (n + kFinThreads - 1) / kFinThreads;
     if (nb > kMaxReduceBlocks) nb = kMaxReduceBlocks;
-    finalize_kernel<<<(int)nb, kFinThreads, 0, s>>>(
-        reinterpret_cast<const unsigned long long *>(ws + L.off_keys),
-        reinterpret_cast<const float *>(ws + L.off_xnorm), (int)n, labels, best, inertia,
-        reinterpret_cast<double *>(ws + L.off_partial), reinterpret_cast<WsHeader *>(ws));
-    return cudaGetLastError();
+    return launch_kernel(true, finalize_kernel, dim3((unsigned)nb), dim3(kFinThreads), 0, s,
+                         reinterpret_cast<const unsigned long long *>(ws + L.off_keys),
+                         reinterpret_cast<const float *>(ws + L.off_xnorm), (int)n, labels, best, inertia,
+                         reinterpret_cast<double *>(ws + L.off_partial), reinterpret_cast<WsHeader *>(ws));
 }
 
 }  // namespace km

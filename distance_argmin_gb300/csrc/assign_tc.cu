@@ -52,6 +52,7 @@
 
 #include "assign_common.cuh"
 #include "common.cuh"
+#include "trace.cuh"
 #include "ptx.cuh"
 
 namespace km {
@@ -215,6 +216,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     cluster_sync();  // both CTAs' barriers exist before anyone arrives remotely
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    griddep_wait();  // the centroid copies, norms and reset keys are written
 
     if (warp < tc::SPLIT_WARPS) {
         // ------------------------------------------------ split X into hi / lo
@@ -515,8 +517,11 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     const int max_pairs = resident_pairs();
     const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
     const int grid = 2 * (pairs > 0 ? pairs : 1);
-    assign_tc_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, stream>>>(tmX, tmChi, tmClo, p);
-    return cudaGetLastError();
+    trace_mark(kTraceAssignTc, false, stream);
+    const cudaError_t e = launch_kernel(true, assign_tc_kernel, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,
+                                        tmX, tmChi, tmClo, p);
+    trace_mark(kTraceAssignTc, true, stream);
+    return e;
 }
 
 }  // namespace km

@@ -5,9 +5,44 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/kmeans_gb300.h"
 
 namespace km {
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Inside one entry point the kernels form a
+// chain on one stream; every kernel after the first is launched so that it
+// may be scheduled while the kernel before it drains, and each kernel in the
+// chain calls griddep_wait() before its first global read or write.  That
+// wait returns once the previous kernel has completed and its writes are
+// visible; since every kernel waits before it exits, completion is transitive
+// along the chain.  No kernel signals its dependents early: a dependent that
+// is resident while its predecessor still runs only takes resources from it
+// (measured: early signals made the update slower).  The wait is a no-op for
+// a kernel launched the ordinary way, which is how the first kernel of every
+// entry point starts.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kernel`; with `chained` set it may overlap the tail of the kernel
+// launched before it on `s` (see above).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(bool chained, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = chained ? attr : nullptr;
+    cfg.numAttrs = chained ? 1u : 0u;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------------------
 // Device status word.  Lives in the first bytes of the caller's workspace and

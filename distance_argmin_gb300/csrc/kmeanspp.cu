@@ -21,6 +21,7 @@
 
 #include "common.cuh"
 #include "kmeanspp.cuh"
+#include "trace.cuh"
 
 namespace km {
 
@@ -434,10 +435,12 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
 
     auto dist_pass = [&](int Tn, const double *d2) {
         for (int t0 = 0; t0 < Tn; t0 += kd::KT) {
+            trace_mark(kTraceKppDist, false, s);
             if (vec)
                 kpp_dist_part_kernel<true><<<dgrid, kd::THREADS, smem, s>>>(X, n, (int)d, cand, Tn, t0, L.W, dpart);
             else
                 kpp_dist_part_kernel<false><<<dgrid, kd::THREADS, smem, s>>>(X, n, (int)d, cand, Tn, t0, L.W, dpart);
+            trace_mark(kTraceKppDist, true, s);
             const int nt = Tn - t0 < kd::KT ? Tn - t0 : kd::KT;
             kpp_combine_kernel<<<dim3((unsigned)L.n_blocks, (unsigned)nt), kBsThreads, 0, s>>>(dpart, L.S, n, t0, d2,
                                                                                               dist, bpot, L.n_blocks);

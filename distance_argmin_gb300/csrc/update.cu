@@ -17,7 +17,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "common.cuh"
+#include "trace.cuh"
 #include "update.cuh"
 
 namespace km {
@@ -176,6 +179,7 @@ __global__ void __launch_bounds__(256)
     upd_tile_count_kernel(const int64_t *__restrict__ labels, int n, int k, int tile, int32_t *__restrict__ table,
                           uint32_t *status, WsHeader *hdr, int clear_header) {
     extern __shared__ int32_t cnt[];
+    griddep_wait();
     if (clear_header && blockIdx.x == 0 && threadIdx.x == 0) {
         hdr->status = 0u;
         hdr->done_blocks = 0u;
@@ -208,6 +212,7 @@ __global__ void __launch_bounds__(kFinCountThreads)
     extern __shared__ int32_t cnt[];
     __shared__ double red[kFinCountThreads / 32];
     __shared__ int is_last;
+    griddep_wait();
     for (int j = threadIdx.x; j < k; j += blockDim.x) cnt[j] = 0;
     __syncthreads();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -250,10 +255,18 @@ __global__ void __launch_bounds__(kFinCountThreads)
     __syncthreads();
     if (!is_last) return;
     __threadfence();
+    // fixed order: strided per-thread sums, then the same warp and block tree
+    double v = 0.0;
+    for (int b = threadIdx.x; b < (int)gridDim.x; b += blockDim.x) v += __ldcg(partial + b);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
     if (threadIdx.x == 0) {
-        double v = 0.0;
-        for (int b = 0; b < (int)gridDim.x; ++b) v += __ldcg(partial + b);
-        *inertia = v;
+        double t = 0.0;
+        for (int w = 0; w < kFinCountThreads / 32; ++w) t += red[w];
+        *inertia = t;
         hdr->done_blocks = 0u;
     }
 }
@@ -261,10 +274,15 @@ __global__ void __launch_bounds__(kFinCountThreads)
 // Per cluster: table[t][j] <- members of j in tiles before t; totals[j].
 // One block covers kPrefixCols clusters; thread t holds tile t (the tile
 // count equals the block size) and the tiles are scanned across the block.
+// The last block to finish turns the totals into the exclusive offsets
+// (k + 1 entries, the member total last).
 constexpr int kPrefixCols = 8;
 __global__ void __launch_bounds__(kCountingTiles)
-    upd_col_prefix_kernel(int32_t *__restrict__ table, int k, int32_t *__restrict__ totals) {
+    upd_col_prefix_kernel(int32_t *__restrict__ table, int k, int32_t *__restrict__ totals,
+                          int32_t *__restrict__ offsets, WsHeader *hdr) {
     __shared__ int32_t wsum[kCountingTiles / 32][kPrefixCols];
+    __shared__ int is_last;
+    griddep_wait();
     const int t = threadIdx.x;
     const int lane = t & 31, wid = t >> 5;
     const int j0 = blockIdx.x * kPrefixCols;
@@ -297,6 +315,55 @@ __global__ void __launch_bounds__(kCountingTiles)
             if (t == kCountingTiles - 1) totals[j0 + u] = total;
         }
     }
+    __threadfence();
+    __syncthreads();
+    if (t == 0) is_last = atomicAdd(&hdr->done_blocks, 1u) == gridDim.x - 1u;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // exclusive scan of totals[0..k) in rounds of kCountingTiles x 8 values,
+    // thread t holding 8 consecutive ones; `carry` is the sum of the rounds
+    // before
+    __shared__ int32_t carry;
+    if (t == 0) carry = 0;
+    for (int base = 0; base < k; base += kCountingTiles * 8) {
+        const int j = base + t * 8;
+        int32_t q[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] = j + e < k ? __ldcg(totals + j + e) : 0;
+        int32_t run = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) run += q[e];
+        int32_t x = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        __syncthreads();  // carry and wsum of the previous round are read
+        if (lane == 31) wsum[wid][0] = x;
+        __syncthreads();
+        int32_t before = carry + x - run;
+        int32_t round_total = 0;
+#pragma unroll
+        for (int w = 0; w < kCountingTiles / 32; ++w) {
+            const int32_t ws = wsum[w][0];
+            if (w < wid) before += ws;
+            round_total += ws;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (j + e < k) offsets[j + e] = before;
+            before += q[e];
+        }
+        __syncthreads();
+        if (t == 0) carry += round_total;
+    }
+    __syncthreads();
+    if (t == 0) {
+        offsets[k] = carry;
+        hdr->done_blocks = 0u;
+    }
 }
 
 // One warp walks its tile in index order, 32 samples at a time; the cursor of
@@ -310,6 +377,7 @@ __global__ void __launch_bounds__(256)
                             int32_t *__restrict__ perm, uint32_t *__restrict__ sorted_labels, uint32_t *status) {
     extern __shared__ int32_t cur[];
     __shared__ uint32_t lab_s[kMaxCountingTile];
+    griddep_wait();
     const int32_t *row = table + (size_t)blockIdx.x * k;
     for (int j = threadIdx.x; j < k; j += blockDim.x) cur[j] = offsets[j] + row[j];
     const int lane = threadIdx.x & 31;
@@ -360,6 +428,7 @@ __global__ void __launch_bounds__(kMeanThreads)
                           int n, int d, int chunk, float *__restrict__ C_new, float *__restrict__ head,
                           float *__restrict__ tail, int32_t *__restrict__ tailc) {
     extern __shared__ int32_t s_members[];  // [chunk] sample indices, then [chunk] labels
+    griddep_wait();
     int32_t *s_perm = s_members;
     uint32_t *s_lab = reinterpret_cast<uint32_t *>(s_members + chunk);
     const int c = blockIdx.x;
@@ -472,12 +541,21 @@ __global__ void __launch_bounds__(kMeanThreads)
 // Fix-up of the counting path: block c finishes the cluster that leaves
 // chunk c (its tail partial plus the head partials of the chunks it covers, in
 // chunk order); every block then copies the old row of empty clusters in its
-// stride and writes the counts.
-__global__ void __launch_bounds__(kMeanThreads)
+// stride and writes the counts.  A thread keeps kFixUnroll column groups (four
+// columns each when VEC) in flight at once.
+constexpr int kFixThreads = 256;
+constexpr int kFixUnroll = 4;
+
+template <bool VEC>
+__global__ void __launch_bounds__(kFixThreads)
     mean_fixup_chunks_kernel(const int32_t *__restrict__ offsets, const int32_t *__restrict__ totals,
                              const float *__restrict__ head, const float *__restrict__ tail,
                              const int32_t *__restrict__ tailc, int n_chunks, const float *__restrict__ C_old,
                              float *__restrict__ C_new, int32_t *__restrict__ counts_out, int k, int d, int chunk) {
+    using V = typename std::conditional<VEC, float4, float>::type;
+    griddep_wait();
+    constexpr int W = VEC ? 4 : 1;
+    const int dv = d / W;  // VEC: d % 4 == 0
     for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
         const int j = tailc[c];
         if (j < 0) continue;
@@ -485,33 +563,59 @@ __global__ void __launch_bounds__(kMeanThreads)
         const int seg1 = offsets[j + 1];
         const int ce = (seg1 - 1) / chunk;
         const float cnt = (float)(seg1 - seg0);
-        // columns in groups of 4 per thread, each group's partials loaded before the adds
-        for (int f0 = threadIdx.x * 4; f0 < d; f0 += kMeanThreads * 4) {
-            float s[4], cmp[4] = {0.f, 0.f, 0.f, 0.f};
+        const V *tl = reinterpret_cast<const V *>(tail + (size_t)c * d);
+        V *out = reinterpret_cast<V *>(C_new + (size_t)j * d);
+        for (int g0 = threadIdx.x; g0 < dv; g0 += kFixThreads * kFixUnroll) {
+            float s[kFixUnroll][W], cmp[kFixUnroll][W];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) s[u] = f0 + u < d ? tail[(size_t)c * d + f0 + u] : 0.f;
+            for (int u = 0; u < kFixUnroll; ++u) {
+                const int g = g0 + u * kFixThreads;
+                V x;
+                if (g < dv) x = tl[g]; else x = V{};
+                const float *xf = reinterpret_cast<const float *>(&x);
+#pragma unroll
+                for (int e = 0; e < W; ++e) {
+                    s[u][e] = xf[e];
+                    cmp[u][e] = 0.f;
+                }
+            }
             for (int cc = c + 1; cc <= ce; ++cc) {
-                float v[4];
+                const V *hd = reinterpret_cast<const V *>(head + (size_t)cc * d);
+                V v[kFixUnroll];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = f0 + u < d ? head[(size_t)cc * d + f0 + u] : 0.f;
+                for (int u = 0; u < kFixUnroll; ++u) {
+                    const int g = g0 + u * kFixThreads;
+                    if (g < dv) v[u] = hd[g]; else v[u] = V{};
+                }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float y = v[u] - cmp[u];
-                    const float t = s[u] + y;
-                    cmp[u] = (t - s[u]) - y;
-                    s[u] = t;
+                for (int u = 0; u < kFixUnroll; ++u) {
+                    const float *vf = reinterpret_cast<const float *>(&v[u]);
+#pragma unroll
+                    for (int e = 0; e < W; ++e) {
+                        const float y = vf[e] - cmp[u][e];
+                        const float t = s[u][e] + y;
+                        cmp[u][e] = (t - s[u][e]) - y;
+                        s[u][e] = t;
+                    }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (f0 + u < d) C_new[(size_t)j * d + f0 + u] = (s[u] - cmp[u]) / cnt;
+            for (int u = 0; u < kFixUnroll; ++u) {
+                const int g = g0 + u * kFixThreads;
+                if (g >= dv) continue;
+                V r;
+                float *rf = reinterpret_cast<float *>(&r);
+#pragma unroll
+                for (int e = 0; e < W; ++e) rf[e] = (s[u][e] - cmp[u][e]) / cnt;
+                out[g] = r;
+            }
         }
     }
     for (int j = blockIdx.x; j < k; j += gridDim.x) {
         const int cnt = totals[j];
         if (counts_out && threadIdx.x == 0) counts_out[j] = cnt;
         if (cnt == 0 && C_new != C_old)
-            for (int f = threadIdx.x; f < d; f += kMeanThreads) C_new[(size_t)j * d + f] = C_old[(size_t)j * d + f];
+            for (int f = threadIdx.x; f < d; f += kFixThreads) C_new[(size_t)j * d + f] = C_old[(size_t)j * d + f];
     }
 }
 
@@ -565,25 +669,37 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
         const int ut = (int)L.n_utiles;
         const size_t csmem = (size_t)k * 4;
         set_counting_smem_limits(k);
+        cudaError_t e = cudaSuccess;
+        // the first kernel of a standalone update starts the ordinary way
         if (!tile_counts_ready)
-            upd_tile_count_kernel<<<ut, 256, csmem, s>>>(labels, (int)n, (int)k, (int)L.utile, table, status, hdr,
-                                                         clear_header ? 1 : 0);
-        upd_col_prefix_kernel<<<(int)((k + kPrefixCols - 1) / kPrefixCols), kCountingTiles, 0, s>>>(table, (int)k,
-                                                                                                   counts);
-        exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, offsets, k, offsets + k);
-        upd_tile_scatter_kernel<<<ut, 256, csmem, s>>>(labels, (int)n, (int)k, (int)L.utile, table, offsets, perm,
-                                                       slab, status);
-        if (vec)
-            segmented_mean_kernel<true><<<mgrid, kMeanThreads, msmem, s>>>(X, perm, slab, offsets, (int)n, (int)d,
-                                                                           (int)L.chunk, C_new, head, tail, tailc);
-        else
-            segmented_mean_kernel<false><<<mgrid, kMeanThreads, msmem, s>>>(X, perm, slab, offsets, (int)n, (int)d,
-                                                                            (int)L.chunk, C_new, head, tail, tailc);
+            e = launch_kernel(!clear_header, upd_tile_count_kernel, dim3(ut), dim3(256), csmem, s, labels, (int)n,
+                              (int)k, (int)L.utile, table, status, hdr, clear_header ? 1 : 0);
+        if (e == cudaSuccess)
+            e = launch_kernel(true, upd_col_prefix_kernel, dim3((unsigned)((k + kPrefixCols - 1) / kPrefixCols)),
+                              dim3(kCountingTiles), 0, s, table, (int)k, counts, offsets, hdr);
+        if (e == cudaSuccess)
+            e = launch_kernel(true, upd_tile_scatter_kernel, dim3(ut), dim3(256), csmem, s, labels, (int)n, (int)k,
+                              (int)L.utile, (const int32_t *)table, (const int32_t *)offsets, perm, slab, status);
+        trace_mark(kTraceUpdateMean, false, s);
+        if (e == cudaSuccess)
+            e = vec ? launch_kernel(true, segmented_mean_kernel<true>, mgrid, dim3(kMeanThreads), msmem, s, X,
+                                    (const int32_t *)perm, (const uint32_t *)slab, (const int32_t *)offsets, (int)n,
+                                    (int)d, (int)L.chunk, C_new, head, tail, tailc)
+                    : launch_kernel(true, segmented_mean_kernel<false>, mgrid, dim3(kMeanThreads), msmem, s, X,
+                                    (const int32_t *)perm, (const uint32_t *)slab, (const int32_t *)offsets, (int)n,
+                                    (int)d, (int)L.chunk, C_new, head, tail, tailc);
+        trace_mark(kTraceUpdateMean, true, s);
         const int fgrid = (int)(L.n_chunks > 256 ? L.n_chunks : 256);
-        mean_fixup_chunks_kernel<<<fgrid, kMeanThreads, 0, s>>>(offsets, counts, head, tail, tailc, (int)L.n_chunks,
-                                                               C_old, C_new, counts_out, (int)k, (int)d,
-                                                               (int)L.chunk);
-        return cudaGetLastError();
+        if (e == cudaSuccess)
+            e = vec ? launch_kernel(true, mean_fixup_chunks_kernel<true>, dim3(fgrid), dim3(kFixThreads), 0, s,
+                                    (const int32_t *)offsets, (const int32_t *)counts, (const float *)head,
+                                    (const float *)tail, (const int32_t *)tailc, (int)L.n_chunks, C_old, C_new,
+                                    counts_out, (int)k, (int)d, (int)L.chunk)
+                    : launch_kernel(true, mean_fixup_chunks_kernel<false>, dim3(fgrid), dim3(kFixThreads), 0, s,
+                                    (const int32_t *)offsets, (const int32_t *)counts, (const float *)head,
+                                    (const float *)tail, (const int32_t *)tailc, (int)L.n_chunks, C_old, C_new,
+                                    counts_out, (int)k, (int)d, (int)L.chunk);
+        return e;
     }
 
     update_clear_kernel<<<(int)((k + 255) / 256 < 1024 ? (k + 255) / 256 : 1024), 256, 0, s>>>(
@@ -607,12 +723,14 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
     // counts -> offsets (k + 1 entries: the scan writes the total at [k])
     exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, offsets, k, offsets + k);
 
+    trace_mark(kTraceUpdateMean, false, s);
     if (vec)
         segmented_mean_kernel<true><<<mgrid, kMeanThreads, msmem, s>>>(X, vin, kin, offsets, (int)n, (int)d,
                                                                        (int)L.chunk, C_new, head, tail, nullptr);
     else
         segmented_mean_kernel<false><<<mgrid, kMeanThreads, msmem, s>>>(X, vin, kin, offsets, (int)n, (int)d,
                                                                         (int)L.chunk, C_new, head, tail, nullptr);
+    trace_mark(kTraceUpdateMean, true, s);
     const int fix_grid = (int)(k < 4096 ? k : 4096);
     mean_fixup_kernel<<<fix_grid, kMeanThreads, 0, s>>>(offsets, head, tail, C_old, C_new, counts_out, (int)k,
                                                        (int)d, (int)L.chunk);
@@ -622,11 +740,11 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
 cudaError_t launch_finalize_counting(int64_t n, int64_t k, const AssignLayout &A, const UpdateLayout &U,
                                      uint8_t *ws, int64_t *labels, float *best, double *inertia, cudaStream_t s) {
     set_counting_smem_limits(k);
-    fin_tile_count_kernel<<<(int)U.n_utiles, kFinCountThreads, (size_t)k * 4, s>>>(
-        reinterpret_cast<const unsigned long long *>(ws + A.off_keys), reinterpret_cast<const float *>(ws + A.off_xnorm),
-        (int)n, (int)k, (int)U.utile, labels, best, inertia, reinterpret_cast<double *>(ws + U.off_fin_partial),
-        reinterpret_cast<int32_t *>(ws + U.off_table), reinterpret_cast<WsHeader *>(ws));
-    return cudaGetLastError();
+    return launch_kernel(true, fin_tile_count_kernel, dim3((unsigned)U.n_utiles), dim3(kFinCountThreads),
+                         (size_t)k * 4, s, reinterpret_cast<const unsigned long long *>(ws + A.off_keys),
+                         reinterpret_cast<const float *>(ws + A.off_xnorm), (int)n, (int)k, (int)U.utile, labels,
+                         best, inertia, reinterpret_cast<double *>(ws + U.off_fin_partial),
+                         reinterpret_cast<int32_t *>(ws + U.off_table), reinterpret_cast<WsHeader *>(ws));
 }
 
 }  // namespace km

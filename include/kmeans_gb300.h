@@ -176,6 +176,33 @@ int kmeans_assign_noalloc(const float *X, const float *C, int64_t n, int64_t k, 
                           int64_t *labels, float *best_dist, double *inertia, uint64_t seed,
                           void *stream);
 
+/* Kernel timing for measurement tools (the pages have no counterpart: it
+ * exists to hold each kernel against its roofline).
+ * kmeans_trace_start(capacity) turns tracing on and clears earlier records.
+ * From then on every call brackets its dominant kernel with a pair of CUDA
+ * events recorded on the call's stream: the tensor-core assignment kernel
+ * (kmeans_assign, kmeans_lloyd_iter, kmeans_assign_noalloc), the segmented
+ * mean of the update (kmeans_update, kmeans_lloyd_iter) and the distance pass
+ * of k-means++ seeding (kmeanspp_init).  Each kernel kind has `capacity`
+ * event pairs (1 <= capacity <= KMEANS_TRACE_MAX_CAPACITY), created on the
+ * current device; launches beyond the capacity are counted, not timed.
+ * kmeans_trace_read waits for the recorded events of one kind and returns the
+ * summed durations (milliseconds; each includes the kernel's launch latency
+ * on the device), the number of timed launches and of all launches seen
+ * (either count pointer may be NULL).  kmeans_trace_stop turns tracing off and
+ * releases the events.  Tracing adds two stream operations per traced
+ * launch; do not trace while a stream is being captured.  Start, read and
+ * stop must not race with each other. */
+#define KMEANS_TRACE_MAX_CAPACITY 65536
+enum {
+    KMEANS_KERNEL_ASSIGN_TC = 0,
+    KMEANS_KERNEL_UPDATE_MEAN = 1,
+    KMEANS_KERNEL_KMEANSPP_DIST = 2
+};
+int kmeans_trace_start(int capacity);
+int kmeans_trace_read(int kernel, double *ms_total, int64_t *timed_launches, int64_t *launches);
+int kmeans_trace_stop(void);
+
 /* Build identification of the library: target architecture, tile shapes and
  * pipeline depth (static storage). */
 const char *kmeans_build_info(void);
