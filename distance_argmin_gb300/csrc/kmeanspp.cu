@@ -151,6 +151,7 @@ __global__ void kpp_pick_kernel(const double *__restrict__ bsum, int64_t n_block
 namespace kd {
 constexpr int KT = kKppGroupTrials;  // trial candidates per pass over X
 constexpr int ROWS = 2;              // samples per warp at a time
+constexpr int MIN_BLOCKS = 3;        // resident blocks per SM (64 KiB of candidates each)
 constexpr int WARPS = 8;
 constexpr int THREADS = WARPS * 32;
 constexpr int GROUP = WARPS * ROWS;
@@ -170,19 +171,33 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     e = (a - (s - bb)) + (b - bb);
 }
 
-// Warp sum of double-float values (hi + lo) with a butterfly: every level
-// adds exactly with TwoSum and renormalises, so the result keeps about 44 bits
-// and is the same on every lane (each step is symmetric in its operands).
-__device__ __forceinline__ void lane_sum_double_float(float &hi, float &lo) {
+// (hi, lo) += (ohi, olo) in double-float: TwoSum of the high parts, the low
+// parts added to its error, renormalised.  Symmetric in its operands, so two
+// lanes that add each other's values get the same bits.
+__device__ __forceinline__ void df_add(float &hi, float &lo, float ohi, float olo) {
+    float s, e;
+    two_sum(hi, ohi, s, e);
+    e += lo + olo;
+    hi = s + e;
+    lo = e - (hi - s);
+}
+
+// One reduce-scatter level over 2H double-float values: the lane whose `bit`
+// is set keeps the upper half, its partner (lane ^ bit) the lower half; each
+// sends the half it drops and adds the half it receives.  Values 0..H-1 hold
+// the result.
+template <int N, int H>
+__device__ __forceinline__ void reduce_scatter_level(float (&hi)[N], float (&lo)[N], int lane, int bit) {
+    const bool up = (lane & bit) != 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ohi = __shfl_xor_sync(0xffffffffu, hi, o);
-        const float olo = __shfl_xor_sync(0xffffffffu, lo, o);
-        float s, e;
-        two_sum(hi, ohi, s, e);
-        e += lo + olo;
-        hi = s + e;
-        lo = e - (hi - s);
+    for (int i = 0; i < H; ++i) {
+        const float kh = up ? hi[H + i] : hi[i], kl = up ? lo[H + i] : lo[i];
+        const float sh = up ? hi[i] : hi[H + i], sl = up ? lo[i] : lo[H + i];
+        const float rh = __shfl_xor_sync(0xffffffffu, sh, bit);
+        const float rl = __shfl_xor_sync(0xffffffffu, sl, bit);
+        hi[i] = kh;
+        lo[i] = kl;
+        df_add(hi[i], lo[i], rh, rl);
     }
 }
 
@@ -209,7 +224,7 @@ __device__ __forceinline__ void load8(const float *__restrict__ p, int avail, fl
 // Differences and squares use the packed two-float instructions; each run of
 // 8 features is added to a compensated per-lane sum.
 template <bool VEC>
-__global__ void __launch_bounds__(kd::THREADS, 3)
+__global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand, int T,
                          int t0, int W, float2 *__restrict__ dpart) {
     extern __shared__ __align__(16) float cs[];  // [KT][W], negated
@@ -235,22 +250,19 @@ __global__ void __launch_bounds__(kd::THREADS, 3)
         for (int r = 0; r < kd::ROWS; ++r)
 #pragma unroll
             for (int t = 0; t < kd::KT; ++t) s[r][t] = c[r][t] = 0.f;
-        // the next step's samples are loaded before this step's arithmetic
-        float2 x[kd::ROWS][4], xn[kd::ROWS][4];
-        auto fetch = [&](int f, float2 (&dst)[kd::ROWS][4]) {
+        // no register prefetch of the next step: with it the kernel spills and
+        // runs slower; the other resident warps hide the load latency
+        float2 x[kd::ROWS][4];
+        for (int f = lane * 8; f < width; f += 256) {
 #pragma unroll
             for (int r = 0; r < kd::ROWS; ++r) {
-                if (r0 + r < n && f < width) {
-                    load8<VEC>(X + (r0 + r) * (int64_t)d + fb + f, width - f, dst[r]);
+                if (r0 + r < n) {
+                    load8<VEC>(X + (r0 + r) * (int64_t)d + fb + f, width - f, x[r]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) dst[r][e] = make_float2(0.f, 0.f);
+                    for (int e = 0; e < 4; ++e) x[r][e] = make_float2(0.f, 0.f);
                 }
             }
-        };
-        fetch(lane * 8, x);
-        for (int f = lane * 8; f < width; f += 256) {
-            fetch(f + 256, xn);
 #pragma unroll
             for (int t = 0; t < kd::KT; ++t) {
                 const float4 ca = *reinterpret_cast<const float4 *>(&cs[t * W + f]);
@@ -269,23 +281,42 @@ __global__ void __launch_bounds__(kd::THREADS, 3)
                     kahan(s[r][t], c[r][t], run.x + run.y);
                 }
             }
-#pragma unroll
-            for (int r = 0; r < kd::ROWS; ++r)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) x[r][e] = xn[r][e];
         }
-        // lanes -> one partial per (row, trial): a double-float butterfly in
-        // float32 (the float64 pipe of this part is far too slow for it)
+        // lanes -> one partial per (row, trial), as double-float values in
+        // float32 (the float64 pipe of this part is far too slow for it).  A
+        // reduce-scatter over the ROWS x KT sums: at each level (lane xor 16,
+        // 8, 4, 2) a lane keeps half of its values, sends the other half to
+        // its partner and adds what it receives; the last level (xor 1) is a
+        // full exchange.  Every sum gets the same pairing tree as a full
+        // butterfly, with far fewer shuffles and additions.
+        constexpr int NS = kd::ROWS * kd::KT;
+        static_assert(NS == 16 || NS == 32, "the reduce-scatter below handles 16 or 32 sums");
+        float hi[NS], lo[NS];
 #pragma unroll
-        for (int r = 0; r < kd::ROWS; ++r) {
-            const int64_t row = r0 + r;
+        for (int r = 0; r < kd::ROWS; ++r)
 #pragma unroll
             for (int t = 0; t < kd::KT; ++t) {
-                float hi = s[r][t], lo = -c[r][t];
-                lane_sum_double_float(hi, lo);
-                if (lane == 0 && t < nt && row < n) dpart[((int64_t)slice * kd::KT + t) * n + row] = make_float2(hi, lo);
+                hi[r * kd::KT + t] = s[r][t];
+                lo[r * kd::KT + t] = -c[r][t];
             }
+        reduce_scatter_level<NS, NS / 2>(hi, lo, lane, 16);
+        reduce_scatter_level<NS, NS / 4>(hi, lo, lane, 8);
+        reduce_scatter_level<NS, NS / 8>(hi, lo, lane, 4);
+        reduce_scatter_level<NS, NS / 16>(hi, lo, lane, 2);
+        if constexpr (NS == 32) {
+            reduce_scatter_level<NS, 1>(hi, lo, lane, 1);
+        } else {
+            const float ohi = __shfl_xor_sync(0xffffffffu, hi[0], 1);
+            const float olo = __shfl_xor_sync(0xffffffffu, lo[0], 1);
+            df_add(hi[0], lo[0], ohi, olo);
         }
+        // lane l holds sum v = row * KT + trial: v = l (32 sums) or l / 2 (16
+        // sums, held by both lanes of a pair)
+        const int v = NS == 32 ? lane : lane >> 1;
+        const int t = v % kd::KT;
+        const int64_t row = r0 + v / kd::KT;
+        if ((NS == 32 || (lane & 1) == 0) && t < nt && row < n)
+            dpart[((int64_t)slice * kd::KT + t) * n + row] = make_float2(hi[0], lo[0]);
     }
 }
 
