@@ -222,7 +222,7 @@ struct KppLayout {
     int T;
     int64_t n_blocks;     // 1024-sample blocks of the scan / potential reductions
     int S;                // feature slices (the distance pass splits d so a slice of the candidates stays resident)
-    int W;                // features per slice (multiple of 8)
+    int W;                // features per slice (multiple of 256: whole 256-feature steps of the distance pass)
     int64_t off_d2;       // n x f64 current D^2
     int64_t off_dist;     // T x n x f64 distances to the trial candidates
     int64_t off_dpart;    // S x 8 x n x (f32 hi, f32 lo) per-slice partial distances of one pass
@@ -238,7 +238,7 @@ inline KppLayout kpp_layout(int64_t n, int64_t d, int T) {
     L.T = T;
     L.n_blocks = (n + kKppScanBlock - 1) / kKppScanBlock;
     L.S = (int)((d + kKppSliceFloats - 1) / kKppSliceFloats);
-    L.W = (int)align_up((d + L.S - 1) / L.S, 8);
+    L.W = (int)align_up((d + L.S - 1) / L.S, 256);
     int64_t o = sizeof(WsHeader);
     o = align_up(o, 1024); L.off_d2 = o; o += n * 8;
     o = align_up(o, 1024); L.off_dist = o; o += (int64_t)T * n * 8;

@@ -201,19 +201,24 @@ __device__ __forceinline__ void reduce_scatter_level(float (&hi)[N], float (&lo)
     }
 }
 
+// Features p[0..3] and p[128..131] of a row (zeros past `avail`, the
+// features left in the slice from p on).
 template <bool VEC>
-__device__ __forceinline__ void load8(const float *__restrict__ p, int avail, float2 (&v)[4]) {
-    if (VEC && avail >= 8) {
+__device__ __forceinline__ void load4x2(const float *__restrict__ p, int avail, float2 (&v)[4]) {
+    if (VEC && avail >= 132) {
         const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(p + 4));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p + 128));
         v[0] = make_float2(a.x, a.y);
         v[1] = make_float2(a.z, a.w);
         v[2] = make_float2(b.x, b.y);
         v[3] = make_float2(b.z, b.w);
     } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
+        for (int e = 0; e < 2; ++e) {
             v[e] = make_float2(2 * e < avail ? __ldg(p + 2 * e) : 0.f, 2 * e + 1 < avail ? __ldg(p + 2 * e + 1) : 0.f);
+            v[2 + e] = make_float2(128 + 2 * e < avail ? __ldg(p + 128 + 2 * e) : 0.f,
+                                   128 + 2 * e + 1 < avail ? __ldg(p + 128 + 2 * e + 1) : 0.f);
+        }
     }
 }
 
@@ -222,7 +227,7 @@ __device__ __forceinline__ void load8(const float *__restrict__ p, int avail, fl
 // The block stages its slice of the candidates (negated) in shared memory once
 // and then streams its share of the samples, each sample read exactly once.
 // Differences and squares use the packed two-float instructions; each run of
-// 8 features is added to a compensated per-lane sum.
+// a lane's 8 features of a step is added to a compensated per-lane sum.
 template <bool VEC>
 __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand, int T,
@@ -253,11 +258,16 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
         // no register prefetch of the next step: with it the kernel spills and
         // runs slower; the other resident warps hide the load latency
         float2 x[kd::ROWS][4];
-        for (int f = lane * 8; f < width; f += 256) {
+        // a lane owns features f .. f+3 and f+128 .. f+131 of each 256-feature
+        // step, so every 16-byte load of the warp (global and shared) covers
+        // 512 contiguous bytes
+        for (int f0 = 0; f0 < width; f0 += 256) {
+            const int f = f0 + lane * 4;
 #pragma unroll
             for (int r = 0; r < kd::ROWS; ++r) {
+                const float *xp = X + (r0 + r) * (int64_t)d + fb + f;
                 if (r0 + r < n) {
-                    load8<VEC>(X + (r0 + r) * (int64_t)d + fb + f, width - f, x[r]);
+                    load4x2<VEC>(xp, width - f, x[r]);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) x[r][e] = make_float2(0.f, 0.f);
@@ -266,7 +276,7 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
 #pragma unroll
             for (int t = 0; t < kd::KT; ++t) {
                 const float4 ca = *reinterpret_cast<const float4 *>(&cs[t * W + f]);
-                const float4 cb = *reinterpret_cast<const float4 *>(&cs[t * W + f + 4]);
+                const float4 cb = *reinterpret_cast<const float4 *>(&cs[t * W + f + 128]);
                 const float2 nc[4] = {make_float2(ca.x, ca.y), make_float2(ca.z, ca.w), make_float2(cb.x, cb.y),
                                       make_float2(cb.z, cb.w)};
 #pragma unroll
