@@ -86,9 +86,16 @@ constexpr int BAR_BASE = A_BASE + SA * A_STAGE;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = BAR_BASE + BAR_BYTES + 1024;  // + alignment slack
 constexpr int TX_BYTES = XB_STAGE;
-constexpr int ACC_MAIN = 0;                    // tensor-memory columns
+constexpr int ACC_MAIN = 0;                    // tensor-memory columns (separate accumulators)
 constexpr int ACC_CORR = BN;
-constexpr int TMEM_COLS = 2 * BN;
+constexpr int TMEM_COLS = 2 * BN;              // either main + corrections, or two single accumulators
+// Up to this many features the three products share one accumulator per
+// tile and the accumulators are double-buffered, so the epilogue of one tile
+// overlaps the MMAs of the next.  The tensor cores' truncating float32
+// accumulation then costs about 6e-9 * d relative (measured 1.01e-4 at
+// d = 16384); beyond this size the correction products keep their own
+// accumulator (single-buffered), which is about 3x more accurate.
+constexpr int SINGLE_ACC_MAX_D = 4096;
 constexpr int GROUP_M = 8;                     // pair sample blocks per raster band
 constexpr uint32_t SBO_64B = 8 * 64;           // 8 rows x 64 bytes per swizzle atom
 constexpr uint16_t PAIR_MASK = 0x3;
@@ -97,7 +104,7 @@ static_assert(SPLIT_WARPS % 4 == 0 && WARP_EPI % 4 == 0, "epilogue warps start o
 static_assert(SMEM_BYTES <= 232448, "fits the 227 KiB opt-in limit");
 // barrier slots
 constexpr int XB_FULL = 0, XB_EMPTY = SXB, A_FULL = 2 * SXB, A_EMPTY = 2 * SXB + SA;
-constexpr int T_FULL = 2 * SXB + 2 * SA, T_EMPTY = T_FULL + 1, DRAIN = T_FULL + 2, NUM_BARS = T_FULL + 3;
+constexpr int T_FULL = 2 * SXB + 2 * SA, T_EMPTY = T_FULL + 2, DRAIN = T_FULL + 4, NUM_BARS = T_FULL + 5;  // 2 accumulator slots
 static_assert(NUM_BARS * 8 + 16 <= BAR_BYTES, "barriers fit");
 }  // namespace tc
 
@@ -176,6 +183,7 @@ __device__ __forceinline__ void split_kblock(const uint8_t *xs, uint8_t *ahi, in
     }
 }
 
+template <bool DB>  // DB: one accumulator per tile, double-buffered (d <= SINGLE_ACC_MAX_D)
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     assign_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmChi,
                      const __grid_constant__ CUtensorMap tmClo, const TcParams p) {
@@ -203,8 +211,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             mbar_init(bar(tc::A_FULL + s), 2 * tc::SPLIT_WARPS);  // split warps of both CTAs (even CTA's copy)
             mbar_init(bar(tc::A_EMPTY + s), 1);
         }
-        mbar_init(bar(tc::T_FULL), 1);
-        mbar_init(bar(tc::T_EMPTY), 2 * tc::EPI_WARPS);  // epilogue warps of both CTAs (even CTA's copy)
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(tc::T_FULL + b), 1);
+            mbar_init(bar(tc::T_EMPTY + b), 2 * tc::EPI_WARPS);  // epilogue warps of both CTAs (even CTA's copy)
+        }
         mbar_init(bar(tc::DRAIN), 1);
         fence_barrier_init();
     }
@@ -265,13 +275,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;              // tensor-memory lane quarter this warp may read
         const int part = (warp - tc::WARP_EPI) >> 2;  // which EPI_COLS of the tile's 256 columns
-        const uint32_t t_empty = map_to_cta(bar(tc::T_EMPTY), 0);
         int tile_iter = 0;
         for (int tile = pair; tile < p.num_tiles; tile += num_pairs, ++tile_iter) {
             int mb, nb;
             tile_coords(tile, p.num_m, p.num_n, mb, nb);
-            if (!mbar_wait_warp(bar(tc::T_FULL), tile_iter & 1, p.status)) break;
+            const int buf = DB ? (tile_iter & 1) : 0;
+            const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (tile_iter & 1);
+            if (!mbar_wait_warp(bar(tc::T_FULL + buf), phase, p.status)) break;
             tc_fence_after();
+            const uint32_t acc_base = tmem_base + (DB ? (uint32_t)(buf * tc::BN) : (uint32_t)tc::ACC_MAIN);
             const int n0 = nb * tc::BN + part * tc::EPI_COLS;
             float best = __int_as_float(0x7f800000);  // +inf
             int arg = -1;
@@ -281,18 +293,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 if (j0 >= p.k) break;
                 const uint32_t col = (uint32_t)(part * tc::EPI_COLS + ch * tc::EPI_CHUNK);
                 const uint32_t lanes = (uint32_t)(q * 32) << 16;
+                // x.c of this chunk's columns: one accumulator, or main + corrections
                 float vm[tc::EPI_CHUNK], vc[tc::EPI_CHUNK];
-                tmem_ld_pair<tc::EPI_CHUNK>(tmem_base + lanes + tc::ACC_MAIN + col,
-                                            tmem_base + lanes + tc::ACC_CORR + col, vm, vc);
+                if constexpr (DB) {
+                    tmem_ld_one<tc::EPI_CHUNK>(acc_base + lanes + col, vm);
+                } else {
+                    tmem_ld_pair<tc::EPI_CHUNK>(acc_base + lanes + col, tmem_base + lanes + tc::ACC_CORR + col, vm, vc);
+#pragma unroll
+                    for (int u = 0; u < tc::EPI_CHUNK; ++u) vm[u] += vc[u];
+                }
                 const float4 *cn4 = reinterpret_cast<const float4 *>(p.cnorm + j0);
                 if (j0 + tc::EPI_CHUNK <= p.k) {
 #pragma unroll
                     for (int u4 = 0; u4 < tc::EPI_CHUNK / 4; ++u4) {
                         const float4 cn = __ldg(cn4 + u4);
-                        const float s0 = fmaf(-2.f, vm[4 * u4 + 0] + vc[4 * u4 + 0], cn.x);
-                        const float s1 = fmaf(-2.f, vm[4 * u4 + 1] + vc[4 * u4 + 1], cn.y);
-                        const float s2 = fmaf(-2.f, vm[4 * u4 + 2] + vc[4 * u4 + 2], cn.z);
-                        const float s3 = fmaf(-2.f, vm[4 * u4 + 3] + vc[4 * u4 + 3], cn.w);
+                        const float s0 = fmaf(-2.f, vm[4 * u4 + 0], cn.x);
+                        const float s1 = fmaf(-2.f, vm[4 * u4 + 1], cn.y);
+                        const float s2 = fmaf(-2.f, vm[4 * u4 + 2], cn.z);
+                        const float s3 = fmaf(-2.f, vm[4 * u4 + 3], cn.w);
                         if (s0 < best) { best = s0; arg = j0 + 4 * u4 + 0; }
                         if (s1 < best) { best = s1; arg = j0 + 4 * u4 + 1; }
                         if (s2 < best) { best = s2; arg = j0 + 4 * u4 + 2; }
@@ -302,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
 #pragma unroll
                     for (int u = 0; u < tc::EPI_CHUNK; ++u) {
                         if (j0 + u < p.k) {
-                            const float s = fmaf(-2.f, vm[u] + vc[u], __ldg(p.cnorm + j0 + u));
+                            const float s = fmaf(-2.f, vm[u], __ldg(p.cnorm + j0 + u));
                             if (s < best) { best = s; arg = j0 + u; }
                         }
                     }
@@ -310,7 +328,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(t_empty);
+            if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(tc::T_EMPTY + buf), 0));
             const int row = mb * (2 * tc::BM) + (int)rank * tc::BM + q * 32 + lane;
             if (row < p.n && arg >= 0) atomicMin(p.keys + row, make_key(best, (uint32_t)arg));
         }
@@ -355,8 +373,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             int it = 0, tile_iter = 0;
             bool ok = true;
             for (int tile = pair; tile < p.num_tiles && ok; tile += num_pairs, ++tile_iter) {
-                if (!mbar_wait_cluster(bar(tc::T_EMPTY), (tile_iter & 1) ^ 1, p.status)) break;
+                const int buf = DB ? (tile_iter & 1) : 0;
+                const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (tile_iter & 1);
+                if (!mbar_wait_cluster(bar(tc::T_EMPTY + buf), phase ^ 1, p.status)) break;
                 tc_fence_after();
+                const uint32_t dm = DB ? tmem_base + (uint32_t)(buf * tc::BN) : d_main;
+                const uint32_t dc = DB ? dm : d_corr;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                     const int s = it % tc::SXB;
                     const int as = it % tc::SA;
@@ -377,15 +399,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                         const uint64_t dbh = umma_smem_desc(bhi + kk * 32, tc::SBO_64B, kLayoutSW64);
                         const uint64_t dbl = umma_smem_desc(blo + kk * 32, tc::SBO_64B, kLayoutSW64);
                         const uint32_t first = (kb | kk) != 0 ? 1u : 0u;
-                        mma_bf16_ss_pair(d_main, dah, dbh, idesc, first);
-                        mma_bf16_ss_pair(d_corr, dal, dbh, idesc, first);
-                        mma_bf16_ss_pair(d_corr, dah, dbl, idesc, 1u);
+                        mma_bf16_ss_pair(dm, dah, dbh, idesc, first);
+                        mma_bf16_ss_pair(dc, dal, dbh, idesc, DB ? 1u : first);
+                        mma_bf16_ss_pair(dc, dah, dbl, idesc, 1u);
                     }
                     mma_commit_pair_multicast(bar(tc::XB_EMPTY + s), tc::PAIR_MASK);
                     mma_commit_pair_multicast(bar(tc::A_EMPTY + as), tc::PAIR_MASK);
                 }
                 if (!ok) break;
-                mma_commit_pair_multicast(bar(tc::T_FULL), tc::PAIR_MASK);
+                mma_commit_pair_multicast(bar(tc::T_FULL + buf), tc::PAIR_MASK);
             }
             // no MMA may still be writing tensor memory when it is released
             mma_commit_pair(bar(tc::DRAIN));
@@ -467,7 +489,7 @@ static int resident_pairs() {
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&clusters, assign_tc_kernel, &cfg) != cudaSuccess || clusters < 1) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, assign_tc_kernel<true>, &cfg) != cudaSuccess || clusters < 1) {
             cudaGetLastError();  // clear
             clusters = device_sm_count() / 2;
         }
@@ -481,8 +503,11 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(assign_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(assign_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         tc::SMEM_BYTES);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(assign_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            tc::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
@@ -518,8 +543,12 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
     const int grid = 2 * (pairs > 0 ? pairs : 1);
     trace_mark(kTraceAssignTc, false, stream);
-    const cudaError_t e = launch_kernel(true, assign_tc_kernel, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,
-                                        tmX, tmChi, tmClo, p);
+    const cudaError_t e =
+        d <= tc::SINGLE_ACC_MAX_D
+            ? launch_kernel(true, assign_tc_kernel<true>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream, tmX,
+                            tmChi, tmClo, p)
+            : launch_kernel(true, assign_tc_kernel<false>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream, tmX,
+                            tmChi, tmClo, p);
     trace_mark(kTraceAssignTc, true, stream);
     return e;
 }

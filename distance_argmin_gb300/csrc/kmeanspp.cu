@@ -83,6 +83,7 @@ __device__ __forceinline__ double warp_incl_scan(double v, int lane) {
 // trial, so all trials see one consistent running sum.
 __global__ void kpp_pick_kernel(const double *__restrict__ bsum, int64_t n_blocks, const double *__restrict__ D2,
                                 int64_t n, uint64_t seed, uint64_t draw_base, int T, int64_t *__restrict__ cand) {
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int t = threadIdx.x >> 5;
     if (t >= T) return;
@@ -232,6 +233,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand, int T,
                          int t0, int W, float2 *__restrict__ dpart) {
+    griddep_wait();
     extern __shared__ __align__(16) float cs[];  // [KT][W], negated
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -336,6 +338,7 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
 __global__ void __launch_bounds__(kBsThreads)
     kpp_combine_kernel(const float2 *__restrict__ dpart, int S, int64_t n, int t0, const double *__restrict__ D2,
                        double *__restrict__ dist, double *__restrict__ bpot, int64_t n_blocks) {
+    griddep_wait();
     __shared__ double red[kBsThreads];
     const int t = blockIdx.y;
     const int64_t base = (int64_t)blockIdx.x * kKppScanBlock;
@@ -400,6 +403,7 @@ __global__ void __launch_bounds__(kBsThreads)
     kpp_update_kernel(const double *__restrict__ dist, const double *__restrict__ bpot, int T, int64_t n,
                       int64_t n_blocks, const int64_t *__restrict__ cand, int64_t *__restrict__ indices,
                       int64_t prev, int init, double *__restrict__ D2, double *__restrict__ bsum) {
+    griddep_wait();
     __shared__ double red[kBsThreads];
     int best = 0;
     if (!init) {
@@ -431,12 +435,14 @@ __global__ void __launch_bounds__(kBsThreads)
 // Winner of the last center.
 __global__ void kpp_select_last_kernel(const double *__restrict__ bpot, int T, int64_t n_blocks,
                                        const int64_t *__restrict__ cand, int64_t *__restrict__ indices, int64_t c) {
+    griddep_wait();
     const int best = select_best_trial(bpot, T, n_blocks);
     if (threadIdx.x == 0) indices[c] = cand[best];
 }
 
 __global__ void gather_rows_kernel(const float *__restrict__ X, const int64_t *__restrict__ idx, int64_t k, int d,
                                    float *__restrict__ out) {
+    griddep_wait();
     for (int64_t j = blockIdx.x; j < k; j += gridDim.x) {
         const float *src = X + idx[j] * (int64_t)d;
         for (int f = threadIdx.x; f < d; f += blockDim.x) out[j * (int64_t)d + f] = src[f];
@@ -474,35 +480,46 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
     if (gx > groups) gx = groups;
     const dim3 dgrid((unsigned)(gx < 1 ? 1 : gx), (unsigned)L.S);
 
+    // every kernel after the first is chained to the one before it (see
+    // launch_kernel); each waits for its predecessor before touching memory
+    cudaError_t e = cudaSuccess;
+    auto chain = [&](cudaError_t r) {
+        if (e == cudaSuccess) e = r;
+    };
     auto dist_pass = [&](int Tn, const double *d2) {
         for (int t0 = 0; t0 < Tn; t0 += kd::KT) {
             trace_mark(kTraceKppDist, false, s);
-            if (vec)
-                kpp_dist_part_kernel<true><<<dgrid, kd::THREADS, smem, s>>>(X, n, (int)d, cand, Tn, t0, L.W, dpart);
-            else
-                kpp_dist_part_kernel<false><<<dgrid, kd::THREADS, smem, s>>>(X, n, (int)d, cand, Tn, t0, L.W, dpart);
+            chain(vec ? launch_kernel(true, kpp_dist_part_kernel<true>, dgrid, dim3(kd::THREADS), smem, s, X, n,
+                                      (int)d, (const int64_t *)cand, Tn, t0, L.W, dpart)
+                      : launch_kernel(true, kpp_dist_part_kernel<false>, dgrid, dim3(kd::THREADS), smem, s, X, n,
+                                      (int)d, (const int64_t *)cand, Tn, t0, L.W, dpart));
             trace_mark(kTraceKppDist, true, s);
             const int nt = Tn - t0 < kd::KT ? Tn - t0 : kd::KT;
-            kpp_combine_kernel<<<dim3((unsigned)L.n_blocks, (unsigned)nt), kBsThreads, 0, s>>>(dpart, L.S, n, t0, d2,
-                                                                                              dist, bpot, L.n_blocks);
+            chain(launch_kernel(true, kpp_combine_kernel, dim3((unsigned)L.n_blocks, (unsigned)nt), dim3(kBsThreads), 0,
+                                s, (const float2 *)dpart, L.S, n, t0, d2, dist, bpot, L.n_blocks));
         }
     };
 
     kpp_first_kernel<<<1, 1, 0, s>>>(n, seed, cand, indices, hdr);
+    chain(cudaGetLastError());
     dist_pass(1, nullptr);  // distances to the first center
-    for (int64_t c = 1; c < k; ++c) {
-        kpp_update_kernel<<<(int)L.n_blocks, kBsThreads, 0, s>>>(dist, bpot, T, n, L.n_blocks, cand, indices, c - 1,
-                                                                 c == 1 ? 1 : 0, D2, bsum);
-        kpp_pick_kernel<<<1, 32 * T, 0, s>>>(bsum, L.n_blocks, D2, n, seed, 1 + (uint64_t)(c - 1) * (uint64_t)T, T,
-                                             cand);
+    for (int64_t c = 1; c < k && e == cudaSuccess; ++c) {
+        chain(launch_kernel(true, kpp_update_kernel, dim3((unsigned)L.n_blocks), dim3(kBsThreads), 0, s,
+                            (const double *)dist, (const double *)bpot, T, n, L.n_blocks, (const int64_t *)cand, indices,
+                            c - 1, c == 1 ? 1 : 0, D2, bsum));
+        chain(launch_kernel(true, kpp_pick_kernel, dim3(1), dim3(32 * T), 0, s, (const double *)bsum, L.n_blocks,
+                            (const double *)D2, n, seed, 1 + (uint64_t)(c - 1) * (uint64_t)T, T, cand));
         dist_pass(T, D2);
     }
-    if (k > 1) kpp_select_last_kernel<<<1, 256, 0, s>>>(bpot, T, L.n_blocks, cand, indices, k - 1);
+    if (k > 1)
+        chain(launch_kernel(true, kpp_select_last_kernel, dim3(1), dim3(256), 0, s, (const double *)bpot, T,
+                            L.n_blocks, (const int64_t *)cand, indices, k - 1));
     if (centers) {
         const int g = (int)(k < 4096 ? k : 4096);
-        gather_rows_kernel<<<g, 256, 0, s>>>(X, indices, k, (int)d, centers);
+        chain(launch_kernel(true, gather_rows_kernel, dim3(g), dim3(256), 0, s, X, (const int64_t *)indices, k, (int)d,
+                            centers));
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace km

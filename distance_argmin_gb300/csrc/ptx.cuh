@@ -243,6 +243,12 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[32
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+template <int W>
+__device__ __forceinline__ void tmem_ld_one(uint32_t taddr, float (&v)[W]) {
+    static_assert(W == 32, "32 columns");
+    tmem_ld_32x32b_x32(taddr, v);
+}
+
 // Two 32-column loads (e.g. two accumulators of the same rows) and one wait.
 __device__ __forceinline__ void tmem_ld_2x_32x32b_x32(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32]) {
     uint32_t r[64];

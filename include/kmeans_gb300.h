@@ -29,8 +29,12 @@
  *  - Precision: inputs must be finite.  The assignment contraction runs on the
  *    tensor cores as three bf16 products of an error-compensated split of
  *    each float32 operand (hi = bf16(v), lo = bf16(v - hi)) with float32
- *    accumulation; the reported distance is within 1e-4 * (||x||^2 + ||c||^2)
- *    of the exact one.  Ties between centroids go to the lowest index.
+ *    accumulation (up to d = 4096 the three products share one accumulator;
+ *    above, the two correction products keep their own, which is about three
+ *    times more accurate); the reported distance is within
+ *    1e-4 * (||x||^2 + ||c||^2) of the exact one for d up to about 16384 (the
+ *    error of the float32 tensor-core accumulation grows about linearly with
+ *    d).  Ties between centroids go to the lowest index.
  *  - Workspace: `ws` is a device buffer of at least
  *    kmeans_workspace_bytes(op, n, k, d) bytes, 256-byte aligned, owned by the
  *    caller.  Its size has no n*k term: no (n, k) buffer exists anywhere.

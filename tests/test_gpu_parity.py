@@ -264,6 +264,21 @@ def test_large_workload_one_iteration(gpu_lib, name):
     assert np.isfinite(bd).all() and (bd >= 0).all()
 
 
+@pytest.mark.parametrize("d", [4096, 4100])
+def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d):
+    # up to 4096 features the three split products share one double-buffered
+    # accumulator per tile; above, the corrections keep their own.  Several
+    # tiles per CTA pair, ragged sample and centroid tiles.
+    n, k = 20000, 700
+    X, _, _ = synth.planted_blobs(n, d, 64, seed=91)
+    C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=92)])
+    labels, best, inertia = gpu_lib.kmeans_assign(dev_tensor(X), dev_tensor(C))
+    rows = _sample_rows(n, 512, 93)
+    o_l, o_b, o_s, _ = oracle.assign(X[rows], C)
+    flips, worst = check_assign(X[rows], C, host(labels), host(best), o_l, o_b, o_s, rows=rows, what=f"d={d}")
+    print(f"d={d}: worst relative distance error {worst:.3e}, near-tie flips {flips} of {len(rows)}")
+
+
 @pytest.mark.slow
 def test_kmeanspp_workload_prefix(gpu_lib):
     w = synth.KMEANSPP
