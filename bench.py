@@ -377,13 +377,14 @@ def run_gb300(args):
         Cn = torch.empty_like(C0d)
         e2e_steps = max(1, min(steps, 50))
 
-        chunks = 16  # measured: 2 -> 3.03 ms, 4 -> 2.93, 8 -> 2.87, 16 -> 2.86 per step
-        parts_h = torch.empty(chunks, dtype=torch.float64).pin_memory()
+        slices = 16  # measured per step: 2 -> 3.00 ms, 4 -> 2.91, 8 -> 2.86, 16 -> 2.84
         copy_stream = torch.cuda.Stream(dev)
+        inertia_d = torch.empty(1, dtype=torch.float64, device=dev)
 
         def e2e_step():
-            km.kmeans_lloyd_iter_host(Xh, Ch, Xe, Ce, Cn, labels, best, counts, C_out_h, lab_h, parts_h,
-                                      chunks=chunks, ws=ws, copy_stream=copy_stream, stream=stream)
+            km.kmeans_lloyd_iter_host(Xh, Ch, Xe, Ce, Cn, labels, best, counts, C_out_h, lab_h, in_h,
+                                      slices=slices, ws=ws, inertia=inertia_d, copy_stream=copy_stream,
+                                      stream=stream)
 
         for _ in range(min(warm, 3)):
             e2e_step()
@@ -395,10 +396,11 @@ def run_gb300(args):
         barrier()
         t_e2e = ev0.elapsed_time(ev1) / 1e3 / e2e_steps
         e2e = {"value": flop / t_e2e / 1e12, "unit": "TFLOP/s", "ms_per_step": 1e3 * t_e2e,
-               "steps": e2e_steps, "pipeline": f"{chunks} row slices copied on a second stream, each assigned "
-                                               "as it lands; update; results copied back",
+               "steps": e2e_steps, "pipeline": f"kmeans_lloyd_iter_host: {slices} row slices copied on a second "
+                                               "stream, each assigned as it lands; finalize and update; C_new, "
+                                               "labels and inertia copied back",
                "h2d_bytes_per_step": int(Xh.numel() * 4 + Ch.numel() * 4),
-               "d2h_bytes_per_step": int(C_out_h.numel() * 4 + lab_h.numel() * 8 + parts_h.numel() * 8)}
+               "d2h_bytes_per_step": int(C_out_h.numel() * 4 + lab_h.numel() * 8 + in_h.numel() * 8)}
 
     # max over ranks
     times = torch.tensor([t_lloyd, t_assign, t_update, e2e["ms_per_step"] / 1e3 if e2e else 0.0],

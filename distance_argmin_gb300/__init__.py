@@ -41,13 +41,14 @@ KERNEL_ASSIGN_TC = 0
 KERNEL_UPDATE_MEAN = 1
 KERNEL_KMEANSPP_DIST = 2
 TRACE_MAX_CAPACITY = 65536
+HOST_MAX_SLICES = 64
 
 # Every symbol the header declares (the ABI test checks the library exports them).
 EXPORTS = (
     "kmeans_workspace_bytes", "kmeans_assign", "kmeans_assign_ffma", "kmeans_update",
     "kmeans_lloyd_iter", "kmeanspp_init", "kmeans_device_status", "kmeans_status_string",
     "kmeans_build_info", "kmeans_assign_noalloc", "kmeans_trace_start", "kmeans_trace_read",
-    "kmeans_trace_stop",
+    "kmeans_trace_stop", "kmeans_lloyd_iter_host",
 )
 
 _lock = threading.Lock()
@@ -98,6 +99,8 @@ def load(path: str | None = None):
         lib.kmeans_trace_start.restype = INT
         lib.kmeans_trace_read.argtypes = [INT, P, P, P]
         lib.kmeans_trace_read.restype = INT
+        lib.kmeans_lloyd_iter_host.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, INT, P, SZ, P, P]
+        lib.kmeans_lloyd_iter_host.restype = INT
         lib.kmeans_trace_stop.argtypes = []
         lib.kmeans_trace_stop.restype = INT
         _lib = lib
@@ -330,50 +333,44 @@ def kmeans_trace_stop() -> None:
 
 
 def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_out_h, labels_h, inertia_h,
-                           chunks: int = 4, ws=None, inertia_parts=None, copy_stream=None, stream=None):
+                           slices: int = 16, ws=None, inertia=None, copy_stream=None, stream=None):
     """One Lloyd iteration on inputs that live in pinned host memory.
 
-    The samples are copied to the device in ``chunks`` row slices on
-    ``copy_stream``; each slice is assigned on ``stream`` as soon as it has
-    landed (kmeans_assign on the slice), overlapping the copy of the next.
-    The mean update then runs on the whole device copy, and C_new, the labels
-    and the per-slice inertias come back to host memory.  Returns the events
-    the caller can wait on; ``inertia_h`` holds the per-slice inertias, whose
-    sum (in slice order) is the iteration's inertia.
+    The library copies the samples to ``Xd`` in ``slices`` row slices on
+    ``copy_stream`` and assigns each slice on ``stream`` as soon as it has
+    landed; the update follows, and C_new, the labels and the inertia come
+    back to ``C_out_h``, ``labels_h`` and ``inertia_h`` (one float64).  The
+    device outputs equal kmeans_lloyd_iter's bit for bit.  Returns an event
+    recorded on ``stream`` after the last copy.
     Xh, Ch, C_out_h, labels_h, inertia_h: pinned host tensors.
     Xd, Cd, C_new, labels, best_dist, counts: device tensors (preallocated).
     """
     torch = _torch()
     n, d = Xh.shape
     k = Ch.shape[0]
+    _check(Xd, "Xd", torch.float32, (n, d))
+    _check(Cd, "Cd", torch.float32, (k, d), Xd.device)
+    _check(C_new, "C_new", torch.float32, (k, d), Xd.device)
+    _check(labels, "labels", torch.int64, (n,), Xd.device)
+    _check(best_dist, "best_dist", torch.float32, (n,), Xd.device)
+    if counts is not None:
+        _check(counts, "counts", torch.int32, (k,), Xd.device)
+    for t, name, dt, shape in ((Xh, "Xh", torch.float32, (n, d)), (Ch, "Ch", torch.float32, (k, d)),
+                               (C_out_h, "C_out_h", torch.float32, (k, d)), (labels_h, "labels_h", torch.int64, (n,)),
+                               (inertia_h, "inertia_h", torch.float64, (1,))):
+        if t.is_cuda or t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous host tensor {dt} {shape}")
     stream = stream or torch.cuda.current_stream()
     copy_stream = copy_stream or torch.cuda.Stream()
-    if inertia_parts is None:
-        inertia_parts = torch.empty(chunks, dtype=torch.float64, device=Xd.device)
+    if inertia is None:
+        inertia = torch.empty(1, dtype=torch.float64, device=Xd.device)
     if ws is None:
         ws = workspace(OP_LLOYD, n, k, d, Xd.device)
-    bounds = [(n * i) // chunks for i in range(chunks + 1)]
-    start = torch.cuda.Event()
-    start.record(stream)
-    copy_stream.wait_event(start)
-    landed = []
-    with torch.cuda.stream(copy_stream):
-        Cd.copy_(Ch, non_blocking=True)
-        for i in range(chunks):
-            r0, r1 = bounds[i], bounds[i + 1]
-            Xd[r0:r1].copy_(Xh[r0:r1], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(copy_stream)
-            landed.append(ev)
-    for i in range(chunks):
-        r0, r1 = bounds[i], bounds[i + 1]
-        stream.wait_event(landed[i])
-        kmeans_assign(Xd[r0:r1], Cd, labels[r0:r1], best_dist[r0:r1], inertia_parts[i:i + 1], ws=ws, stream=stream)
-    kmeans_update(Xd, labels, Cd, C_new, counts, ws=ws, stream=stream)
-    with torch.cuda.stream(stream):
-        C_out_h.copy_(C_new, non_blocking=True)
-        labels_h.copy_(labels, non_blocking=True)
-        inertia_h.copy_(inertia_parts, non_blocking=True)
+    st = load().kmeans_lloyd_iter_host(Xh.data_ptr(), Ch.data_ptr(), _ptr(Xd), _ptr(Cd), _ptr(C_new), _ptr(labels),
+                                       _ptr(best_dist), _ptr(inertia), _ptr(counts), C_out_h.data_ptr(),
+                                       labels_h.data_ptr(), inertia_h.data_ptr(), n, k, d, int(slices), _ptr(ws),
+                                       ws.numel(), _stream_handle(stream), _stream_handle(copy_stream))
+    _raise(st, "kmeans_lloyd_iter_host")
     done = torch.cuda.Event()
     done.record(stream)
     return done

@@ -66,6 +66,22 @@ int run_assign(bool tensor_cores, const float *X, const float *C, int64_t n, int
     return cuda_status(e);
 }
 
+// The Lloyd iteration after the tensor-core pass has written every sample's
+// key: finalize (with the per-tile member count on the counting path), then
+// the mean update.  The update reuses the assignment's workspace: its scratch
+// is dead once the labels are written, and the count table and the fused
+// finalize's block sums lie above the keys and norms that finalize still reads.
+cudaError_t lloyd_finish(const float *X, const float *C_old, float *C_new, int64_t *labels, float *best_dist,
+                         double *inertia, int32_t *counts, int64_t n, int64_t k, int64_t d, const AssignLayout &A,
+                         uint8_t *w, cudaStream_t s) {
+    const UpdateLayout U = update_layout(n, k, d);
+    const bool fused = U.counting && U.off_table >= A.off_xnorm + n * 4 && U.off_table >= A.off_keys + n * 8;
+    cudaError_t e = fused ? launch_finalize_counting(n, k, A, U, w, labels, best_dist, inertia, s)
+                          : launch_finalize(n, A, w, labels, best_dist, inertia, s);
+    if (e == cudaSuccess) e = launch_update(X, labels, C_old, C_new, counts, n, k, d, U, w, false, s, fused);
+    return e;
+}
+
 }  // namespace
 
 extern "C" {
@@ -136,16 +152,70 @@ int kmeans_lloyd_iter(const float *X, const float *C_old, float *C_new, int64_t 
     const AssignLayout A = assign_layout(n, k, d, true);
     cudaError_t e = launch_prep_split(C_old, n, k, d, A, w, s);
     if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, A, w, s);
-    // the update reuses the same workspace: the assignment's scratch is dead
-    // once its labels are written.  On the counting path the finalize step
-    // also counts members per tile; the count table and its block sums lie
-    // above the keys and norms it reads.
-    const UpdateLayout U = update_layout(n, k, d);
-    const bool fused = U.counting && U.off_table >= A.off_xnorm + n * 4 && U.off_table >= A.off_keys + n * 8;
-    if (e == cudaSuccess)
-        e = fused ? launch_finalize_counting(n, k, A, U, w, labels, best_dist, inertia, s)
-                  : launch_finalize(n, A, w, labels, best_dist, inertia, s);
-    if (e == cudaSuccess) e = launch_update(X, labels, C_old, C_new, counts, n, k, d, U, w, false, s, fused);
+    if (e == cudaSuccess) e = lloyd_finish(X, C_old, C_new, labels, best_dist, inertia, counts, n, k, d, A, w, s);
+    return cuda_status(e);
+}
+
+int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, float *C_old, float *C_new,
+                           int64_t *labels, float *best_dist, double *inertia, int32_t *counts, float *C_new_host,
+                           int64_t *labels_host, double *inertia_host, int64_t n, int64_t k, int64_t d, int slices,
+                           void *ws, size_t ws_bytes, void *stream, void *copy_stream) {
+    if (!X_host || !C_host || !X || !C_old || !C_new || !labels || !best_dist) return KMEANS_ERR_INVALID_ARG;
+    if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    if (slices < 1 || slices > KMEANS_HOST_MAX_SLICES) return KMEANS_ERR_INVALID_ARG;
+    if (stream == copy_stream || (inertia_host && !inertia)) return KMEANS_ERR_INVALID_ARG;
+    if (!aligned4(C_new) || (reinterpret_cast<uintptr_t>(labels) & 7u)) return KMEANS_ERR_INVALID_ARG;
+    const int st = tc_path_ok(X, C_old, d);
+    if (st != KMEANS_OK) return st;
+    const size_t need = kmeans_workspace_bytes(KMEANS_OP_LLOYD, n, k, d);
+    const int wst = check_ws(ws, ws_bytes, need);
+    if (wst != KMEANS_OK) return wst;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    // slices of whole 256-sample pair blocks
+    const int64_t per = ((n + slices - 1) / slices + 255) / 256 * 256;
+    const int used = (int)((n + per - 1) / per);
+    // ev[0 .. used-1]: slice i has landed; ev[used]: the entry point on
+    // `stream`; ev[used + 1]: the centroids have landed
+    cudaEvent_t ev[KMEANS_HOST_MAX_SLICES + 2];
+    int made = 0;
+    cudaError_t e = cudaSuccess;
+    for (; made < used + 2 && e == cudaSuccess; ++made) e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+    if (e != cudaSuccess) --made;  // the failed one was not created
+    // the copies wait for everything enqueued on `stream` before this call;
+    // the centroids go first on the copy stream (a copy on `stream` could be
+    // scheduled behind all the sample slices and hold back every slice)
+    if (e == cudaSuccess) e = cudaEventRecord(ev[used], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[used], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(C_old, C_host, (size_t)(k * d) * sizeof(float), cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[used + 1], cs);
+    for (int i = 0; i < used && e == cudaSuccess; ++i) {
+        const int64_t r0 = i * per, rows = (r0 + per <= n ? per : n - r0);
+        e = cudaMemcpyAsync(X + r0 * d, X_host + r0 * d, (size_t)(rows * d) * sizeof(float), cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[i], cs);
+    }
+    // the centroid split once, then each slice's tensor-core pass as soon as
+    // its rows have landed, writing that slice's keys and norms
+    const AssignLayout A = assign_layout(n, k, d, true);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev[used + 1], 0);
+    if (e == cudaSuccess) e = launch_prep_split(C_old, n, k, d, A, w, s);
+    for (int i = 0; i < used && e == cudaSuccess; ++i) {
+        const int64_t r0 = i * per, rows = (r0 + per <= n ? per : n - r0);
+        e = cudaStreamWaitEvent(s, ev[i], 0);
+        AssignLayout Ai = A;
+        Ai.off_keys += r0 * 8;
+        Ai.off_xnorm += r0 * 4;
+        if (e == cudaSuccess) e = launch_assign_tc(X + r0 * d, rows, k, d, Ai, w, s, false);
+    }
+    if (e == cudaSuccess) e = lloyd_finish(X, C_old, C_new, labels, best_dist, inertia, counts, n, k, d, A, w, s);
+    if (e == cudaSuccess && C_new_host)
+        e = cudaMemcpyAsync(C_new_host, C_new, (size_t)(k * d) * sizeof(float), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && labels_host)
+        e = cudaMemcpyAsync(labels_host, labels, (size_t)n * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && inertia_host) e = cudaMemcpyAsync(inertia_host, inertia, sizeof(double), cudaMemcpyDeviceToHost, s);
+    // released by the runtime once the work that uses them has completed
+    for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
     return cuda_status(e);
 }
 

@@ -20,8 +20,10 @@ cudaError_t launch_prep_split(const float *C, int64_t n, int64_t k, int64_t d, c
 cudaError_t launch_prep_norms(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
                               uint8_t *ws, cudaStream_t s);
 
+// `chained`: launched to overlap the tail of the kernel before it on `s`
+// (the prologue's split); false after a wait on an event.
 cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
-                             uint8_t *ws, cudaStream_t s);
+                             uint8_t *ws, cudaStream_t s, bool chained = true);
 
 cudaError_t launch_assign_ffma(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
                                const AssignLayout &L, uint8_t *ws, cudaStream_t s);

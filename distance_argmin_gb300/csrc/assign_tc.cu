@@ -382,26 +382,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                     const int s = it % tc::SXB;
                     const int as = it % tc::SA;
+                    const uint32_t bhi = sbase + s * tc::XB_STAGE + tc::X_BYTES;
+                    const uint32_t blo = bhi + tc::B_BYTES;
+                    const uint32_t ahi = sbase + tc::A_BASE + as * tc::A_STAGE;
+                    const uint32_t alo = ahi + tc::A_BYTES;
+                    // descriptors first: once the split stage lands, only the
+                    // MMAs remain between it and the tensor pipe (measured: the
+                    // issue latency here is on the critical path)
+                    uint64_t dah[tc::BK / 16], dal[tc::BK / 16], dbh[tc::BK / 16], dbl[tc::BK / 16];
+#pragma unroll
+                    for (int kk = 0; kk < tc::BK / 16; ++kk) {
+                        dah[kk] = umma_smem_desc(ahi + kk * 32, tc::SBO_64B, kLayoutSW64);
+                        dal[kk] = umma_smem_desc(alo + kk * 32, tc::SBO_64B, kLayoutSW64);
+                        dbh[kk] = umma_smem_desc(bhi + kk * 32, tc::SBO_64B, kLayoutSW64);
+                        dbl[kk] = umma_smem_desc(blo + kk * 32, tc::SBO_64B, kLayoutSW64);
+                    }
                     // both CTAs' split warps have seen their X and C stage land
                     if (!mbar_wait_cluster(bar(tc::A_FULL + as), (it / tc::SA) & 1, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t bhi = sbase + s * tc::XB_STAGE + tc::X_BYTES;
-                    const uint32_t blo = bhi + tc::B_BYTES;
-                    const uint32_t ahi = sbase + tc::A_BASE + as * tc::A_STAGE;
-                    const uint32_t alo = ahi + tc::A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < tc::BK / 16; ++kk) {
-                        const uint64_t dah = umma_smem_desc(ahi + kk * 32, tc::SBO_64B, kLayoutSW64);
-                        const uint64_t dal = umma_smem_desc(alo + kk * 32, tc::SBO_64B, kLayoutSW64);
-                        const uint64_t dbh = umma_smem_desc(bhi + kk * 32, tc::SBO_64B, kLayoutSW64);
-                        const uint64_t dbl = umma_smem_desc(blo + kk * 32, tc::SBO_64B, kLayoutSW64);
                         const uint32_t first = (kb | kk) != 0 ? 1u : 0u;
-                        mma_bf16_ss_pair(dm, dah, dbh, idesc, first);
-                        mma_bf16_ss_pair(dc, dal, dbh, idesc, DB ? 1u : first);
-                        mma_bf16_ss_pair(dc, dah, dbl, idesc, 1u);
+                        mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
+                        mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
+                        mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
                     }
                     mma_commit_pair_multicast(bar(tc::XB_EMPTY + s), tc::PAIR_MASK);
                     mma_commit_pair_multicast(bar(tc::A_EMPTY + as), tc::PAIR_MASK);
@@ -499,7 +506,7 @@ static int resident_pairs() {
 }
 
 cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
-                             uint8_t *ws, cudaStream_t stream) {
+                             uint8_t *ws, cudaStream_t stream, bool chained) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -545,10 +552,10 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     trace_mark(kTraceAssignTc, false, stream);
     const cudaError_t e =
         d <= tc::SINGLE_ACC_MAX_D
-            ? launch_kernel(true, assign_tc_kernel<true>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream, tmX,
-                            tmChi, tmClo, p)
-            : launch_kernel(true, assign_tc_kernel<false>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream, tmX,
-                            tmChi, tmClo, p);
+            ? launch_kernel(chained, assign_tc_kernel<true>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,
+                            tmX, tmChi, tmClo, p)
+            : launch_kernel(chained, assign_tc_kernel<false>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,
+                            tmX, tmChi, tmClo, p);
     trace_mark(kTraceAssignTc, true, stream);
     return e;
 }

@@ -127,6 +127,33 @@ int kmeans_lloyd_iter(const float *X, const float *C_old, float *C_new, int64_t 
                       int64_t n, int64_t k, int64_t d,
                       void *ws, size_t ws_bytes, uint64_t seed, void *stream);
 
+/* Most slices kmeans_lloyd_iter_host splits the samples into. */
+#define KMEANS_HOST_MAX_SLICES 64
+
+/* One Lloyd iteration [U] on inputs that live in host memory (the pages have
+ * no counterpart: it serves callers whose data is not resident on the GPU).
+ * X_host (n, d) and C_host (k, d) are host arrays, page-locked for the copies
+ * to overlap; X and C_old are the device arrays they are copied into (and
+ * then hold).  The samples travel in `slices` row slices (1 <= slices <=
+ * KMEANS_HOST_MAX_SLICES, each a whole number of 256-sample blocks) on
+ * `copy_stream`; on `stream` the centroids are copied and split once, and
+ * each slice's tensor-core pass starts as soon as its rows have landed, so
+ * the copies and the assignment overlap.  Finalize and the mean update then
+ * run on `stream` exactly as in kmeans_lloyd_iter, whose outputs (C_new,
+ * labels, best_dist, *inertia, counts) these are, bit for bit.  Finally
+ * C_new, the labels and *inertia are copied to C_new_host, labels_host and
+ * *inertia_host (each may be NULL; inertia_host needs inertia).
+ * The copies into X wait for the work enqueued on `stream` before the call;
+ * everything the call enqueues is complete when `stream` reaches the point
+ * after it (the copy stream's part is joined back into `stream`).
+ * copy_stream must differ from stream.  Same requirements as
+ * kmeans_lloyd_iter; the workspace is the KMEANS_OP_LLOYD one. */
+int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, float *C_old, float *C_new,
+                           int64_t *labels, float *best_dist, double *inertia, int32_t *counts,
+                           float *C_new_host, int64_t *labels_host, double *inertia_host,
+                           int64_t n, int64_t k, int64_t d, int slices,
+                           void *ws, size_t ws_bytes, void *stream, void *copy_stream);
+
 /* Greedy k-means++ seeding [K].
  * indices (device int64, k) receives the chosen sample indices, centers
  * (device float32 (k, d), may be NULL) the chosen rows of X.

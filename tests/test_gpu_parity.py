@@ -2,6 +2,8 @@
 the same seeded inputs.  Small shapes are compared on every row; full-size
 workloads on a seeded sample of rows (assignment) and on every row (update,
 with the GPU's own labels so near-tie flips do not cascade)."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -311,8 +313,9 @@ def test_starved_pipeline_times_out_and_reports(gpu_lib, monkeypatch):
 
 
 def test_lloyd_iteration_from_host_buffers_matches_device_call(gpu_lib):
-    # the pipelined host-input iteration (row slices assigned as they land)
-    # gives the same labels, centroids and inertia as the device-resident call
+    # the host-input iteration (row slices assigned as they land) gives the
+    # device-resident call's labels, centroids, counts and inertia bit for bit;
+    # 5 slices of 6144 rows over 30000 samples leave a ragged last slice
     w = synth.Workload("t", 30000, 300, 132, 300, 1, 51, 52, "")
     X, C0, _ = synth.workload_inputs(w)
     n, k, d = w.n, w.k, w.d
@@ -326,11 +329,25 @@ def test_lloyd_iteration_from_host_buffers_matches_device_call(gpu_lib):
     counts = torch.empty(k, dtype=torch.int32, device="cuda")
     C_out_h = torch.empty((k, d), dtype=torch.float32).pin_memory()
     lab_h = torch.empty(n, dtype=torch.int64).pin_memory()
-    parts_h = torch.empty(3, dtype=torch.float64).pin_memory()
-    done = gpu_lib.kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best, counts, C_out_h, lab_h, parts_h,
-                                          chunks=3)
-    done.synchronize()
-    np.testing.assert_array_equal(lab_h.numpy(), host(ref[1]))
-    assert C_out_h.numpy().tobytes() == host(ref[0]).tobytes()
-    scale = (sq_norms(X) + sq_norms(C0)[lab_h.numpy()]).sum()
-    assert abs(float(parts_h.numpy().sum()) - float(ref[3].item())) <= 1e-6 * scale
+    in_h = torch.empty(1, dtype=torch.float64).pin_memory()
+    for slices in (5, 1):
+        done = gpu_lib.kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best, counts, C_out_h, lab_h, in_h,
+                                              slices=slices)
+        done.synchronize()
+        np.testing.assert_array_equal(lab_h.numpy(), host(ref[1]))
+        assert C_out_h.numpy().tobytes() == host(ref[0]).tobytes()
+        assert host(best).tobytes() == host(ref[2]).tobytes()
+        assert float(in_h[0]) == float(ref[3].item())
+        np.testing.assert_array_equal(host(counts), host(ref[4]))
+        assert Xd.cpu().numpy().tobytes() == X.tobytes()
+
+
+def test_lloyd_iteration_from_host_buffers_rejects_bad_arguments(gpu_lib):
+    lib = gpu_lib.load()
+    fake = ctypes.c_void_p(0x10000)  # validation fails before any pointer is used
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = lambda slices, cs: (fake, fake, fake, fake, fake, fake, fake, None, None, None, None, None, 1024, 16, 32,
+                               slices, fake, 1 << 30, s, cs)
+    assert lib.kmeans_lloyd_iter_host(*args(0, None)) == gpu_lib.KMEANS_ERR_INVALID_ARG
+    assert lib.kmeans_lloyd_iter_host(*args(gpu_lib.HOST_MAX_SLICES + 1, None)) == gpu_lib.KMEANS_ERR_INVALID_ARG
+    assert lib.kmeans_lloyd_iter_host(*args(4, s)) == gpu_lib.KMEANS_ERR_INVALID_ARG  # copy stream == stream
