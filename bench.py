@@ -154,6 +154,22 @@ def env_rank():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise maximum of this rank's timings over all ranks (the
+    slowest rank sets every time); a plain copy when world == 1."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def whole_job_tflops(flop_per_rank, world, seconds):
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return world * flop_per_rank / seconds / 1e12
+
+
 def oracle_sample_step(oracle, X, C, rows):
     """One bounded-sample Lloyd step of the oracle: assign the sampled rows,
     then the mean update over those rows.  Returns seconds."""
@@ -403,13 +419,10 @@ def run_gb300(args):
                "d2h_bytes_per_step": int(C_out_h.numel() * 4 + lab_h.numel() * 8 + in_h.numel() * 8)}
 
     # max over ranks
-    times = torch.tensor([t_lloyd, t_assign, t_update, e2e["ms_per_step"] / 1e3 if e2e else 0.0],
-                         dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_lloyd, t_assign, t_update, t_e2e_max = [float(v) for v in times.cpu()]
+    t_lloyd, t_assign, t_update, t_e2e_max = max_over_ranks(
+        [t_lloyd, t_assign, t_update, e2e["ms_per_step"] / 1e3 if e2e else 0.0], world, dev)
     if e2e and world > 1:
-        e2e["value"] = world * flop / t_e2e_max / 1e12
+        e2e["value"] = whole_job_tflops(flop, world, t_e2e_max)
 
     peaks, peaks_src = load_peaks()
     r_peak = peaks["bf16_tflops"] / SPLIT_PRODUCTS
@@ -420,7 +433,7 @@ def run_gb300(args):
     mean_bytes = 4.0 * n * d + 8.0 * n + 4.0 * k * d
     line = {
         "metric": METRIC,
-        "value": world * flop / t_lloyd / 1e12,
+        "value": whole_job_tflops(flop, world, t_lloyd),
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": steps,
