@@ -36,6 +36,10 @@ OP_ASSIGN_FFMA = 1
 OP_UPDATE = 2
 OP_LLOYD = 3
 OP_KMEANSPP = 4
+OP_FIT = 5
+
+INIT_GIVEN = 0
+INIT_KMEANSPP = 1
 
 KERNEL_ASSIGN_TC = 0
 KERNEL_UPDATE_MEAN = 1
@@ -48,7 +52,7 @@ EXPORTS = (
     "kmeans_workspace_bytes", "kmeans_assign", "kmeans_assign_ffma", "kmeans_update",
     "kmeans_lloyd_iter", "kmeanspp_init", "kmeans_device_status", "kmeans_status_string",
     "kmeans_build_info", "kmeans_assign_noalloc", "kmeans_trace_start", "kmeans_trace_read",
-    "kmeans_trace_stop", "kmeans_lloyd_iter_host",
+    "kmeans_trace_stop", "kmeans_lloyd_iter_host", "kmeans_fit",
 )
 
 _lock = threading.Lock()
@@ -101,6 +105,8 @@ def load(path: str | None = None):
         lib.kmeans_trace_read.restype = INT
         lib.kmeans_lloyd_iter_host.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, INT, P, SZ, P, P]
         lib.kmeans_lloyd_iter_host.restype = INT
+        lib.kmeans_fit.argtypes = [P, P, P, P, P, I64, I64, I64, INT, U64, INT, ctypes.c_double, P, P, P, SZ, P]
+        lib.kmeans_fit.restype = INT
         lib.kmeans_trace_stop.argtypes = []
         lib.kmeans_trace_stop.restype = INT
         _lib = lib
@@ -308,6 +314,48 @@ def kmeanspp_init(X, k: int, seed: int, n_trials: int = 0, centers=None, indices
 def kmeans_device_status(ws, stream=None) -> int:
     """Synchronise the stream; status of the last call that used ``ws``."""
     return int(load().kmeans_device_status(_ptr(ws), _stream_handle(stream)))
+
+
+def kmeans_fit(X, k: int = None, C=None, init: str = "kmeans++", seed: int = 0, max_iter: int = 300,
+               tol: float = 1e-4, labels=None, best_dist=None, counts=None, ws=None, stream=None):
+    """Lloyd iterations until the relative inertia improvement is at most
+    ``tol`` (or ``max_iter``) -> ``(C, labels, best_dist, counts,
+    inertia_history, n_iter)``.  ``init="kmeans++"`` seeds ``k`` centroids
+    with ``seed``; ``init="given"`` starts from ``C`` (updated in place).
+    Synchronises the stream once per iteration."""
+    import numpy as np
+    torch = _torch()
+    _check(X, "X", torch.float32)
+    n, d = X.shape
+    if init == "kmeans++":
+        if k is None:
+            raise ValueError("init='kmeans++' needs k")
+        if C is None:
+            C = torch.empty((int(k), d), dtype=torch.float32, device=X.device)
+        code = INIT_KMEANSPP
+    elif init == "given":
+        if C is None:
+            raise ValueError("init='given' needs C")
+        code = INIT_GIVEN
+    else:
+        raise ValueError(f"unknown init {init!r}")
+    _check(C, "C", torch.float32, device=X.device)
+    k = C.shape[0]
+    if labels is None:
+        labels = torch.empty(n, dtype=torch.int64, device=X.device)
+    if best_dist is None:
+        best_dist = torch.empty(n, dtype=torch.float32, device=X.device)
+    if counts is None:
+        counts = torch.empty(k, dtype=torch.int32, device=X.device)
+    if ws is None:
+        ws = workspace(OP_FIT, n, k, d, X.device)
+    hist = np.zeros(int(max_iter), dtype=np.float64)
+    n_iter = ctypes.c_int(0)
+    st = load().kmeans_fit(_ptr(X), _ptr(C), _ptr(labels), _ptr(best_dist), _ptr(counts), n, k, d, code,
+                           int(seed) & (2**64 - 1), int(max_iter), float(tol), ctypes.byref(n_iter),
+                           hist.ctypes.data_as(ctypes.c_void_p), _ptr(ws), ws.numel(), _stream_handle(stream))
+    _raise(st, "kmeans_fit")
+    return C, labels, best_dist, counts, hist[:n_iter.value].copy(), n_iter.value
 
 
 def kmeans_trace_start(capacity: int = 1024) -> None:

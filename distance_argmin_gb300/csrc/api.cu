@@ -66,6 +66,32 @@ int run_assign(bool tensor_cores, const float *X, const float *C, int64_t n, int
     return cuda_status(e);
 }
 
+// kmeans_fit's workspace: the Lloyd / k-means++ scratch at the base (so the
+// status word sits where kmeans_device_status looks), then the second
+// centroid buffer of the ping-pong, the seeding's indices and the inertia.
+struct FitLayout {
+    int64_t shared;       // max(Lloyd, k-means++) scratch
+    int64_t off_calt;     // k x d f32
+    int64_t off_indices;  // k x i64
+    int64_t off_inertia;  // f64
+    int64_t bytes;
+};
+
+FitLayout fit_layout(int64_t n, int64_t k, int64_t d) {
+    FitLayout F{};
+    const int64_t a = assign_layout(n, k, d, true).bytes;
+    const int64_t u = update_layout(n, k, d).bytes;
+    const int64_t p = kpp_layout(n, d, default_trials(k)).bytes;
+    F.shared = a > u ? a : u;
+    if (p > F.shared) F.shared = p;
+    int64_t o = align_up(F.shared, 1024);
+    F.off_calt = o; o = align_up(o + k * d * 4, 1024);
+    F.off_indices = o; o = align_up(o + k * 8, 1024);
+    F.off_inertia = o; o = align_up(o + 8, 1024);
+    F.bytes = o;
+    return F;
+}
+
 // The Lloyd iteration after the tensor-core pass has written every sample's
 // key: finalize (with the per-tile member count on the counting path), then
 // the mean update.  The update reuses the assignment's workspace: its scratch
@@ -102,6 +128,8 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
         }
         case KMEANS_OP_KMEANSPP:
             return (size_t)kpp_layout(n, d, kKppMaxTrials).bytes;
+        case KMEANS_OP_FIT:
+            return (size_t)fit_layout(n, k, d).bytes;
         default:
             return 0;
     }
@@ -216,6 +244,63 @@ int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, f
     if (e == cudaSuccess && inertia_host) e = cudaMemcpyAsync(inertia_host, inertia, sizeof(double), cudaMemcpyDeviceToHost, s);
     // released by the runtime once the work that uses them has completed
     for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
+    return cuda_status(e);
+}
+
+int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int32_t *counts, int64_t n, int64_t k,
+               int64_t d, int init, uint64_t seed, int max_iter, double tol, int *n_iter, double *inertia_history,
+               void *ws, size_t ws_bytes, void *stream) {
+    if (!X || !C || !labels || !best_dist || !n_iter) return KMEANS_ERR_INVALID_ARG;
+    if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    if (init != KMEANS_INIT_GIVEN && init != KMEANS_INIT_KMEANSPP) return KMEANS_ERR_INVALID_ARG;
+    if (max_iter < 1 || max_iter > 1000000 || !(tol >= 0.0) || tol > 1e300) return KMEANS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(labels) & 7u)) return KMEANS_ERR_INVALID_ARG;
+    const int st = tc_path_ok(X, C, d);
+    if (st != KMEANS_OK) return st;
+    const FitLayout F = fit_layout(n, k, d);
+    const int wst = check_ws(ws, ws_bytes, (size_t)F.bytes);
+    if (wst != KMEANS_OK) return wst;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    float *calt = reinterpret_cast<float *>(w + F.off_calt);
+    double *inertia_d = reinterpret_cast<double *>(w + F.off_inertia);
+    *n_iter = 0;
+    cudaError_t e = cudaSuccess;
+    if (init == KMEANS_INIT_KMEANSPP) {
+        const int T = default_trials(k);
+        if (T > kKppMaxTrials) return KMEANS_ERR_UNSUPPORTED;
+        e = launch_kmeanspp(X, n, d, k, T, seed, C, reinterpret_cast<int64_t *>(w + F.off_indices),
+                            kpp_layout(n, d, T), w, s);
+    }
+    const AssignLayout A = assign_layout(n, k, d, true);
+    float *cur = C, *nxt = calt;
+    double prev = 0.0;
+    int it = 0;
+    while (e == cudaSuccess && it < max_iter) {
+        e = launch_prep_split(cur, n, k, d, A, w, s);
+        if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, A, w, s);
+        if (e == cudaSuccess) e = lloyd_finish(X, cur, nxt, labels, best_dist, inertia_d, counts, n, k, d, A, w, s);
+        double inertia = 0.0;
+        uint32_t flags = 0;
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&inertia, inertia_d, sizeof(double), cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&flags, w, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) break;
+        ++it;
+        *n_iter = it;
+        if (flags & kFlagTimeout) return KMEANS_ERR_DEVICE_TIMEOUT;
+        if (flags & kFlagBadLabel) return KMEANS_ERR_DEVICE_LABEL;
+        if (inertia_history) inertia_history[it - 1] = inertia;
+        float *t = cur;
+        cur = nxt;
+        nxt = t;
+        // relative improvement over the previous iteration at most tol
+        if (it > 1 && inertia >= prev * (1.0 - tol)) break;
+        prev = inertia;
+    }
+    // the last update wrote `cur`; the caller's C must hold it
+    if (e == cudaSuccess && cur != C) e = cudaMemcpyAsync(C, cur, (size_t)(k * d) * sizeof(float), cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return cuda_status(e);
 }
 

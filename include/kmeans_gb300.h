@@ -77,7 +77,14 @@ enum {
     KMEANS_OP_ASSIGN_FFMA = 1,
     KMEANS_OP_UPDATE = 2,
     KMEANS_OP_LLOYD = 3,
-    KMEANS_OP_KMEANSPP = 4
+    KMEANS_OP_KMEANSPP = 4,
+    KMEANS_OP_FIT = 5
+};
+
+/* Initialisation of kmeans_fit. */
+enum {
+    KMEANS_INIT_GIVEN = 0,    /* start from the centroids in C            */
+    KMEANS_INIT_KMEANSPP = 1  /* greedy k-means++ seeding (kmeanspp_init) */
 };
 
 /* Bytes of device workspace the operation needs for these sizes (0 when the
@@ -169,6 +176,27 @@ int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, f
 int kmeanspp_init(const float *X, int64_t n, int64_t d, int64_t k, int n_trials,
                   uint64_t seed, float *centers, int64_t *indices,
                   void *ws, size_t ws_bytes, void *stream);
+
+/* A full fit: Lloyd iterations [U] until the inertia stops improving (the
+ * pages fix no stopping rule; this is the plain one).  With
+ * init == KMEANS_INIT_KMEANSPP, C is first seeded by kmeanspp_init with the
+ * default trial count and `seed`; with KMEANS_INIT_GIVEN, C holds the
+ * starting centroids.  Iteration t assigns X to C_t (inertia_t) and updates
+ * to C_{t+1}; the fit stops after iteration t when
+ * inertia_t >= (1 - tol) * inertia_{t-1} (relative improvement at most tol;
+ * tol = 0 runs to a fixed point, where the inertia no longer drops), or after
+ * max_iter iterations.  On return C holds the last updated centroids, labels,
+ * best_dist and counts those of the last iteration (its assignment was to the
+ * centroids before that update; at a fixed point they agree).
+ * *n_iter (host) receives the iterations run and inertia_history (host,
+ * max_iter doubles, may be NULL) each iteration's inertia.  Unlike the other
+ * entry points this one synchronises `stream` once per iteration to read the
+ * inertia; device faults end the fit with their status.  counts may be NULL.
+ * Requirements as kmeans_lloyd_iter (C 16-byte aligned); 1 <= max_iter <=
+ * 1000000, tol >= 0; workspace KMEANS_OP_FIT. */
+int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int32_t *counts,
+               int64_t n, int64_t k, int64_t d, int init, uint64_t seed, int max_iter, double tol,
+               int *n_iter, double *inertia_history, void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronises `stream` and returns the device status word of the last call
  * that used `ws` (KMEANS_OK, KMEANS_ERR_DEVICE_TIMEOUT or

@@ -156,6 +156,25 @@ def lloyd_iter(X, C_old, nthreads: int = 0):
     return C_new, labels, best, second, inertia, counts
 
 
+def fit(X, C0, max_iter: int, tol: float, nthreads: int = 0):
+    """Lloyd iterations from C0 until the relative inertia improvement is at
+    most ``tol`` or ``max_iter`` iterations have run (the pages fix no
+    stopping rule; this is the plain one, the same as the library's).
+    Iteration t assigns X to C_t (inertia_t) and updates to C_{t+1}; the fit
+    stops after iteration t when inertia_t >= (1 - tol) * inertia_{t-1}.
+    Returns ``(C_last, labels_last, best_last, inertia_history, n_iter)``."""
+    C = _f32(C0)
+    hist = []
+    labels = best = None
+    for it in range(max_iter):
+        C_new, labels, best, _, inertia, _ = lloyd_iter(X, C, nthreads)
+        hist.append(inertia)
+        C = C_new
+        if it > 0 and inertia >= hist[-2] * (1.0 - tol):
+            break
+    return C, labels, best, np.array(hist), len(hist)
+
+
 def n_trials_for(k: int) -> int:
     """2 + floor(ln k): the candidate count per new center."""
     import math

@@ -97,6 +97,17 @@ def test_lloyd_workspace_is_the_larger_of_its_steps(km):
         assert km.kmeans_workspace_bytes(km.OP_LLOYD, n, k, d) == max(a, u)
 
 
+def test_fit_workspace_is_the_shared_scratch_plus_a_centroid_buffer(km):
+    import math
+    for n, k, d in [(4096, 256, 512), (65536, 1024, 2048), (131072, 8192, 8192)]:
+        lloyd = km.kmeans_workspace_bytes(km.OP_LLOYD, n, k, d)
+        fit = km.kmeans_workspace_bytes(km.OP_FIT, n, k, d)
+        extra = fit - lloyd
+        assert k * d * 4 <= extra <= k * d * 4 + k * 8 + 8 + 4 * 1024 + \
+            max(0, km.kmeans_workspace_bytes(km.OP_KMEANSPP, n, k, d) - lloyd)
+        assert fit < n * k * 4
+
+
 def test_workspace_far_below_the_distance_matrix_at_every_workload(km):
     import synth
     for w in list(synth.WORKLOADS.values()) + [synth.KMEANSPP]:

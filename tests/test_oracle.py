@@ -227,6 +227,47 @@ def test_lloyd_inertia_never_increases():
         prev = inertia
 
 
+def test_fit_runs_to_a_fixed_point_with_zero_tolerance():
+    # catches a stopping rule that fires early or a returned C that is not
+    # the last update: at tol = 0 the fit ends where another iteration
+    # changes nothing (same labels, same centroids bit for bit)
+    X, C0, _ = synth.workload_inputs(synth.Workload("t", 3000, 24, 16, 24, 1, 31, 32, ""))
+    C, labels, best, hist, n_iter = oracle.fit(X, C0, max_iter=200, tol=0.0)
+    assert n_iter < 200 and len(hist) == n_iter
+    C_again, labels_again, _, _, inertia_again, _ = oracle.lloyd_iter(X, C)
+    np.testing.assert_array_equal(labels_again, labels)
+    assert C_again.tobytes() == C.tobytes()
+    assert inertia_again == hist[-1]
+    assert np.all(np.diff(hist) <= 1e-12 * hist[:-1])
+
+
+def test_fit_stops_at_the_first_small_relative_improvement():
+    # catches an off-by-one in the iteration count or a reversed comparison
+    X, C0, _ = synth.workload_inputs(synth.Workload("t", 3000, 24, 16, 24, 1, 33, 34, ""))
+    full = oracle.fit(X, C0, max_iter=200, tol=0.0)[3]
+    tol = 1e-3
+    _, _, _, hist, n_iter = oracle.fit(X, C0, max_iter=200, tol=tol)
+    np.testing.assert_array_equal(hist, full[:n_iter])
+    rel = (full[:-1] - full[1:]) / full[:-1]  # rel[t - 1]: improvement of iteration t
+    first = int(np.argmax(rel <= tol)) + 1    # the first iteration whose improvement is small
+    assert n_iter == first + 1
+    assert oracle.fit(X, C0, max_iter=3, tol=0.0)[4] == 3
+
+
+def test_fit_from_planted_centers_stops_one_iteration_after_the_fixed_point():
+    # planted, well separated blobs with C0 = the blob centers: iteration 1
+    # moves each centroid to its blob's mean without changing any label;
+    # iteration 2 (inertia against the means, lower) keeps them; iteration 3
+    # sees the same inertia again and the fit stops
+    X, centers, blob = synth.planted_blobs(2048, 32, 16, seed=41)
+    C, labels, _, hist, n_iter = oracle.fit(X, centers, max_iter=50, tol=0.0)
+    assert n_iter == 3
+    assert hist[1] < hist[0] and hist[2] == hist[1]
+    np.testing.assert_array_equal(labels, blob)
+    means = np.stack([X[blob == j].astype(np.float64).mean(0) for j in range(16)])
+    assert np.abs(C - means).max() <= 1e-6 * np.abs(means).max()
+
+
 def test_oracle_thread_count_does_not_change_bits():
     X = synth.gaussian((777, 45), seed=91)
     C = synth.gaussian((31, 45), seed=92)
