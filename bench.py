@@ -43,6 +43,7 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "assign_tc_kernel_lloyd10.md")
 KERNEL_SOURCE = os.path.join(ROOT, "distance_argmin_gb300", "csrc", "assign_tc.cu")
 METRIC = "Lloyd iter time & assign TFLOP/s (2nkd/t) at 1 GB300, % of fp32-accurate roofline"
 SPLIT_PRODUCTS = 3  # bf16x3: hi*hi + hi*lo + lo*hi per fp32 product
+TF32_NOMINAL_TFLOPS = 1100.0  # dense, per GPU (context; no measured TF32 peak)
 
 
 def parse_args():
@@ -374,6 +375,21 @@ def run_gb300(args):
     barrier()
     t_ffma = ev0.elapsed_time(ev1) / 1e3 / f_steps
     del ws_f
+
+    # the 3xTF32 comparator of the operand split: the same kernel with
+    # kind::tf32 MMAs (TF32 runs at half the bf16 rate)
+    ws_t = km.workspace(km.OP_ASSIGN_3XTF32, n, k, d, dev)
+    t_steps = max(1, min(steps, 50))
+    for _ in range(2):
+        km.kmeans_assign_3xtf32(Xd, C0d, labels, best, inertia_a, ws=ws_t, stream=stream)
+    barrier()
+    ev0.record(stream)
+    for _ in range(t_steps):
+        km.kmeans_assign_3xtf32(Xd, C0d, labels, best, inertia_a, ws=ws_t, stream=stream)
+    ev1.record(stream)
+    barrier()
+    t_tf32 = ev0.elapsed_time(ev1) / 1e3 / t_steps
+    del ws_t
     clocks = sampler.stop()
 
     kpp = None
@@ -457,6 +473,11 @@ def run_gb300(args):
                                              "timed": "in the Lloyd timed region"}},
         "assign_ffma": {"ms": 1e3 * t_ffma, "tflops": flop / t_ffma / 1e12,
                         "speedup_of_tensor_path": t_ffma / t_assign},
+        "assign_3xtf32": {"ms": 1e3 * t_tf32, "tflops": flop / t_tf32 / 1e12,
+                          "frac_of_tf32_R": flop / t_tf32 / 1e12 / (TF32_NOMINAL_TFLOPS / SPLIT_PRODUCTS),
+                          "speedup_of_bf16x3": t_tf32 / t_assign,
+                          "note": "whole kmeans_assign_3xtf32 call against the nominal dense TF32 rate "
+                                  f"{TF32_NOMINAL_TFLOPS} TFLOP/s / 3 (no measured TF32 peak)"},
         "lloyd_frac_of_roofline": (flop / (r_peak * 1e12) + upd_bytes / (peaks["hbm_gbs"] * 1e9)) / t_lloyd,
         "roofline": {"bound": "tensor", "achieved": tc_tflops, "peak": r_peak, "unit": "TFLOP/s",
                      "frac": tc_tflops / r_peak, "traffic": recorded_traffic(),

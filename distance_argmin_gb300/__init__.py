@@ -37,6 +37,7 @@ OP_UPDATE = 2
 OP_LLOYD = 3
 OP_KMEANSPP = 4
 OP_FIT = 5
+OP_ASSIGN_3XTF32 = 6
 
 INIT_GIVEN = 0
 INIT_KMEANSPP = 1
@@ -52,7 +53,7 @@ EXPORTS = (
     "kmeans_workspace_bytes", "kmeans_assign", "kmeans_assign_ffma", "kmeans_update",
     "kmeans_lloyd_iter", "kmeanspp_init", "kmeans_device_status", "kmeans_status_string",
     "kmeans_build_info", "kmeans_assign_noalloc", "kmeans_trace_start", "kmeans_trace_read",
-    "kmeans_trace_stop", "kmeans_lloyd_iter_host", "kmeans_fit",
+    "kmeans_trace_stop", "kmeans_lloyd_iter_host", "kmeans_fit", "kmeans_assign_3xtf32",
 )
 
 _lock = threading.Lock()
@@ -83,6 +84,8 @@ def load(path: str | None = None):
         assign_sig = [P, P, I64, I64, I64, P, P, P, P, SZ, U64, P]
         lib.kmeans_assign.argtypes = assign_sig
         lib.kmeans_assign.restype = INT
+        lib.kmeans_assign_3xtf32.argtypes = assign_sig
+        lib.kmeans_assign_3xtf32.restype = INT
         lib.kmeans_assign_ffma.argtypes = assign_sig
         lib.kmeans_assign_ffma.restype = INT
         lib.kmeans_assign_noalloc.argtypes = [P, P, I64, I64, I64, P, P, P, U64, P]
@@ -219,6 +222,11 @@ def kmeans_assign(X, C, labels=None, best_dist=None, inertia=None, ws=None, seed
 def kmeans_assign_ffma(X, C, labels=None, best_dist=None, inertia=None, ws=None, seed=0, stream=None):
     """The same assignment with float32 FMA on the CUDA cores (comparator)."""
     return _assign("kmeans_assign_ffma", OP_ASSIGN_FFMA, X, C, labels, best_dist, inertia, ws, seed, stream)
+
+
+def kmeans_assign_3xtf32(X, C, labels=None, best_dist=None, inertia=None, ws=None, seed=0, stream=None):
+    """The tensor-core assignment with the 3xTF32 split (comparator of bf16x3)."""
+    return _assign("kmeans_assign_3xtf32", OP_ASSIGN_3XTF32, X, C, labels, best_dist, inertia, ws, seed, stream)
 
 
 def kmeans_assign_noalloc(X, C, labels, best_dist, inertia=None, seed=0, stream=None):

@@ -39,25 +39,33 @@ int tc_path_ok(const float *X, const float *C, int64_t d) {
 
 int default_trials(int64_t k) { return 2 + (int)floor(log((double)k)); }
 
-int run_assign(bool tensor_cores, const float *X, const float *C, int64_t n, int64_t k, int64_t d, int64_t *labels,
+// The three assignment paths: the bf16x3 tensor-core kernel, the 3xTF32
+// tensor-core kernel and the float32 FFMA comparator.
+enum class AssignPath { kBf16x3, kTf32x3, kFfma };
+
+int run_assign(AssignPath path, const float *X, const float *C, int64_t n, int64_t k, int64_t d, int64_t *labels,
                float *best_dist, double *inertia, void *ws, size_t ws_bytes, cudaStream_t s) {
     if (!X || !C || !labels || !best_dist) return KMEANS_ERR_INVALID_ARG;
     if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
     if (!aligned4(X) || !aligned4(C)) return KMEANS_ERR_INVALID_ARG;
+    const bool tensor_cores = path != AssignPath::kFfma;
     if (tensor_cores) {
         const int st = tc_path_ok(X, C, d);
         if (st != KMEANS_OK) return st;
     } else if ((k + 127) / 128 > 65535) {
         return KMEANS_ERR_UNSUPPORTED;
     }
-    const AssignLayout L = assign_layout(n, k, d, tensor_cores);
+    const AssignLayout L = assign_layout(n, k, d, tensor_cores, path == AssignPath::kTf32x3 ? 4 : 2);
     const int wst = check_ws(ws, ws_bytes, (size_t)L.bytes);
     if (wst != KMEANS_OK) return wst;
     uint8_t *w = static_cast<uint8_t *>(ws);
     cudaError_t e;
-    if (tensor_cores) {
+    if (path == AssignPath::kBf16x3) {
         e = launch_prep_split(C, n, k, d, L, w, s);
         if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, L, w, s);
+    } else if (path == AssignPath::kTf32x3) {
+        e = launch_prep_split_tf32(C, n, k, d, L, w, s);
+        if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, L, w, s, true, true);
     } else {
         e = launch_prep_norms(C, n, k, d, L, w, s);
         if (e == cudaSuccess) e = launch_assign_ffma(X, C, n, k, d, L, w, s);
@@ -119,6 +127,8 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
             return (size_t)assign_layout(n, k, d, true).bytes;
         case KMEANS_OP_ASSIGN_FFMA:
             return (size_t)assign_layout(n, k, d, false).bytes;
+        case KMEANS_OP_ASSIGN_3XTF32:
+            return (size_t)assign_layout(n, k, d, true, 4).bytes;
         case KMEANS_OP_UPDATE:
             return (size_t)update_layout(n, k, d).bytes;
         case KMEANS_OP_LLOYD: {
@@ -138,14 +148,21 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
 int kmeans_assign(const float *X, const float *C, int64_t n, int64_t k, int64_t d, int64_t *labels,
                   float *best_dist, double *inertia, void *ws, size_t ws_bytes, uint64_t seed, void *stream) {
     (void)seed;
-    return run_assign(true, X, C, n, k, d, labels, best_dist, inertia, ws, ws_bytes,
+    return run_assign(AssignPath::kBf16x3, X, C, n, k, d, labels, best_dist, inertia, ws, ws_bytes,
                       static_cast<cudaStream_t>(stream));
 }
 
 int kmeans_assign_ffma(const float *X, const float *C, int64_t n, int64_t k, int64_t d, int64_t *labels,
                        float *best_dist, double *inertia, void *ws, size_t ws_bytes, uint64_t seed, void *stream) {
     (void)seed;
-    return run_assign(false, X, C, n, k, d, labels, best_dist, inertia, ws, ws_bytes,
+    return run_assign(AssignPath::kFfma, X, C, n, k, d, labels, best_dist, inertia, ws, ws_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int kmeans_assign_3xtf32(const float *X, const float *C, int64_t n, int64_t k, int64_t d, int64_t *labels,
+                         float *best_dist, double *inertia, void *ws, size_t ws_bytes, uint64_t seed, void *stream) {
+    (void)seed;
+    return run_assign(AssignPath::kTf32x3, X, C, n, k, d, labels, best_dist, inertia, ws, ws_bytes,
                       static_cast<cudaStream_t>(stream));
 }
 

@@ -96,6 +96,58 @@ __global__ void __launch_bounds__(kPrepThreads)
         keys[i] = kEmptyKey;
 }
 
+__device__ __forceinline__ float tf32_bits_trunc(float v) {
+    return __uint_as_float(__float_as_uint(v) & 0xffffe000u);
+}
+
+// The 3xTF32 prologue: hi = c with its low 13 mantissa bits cleared, lo =
+// (c - hi) with its low 13 bits cleared, both fp32 at row pitch d_pad (so the
+// tensor cores read them exactly whether they round or truncate), ||c_j||^2
+// from the exact c; otherwise as prep_split_kernel.
+__global__ void __launch_bounds__(kPrepThreads)
+    prep_split_tf32_kernel(const float *__restrict__ C, int k, int d, int d_pad, float *__restrict__ chi,
+                           float *__restrict__ clo, float *__restrict__ cnorm,
+                           unsigned long long *__restrict__ keys, int n, WsHeader *hdr) {
+    __shared__ float red[kPrepThreads / 32];
+    griddep_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr->status = 0u;
+        hdr->done_blocks = 0u;
+    }
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int j = blockIdx.x; j < k; j += gridDim.x) {
+        const float *row = C + (size_t)j * d;
+        float sum = 0.f, comp = 0.f;
+        for (int f = threadIdx.x * 4; f < d_pad; f += kPrepThreads * 4) {
+            const float4 v = f < d ? __ldg(reinterpret_cast<const float4 *>(row + f)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 h = make_float4(tf32_bits_trunc(v.x), tf32_bits_trunc(v.y), tf32_bits_trunc(v.z),
+                                         tf32_bits_trunc(v.w));
+            const float4 l = make_float4(tf32_bits_trunc(v.x - h.x), tf32_bits_trunc(v.y - h.y),
+                                         tf32_bits_trunc(v.z - h.z), tf32_bits_trunc(v.w - h.w));
+            const size_t o = (size_t)j * d_pad + f;
+            *reinterpret_cast<float4 *>(chi + o) = h;
+            *reinterpret_cast<float4 *>(clo + o) = l;
+            float q = v.x * v.x;
+            q = fmaf(v.y, v.y, q);
+            q = fmaf(v.z, v.z, q);
+            q = fmaf(v.w, v.w, q);
+            kahan_add(sum, comp, q);
+        }
+        const float part = warp_sum(sum - comp);
+        if (lane == 0) red[wid] = part;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kPrepThreads / 32; ++w) tot += red[w];
+            cnorm[j] = tot;
+        }
+        __syncthreads();
+    }
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        keys[i] = kEmptyKey;
+}
+
 // Norms only (any d, any 4-byte alignment).
 __global__ void prep_norms_kernel(const float *__restrict__ C, int k, int d, float *__restrict__ cnorm,
                                   unsigned long long *__restrict__ keys, int n, WsHeader *hdr) {
@@ -191,6 +243,16 @@ cudaError_t launch_prep_split(const float *C, int64_t n, int64_t k, int64_t d, c
     prep_split_kernel<<<prep_grid(k, n), kPrepThreads, 0, s>>>(
         C, (int)k, (int)d, (int)L.d_pad, reinterpret_cast<__nv_bfloat16 *>(ws + L.off_chi),
         reinterpret_cast<__nv_bfloat16 *>(ws + L.off_clo), reinterpret_cast<float *>(ws + L.off_cnorm),
+        reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_split_tf32(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
+                                   uint8_t *ws, cudaStream_t s) {
+    if (L.split_elem_bytes != 4) return cudaErrorInvalidValue;
+    prep_split_tf32_kernel<<<prep_grid(k, n), kPrepThreads, 0, s>>>(
+        C, (int)k, (int)d, (int)L.d_pad, reinterpret_cast<float *>(ws + L.off_chi),
+        reinterpret_cast<float *>(ws + L.off_clo), reinterpret_cast<float *>(ws + L.off_cnorm),
         reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws));
     return cudaGetLastError();
 }

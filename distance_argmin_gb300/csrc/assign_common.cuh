@@ -21,9 +21,16 @@ cudaError_t launch_prep_norms(const float *C, int64_t n, int64_t k, int64_t d, c
                               uint8_t *ws, cudaStream_t s);
 
 // `chained`: launched to overlap the tail of the kernel before it on `s`
-// (the prologue's split); false after a wait on an event.
+// (the prologue's split); false after a wait on an event.  `tf32`: the
+// 3xTF32 operand split (L from assign_layout(..., true, 4) and the centroid
+// copies from launch_prep_split_tf32) instead of bf16x3.
 cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
-                             uint8_t *ws, cudaStream_t s, bool chained = true);
+                             uint8_t *ws, cudaStream_t s, bool chained = true, bool tf32 = false);
+
+// launch_prep_split for the 3xTF32 path: C's hi (low 13 mantissa bits
+// cleared) and lo (C - hi, low 13 bits cleared) as fp32, row pitch L.d_pad.
+cudaError_t launch_prep_split_tf32(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
+                                   uint8_t *ws, cudaStream_t s);
 
 cudaError_t launch_assign_ffma(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
                                const AssignLayout &L, uint8_t *ws, cudaStream_t s);

@@ -62,8 +62,6 @@ constexpr int BM = 128;                        // samples per CTA (the pair's MM
 constexpr int BN = 256;                        // centroids per pair tile (UMMA N)
 constexpr int BN_CTA = BN / 2;                 // centroid rows each CTA loads
 constexpr int BK = 32;                         // features per pipeline stage
-constexpr int SXB = 4;                         // X + C stages (TMA ring)
-constexpr int SA = 6;                          // split-X stages
 constexpr int SPLIT_WARPS = 8;                 // warps converting X to bf16 hi / lo
 constexpr int EPI_WARPS = 8;                   // 4 or 8: one or two warps per tensor-memory lane quarter
 constexpr int EPI_COLS = BN * 4 / EPI_WARPS;   // accumulator columns each epilogue warp reads
@@ -77,15 +75,7 @@ constexpr int SPLIT_GROUPS = BK / 8;                            // 8-feature gro
 constexpr int ROWS_PER_SPLIT_THREAD = BM * SPLIT_GROUPS / SPLIT_THREADS;
 constexpr int SPLIT_ROW_STRIDE = SPLIT_THREADS / SPLIT_GROUPS;
 constexpr int X_BYTES = BM * BK * 4;           // fp32 X tile, 128-byte swizzle
-constexpr int B_BYTES = BN_CTA * BK * 2;       // one bf16 C part, 64-byte swizzle
-constexpr int A_BYTES = BM * BK * 2;           // one bf16 X part, 64-byte swizzle
-constexpr int XB_STAGE = X_BYTES + 2 * B_BYTES;
-constexpr int A_STAGE = 2 * A_BYTES;
-constexpr int A_BASE = SXB * XB_STAGE;
-constexpr int BAR_BASE = A_BASE + SA * A_STAGE;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = BAR_BASE + BAR_BYTES + 1024;  // + alignment slack
-constexpr int TX_BYTES = XB_STAGE;
 constexpr int ACC_MAIN = 0;                    // tensor-memory columns (separate accumulators)
 constexpr int ACC_CORR = BN;
 constexpr int TMEM_COLS = 2 * BN;              // either main + corrections, or two single accumulators
@@ -96,16 +86,49 @@ constexpr int TMEM_COLS = 2 * BN;              // either main + corrections, or 
 // d = 16384); beyond this size the correction products keep their own
 // accumulator (single-buffered), which is about 3x more accurate.
 constexpr int SINGLE_ACC_MAX_D = 4096;
+// 3xTF32 issues an MMA per 8 features instead of 16, twice the truncating
+// adds (measured 8.4e-5 relative with one accumulator at d = 4096, against
+// 2.7e-5 for bf16x3), so its single-accumulator limit is half as large.
+constexpr int SINGLE_ACC_MAX_D_TF32 = 2048;
 constexpr int GROUP_M = 8;                     // pair sample blocks per raster band
-constexpr uint32_t SBO_64B = 8 * 64;           // 8 rows x 64 bytes per swizzle atom
 constexpr uint16_t PAIR_MASK = 0x3;
-static_assert(XB_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages stay 1 KiB aligned");
 static_assert(SPLIT_WARPS % 4 == 0 && WARP_EPI % 4 == 0, "epilogue warps start on a lane-quarter boundary");
-static_assert(SMEM_BYTES <= 232448, "fits the 227 KiB opt-in limit");
-// barrier slots
-constexpr int XB_FULL = 0, XB_EMPTY = SXB, A_FULL = 2 * SXB, A_EMPTY = 2 * SXB + SA;
-constexpr int T_FULL = 2 * SXB + 2 * SA, T_EMPTY = T_FULL + 2, DRAIN = T_FULL + 4, NUM_BARS = T_FULL + 5;  // 2 accumulator slots
-static_assert(NUM_BARS * 8 + 16 <= BAR_BYTES, "barriers fit");
+
+// What depends on the operand format.
+//  bf16x3: hi = bf16(v), lo = bf16(v - hi), both written by the split warps
+//          (X) or the prologue (C) in the 64-byte-swizzled K-major layout;
+//          an MMA covers K = 16.
+//  3xTF32: hi = v with its low 13 mantissa bits cleared, lo = (v - hi) with
+//          its low 13 bits cleared, both exact as TF32 values; the split
+//          warps clear X's bits in place in the fp32 TMA tile (the A operand
+//          hi) and write lo beside it, the prologue writes C's hi and lo as
+//          fp32; everything keeps the 128-byte-swizzled K-major layout of
+//          the fp32 tiles, and an MMA covers K = 8.
+template <bool TF32>
+struct Fmt {
+    static constexpr int B_BYTES = BN_CTA * BK * (TF32 ? 4 : 2);  // one C part per CTA
+    static constexpr int A_STAGE = TF32 ? BM * BK * 4 : 2 * BM * BK * 2;  // lo (tf32) or hi + lo (bf16)
+    static constexpr int A_LO = TF32 ? 0 : BM * BK * 2;                   // offset of lo in an A stage
+    static constexpr int XB_STAGE = X_BYTES + 2 * B_BYTES;
+    static constexpr int SXB = TF32 ? 3 : 4;   // X + C stages (TMA ring)
+    static constexpr int SA = TF32 ? 4 : 6;    // split-X stages
+    static constexpr int A_BASE = SXB * XB_STAGE;
+    static constexpr int BAR_BASE = A_BASE + SA * A_STAGE;
+    static constexpr int SMEM_BYTES = BAR_BASE + BAR_BYTES + 1024;  // + alignment slack
+    static constexpr int TX_BYTES = XB_STAGE;
+    static constexpr int K_STEP_BYTES = 32;                  // one MMA's K extent: 16 bf16 or 8 tf32
+    static constexpr int K_STEPS = BK * (TF32 ? 4 : 2) / K_STEP_BYTES;
+    static constexpr uint32_t ROW_BYTES = TF32 ? 128u : 64u;  // K-major row of one tile
+    static constexpr uint32_t SBO = 8 * ROW_BYTES;           // 8 rows per swizzle atom
+    static constexpr uint32_t LAYOUT = TF32 ? kLayoutSW128 : kLayoutSW64;
+    // barrier slots
+    static constexpr int XB_FULL = 0, XB_EMPTY = SXB, A_FULL = 2 * SXB, A_EMPTY = 2 * SXB + SA;
+    static constexpr int T_FULL = 2 * SXB + 2 * SA, T_EMPTY = T_FULL + 2, DRAIN = T_FULL + 4;  // 2 accumulator slots
+    static constexpr int NUM_BARS = T_FULL + 5;
+    static_assert(XB_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages stay 1 KiB aligned");
+    static_assert(SMEM_BYTES <= 232448, "fits the 227 KiB opt-in limit");
+    static_assert(NUM_BARS * 8 + 16 <= BAR_BYTES, "barriers fit");
+};
 }  // namespace tc
 
 struct TcParams {
@@ -151,7 +174,7 @@ template <bool NORM>
 __device__ __forceinline__ void split_kblock(const uint8_t *xs, uint8_t *ahi, int t,
                                              float (&acc)[tc::ROWS_PER_SPLIT_THREAD],
                                              float (&comp)[tc::ROWS_PER_SPLIT_THREAD]) {
-    uint8_t *alo = ahi + tc::A_BYTES;
+    uint8_t *alo = ahi + tc::Fmt<false>::A_LO;
     const int g = t & (tc::SPLIT_GROUPS - 1);
 #pragma unroll
     for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) {
@@ -183,18 +206,60 @@ __device__ __forceinline__ void split_kblock(const uint8_t *xs, uint8_t *ahi, in
     }
 }
 
-template <bool DB>  // DB: one accumulator per tile, double-buffered (d <= SINGLE_ACC_MAX_D)
+__device__ __forceinline__ float tf32_trunc(float v) { return __uint_as_float(__float_as_uint(v) & 0xffffe000u); }
+
+// One k-block of the 3xTF32 split: the fp32 X tile (128 rows x 32,
+// 128-byte swizzled) keeps hi = v with its low 13 mantissa bits cleared,
+// written back in place (it is the A operand hi), and lo = (v - hi) with its
+// low 13 bits cleared goes to the same position of the lo tile (v - hi is
+// exact; clearing its low bits drops at most 2 of them).  Thread t owns row
+// t / 2 and four of that row's eight 16-byte chunks, at swizzled positions so
+// that the eight threads of a quarter-warp hit distinct banks.  With NORM it
+// also adds the squares of its 16 values (the exact v) into a compensated
+// running sum.
+template <bool NORM>
+__device__ __forceinline__ void split_kblock_tf32(uint8_t *xs, uint8_t *alo, int t, float &acc, float &comp) {
+    const int r = t >> 1;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t off = r * 128 + ((((t & 1) * 4 + i) ^ (r & 7)) << 4);
+        const float4 v = *reinterpret_cast<const float4 *>(xs + off);
+        const float4 h = make_float4(tf32_trunc(v.x), tf32_trunc(v.y), tf32_trunc(v.z), tf32_trunc(v.w));
+        const float4 l = make_float4(tf32_trunc(v.x - h.x), tf32_trunc(v.y - h.y), tf32_trunc(v.z - h.z),
+                                     tf32_trunc(v.w - h.w));
+        *reinterpret_cast<float4 *>(xs + off) = h;
+        *reinterpret_cast<float4 *>(alo + off) = l;
+        if (NORM) {
+            q = fmaf(v.x, v.x, q);
+            q = fmaf(v.y, v.y, q);
+            q = fmaf(v.z, v.z, q);
+            q = fmaf(v.w, v.w, q);
+        }
+    }
+    if (NORM) {
+        const float y = q - comp;
+        const float tsum = acc + y;
+        comp = (tsum - acc) - y;
+        acc = tsum;
+    }
+}
+
+// DB: one accumulator per tile, double-buffered (d <= SINGLE_ACC_MAX_D); TF32:
+// the 3xTF32 operand split instead of bf16x3 (see Fmt)
+template <bool DB, bool TF32>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     assign_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmChi,
                      const __grid_constant__ CUtensorMap tmClo, const TcParams p) {
+    using F = tc::Fmt<TF32>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = smem_addr(smem);
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + tc::BAR_BASE);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + F::BAR_BASE);
     auto bar = [&](int i) { return smem_addr(bars + i); };
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + tc::NUM_BARS);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + F::NUM_BARS);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -203,19 +268,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     const int num_pairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < tc::SXB; ++s) {
-            mbar_init(bar(tc::XB_FULL + s), 1);
-            mbar_init(bar(tc::XB_EMPTY + s), tc::SPLIT_WARPS + 1);  // split warps + the MMA commit
+        for (int s = 0; s < F::SXB; ++s) {
+            mbar_init(bar(F::XB_FULL + s), 1);
+            mbar_init(bar(F::XB_EMPTY + s), tc::SPLIT_WARPS + 1);  // split warps + the MMA commit
         }
-        for (int s = 0; s < tc::SA; ++s) {
-            mbar_init(bar(tc::A_FULL + s), 2 * tc::SPLIT_WARPS);  // split warps of both CTAs (even CTA's copy)
-            mbar_init(bar(tc::A_EMPTY + s), 1);
+        for (int s = 0; s < F::SA; ++s) {
+            mbar_init(bar(F::A_FULL + s), 2 * tc::SPLIT_WARPS);  // split warps of both CTAs (even CTA's copy)
+            mbar_init(bar(F::A_EMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(tc::T_FULL + b), 1);
-            mbar_init(bar(tc::T_EMPTY + b), 2 * tc::EPI_WARPS);  // epilogue warps of both CTAs (even CTA's copy)
+            mbar_init(bar(F::T_FULL + b), 1);
+            mbar_init(bar(F::T_EMPTY + b), 2 * tc::EPI_WARPS);  // epilogue warps of both CTAs (even CTA's copy)
         }
-        mbar_init(bar(tc::DRAIN), 1);
+        mbar_init(bar(F::DRAIN), 1);
         fence_barrier_init();
     }
     if (warp == tc::WARP_MMA) {
@@ -241,34 +306,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) acc[i] = comp[i] = 0.f;
             for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                const int s = it % tc::SXB;
-                const int as = it % tc::SA;
-                if (!mbar_wait_warp(bar(tc::XB_FULL + s), (it / tc::SXB) & 1, p.status) ||
-                    !mbar_wait_warp(bar(tc::A_EMPTY + as), ((it / tc::SA) & 1) ^ 1, p.status)) {
+                const int s = it % F::SXB;
+                const int as = it % F::SA;
+                if (!mbar_wait_warp(bar(F::XB_FULL + s), (it / F::SXB) & 1, p.status) ||
+                    !mbar_wait_warp(bar(F::A_EMPTY + as), ((it / F::SA) & 1) ^ 1, p.status)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *xs = smem + s * tc::XB_STAGE;
-                uint8_t *ahi = smem + tc::A_BASE + as * tc::A_STAGE;
-                if (nb == 0)
-                    split_kblock<true>(xs, ahi, t, acc, comp);  // this tile also reports ||x||^2
-                else
-                    split_kblock<false>(xs, ahi, t, acc, comp);
+                uint8_t *xs = smem + s * F::XB_STAGE;
+                uint8_t *ast = smem + F::A_BASE + as * F::A_STAGE;
+                if constexpr (TF32) {
+                    if (nb == 0)
+                        split_kblock_tf32<true>(xs, ast, t, acc[0], comp[0]);  // this tile also reports ||x||^2
+                    else
+                        split_kblock_tf32<false>(xs, ast, t, acc[0], comp[0]);
+                } else {
+                    if (nb == 0)
+                        split_kblock<true>(xs, ast, t, acc, comp);  // this tile also reports ||x||^2
+                    else
+                        split_kblock<false>(xs, ast, t, acc, comp);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive_cluster(map_to_cta(bar(tc::A_FULL + as), 0));
-                    mbar_arrive(bar(tc::XB_EMPTY + s));  // the fp32 X tile has been read
+                    mbar_arrive_cluster(map_to_cta(bar(F::A_FULL + as), 0));
+                    mbar_arrive(bar(F::XB_EMPTY + s));  // this warp is done with the X tile
                 }
             }
             if (!ok) break;
-#pragma unroll
-            for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) {
-                float v = acc[i] - comp[i];
+            if constexpr (TF32) {
+                // two threads per row
+                float v = acc[0] - comp[0];
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                const int row = m0 + tc::SPLIT_ROW_STRIDE * i + t / tc::SPLIT_GROUPS;
-                if (nb == 0 && (t & (tc::SPLIT_GROUPS - 1)) == 0 && row < p.n) p.xnorm[row] = v;
+                const int row = m0 + (t >> 1);
+                if (nb == 0 && (t & 1) == 0 && row < p.n) p.xnorm[row] = v;
+            } else {
+#pragma unroll
+                for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) {
+                    float v = acc[i] - comp[i];
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    const int row = m0 + tc::SPLIT_ROW_STRIDE * i + t / tc::SPLIT_GROUPS;
+                    if (nb == 0 && (t & (tc::SPLIT_GROUPS - 1)) == 0 && row < p.n) p.xnorm[row] = v;
+                }
             }
         }
     } else if (warp < tc::WARP_EPI + tc::EPI_WARPS) {
@@ -281,7 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             tile_coords(tile, p.num_m, p.num_n, mb, nb);
             const int buf = DB ? (tile_iter & 1) : 0;
             const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (tile_iter & 1);
-            if (!mbar_wait_warp(bar(tc::T_FULL + buf), phase, p.status)) break;
+            if (!mbar_wait_warp(bar(F::T_FULL + buf), phase, p.status)) break;
             tc_fence_after();
             const uint32_t acc_base = tmem_base + (DB ? (uint32_t)(buf * tc::BN) : (uint32_t)tc::ACC_MAIN);
             const int n0 = nb * tc::BN + part * tc::EPI_COLS;
@@ -328,7 +408,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(tc::T_EMPTY + buf), 0));
+            if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(F::T_EMPTY + buf), 0));
             const int row = mb * (2 * tc::BM) + (int)rank * tc::BM + q * 32 + lane;
             if (row < p.n && arg >= 0) atomicMin(p.keys + row, make_key(best, (uint32_t)arg));
         }
@@ -346,28 +426,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 const int m0 = mb * (2 * tc::BM) + (int)rank * tc::BM;
                 const int c0 = nb * tc::BN + (int)rank * tc::BN_CTA;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const int s = it % tc::SXB;
-                    if (!mbar_wait(bar(tc::XB_EMPTY + s), ((it / tc::SXB) & 1) ^ 1, p.status)) {
+                    const int s = it % F::SXB;
+                    if (!mbar_wait(bar(F::XB_EMPTY + s), ((it / F::SXB) & 1) ^ 1, p.status)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t st = sbase + s * tc::XB_STAGE;
-                    mbar_arrive_expect_tx(bar(tc::XB_FULL + s), tc::TX_BYTES);
-                    tma_load_2d(st, &tmX, bar(tc::XB_FULL + s), kb * tc::BK, m0);
-                    tma_load_2d(st + tc::X_BYTES, &tmChi, bar(tc::XB_FULL + s), kb * tc::BK, c0);
-                    tma_load_2d(st + tc::X_BYTES + tc::B_BYTES, &tmClo, bar(tc::XB_FULL + s), kb * tc::BK, c0);
+                    const uint32_t st = sbase + s * F::XB_STAGE;
+                    mbar_arrive_expect_tx(bar(F::XB_FULL + s), F::TX_BYTES);
+                    tma_load_2d(st, &tmX, bar(F::XB_FULL + s), kb * tc::BK, m0);
+                    tma_load_2d(st + tc::X_BYTES, &tmChi, bar(F::XB_FULL + s), kb * tc::BK, c0);
+                    tma_load_2d(st + tc::X_BYTES + F::B_BYTES, &tmClo, bar(F::XB_FULL + s), kb * tc::BK, c0);
                 }
             }
             if (!ok) {
                 // let copies already in flight land before the CTA exits
-                for (int j = max(0, it - tc::SXB); j < it; ++j)
-                    mbar_wait_drain(bar(tc::XB_FULL + (j % tc::SXB)), (j / tc::SXB) & 1);
+                for (int j = max(0, it - F::SXB); j < it; ++j)
+                    mbar_wait_drain(bar(F::XB_FULL + (j % F::SXB)), (j / F::SXB) & 1);
             }
         }
     } else {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16_f32(2 * tc::BM, tc::BN);
+            constexpr uint32_t idesc =
+                TF32 ? umma_idesc_tf32_f32(2 * tc::BM, tc::BN) : umma_idesc_bf16_f32(2 * tc::BM, tc::BN);
             const uint32_t d_main = tmem_base + tc::ACC_MAIN;
             const uint32_t d_corr = tmem_base + tc::ACC_CORR;
             int it = 0, tile_iter = 0;
@@ -375,50 +456,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             for (int tile = pair; tile < p.num_tiles && ok; tile += num_pairs, ++tile_iter) {
                 const int buf = DB ? (tile_iter & 1) : 0;
                 const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (tile_iter & 1);
-                if (!mbar_wait_cluster(bar(tc::T_EMPTY + buf), phase ^ 1, p.status)) break;
+                if (!mbar_wait_cluster(bar(F::T_EMPTY + buf), phase ^ 1, p.status)) break;
                 tc_fence_after();
                 const uint32_t dm = DB ? tmem_base + (uint32_t)(buf * tc::BN) : d_main;
                 const uint32_t dc = DB ? dm : d_corr;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const int s = it % tc::SXB;
-                    const int as = it % tc::SA;
-                    const uint32_t bhi = sbase + s * tc::XB_STAGE + tc::X_BYTES;
-                    const uint32_t blo = bhi + tc::B_BYTES;
-                    const uint32_t ahi = sbase + tc::A_BASE + as * tc::A_STAGE;
-                    const uint32_t alo = ahi + tc::A_BYTES;
+                    const int s = it % F::SXB;
+                    const int as = it % F::SA;
+                    // operands of this stage: bf16 hi and lo of X in the A stage;
+                    // 3xTF32 hi of X in place in the fp32 tile, lo in the A stage
+                    const uint32_t xb = sbase + s * F::XB_STAGE;
+                    const uint32_t bhi = xb + tc::X_BYTES;
+                    const uint32_t blo = bhi + F::B_BYTES;
+                    const uint32_t ast = sbase + F::A_BASE + as * F::A_STAGE;
+                    const uint32_t ahi = TF32 ? xb : ast;
+                    const uint32_t alo = TF32 ? ast : ast + F::A_LO;
                     // descriptors first: once the split stage lands, only the
                     // MMAs remain between it and the tensor pipe (measured: the
                     // issue latency here is on the critical path)
-                    uint64_t dah[tc::BK / 16], dal[tc::BK / 16], dbh[tc::BK / 16], dbl[tc::BK / 16];
+                    uint64_t dah[F::K_STEPS], dal[F::K_STEPS], dbh[F::K_STEPS], dbl[F::K_STEPS];
 #pragma unroll
-                    for (int kk = 0; kk < tc::BK / 16; ++kk) {
-                        dah[kk] = umma_smem_desc(ahi + kk * 32, tc::SBO_64B, kLayoutSW64);
-                        dal[kk] = umma_smem_desc(alo + kk * 32, tc::SBO_64B, kLayoutSW64);
-                        dbh[kk] = umma_smem_desc(bhi + kk * 32, tc::SBO_64B, kLayoutSW64);
-                        dbl[kk] = umma_smem_desc(blo + kk * 32, tc::SBO_64B, kLayoutSW64);
+                    for (int kk = 0; kk < F::K_STEPS; ++kk) {
+                        dah[kk] = umma_smem_desc(ahi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                        dal[kk] = umma_smem_desc(alo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                        dbh[kk] = umma_smem_desc(bhi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                        dbl[kk] = umma_smem_desc(blo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
                     }
                     // both CTAs' split warps have seen their X and C stage land
-                    if (!mbar_wait_cluster(bar(tc::A_FULL + as), (it / tc::SA) & 1, p.status)) {
+                    if (!mbar_wait_cluster(bar(F::A_FULL + as), (it / F::SA) & 1, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < tc::BK / 16; ++kk) {
+                    for (int kk = 0; kk < F::K_STEPS; ++kk) {
                         const uint32_t first = (kb | kk) != 0 ? 1u : 0u;
-                        mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
-                        mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
-                        mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                        if constexpr (TF32) {
+                            mma_tf32_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
+                            mma_tf32_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
+                            mma_tf32_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                        } else {
+                            mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
+                            mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
+                            mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                        }
                     }
-                    mma_commit_pair_multicast(bar(tc::XB_EMPTY + s), tc::PAIR_MASK);
-                    mma_commit_pair_multicast(bar(tc::A_EMPTY + as), tc::PAIR_MASK);
+                    mma_commit_pair_multicast(bar(F::XB_EMPTY + s), tc::PAIR_MASK);
+                    mma_commit_pair_multicast(bar(F::A_EMPTY + as), tc::PAIR_MASK);
                 }
                 if (!ok) break;
-                mma_commit_pair_multicast(bar(tc::T_FULL + buf), tc::PAIR_MASK);
+                mma_commit_pair_multicast(bar(F::T_FULL + buf), tc::PAIR_MASK);
             }
             // no MMA may still be writing tensor memory when it is released
-            mma_commit_pair(bar(tc::DRAIN));
-            mbar_wait_drain(bar(tc::DRAIN), 0);
+            mma_commit_pair(bar(F::DRAIN));
+            mbar_wait_drain(bar(F::DRAIN), 0);
         }
     }
 
@@ -474,7 +565,7 @@ int device_sm_count() {
     return cached[dev];
 }
 
-int assign_tc_smem_bytes() { return tc::SMEM_BYTES; }
+int assign_tc_smem_bytes() { return tc::Fmt<false>::SMEM_BYTES; }
 
 // CTA pairs that can be resident at once (the persistent grid never exceeds
 // it, so no pair waits for another to finish).
@@ -488,7 +579,7 @@ static int resident_pairs() {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
         cfg.blockDim = dim3(tc::THREADS, 1, 1);
-        cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+        cfg.dynamicSmemBytes = tc::Fmt<false>::SMEM_BYTES;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
         attr.val.clusterDim.x = 2;
@@ -496,7 +587,8 @@ static int resident_pairs() {
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&clusters, assign_tc_kernel<true>, &cfg) != cudaSuccess || clusters < 1) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, assign_tc_kernel<true, false>, &cfg) != cudaSuccess ||
+            clusters < 1) {
             cudaGetLastError();  // clear
             clusters = device_sm_count() / 2;
         }
@@ -505,28 +597,38 @@ static int resident_pairs() {
     return cached[dev];
 }
 
+template <bool DB, bool TF32>
+static cudaError_t set_smem_limit() {
+    return cudaFuncSetAttribute(assign_tc_kernel<DB, TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                tc::Fmt<TF32>::SMEM_BYTES);
+}
+
 cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
-                             uint8_t *ws, cudaStream_t stream, bool chained) {
+                             uint8_t *ws, cudaStream_t stream, bool chained, bool tf32) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(assign_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        tc::SMEM_BYTES);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(assign_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            tc::SMEM_BYTES);
+        attr_err = set_smem_limit<true, false>();
+        if (attr_err == cudaSuccess) attr_err = set_smem_limit<false, false>();
+        if (attr_err == cudaSuccess) attr_err = set_smem_limit<true, true>();
+        if (attr_err == cudaSuccess) attr_err = set_smem_limit<false, true>();
     });
     if (attr_err != cudaSuccess) return attr_err;
 
+    // C hi / lo: bf16 (64-byte swizzle) or, for 3xTF32, fp32 (128-byte swizzle)
     CUtensorMap tmX, tmChi, tmClo;
     const void *chi = ws + L.off_chi;
     const void *clo = ws + L.off_clo;
+    const CUtensorMapDataType cdt = tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int cbytes = tf32 ? 4 : 2;
+    const CUtensorMapSwizzle cswz = tf32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (L.split_elem_bytes != cbytes) return cudaErrorInvalidValue;
     if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, X, (uint64_t)d, (uint64_t)n, (uint64_t)d,
                    tc::BK, tc::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmChi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, chi, (uint64_t)L.d_pad, (uint64_t)k,
-                   (uint64_t)L.d_pad, tc::BK, tc::BN_CTA, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !encode_2d(&tmClo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, clo, (uint64_t)L.d_pad, (uint64_t)k,
-                   (uint64_t)L.d_pad, tc::BK, tc::BN_CTA, CU_TENSOR_MAP_SWIZZLE_64B))
+        !encode_2d(&tmChi, cdt, cbytes, chi, (uint64_t)L.d_pad, (uint64_t)k, (uint64_t)L.d_pad, tc::BK, tc::BN_CTA,
+                   cswz) ||
+        !encode_2d(&tmClo, cdt, cbytes, clo, (uint64_t)L.d_pad, (uint64_t)k, (uint64_t)L.d_pad, tc::BK, tc::BN_CTA,
+                   cswz))
         return cudaErrorInvalidValue;
 
     TcParams p{};
@@ -550,12 +652,19 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
     const int grid = 2 * (pairs > 0 ? pairs : 1);
     trace_mark(kTraceAssignTc, false, stream);
-    const cudaError_t e =
-        d <= tc::SINGLE_ACC_MAX_D
-            ? launch_kernel(chained, assign_tc_kernel<true>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,
-                            tmX, tmChi, tmClo, p)
-            : launch_kernel(chained, assign_tc_kernel<false>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,
-                            tmX, tmChi, tmClo, p);
+    const bool db = d <= (tf32 ? tc::SINGLE_ACC_MAX_D_TF32 : tc::SINGLE_ACC_MAX_D);
+    const dim3 g(grid), b(tc::THREADS);
+    cudaError_t e;
+    if (tf32)
+        e = db ? launch_kernel(chained, assign_tc_kernel<true, true>, g, b, tc::Fmt<true>::SMEM_BYTES, stream, tmX, tmChi,
+                               tmClo, p)
+               : launch_kernel(chained, assign_tc_kernel<false, true>, g, b, tc::Fmt<true>::SMEM_BYTES, stream, tmX,
+                               tmChi, tmClo, p);
+    else
+        e = db ? launch_kernel(chained, assign_tc_kernel<true, false>, g, b, tc::Fmt<false>::SMEM_BYTES, stream, tmX,
+                               tmChi, tmClo, p)
+               : launch_kernel(chained, assign_tc_kernel<false, false>, g, b, tc::Fmt<false>::SMEM_BYTES, stream, tmX,
+                               tmChi, tmClo, p);
     trace_mark(kTraceAssignTc, true, stream);
     return e;
 }

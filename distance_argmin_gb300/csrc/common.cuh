@@ -115,21 +115,23 @@ struct AssignLayout {
     int64_t off_chi;     // k x d_pad bf16 hi part of C
     int64_t off_clo;     // k x d_pad bf16 lo part of C
     int64_t off_partial; // kMaxReduceBlocks x f64 inertia partial sums
+    int64_t split_elem_bytes;  // 2: bf16 hi / lo of C; 4: fp32 (3xTF32) hi / lo
     int64_t bytes;
 };
 
 constexpr int kMaxReduceBlocks = 1024;
 
-inline AssignLayout assign_layout(int64_t n, int64_t k, int64_t d, bool split) {
+inline AssignLayout assign_layout(int64_t n, int64_t k, int64_t d, bool split, int split_elem_bytes = 2) {
     AssignLayout L{};
     L.d_pad = align_up(d, 64);
+    L.split_elem_bytes = split ? split_elem_bytes : 0;
     int64_t o = sizeof(WsHeader);
     o = align_up(o, 1024); L.off_keys = o; o += n * 8;
     o = align_up(o, 1024); L.off_xnorm = o; o += n * 4;
     o = align_up(o, 1024); L.off_cnorm = o; o += k * 4;
     if (split) {
-        o = align_up(o, 1024); L.off_chi = o; o += k * L.d_pad * 2;
-        o = align_up(o, 1024); L.off_clo = o; o += k * L.d_pad * 2;
+        o = align_up(o, 1024); L.off_chi = o; o += k * L.d_pad * split_elem_bytes;
+        o = align_up(o, 1024); L.off_clo = o; o += k * L.d_pad * split_elem_bytes;
     } else {
         L.off_chi = L.off_clo = 0;
     }

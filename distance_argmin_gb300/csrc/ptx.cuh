@@ -337,6 +337,17 @@ __device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_des
         : "memory");
 }
 
+// The same pair MMA on tf32 operands (kind::tf32, K = 8 per instruction).
+__device__ __forceinline__ void mma_tf32_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the barrier at this shared offset in every CTA of `mask`
 // when all tcgen05 operations issued so far by this thread have completed.
 __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t mask) {
@@ -370,6 +381,15 @@ __device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t sbo_
     d |= static_cast<uint64_t>(1u) << 46;  // descriptor version
     d |= static_cast<uint64_t>(layout & 7u) << 61;
     return d;
+}
+
+// Instruction descriptor of kind::tf32: tf32 A and B (both K-major), f32 D.
+__host__ __device__ constexpr uint32_t umma_idesc_tf32_f32(int M, int N) {
+    return (1u << 4)                                  // D format: f32
+           | (2u << 7)                                // A format: tf32
+           | (2u << 10)                               // B format: tf32
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
 // Instruction descriptor of kind::f16: bf16 A and B (both K-major), f32 D.

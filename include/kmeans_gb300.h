@@ -78,7 +78,8 @@ enum {
     KMEANS_OP_UPDATE = 2,
     KMEANS_OP_LLOYD = 3,
     KMEANS_OP_KMEANSPP = 4,
-    KMEANS_OP_FIT = 5
+    KMEANS_OP_FIT = 5,
+    KMEANS_OP_ASSIGN_3XTF32 = 6
 };
 
 /* Initialisation of kmeans_fit. */
@@ -111,6 +112,20 @@ int kmeans_assign(const float *X, const float *C, int64_t n, int64_t k, int64_t 
 int kmeans_assign_ffma(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
                        int64_t *labels, float *best_dist, double *inertia,
                        void *ws, size_t ws_bytes, uint64_t seed, void *stream);
+
+/* The same assignment [G][R][S] on the tensor cores with the 3xTF32 split
+ * instead of bf16x3 (a comparator of the operand split; the pages run
+ * float32 with TF32 off): hi = v with its low 13 mantissa bits cleared, lo =
+ * (v - hi) with its low 13 bits cleared, x.c = hi.hi + lo.hi + hi.lo from
+ * kind::tf32 MMAs.  TF32 runs at half the bf16 rate, so about half the
+ * throughput; and an MMA covers 8 features instead of 16, so the float32
+ * accumulator takes twice the truncating adds: the operands are more exact
+ * but the distances less (one accumulator up to d = 2048, separate ones
+ * above; the 1e-4 bound holds for d up to about 8192).
+ * Same requirements as kmeans_assign; workspace KMEANS_OP_ASSIGN_3XTF32. */
+int kmeans_assign_3xtf32(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
+                         int64_t *labels, float *best_dist, double *inertia,
+                         void *ws, size_t ws_bytes, uint64_t seed, void *stream);
 
 /* Mean update [U].
  * C_new[j] = mean of the rows X[i] with labels[i] == j, summed in float32 with

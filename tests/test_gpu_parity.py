@@ -37,8 +37,11 @@ SMALL = [
 ]
 
 
+ASSIGN_IMPLS = {"tc": "kmeans_assign", "tf32": "kmeans_assign_3xtf32", "ffma": "kmeans_assign_ffma"}
+
+
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
-@pytest.mark.parametrize("impl", ["tc", "ffma"])
+@pytest.mark.parametrize("impl", list(ASSIGN_IMPLS))
 @pytest.mark.parametrize("data", ["blobs", "gauss"])
 def test_assign_matches_oracle(gpu_lib, shape, impl, data):
     n, k, d = shape
@@ -48,7 +51,7 @@ def test_assign_matches_oracle(gpu_lib, shape, impl, data):
     else:
         X = synth.gaussian((n, d), seed=n * 3 + 1, scale=2.0)
         C = synth.gaussian((k, d), seed=k * 7 + 2, scale=2.0)
-    fn = gpu_lib.kmeans_assign if impl == "tc" else gpu_lib.kmeans_assign_ffma
+    fn = getattr(gpu_lib, ASSIGN_IMPLS[impl])
     labels, best, inertia = fn(dev_tensor(X), dev_tensor(C))
     o_l, o_b, o_s, o_in = oracle.assign(X, C)
     check_assign(X, C, host(labels), host(best), o_l, o_b, o_s, what=f"{impl} {shape}")
@@ -57,14 +60,14 @@ def test_assign_matches_oracle(gpu_lib, shape, impl, data):
     assert abs(float(inertia.item()) - o_in) <= 1e-4 * scale
 
 
-@pytest.mark.parametrize("impl", ["tc", "ffma"])
+@pytest.mark.parametrize("impl", list(ASSIGN_IMPLS))
 def test_duplicate_centroids_resolve_to_lowest_index(gpu_lib, impl):
     X = synth.gaussian((1500, 96), seed=5)
     C = synth.gaussian((600, 96), seed=6)
     C[517] = C[3]      # across centroid tiles
     C[40] = C[39]      # inside one tile
     C[299] = C[260]
-    fn = gpu_lib.kmeans_assign if impl == "tc" else gpu_lib.kmeans_assign_ffma
+    fn = getattr(gpu_lib, ASSIGN_IMPLS[impl])
     labels, best, _ = fn(dev_tensor(X), dev_tensor(C))
     lab = host(labels)
     assert not np.isin(lab, [517, 40, 299]).any()
@@ -266,19 +269,21 @@ def test_large_workload_one_iteration(gpu_lib, name):
     assert np.isfinite(bd).all() and (bd >= 0).all()
 
 
-@pytest.mark.parametrize("d", [4096, 4100])
-def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d):
-    # up to 4096 features the three split products share one double-buffered
-    # accumulator per tile; above, the corrections keep their own.  Several
-    # tiles per CTA pair, ragged sample and centroid tiles.
+@pytest.mark.parametrize("impl,d", [("tc", 4096), ("tc", 4100), ("tf32", 2048), ("tf32", 2052), ("tf32", 8192)])
+def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d, impl):
+    # up to 4096 features (bf16x3; 2048 for 3xTF32) the three split products
+    # share one double-buffered accumulator per tile; above, the corrections
+    # keep their own.  Several tiles per CTA pair, ragged sample and centroid
+    # tiles.
     n, k = 20000, 700
     X, _, _ = synth.planted_blobs(n, d, 64, seed=91)
     C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=92)])
-    labels, best, inertia = gpu_lib.kmeans_assign(dev_tensor(X), dev_tensor(C))
+    labels, best, inertia = getattr(gpu_lib, ASSIGN_IMPLS[impl])(dev_tensor(X), dev_tensor(C))
     rows = _sample_rows(n, 512, 93)
     o_l, o_b, o_s, _ = oracle.assign(X[rows], C)
-    flips, worst = check_assign(X[rows], C, host(labels), host(best), o_l, o_b, o_s, rows=rows, what=f"d={d}")
-    print(f"d={d}: worst relative distance error {worst:.3e}, near-tie flips {flips} of {len(rows)}")
+    flips, worst = check_assign(X[rows], C, host(labels), host(best), o_l, o_b, o_s, rows=rows,
+                                what=f"{impl} d={d}")
+    print(f"{impl} d={d}: worst relative distance error {worst:.3e}, near-tie flips {flips} of {len(rows)}")
 
 
 @pytest.mark.slow
