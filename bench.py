@@ -376,6 +376,23 @@ def run_gb300(args):
     t_ffma = ev0.elapsed_time(ev1) / 1e3 / f_steps
     del ws_f
 
+    # the Lloyd iteration with the update fused into the assignment (float
+    # atomics, not bitwise reproducible), against the sorted pass above
+    t_fused = None
+    if d <= 4096:
+        ws_fu = km.workspace(km.OP_LLOYD_FUSED, n, k, d, dev)
+        C_fu = torch.empty_like(C0d)
+        for _ in range(3):
+            km.kmeans_lloyd_iter_fused(Xd, C0d, C_fu, labels, best, inertia_a, counts, ws=ws_fu, stream=stream)
+        barrier()
+        ev0.record(stream)
+        for _ in range(steps):
+            km.kmeans_lloyd_iter_fused(Xd, C0d, C_fu, labels, best, inertia_a, counts, ws=ws_fu, stream=stream)
+        ev1.record(stream)
+        barrier()
+        t_fused = ev0.elapsed_time(ev1) / 1e3 / steps
+        del ws_fu
+
     # the 3xTF32 comparator of the operand split: the same kernel with
     # kind::tf32 MMAs (TF32 runs at half the bf16 rate)
     ws_t = km.workspace(km.OP_ASSIGN_3XTF32, n, k, d, dev)
@@ -473,6 +490,10 @@ def run_gb300(args):
                                              "timed": "in the Lloyd timed region"}},
         "assign_ffma": {"ms": 1e3 * t_ffma, "tflops": flop / t_ffma / 1e12,
                         "speedup_of_tensor_path": t_ffma / t_assign},
+        "lloyd_fused": None if t_fused is None else {
+            "ms": 1e3 * t_fused, "tflops": flop / t_fused / 1e12, "speedup_over_sorted_update": t_lloyd / t_fused,
+            "note": "kmeans_lloyd_iter_fused from the same centroids every step: the update fused into the "
+                    "assignment epilogue with float atomics (C_new not bitwise reproducible)"},
         "assign_3xtf32": {"ms": 1e3 * t_tf32, "tflops": flop / t_tf32 / 1e12,
                           "frac_of_tf32_R": flop / t_tf32 / 1e12 / (TF32_NOMINAL_TFLOPS / SPLIT_PRODUCTS),
                           "speedup_of_bf16x3": t_tf32 / t_assign,

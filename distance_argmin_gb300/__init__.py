@@ -38,6 +38,7 @@ OP_LLOYD = 3
 OP_KMEANSPP = 4
 OP_FIT = 5
 OP_ASSIGN_3XTF32 = 6
+OP_LLOYD_FUSED = 7
 
 INIT_GIVEN = 0
 INIT_KMEANSPP = 1
@@ -54,6 +55,7 @@ EXPORTS = (
     "kmeans_lloyd_iter", "kmeanspp_init", "kmeans_device_status", "kmeans_status_string",
     "kmeans_build_info", "kmeans_assign_noalloc", "kmeans_trace_start", "kmeans_trace_read",
     "kmeans_trace_stop", "kmeans_lloyd_iter_host", "kmeans_fit", "kmeans_assign_3xtf32",
+    "kmeans_lloyd_iter_fused",
 )
 
 _lock = threading.Lock()
@@ -93,6 +95,8 @@ def load(path: str | None = None):
         lib.kmeans_update.argtypes = [P, P, P, P, P, I64, I64, I64, P, SZ, U64, P]
         lib.kmeans_update.restype = INT
         lib.kmeans_lloyd_iter.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, P, SZ, U64, P]
+        lib.kmeans_lloyd_iter_fused.argtypes = lib.kmeans_lloyd_iter.argtypes
+        lib.kmeans_lloyd_iter_fused.restype = INT
         lib.kmeans_lloyd_iter.restype = INT
         lib.kmeanspp_init.argtypes = [P, I64, I64, I64, INT, U64, P, P, P, SZ, P]
         lib.kmeanspp_init.restype = INT
@@ -270,9 +274,7 @@ def kmeans_update(X, labels, C_old, C_new=None, counts=None, ws=None, seed=0, st
     return C_new, counts
 
 
-def kmeans_lloyd_iter(X, C_old, C_new=None, labels=None, best_dist=None, inertia=None, counts=None, ws=None,
-                      seed=0, stream=None):
-    """One Lloyd iteration -> ``(C_new, labels, best_dist, inertia, counts)``."""
+def _lloyd(fn_name, op, X, C_old, C_new, labels, best_dist, inertia, counts, ws, seed, stream):
     torch = _torch()
     _check(X, "X", torch.float32)
     n, d = X.shape
@@ -293,12 +295,27 @@ def kmeans_lloyd_iter(X, C_old, C_new=None, labels=None, best_dist=None, inertia
     _check(best_dist, "best_dist", torch.float32, (n,), X.device)
     _check(inertia, "inertia", torch.float64, (1,), X.device)
     _check(counts, "counts", torch.int32, (k,), X.device)
-    ws = _ws(ws, OP_LLOYD, n, k, d, X.device)
-    st = load().kmeans_lloyd_iter(_ptr(X), _ptr(C_old), _ptr(C_new), _ptr(labels), _ptr(best_dist),
+    ws = _ws(ws, op, n, k, d, X.device)
+    st = getattr(load(), fn_name)(_ptr(X), _ptr(C_old), _ptr(C_new), _ptr(labels), _ptr(best_dist),
                                   _ptr(inertia), _ptr(counts), n, k, d, _ptr(ws), ws.numel(),
                                   seed & (2**64 - 1), _stream_handle(stream))
-    _raise(st, "kmeans_lloyd_iter")
+    _raise(st, fn_name)
     return C_new, labels, best_dist, inertia, counts
+
+
+def kmeans_lloyd_iter(X, C_old, C_new=None, labels=None, best_dist=None, inertia=None, counts=None, ws=None,
+                      seed=0, stream=None):
+    """One Lloyd iteration -> ``(C_new, labels, best_dist, inertia, counts)``."""
+    return _lloyd("kmeans_lloyd_iter", OP_LLOYD, X, C_old, C_new, labels, best_dist, inertia, counts, ws, seed,
+                  stream)
+
+
+def kmeans_lloyd_iter_fused(X, C_old, C_new=None, labels=None, best_dist=None, inertia=None, counts=None, ws=None,
+                            seed=0, stream=None):
+    """One Lloyd iteration with the update fused into the assignment (float
+    atomics: C_new is not bitwise reproducible) -> as kmeans_lloyd_iter."""
+    return _lloyd("kmeans_lloyd_iter_fused", OP_LLOYD_FUSED, X, C_old, C_new, labels, best_dist, inertia, counts,
+                  ws, seed, stream)
 
 
 def kmeanspp_init(X, k: int, seed: int, n_trials: int = 0, centers=None, indices=None, ws=None, stream=None):

@@ -100,6 +100,27 @@ FitLayout fit_layout(int64_t n, int64_t k, int64_t d) {
     return F;
 }
 
+// kmeans_lloyd_iter_fused's workspace: the assignment's scratch, then the
+// zeroed accumulation area (sums, counts, per-32-row completion counters).
+struct FusedLayout {
+    AssignLayout A;
+    int64_t off_sums;  // k x d f32
+    int64_t off_cnt;   // k x i32
+    int64_t off_done;  // ceil(n / 256) x 8 x u32
+    int64_t bytes;
+};
+
+FusedLayout fused_layout(int64_t n, int64_t k, int64_t d) {
+    FusedLayout F{};
+    F.A = assign_layout(n, k, d, true);
+    int64_t o = align_up(F.A.bytes, 1024);
+    F.off_sums = o; o = align_up(o + k * d * 4, 256);
+    F.off_cnt = o; o = align_up(o + k * 4, 256);
+    F.off_done = o; o += ((n + 255) / 256) * 8 * 4;
+    F.bytes = align_up(o, 1024);
+    return F;
+}
+
 // The Lloyd iteration after the tensor-core pass has written every sample's
 // key: finalize (with the per-tile member count on the counting path), then
 // the mean update.  The update reuses the assignment's workspace: its scratch
@@ -140,6 +161,8 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
             return (size_t)kpp_layout(n, d, kKppMaxTrials).bytes;
         case KMEANS_OP_FIT:
             return (size_t)fit_layout(n, k, d).bytes;
+        case KMEANS_OP_LLOYD_FUSED:
+            return (size_t)fused_layout(n, k, d).bytes;
         default:
             return 0;
     }
@@ -198,6 +221,34 @@ int kmeans_lloyd_iter(const float *X, const float *C_old, float *C_new, int64_t 
     cudaError_t e = launch_prep_split(C_old, n, k, d, A, w, s);
     if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, A, w, s);
     if (e == cudaSuccess) e = lloyd_finish(X, C_old, C_new, labels, best_dist, inertia, counts, n, k, d, A, w, s);
+    return cuda_status(e);
+}
+
+int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, int64_t *labels, float *best_dist,
+                            double *inertia, int32_t *counts, int64_t n, int64_t k, int64_t d, void *ws,
+                            size_t ws_bytes, uint64_t seed, void *stream) {
+    (void)seed;
+    if (!X || !C_old || !C_new || !labels || !best_dist || C_new == C_old) return KMEANS_ERR_INVALID_ARG;
+    if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(labels) & 7u)) return KMEANS_ERR_INVALID_ARG;
+    const int st = tc_path_ok(X, C_old, d);
+    if (st != KMEANS_OK) return st;
+    if (!aligned16(C_new) || d > 4096) return KMEANS_ERR_UNSUPPORTED;
+    const FusedLayout F = fused_layout(n, k, d);
+    const int wst = check_ws(ws, ws_bytes, (size_t)F.bytes);
+    if (wst != KMEANS_OK) return wst;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    FusedUpdate fu;
+    fu.X = X;
+    fu.sums = reinterpret_cast<float *>(w + F.off_sums);
+    fu.counts = reinterpret_cast<int32_t *>(w + F.off_cnt);
+    fu.row_done = reinterpret_cast<uint32_t *>(w + F.off_done);
+    cudaError_t e = cudaMemsetAsync(w + F.off_sums, 0, (size_t)(F.bytes - F.off_sums), s);
+    if (e == cudaSuccess) e = launch_prep_split(C_old, n, k, d, F.A, w, s);
+    if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, F.A, w, s, true, false, &fu);
+    if (e == cudaSuccess) e = launch_finalize(n, F.A, w, labels, best_dist, inertia, s);
+    if (e == cudaSuccess) e = launch_fused_mean(fu.sums, fu.counts, C_old, C_new, counts, k, d, s);
     return cuda_status(e);
 }
 

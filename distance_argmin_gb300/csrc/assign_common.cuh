@@ -20,12 +20,23 @@ cudaError_t launch_prep_split(const float *C, int64_t n, int64_t k, int64_t d, c
 cudaError_t launch_prep_norms(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
                               uint8_t *ws, cudaStream_t s);
 
+// Where the update fused into the assignment's epilogue accumulates
+// (kmeans_lloyd_iter_fused): X, the (k, d) sums and (k) counts, zeroed
+// beforehand, and one completion counter per 32 rows of every CTA.
+struct FusedUpdate {
+    const float *X;
+    float *sums;
+    int32_t *counts;
+    uint32_t *row_done;
+};
+
 // `chained`: launched to overlap the tail of the kernel before it on `s`
 // (the prologue's split); false after a wait on an event.  `tf32`: the
 // 3xTF32 operand split (L from assign_layout(..., true, 4) and the centroid
 // copies from launch_prep_split_tf32) instead of bf16x3.
 cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
-                             uint8_t *ws, cudaStream_t s, bool chained = true, bool tf32 = false);
+                             uint8_t *ws, cudaStream_t s, bool chained = true, bool tf32 = false,
+                             const FusedUpdate *fused = nullptr);
 
 // launch_prep_split for the 3xTF32 path: C's hi (low 13 mantissa bits
 // cleared) and lo (C - hi, low 13 bits cleared) as fp32, row pitch L.d_pad.

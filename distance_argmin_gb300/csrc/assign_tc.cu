@@ -139,6 +139,7 @@ struct TcParams {
     unsigned long long *keys;
     uint32_t *status;
     int test_starve;  // test hook: the producer issues no loads, so the pipeline waits run out
+    FusedUpdate fu;   // the update fused into the epilogue (kmeans_lloyd_iter_fused), else all null
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb) {
@@ -245,9 +246,51 @@ __device__ __forceinline__ void split_kblock_tf32(uint8_t *xs, uint8_t *alo, int
     }
 }
 
+// The update fused into the epilogue: the warp that merged the last column
+// tile into 32 rows' keys adds those rows of X (still in L2: every column
+// tile of the row block has just streamed them) into their clusters' sums
+// with vector float atomics, and counts them.  The keys are final: every
+// merging warp fenced its atomicMin before counting itself done.
+__device__ __forceinline__ void fused_accumulate_rows(const TcParams &p, int row0, int lane) {
+    const int i = row0 + lane;
+    int j = -1;
+    if (i < p.n) {
+        const unsigned long long key = __ldcg(p.keys + i);
+        if (key != kEmptyKey) j = (int)(key & 0xffffffffu);
+    }
+    if (j >= 0) atomicAdd(p.fu.counts + j, 1);
+    const int d4 = p.d >> 2;
+    const float4 *X4 = reinterpret_cast<const float4 *>(p.fu.X);
+    float4 *S4 = reinterpret_cast<float4 *>(p.fu.sums);
+    // two rows at a time, 8 chunks of each per lane: 16 loads in flight
+    // before their atomics (one at a time, the loads' latency dominates)
+    constexpr int U = 8;
+    for (int r = 0; r < 32; r += 2) {
+        const int ja = __shfl_sync(0xffffffffu, j, r);
+        const int jb = __shfl_sync(0xffffffffu, j, r + 1);
+        const float4 *xa = X4 + (size_t)(row0 + r) * d4;
+        const float4 *xb = X4 + (size_t)(row0 + r + 1) * d4;
+        for (int c0 = lane; c0 < d4; c0 += 32 * U) {
+            float4 va[U], vb[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + 32 * u;
+                va[u] = (ja >= 0 && c < d4) ? __ldg(xa + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                vb[u] = (jb >= 0 && c < d4) ? __ldg(xb + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + 32 * u;
+                if (ja >= 0 && c < d4) atomicAdd(S4 + (size_t)ja * d4 + c, va[u]);
+                if (jb >= 0 && c < d4) atomicAdd(S4 + (size_t)jb * d4 + c, vb[u]);
+            }
+        }
+    }
+}
+
 // DB: one accumulator per tile, double-buffered (d <= SINGLE_ACC_MAX_D); TF32:
 // the 3xTF32 operand split instead of bf16x3 (see Fmt)
-template <bool DB, bool TF32>
+template <bool DB, bool TF32, bool FUSED = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     assign_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmChi,
                      const __grid_constant__ CUtensorMap tmClo, const TcParams p) {
@@ -411,6 +454,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(F::T_EMPTY + buf), 0));
             const int row = mb * (2 * tc::BM) + (int)rank * tc::BM + q * 32 + lane;
             if (row < p.n && arg >= 0) atomicMin(p.keys + row, make_key(best, (uint32_t)arg));
+            if constexpr (FUSED) {
+                // two warps per lane quarter merge into these 32 rows for each
+                // of the num_n column tiles; the last of them adds the rows
+                static_assert(tc::EPI_WARPS == 8, "two epilogue warps per lane quarter");
+                __threadfence();
+                __syncwarp();
+                unsigned done = 0;
+                if (lane == 0) done = atomicAdd(p.fu.row_done + ((mb * 2 + (int)rank) * 4 + q), 1u);
+                done = __shfl_sync(0xffffffffu, done, 0);
+                if (done == 2u * (unsigned)p.num_n - 1u) {
+                    __threadfence();
+                    fused_accumulate_rows(p, mb * (2 * tc::BM) + (int)rank * tc::BM + q * 32, lane);
+                }
+            }
         }
     } else if (warp == tc::WARP_TMA) {
         // ------------------------------------------------------- TMA producer
@@ -604,7 +661,7 @@ static cudaError_t set_smem_limit() {
 }
 
 cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
-                             uint8_t *ws, cudaStream_t stream, bool chained, bool tf32) {
+                             uint8_t *ws, cudaStream_t stream, bool chained, bool tf32, const FusedUpdate *fused) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -612,6 +669,9 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
         if (attr_err == cudaSuccess) attr_err = set_smem_limit<false, false>();
         if (attr_err == cudaSuccess) attr_err = set_smem_limit<true, true>();
         if (attr_err == cudaSuccess) attr_err = set_smem_limit<false, true>();
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(assign_tc_kernel<true, false, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Fmt<false>::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
@@ -655,7 +715,13 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     const bool db = d <= (tf32 ? tc::SINGLE_ACC_MAX_D_TF32 : tc::SINGLE_ACC_MAX_D);
     const dim3 g(grid), b(tc::THREADS);
     cudaError_t e;
-    if (tf32)
+    if (fused) {
+        // bf16x3 with double-buffered accumulators only
+        if (tf32 || !db) return cudaErrorInvalidValue;
+        p.fu = *fused;
+        e = launch_kernel(chained, assign_tc_kernel<true, false, true>, g, b, tc::Fmt<false>::SMEM_BYTES, stream, tmX,
+                          tmChi, tmClo, p);
+    } else if (tf32)
         e = db ? launch_kernel(chained, assign_tc_kernel<true, true>, g, b, tc::Fmt<true>::SMEM_BYTES, stream, tmX, tmChi,
                                tmClo, p)
                : launch_kernel(chained, assign_tc_kernel<false, true>, g, b, tc::Fmt<true>::SMEM_BYTES, stream, tmX,

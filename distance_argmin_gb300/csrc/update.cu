@@ -619,6 +619,39 @@ __global__ void __launch_bounds__(kFixThreads)
     }
 }
 
+// The mean step after the update fused into the assignment: C_new = sums /
+// count per cluster (the same division as the sorted path), the old row for
+// an empty cluster, and the counts.
+__global__ void __launch_bounds__(256)
+    fused_mean_kernel(const float4 *__restrict__ sums, const int32_t *__restrict__ cnt, const float *__restrict__ C_old,
+                      float *__restrict__ C_new, int32_t *__restrict__ counts_out, int k, int d4) {
+    griddep_wait();
+    const int64_t total = (int64_t)k * d4;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(g / d4);
+        const int c = cnt[j];
+        float4 v;
+        if (c > 0) {
+            const float4 sv = sums[g];
+            const float f = (float)c;
+            v = make_float4(sv.x / f, sv.y / f, sv.z / f, sv.w / f);
+        } else {
+            v = reinterpret_cast<const float4 *>(C_old)[g];
+        }
+        reinterpret_cast<float4 *>(C_new)[g] = v;
+        if (counts_out && g - (int64_t)j * d4 == 0) counts_out[j] = c;
+    }
+}
+
+cudaError_t launch_fused_mean(const float *sums, const int32_t *cnt, const float *C_old, float *C_new,
+                              int32_t *counts_out, int64_t k, int64_t d, cudaStream_t s) {
+    const int64_t total = k * (d / 4);
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    return launch_kernel(true, fused_mean_kernel, dim3((unsigned)(blocks < 1 ? 1 : blocks)), dim3(256), 0, s,
+                         reinterpret_cast<const float4 *>(sums), cnt, C_old, C_new, counts_out, (int)k, (int)(d / 4));
+}
+
 // Per device, once: allow the per-cluster shared-memory counters of the
 // counting path above the 48 KiB default.
 static void set_counting_smem_limits(int64_t k) {

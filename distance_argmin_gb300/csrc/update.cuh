@@ -18,4 +18,9 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
 cudaError_t launch_finalize_counting(int64_t n, int64_t k, const AssignLayout &A, const UpdateLayout &U,
                                      uint8_t *ws, int64_t *labels, float *best, double *inertia, cudaStream_t s);
 
+// Mean step of kmeans_lloyd_iter_fused: C_new = sums / count (d % 4 == 0,
+// 16-byte aligned rows), old rows for empty clusters, counts_out (may be null).
+cudaError_t launch_fused_mean(const float *sums, const int32_t *cnt, const float *C_old, float *C_new,
+                              int32_t *counts_out, int64_t k, int64_t d, cudaStream_t s);
+
 }  // namespace km

@@ -79,7 +79,8 @@ enum {
     KMEANS_OP_LLOYD = 3,
     KMEANS_OP_KMEANSPP = 4,
     KMEANS_OP_FIT = 5,
-    KMEANS_OP_ASSIGN_3XTF32 = 6
+    KMEANS_OP_ASSIGN_3XTF32 = 6,
+    KMEANS_OP_LLOYD_FUSED = 7
 };
 
 /* Initialisation of kmeans_fit. */
@@ -148,6 +149,25 @@ int kmeans_lloyd_iter(const float *X, const float *C_old, float *C_new, int64_t 
                       float *best_dist, double *inertia, int32_t *counts,
                       int64_t n, int64_t k, int64_t d,
                       void *ws, size_t ws_bytes, uint64_t seed, void *stream);
+
+/* One Lloyd iteration [U] with the update fused into the assignment (an
+ * opt-in variant of kmeans_lloyd_iter; the pages have no counterpart).  As
+ * soon as every centroid tile has merged its minimum into a group of 32
+ * samples, the epilogue warp that merged last adds those samples' rows
+ * (still in L2) into their clusters' sums with float atomics; a last pass
+ * divides.  No sorted member list and no second pass over X in HBM.
+ * Labels, best_dist and *inertia are kmeans_lloyd_iter's bit for bit.
+ * C_new differs: the sums are plain float32 in an order that varies from run
+ * to run (not reproducible bit for bit), so a cluster of m members carries a
+ * relative error up to about m * 2^-24 (within 1e-5 up to some 150 members
+ * per cluster); empty clusters keep C_old bit for bit.  counts (may be NULL)
+ * are exact.  Same requirements as kmeans_lloyd_iter plus d <= 4096 and
+ * C_new 16-byte aligned (KMEANS_ERR_UNSUPPORTED otherwise); C_new must not
+ * alias C_old; workspace KMEANS_OP_LLOYD_FUSED. */
+int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, int64_t *labels,
+                            float *best_dist, double *inertia, int32_t *counts,
+                            int64_t n, int64_t k, int64_t d,
+                            void *ws, size_t ws_bytes, uint64_t seed, void *stream);
 
 /* Most slices kmeans_lloyd_iter_host splits the samples into. */
 #define KMEANS_HOST_MAX_SLICES 64
