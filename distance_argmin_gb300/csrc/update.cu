@@ -453,6 +453,24 @@ __global__ void __launch_bounds__(kMeanThreads)
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f), cmp = make_float4(0.f, 0.f, 0.f, 0.f);
         int r = p;
         if (VEC) {
+            // 32 member rows in flight, then 16, 8, 4, 1 (measured: 32 over 8
+            // is 7-9% faster on every workload; the sums keep member order)
+            for (; r + 32 <= q; r += 32) {
+                float4 v[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    v[u] = __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r + u - p0] * d + col));
+#pragma unroll
+                for (int u = 0; u < 32; ++u) kahan4(s, cmp, v[u]);
+            }
+            for (; r + 16 <= q; r += 16) {
+                float4 v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    v[u] = __ldg(reinterpret_cast<const float4 *>(X + (size_t)s_perm[r + u - p0] * d + col));
+#pragma unroll
+                for (int u = 0; u < 16; ++u) kahan4(s, cmp, v[u]);
+            }
             for (; r + 8 <= q; r += 8) {
                 float4 v[8];
 #pragma unroll
