@@ -48,6 +48,7 @@ KERNEL_UPDATE_MEAN = 1
 KERNEL_KMEANSPP_DIST = 2
 TRACE_MAX_CAPACITY = 65536
 HOST_MAX_SLICES = 64
+HOST_OVERLAP_PREVIOUS = 1
 
 # Every symbol the header declares (the ABI test checks the library exports them).
 EXPORTS = (
@@ -110,7 +111,8 @@ def load(path: str | None = None):
         lib.kmeans_trace_start.restype = INT
         lib.kmeans_trace_read.argtypes = [INT, P, P, P]
         lib.kmeans_trace_read.restype = INT
-        lib.kmeans_lloyd_iter_host.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, INT, P, SZ, P, P]
+        lib.kmeans_lloyd_iter_host.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, INT, INT, P, SZ, P,
+                                               P]
         lib.kmeans_lloyd_iter_host.restype = INT
         lib.kmeans_fit.argtypes = [P, P, P, P, P, I64, I64, I64, INT, U64, INT, ctypes.c_double, P, P, P, SZ, P]
         lib.kmeans_fit.restype = INT
@@ -406,7 +408,8 @@ def kmeans_trace_stop() -> None:
 
 
 def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_out_h, labels_h, inertia_h,
-                           slices: int = 16, ws=None, inertia=None, copy_stream=None, stream=None):
+                           slices: int = 16, ws=None, inertia=None, copy_stream=None, stream=None,
+                           overlap_previous: bool = False):
     """One Lloyd iteration on inputs that live in pinned host memory.
 
     The library copies the samples to ``Xd`` in ``slices`` row slices on
@@ -414,7 +417,9 @@ def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_o
     landed; the update follows, and C_new, the labels and the inertia come
     back to ``C_out_h``, ``labels_h`` and ``inertia_h`` (one float64).  The
     device outputs equal kmeans_lloyd_iter's bit for bit.  Returns an event
-    recorded on ``stream`` after the last copy.
+    recorded on ``stream`` after the last copy.  ``overlap_previous``: the
+    copies may overlap earlier work on ``stream`` (the caller guarantees that
+    ``Xd`` and ``Cd`` are not in use, e.g. by alternating two sets).
     Xh, Ch, C_out_h, labels_h, inertia_h: pinned host tensors.
     Xd, Cd, C_new, labels, best_dist, counts: device tensors (preallocated).
     """
@@ -441,7 +446,8 @@ def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_o
         ws = workspace(OP_LLOYD, n, k, d, Xd.device)
     st = load().kmeans_lloyd_iter_host(Xh.data_ptr(), Ch.data_ptr(), _ptr(Xd), _ptr(Cd), _ptr(C_new), _ptr(labels),
                                        _ptr(best_dist), _ptr(inertia), _ptr(counts), C_out_h.data_ptr(),
-                                       labels_h.data_ptr(), inertia_h.data_ptr(), n, k, d, int(slices), _ptr(ws),
+                                       labels_h.data_ptr(), inertia_h.data_ptr(), n, k, d, int(slices),
+                                       HOST_OVERLAP_PREVIOUS if overlap_previous else 0, _ptr(ws),
                                        ws.numel(), _stream_handle(stream), _stream_handle(copy_stream))
     _raise(st, "kmeans_lloyd_iter_host")
     done = torch.cuda.Event()

@@ -255,10 +255,11 @@ int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, in
 int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, float *C_old, float *C_new,
                            int64_t *labels, float *best_dist, double *inertia, int32_t *counts, float *C_new_host,
                            int64_t *labels_host, double *inertia_host, int64_t n, int64_t k, int64_t d, int slices,
-                           void *ws, size_t ws_bytes, void *stream, void *copy_stream) {
+                           int flags, void *ws, size_t ws_bytes, void *stream, void *copy_stream) {
     if (!X_host || !C_host || !X || !C_old || !C_new || !labels || !best_dist) return KMEANS_ERR_INVALID_ARG;
     if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
     if (slices < 1 || slices > KMEANS_HOST_MAX_SLICES) return KMEANS_ERR_INVALID_ARG;
+    if (flags & ~KMEANS_HOST_OVERLAP_PREVIOUS) return KMEANS_ERR_INVALID_ARG;
     if (stream == copy_stream || (inertia_host && !inertia)) return KMEANS_ERR_INVALID_ARG;
     if (!aligned4(C_new) || (reinterpret_cast<uintptr_t>(labels) & 7u)) return KMEANS_ERR_INVALID_ARG;
     const int st = tc_path_ok(X, C_old, d);
@@ -279,11 +280,15 @@ int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, f
     cudaError_t e = cudaSuccess;
     for (; made < used + 2 && e == cudaSuccess; ++made) e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
     if (e != cudaSuccess) --made;  // the failed one was not created
-    // the copies wait for everything enqueued on `stream` before this call;
-    // the centroids go first on the copy stream (a copy on `stream` could be
-    // scheduled behind all the sample slices and hold back every slice)
-    if (e == cudaSuccess) e = cudaEventRecord(ev[used], s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[used], 0);
+    // the copies wait for everything enqueued on `stream` before this call,
+    // unless the caller vouches that X and C_old are free (then they may
+    // overlap the previous call's update); the centroids go first on the
+    // copy stream (a copy on `stream` could be scheduled behind all the
+    // sample slices and hold back every slice)
+    if (!(flags & KMEANS_HOST_OVERLAP_PREVIOUS)) {
+        if (e == cudaSuccess) e = cudaEventRecord(ev[used], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[used], 0);
+    }
     if (e == cudaSuccess) e = cudaMemcpyAsync(C_old, C_host, (size_t)(k * d) * sizeof(float), cudaMemcpyHostToDevice, cs);
     if (e == cudaSuccess) e = cudaEventRecord(ev[used + 1], cs);
     for (int i = 0; i < used && e == cudaSuccess; ++i) {

@@ -172,6 +172,13 @@ int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, in
 /* Most slices kmeans_lloyd_iter_host splits the samples into. */
 #define KMEANS_HOST_MAX_SLICES 64
 
+/* kmeans_lloyd_iter_host flag: the copies into X and C_old do not wait for the
+ * work enqueued on `stream` before the call, so they overlap the previous
+ * iteration's update and read-back.  The caller guarantees that no earlier
+ * unfinished work still uses X or C_old, for example by alternating two sets
+ * of device buffers between successive calls. */
+#define KMEANS_HOST_OVERLAP_PREVIOUS 1
+
 /* One Lloyd iteration [U] on inputs that live in host memory (the pages have
  * no counterpart: it serves callers whose data is not resident on the GPU).
  * X_host (n, d) and C_host (k, d) are host arrays, page-locked for the copies
@@ -185,7 +192,8 @@ int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, in
  * labels, best_dist, *inertia, counts) these are, bit for bit.  Finally
  * C_new, the labels and *inertia are copied to C_new_host, labels_host and
  * *inertia_host (each may be NULL; inertia_host needs inertia).
- * The copies into X wait for the work enqueued on `stream` before the call;
+ * The copies into X wait for the work enqueued on `stream` before the call
+ * (flags = 0) or not (flags = KMEANS_HOST_OVERLAP_PREVIOUS, see there);
  * everything the call enqueues is complete when `stream` reaches the point
  * after it (the copy stream's part is joined back into `stream`).
  * copy_stream must differ from stream.  Same requirements as
@@ -193,7 +201,7 @@ int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, in
 int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, float *C_old, float *C_new,
                            int64_t *labels, float *best_dist, double *inertia, int32_t *counts,
                            float *C_new_host, int64_t *labels_host, double *inertia_host,
-                           int64_t n, int64_t k, int64_t d, int slices,
+                           int64_t n, int64_t k, int64_t d, int slices, int flags,
                            void *ws, size_t ws_bytes, void *stream, void *copy_stream);
 
 /* Greedy k-means++ seeding [K].

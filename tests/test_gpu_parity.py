@@ -347,12 +347,46 @@ def test_lloyd_iteration_from_host_buffers_matches_device_call(gpu_lib):
         assert Xd.cpu().numpy().tobytes() == X.tobytes()
 
 
+def test_back_to_back_host_iterations_overlapping_their_copies(gpu_lib):
+    # two alternating device buffer sets with the overlap flag: each call's
+    # copies may run beside the previous call's update; every call must still
+    # give the device call's results
+    w = synth.Workload("t", 20000, 200, 64, 200, 1, 53, 54, "")
+    X, C0, _ = synth.workload_inputs(w)
+    n, k, d = w.n, w.k, w.d
+    ref = gpu_lib.kmeans_lloyd_iter(dev_tensor(X), dev_tensor(C0))
+    Xh, Ch = torch.from_numpy(X).pin_memory(), torch.from_numpy(C0).pin_memory()
+    Xd = [torch.empty((n, d), device="cuda") for _ in range(2)]
+    Cd = [torch.empty((k, d), device="cuda") for _ in range(2)]
+    C_new = torch.empty((k, d), device="cuda")
+    labels = torch.empty(n, dtype=torch.int64, device="cuda")
+    best = torch.empty(n, device="cuda")
+    counts = torch.empty(k, dtype=torch.int32, device="cuda")
+    outs = [(torch.empty((k, d)).pin_memory(), torch.empty(n, dtype=torch.int64).pin_memory(),
+             torch.empty(1, dtype=torch.float64).pin_memory()) for _ in range(4)]
+    cs = torch.cuda.Stream()
+    done = [None, None]
+    for j in range(4):
+        slot = j % 2
+        if done[slot] is not None:
+            cs.wait_event(done[slot])
+        C_h, lab_h, in_h = outs[j]
+        done[slot] = gpu_lib.kmeans_lloyd_iter_host(Xh, Ch, Xd[slot], Cd[slot], C_new, labels, best, counts, C_h,
+                                                    lab_h, in_h, slices=4, copy_stream=cs, overlap_previous=True)
+    torch.cuda.synchronize()
+    for C_h, lab_h, in_h in outs:
+        np.testing.assert_array_equal(lab_h.numpy(), host(ref[1]))
+        assert C_h.numpy().tobytes() == host(ref[0]).tobytes()
+        assert float(in_h[0]) == float(ref[3].item())
+
+
 def test_lloyd_iteration_from_host_buffers_rejects_bad_arguments(gpu_lib):
     lib = gpu_lib.load()
     fake = ctypes.c_void_p(0x10000)  # validation fails before any pointer is used
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    args = lambda slices, cs: (fake, fake, fake, fake, fake, fake, fake, None, None, None, None, None, 1024, 16, 32,
-                               slices, fake, 1 << 30, s, cs)
+    args = lambda slices, cs, flags=0: (fake, fake, fake, fake, fake, fake, fake, None, None, None, None, None, 1024,
+                                        16, 32, slices, flags, fake, 1 << 30, s, cs)
     assert lib.kmeans_lloyd_iter_host(*args(0, None)) == gpu_lib.KMEANS_ERR_INVALID_ARG
     assert lib.kmeans_lloyd_iter_host(*args(gpu_lib.HOST_MAX_SLICES + 1, None)) == gpu_lib.KMEANS_ERR_INVALID_ARG
     assert lib.kmeans_lloyd_iter_host(*args(4, s)) == gpu_lib.KMEANS_ERR_INVALID_ARG  # copy stream == stream
+    assert lib.kmeans_lloyd_iter_host(*args(4, None, 2)) == gpu_lib.KMEANS_ERR_INVALID_ARG  # unknown flag
