@@ -15,11 +15,17 @@
 // lo_x.lo_c term.  The tensor cores add each 16-wide partial product into the
 // float32 accumulator with a truncating add, so every MMA into an accumulator
 // of magnitude |x.c| costs up to one unit in its last place, always in the
-// same direction.  The large product hi.hi therefore gets an accumulator of
-// its own and the two small correction products another: only d/16 truncating
-// adds act at the magnitude of x.c (not 3 d/16), and the correction
-// accumulator stays about 2^8 times smaller.  The two are added in float32 in
-// the epilogue.
+// same direction.  Two accumulator modes (template DB):
+//   d <= 4096  the three products share one accumulator per tile, and two
+//              such accumulators are double-buffered in tensor memory, so the
+//              epilogue of one tile overlaps the MMAs of the next;
+//   d >  4096  hi.hi gets an accumulator of its own and the two small
+//              correction products another (only d/16 truncating adds act at
+//              the magnitude of x.c, not 3 d/16; the corrections stay about
+//              2^8 smaller), added in float32 in the epilogue, single-buffered.
+// Template TF32 swaps the split for 3xTF32 (see Fmt), a comparator; template
+// FUSED adds the mean update's accumulation to the epilogue
+// (kmeans_lloyd_iter_fused), another comparator.
 //
 // Structure: CTA pairs (clusters of 2, tcgen05 cta_group::2), persistent over
 // a grouped tile order.  A pair owns a 256-sample x 256-centroid tile: each
@@ -32,13 +38,14 @@
 //                centroid tile, then signal the even CTA that this k-block of
 //                A (and B) is ready
 //   warp 17      allocates the pair's tensor memory (both CTAs); in the even
-//                CTA issues tcgen05.mma: per 16-wide K step hi.hi into the
-//                main accumulator, lo.hi and hi.lo into the correction
-//                accumulator; completions are multicast to both CTAs
-//   warps 8-15   epilogue (each CTA, its 128 rows): tcgen05.ld both
-//                accumulators (two warps per lane quarter, 128 columns each),
-//                score = ||c||^2 - 2 (main + corr), row min / argmin,
-//                atomicMin into the per-sample key
+//                CTA issues tcgen05.mma (descriptors built before it waits for
+//                the split stage): per 16-wide K step hi.hi, lo.hi and hi.lo
+//                into the tile's accumulator(s); completions are multicast to
+//                both CTAs
+//   warps 8-15   epilogue (each CTA, its 128 rows): tcgen05.ld the
+//                accumulator(s) (two warps per lane quarter, 128 columns
+//                each), score = ||c||^2 - 2 x.c, row min / argmin, atomicMin
+//                into the per-sample key
 // Every wait is bounded; a timeout raises a flag in the status word and both
 // CTAs wind down without hanging.
 #include <cuda.h>
