@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -67,16 +68,25 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_sha256(path):
+    """sha256 of a C++ source with its comments and blank lines removed, so
+    that a comment edit does not count as a kernel change."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", l).rstrip() for l in text.splitlines()]
+    return hashlib.sha256("\n".join(l for l in lines if l.strip()).encode()).hexdigest()
+
+
 def recorded_traffic():
     """Per-launch DRAM bytes of the assign kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+    summary, if it was taken on the current kernel code; else None."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None
-    sha = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    sha = code_sha256(KERNEL_SOURCE)
     rec_sha, traffic = None, None
     for line in open(PROFILE_SUMMARY):
         line = line.strip().strip("`")
-        if line.startswith("source_sha256:"):
+        if line.startswith("code_sha256:"):
             rec_sha = line.split(":", 1)[1].strip()
         elif line.startswith("traffic_bytes_per_launch:"):
             traffic = float(line.split(":", 1)[1].strip())
