@@ -14,6 +14,10 @@ Every function states the page section it follows:
 * ``update``  -- same page, section "Full Lloyd step": the mean of the members.
 * ``kmeanspp`` -- "004 — tile sizes, a Cython Lloyd step, and k-means++",
   section "k-means++": greedy D^2 seeding with 2 + log(n_clusters) trials.
+* ``relocate_empty`` -- same page, section "Cython timing": the Lloyd step
+  there relocates empty clusters.  The page gives no rule; this is the plain
+  reading (each empty cluster takes one of the samples farthest from their
+  centroid).  It is pure selection, written here in numpy.
 * ``philox4x32_10`` / ``uniform`` -- the counter-based generator of Salmon et
   al. (SC'11), from its published definition.
 """
@@ -156,18 +160,57 @@ def lloyd_iter(X, C_old, nthreads: int = 0):
     return C_new, labels, best, second, inertia, counts
 
 
-def fit(X, C0, max_iter: int, tol: float, nthreads: int = 0):
+def relocate_empty(labels, best, k: int):
+    """Give every empty cluster a member.
+
+    "004 — tile sizes, a Cython Lloyd step, and k-means++", section "Cython
+    timing", says only that the Lloyd step relocates empty clusters.  Reading:
+    with m clusters that have no member, the m samples farthest from the
+    centroid they were assigned to (largest ``best``; equal distances: lower
+    sample index first) leave their clusters; taken in increasing sample
+    index, they become the only members of the empty clusters taken in
+    increasing cluster index.  A cluster that loses all its members this way
+    is empty afterwards (and keeps its centroid in the update).
+
+    ``labels`` (n,) int64 in [0, k) and ``best`` (n,) the assigned squared
+    distances (no NaN).  Returns ``(new_labels int64 (n,), moved int64 (m,))``
+    with ``moved`` the relocated samples in increasing index."""
+    labels = np.array(labels, dtype=np.int64)
+    best = np.asarray(best, dtype=np.float64)
+    n = labels.shape[0]
+    assert best.shape == (n,)
+    counts = np.bincount(labels, minlength=k)
+    assert counts.shape == (k,), "label outside [0, k)"
+    empty = np.flatnonzero(counts == 0)
+    m = empty.size
+    if m == 0:
+        return labels, np.empty(0, dtype=np.int64)
+    # primary key: distance, largest first; then sample index, lowest first
+    farthest = np.lexsort((np.arange(n), -best))[:m]
+    moved = np.sort(farthest)
+    labels[moved] = empty
+    return labels, moved
+
+
+def fit(X, C0, max_iter: int, tol: float, nthreads: int = 0, relocate: bool = False):
     """Lloyd iterations from C0 until the relative inertia improvement is at
     most ``tol`` or ``max_iter`` iterations have run (the pages fix no
     stopping rule; this is the plain one, the same as the library's).
     Iteration t assigns X to C_t (inertia_t) and updates to C_{t+1}; the fit
     stops after iteration t when inertia_t >= (1 - tol) * inertia_{t-1}.
+    With ``relocate`` each assignment's labels pass through
+    ``relocate_empty`` before the update (the inertia stays the
+    assignment's).
     Returns ``(C_last, labels_last, best_last, inertia_history, n_iter)``."""
     C = _f32(C0)
+    k = C.shape[0]
     hist = []
     labels = best = None
     for it in range(max_iter):
-        C_new, labels, best, _, inertia, _ = lloyd_iter(X, C, nthreads)
+        labels, best, _, inertia = assign(X, C, nthreads)
+        if relocate:
+            labels, _ = relocate_empty(labels, best, k)
+        C_new, _ = update(X, labels, C, nthreads)
         hist.append(inertia)
         C = C_new
         if it > 0 and inertia >= hist[-2] * (1.0 - tol):

@@ -268,6 +268,94 @@ def test_fit_from_planted_centers_stops_one_iteration_after_the_fixed_point():
     assert np.abs(C - means).max() <= 1e-6 * np.abs(means).max()
 
 
+# --------------------------------------------------------------------------
+# empty-cluster relocation (the reading of "relocates empty clusters")
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("labels,best,k,want", [
+    # clusters 2 and 4 are empty; the two farthest samples (3 and 7) move,
+    # in index order, to clusters 2 and 4
+    ([0, 0, 1, 1, 1, 0, 3, 3], [1.0, 4.0, 2.0, 9.0, 0.5, 4.0, 3.0, 7.0], 5, [0, 0, 1, 2, 1, 0, 3, 4]),
+    # three samples tie at the largest distance: the two lowest indices move
+    ([0, 0, 0, 0, 1, 1], [5.0, 2.0, 5.0, 1.0, 5.0, 0.0], 4, [2, 0, 3, 0, 1, 1]),
+    # the farthest sample is its cluster's only member: cluster 0 is left empty
+    ([0, 1, 1, 1], [9.0, 1.0, 1.0, 1.0], 3, [2, 1, 1, 1]),
+    # no empty cluster: nothing moves
+    ([2, 0, 1, 0], [3.0, 8.0, 1.0, 2.0], 3, [2, 0, 1, 0]),
+    # every distance zero and one occupied cluster of four: samples 0..2 move
+    ([1, 1, 1, 1, 1], [0.0, 0.0, 0.0, 0.0, 0.0], 4, [0, 2, 3, 1, 1]),
+])
+def test_relocate_hand_worked_cases(labels, best, k, want):
+    # catches: the wrong end of the distance order, ties broken towards the
+    # higher index, pairing by distance instead of by index, a moved sample
+    # keeping its old label
+    got, moved = oracle.relocate_empty(np.array(labels, np.int64), np.array(best, np.float32), k)
+    assert got.tolist() == want
+    assert moved.tolist() == [i for i in range(len(labels)) if labels[i] != want[i]]
+
+
+def _relocate_by_repeated_argmax(labels, best, k):
+    # the rule taken literally: m times, remove the farthest remaining
+    # sample (first among equals); then hand them out in index order
+    labels = [int(v) for v in labels]
+    present = set(labels)
+    empty = [j for j in range(k) if j not in present]
+    left = list(range(len(labels)))
+    taken = []
+    for _ in empty:
+        far = max(best[i] for i in left)
+        i = min(i for i in left if best[i] == far)
+        left.remove(i)
+        taken.append(i)
+    for j, i in zip(empty, sorted(taken)):
+        labels[i] = j
+    return labels
+
+
+def test_relocate_matches_repeated_argmax_on_small_inputs():
+    # catches a mistake in the sort keys on inputs with many ties and many
+    # empty clusters (distances from a handful of values, -0.0 among them)
+    rng = np.random.default_rng(5)
+    for trial in range(300):
+        n = int(rng.integers(1, 40))
+        k = int(rng.integers(1, n + 1))
+        used = rng.choice(k, size=int(rng.integers(1, k + 1)), replace=False)
+        labels = rng.choice(used, size=n).astype(np.int64)
+        best = rng.choice(np.array([0.0, -0.0, 1.0, 2.5, 2.5, 7.0], np.float32), size=n)
+        got, _ = oracle.relocate_empty(labels, best, k)
+        assert got.tolist() == _relocate_by_repeated_argmax(labels, best.astype(np.float64), k), trial
+
+
+def test_fit_relocation_revives_a_far_centroid():
+    # planted, well separated blobs with C0 = the blob centers except one
+    # moved far away.  Keeping empty clusters leaves that centroid unused
+    # for good and one blob merged into another; relocating hands it the
+    # farthest sample (one of the orphaned blob's), and the fit recovers
+    # every blob with a lower inertia
+    X, centers, blob = synth.planted_blobs(2048, 32, 16, seed=43)
+    C0 = centers.copy()
+    C0[3] += np.float32(1e3)
+    C_keep, labels_keep, _, hist_keep, _ = oracle.fit(X, C0, max_iter=50, tol=0.0)
+    assert np.bincount(labels_keep, minlength=16)[3] == 0
+    assert C_keep[3].tobytes() == C0[3].tobytes()
+    C_rel, labels_rel, _, hist_rel, _ = oracle.fit(X, C0, max_iter=50, tol=0.0, relocate=True)
+    np.testing.assert_array_equal(labels_rel, blob)
+    assert hist_rel[-1] < hist_keep[-1]
+    means = np.stack([X[blob == j].astype(np.float64).mean(0) for j in range(16)])
+    assert np.abs(C_rel - means).max() <= 1e-6 * np.abs(means).max()
+    assert np.all(np.diff(hist_rel) <= 1e-12 * hist_rel[:-1])
+
+
+def test_fit_relocation_never_raises_the_inertia():
+    # moving a sample onto its own new centroid lowers its cost, and the
+    # mean update lowers it further: the inertia still never rises, even
+    # from an initialisation with most clusters empty
+    X = synth.gaussian((600, 8), seed=95)
+    C0 = synth.gaussian((60, 8), seed=96) * np.float32(30.0)
+    _, labels, _, hist, n_iter = oracle.fit(X, C0, max_iter=100, tol=0.0, relocate=True)
+    assert np.all(np.diff(hist) <= 1e-12 * hist[:-1])
+    assert (np.bincount(labels, minlength=60) > 0).all()
+
+
 def test_oracle_thread_count_does_not_change_bits():
     X = synth.gaussian((777, 45), seed=91)
     C = synth.gaussian((31, 45), seed=92)
