@@ -417,6 +417,30 @@ def run_gb300(args):
     barrier()
     t_tf32 = ev0.elapsed_time(ev1) / 1e3 / t_steps
     del ws_t
+
+    # empty-cluster relocation, the opt-in step of kmeans_fit: on this
+    # workload's labels (no cluster is empty: one counting pass) and with
+    # every odd cluster emptied (k / 2 clusters relocated); each step first
+    # restores the labels with a device copy of n int64, included in the time
+    ws_r = km.workspace(km.OP_RELOCATE, n, k, 1, dev)
+    r_steps = max(1, min(steps, 50))
+    lab_work = torch.empty_like(labels)
+    lab_src = {"none_empty": labels.clone(), "half_empty": (labels // 2) * 2}
+    t_reloc = {}
+    for case, src in lab_src.items():
+        for _ in range(2):
+            lab_work.copy_(src)
+            km.kmeans_relocate_empty(lab_work, best, k, ws=ws_r, stream=stream)
+        barrier()
+        ev0.record(stream)
+        for _ in range(r_steps):
+            lab_work.copy_(src)
+            km.kmeans_relocate_empty(lab_work, best, k, ws=ws_r, stream=stream)
+        ev1.record(stream)
+        barrier()
+        t_reloc[case] = ev0.elapsed_time(ev1) / 1e3 / r_steps
+    moved = int((lab_work != lab_src["half_empty"]).sum().item())
+    del ws_r, lab_work, lab_src
     clocks = sampler.stop()
 
     kpp = None
@@ -518,6 +542,11 @@ def run_gb300(args):
                           "speedup_of_bf16x3": t_tf32 / t_assign,
                           "note": "whole kmeans_assign_3xtf32 call against the nominal dense TF32 rate "
                                   f"{TF32_NOMINAL_TFLOPS} TFLOP/s / 3 (no measured TF32 peak)"},
+        "relocate_empty": {"us_none_empty": 1e6 * t_reloc["none_empty"],
+                           "us_half_empty": 1e6 * t_reloc["half_empty"], "moved_half_empty": moved,
+                           "share_of_lloyd_none_empty": t_reloc["none_empty"] / t_lloyd,
+                           "note": "kmeans_relocate_empty on this workload's labels and distances; each step "
+                                   "restores the labels first (a device copy of n int64, in the time)"},
         "lloyd_frac_of_roofline": (flop / (r_peak * 1e12) + upd_bytes / (peaks["hbm_gbs"] * 1e9)) / t_lloyd,
         "roofline": {"bound": "tensor", "achieved": tc_tflops, "peak": r_peak, "unit": "TFLOP/s",
                      "frac": tc_tflops / r_peak, "traffic": recorded_traffic(),

@@ -39,9 +39,11 @@ OP_KMEANSPP = 4
 OP_FIT = 5
 OP_ASSIGN_3XTF32 = 6
 OP_LLOYD_FUSED = 7
+OP_RELOCATE = 8
 
 INIT_GIVEN = 0
 INIT_KMEANSPP = 1
+FIT_RELOCATE_EMPTY = 0x100
 
 KERNEL_ASSIGN_TC = 0
 KERNEL_UPDATE_MEAN = 1
@@ -56,7 +58,7 @@ EXPORTS = (
     "kmeans_lloyd_iter", "kmeanspp_init", "kmeans_device_status", "kmeans_status_string",
     "kmeans_build_info", "kmeans_assign_noalloc", "kmeans_trace_start", "kmeans_trace_read",
     "kmeans_trace_stop", "kmeans_lloyd_iter_host", "kmeans_fit", "kmeans_assign_3xtf32",
-    "kmeans_lloyd_iter_fused",
+    "kmeans_lloyd_iter_fused", "kmeans_relocate_empty",
 )
 
 _lock = threading.Lock()
@@ -116,6 +118,8 @@ def load(path: str | None = None):
         lib.kmeans_lloyd_iter_host.restype = INT
         lib.kmeans_fit.argtypes = [P, P, P, P, P, I64, I64, I64, INT, U64, INT, ctypes.c_double, P, P, P, SZ, P]
         lib.kmeans_fit.restype = INT
+        lib.kmeans_relocate_empty.argtypes = [P, P, I64, I64, P, SZ, P]
+        lib.kmeans_relocate_empty.restype = INT
         lib.kmeans_trace_stop.argtypes = []
         lib.kmeans_trace_stop.restype = INT
         _lib = lib
@@ -343,12 +347,29 @@ def kmeans_device_status(ws, stream=None) -> int:
     return int(load().kmeans_device_status(_ptr(ws), _stream_handle(stream)))
 
 
+def kmeans_relocate_empty(labels, best_dist, k: int, ws=None, stream=None):
+    """Move the samples farthest from their centroids into the empty
+    clusters (labels rewritten in place) -> ``labels``."""
+    torch = _torch()
+    _check(labels, "labels", torch.int64)
+    n = labels.shape[0]
+    _check(best_dist, "best_dist", torch.float32, (n,), labels.device)
+    ws = _ws(ws, OP_RELOCATE, n, k, 1, labels.device)
+    st = load().kmeans_relocate_empty(_ptr(labels), _ptr(best_dist), n, int(k), _ptr(ws), ws.numel(),
+                                      _stream_handle(stream))
+    _raise(st, "kmeans_relocate_empty")
+    return labels
+
+
 def kmeans_fit(X, k: int = None, C=None, init: str = "kmeans++", seed: int = 0, max_iter: int = 300,
-               tol: float = 1e-4, labels=None, best_dist=None, counts=None, ws=None, stream=None):
+               tol: float = 1e-4, labels=None, best_dist=None, counts=None, ws=None, stream=None,
+               relocate_empty: bool = False):
     """Lloyd iterations until the relative inertia improvement is at most
     ``tol`` (or ``max_iter``) -> ``(C, labels, best_dist, counts,
     inertia_history, n_iter)``.  ``init="kmeans++"`` seeds ``k`` centroids
     with ``seed``; ``init="given"`` starts from ``C`` (updated in place).
+    ``relocate_empty`` passes each iteration's labels through
+    kmeans_relocate_empty before the update.
     Synchronises the stream once per iteration."""
     import numpy as np
     torch = _torch()
@@ -378,6 +399,8 @@ def kmeans_fit(X, k: int = None, C=None, init: str = "kmeans++", seed: int = 0, 
         ws = workspace(OP_FIT, n, k, d, X.device)
     hist = np.zeros(int(max_iter), dtype=np.float64)
     n_iter = ctypes.c_int(0)
+    if relocate_empty:
+        code |= FIT_RELOCATE_EMPTY
     st = load().kmeans_fit(_ptr(X), _ptr(C), _ptr(labels), _ptr(best_dist), _ptr(counts), n, k, d, code,
                            int(seed) & (2**64 - 1), int(max_iter), float(tol), ctypes.byref(n_iter),
                            hist.ctypes.data_as(ctypes.c_void_p), _ptr(ws), ws.numel(), _stream_handle(stream))

@@ -10,6 +10,7 @@
 #include "assign_common.cuh"
 #include "common.cuh"
 #include "kmeanspp.cuh"
+#include "relocate.cuh"
 #include "update.cuh"
 
 using namespace km;
@@ -76,12 +77,15 @@ int run_assign(AssignPath path, const float *X, const float *C, int64_t n, int64
 
 // kmeans_fit's workspace: the Lloyd / k-means++ scratch at the base (so the
 // status word sits where kmeans_device_status looks), then the second
-// centroid buffer of the ping-pong, the seeding's indices and the inertia.
+// centroid buffer of the ping-pong, the seeding's indices, the inertia and
+// the relocation's scratch.
 struct FitLayout {
     int64_t shared;       // max(Lloyd, k-means++) scratch
     int64_t off_calt;     // k x d f32
     int64_t off_indices;  // k x i64
     int64_t off_inertia;  // f64
+    int64_t off_nempty;   // u32 number of empty clusters after an update
+    RelocLayout reloc;    // counts and empty list, 2 x k x i32
     int64_t bytes;
 };
 
@@ -95,8 +99,10 @@ FitLayout fit_layout(int64_t n, int64_t k, int64_t d) {
     int64_t o = align_up(F.shared, 1024);
     F.off_calt = o; o = align_up(o + k * d * 4, 1024);
     F.off_indices = o; o = align_up(o + k * 8, 1024);
-    F.off_inertia = o; o = align_up(o + 8, 1024);
-    F.bytes = o;
+    F.off_inertia = o;
+    F.off_nempty = o + 8; o = align_up(o + 16, 1024);
+    F.reloc = reloc_layout(k, o);
+    F.bytes = align_up(F.reloc.end, 1024);
     return F;
 }
 
@@ -163,6 +169,8 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
             return (size_t)fit_layout(n, k, d).bytes;
         case KMEANS_OP_LLOYD_FUSED:
             return (size_t)fused_layout(n, k, d).bytes;
+        case KMEANS_OP_RELOCATE:
+            return (size_t)reloc_layout(k, sizeof(WsHeader)).end;
         default:
             return 0;
     }
@@ -325,7 +333,10 @@ int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int3
                void *ws, size_t ws_bytes, void *stream) {
     if (!X || !C || !labels || !best_dist || !n_iter) return KMEANS_ERR_INVALID_ARG;
     if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    const bool relocate = (init & KMEANS_FIT_RELOCATE_EMPTY) != 0;
+    init &= ~KMEANS_FIT_RELOCATE_EMPTY;
     if (init != KMEANS_INIT_GIVEN && init != KMEANS_INIT_KMEANSPP) return KMEANS_ERR_INVALID_ARG;
+    if (relocate && !aligned4(best_dist)) return KMEANS_ERR_INVALID_ARG;
     if (max_iter < 1 || max_iter > 1000000 || !(tol >= 0.0) || tol > 1e300) return KMEANS_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(labels) & 7u)) return KMEANS_ERR_INVALID_ARG;
     const int st = tc_path_ok(X, C, d);
@@ -346,23 +357,40 @@ int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int3
                             kpp_layout(n, d, T), w, s);
     }
     const AssignLayout A = assign_layout(n, k, d, true);
+    const UpdateLayout U = update_layout(n, k, d);
+    // with relocation the update's counts show whether a cluster emptied;
+    // without caller counts they go to the relocation's count scratch, which
+    // the relocation itself rewrites only after they have been read
+    int32_t *cnt = counts;
+    if (relocate && !cnt) cnt = reinterpret_cast<int32_t *>(w + F.reloc.off_counts);
+    uint32_t *nempty_d = reinterpret_cast<uint32_t *>(w + F.off_nempty);
     float *cur = C, *nxt = calt;
     double prev = 0.0;
     int it = 0;
     while (e == cudaSuccess && it < max_iter) {
         e = launch_prep_split(cur, n, k, d, A, w, s);
         if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, A, w, s);
-        if (e == cudaSuccess) e = lloyd_finish(X, cur, nxt, labels, best_dist, inertia_d, counts, n, k, d, A, w, s);
+        if (e == cudaSuccess) e = lloyd_finish(X, cur, nxt, labels, best_dist, inertia_d, cnt, n, k, d, A, w, s);
+        if (e == cudaSuccess && relocate) e = launch_count_empty(cnt, k, nempty_d, s);
         double inertia = 0.0;
-        uint32_t flags = 0;
+        uint32_t flags = 0, nempty = 0;
         if (e == cudaSuccess) e = cudaMemcpyAsync(&inertia, inertia_d, sizeof(double), cudaMemcpyDeviceToHost, s);
         if (e == cudaSuccess) e = cudaMemcpyAsync(&flags, w, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess && relocate) e = cudaMemcpyAsync(&nempty, nempty_d, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) break;
         ++it;
         *n_iter = it;
         if (flags & kFlagTimeout) return KMEANS_ERR_DEVICE_TIMEOUT;
         if (flags & kFlagBadLabel) return KMEANS_ERR_DEVICE_LABEL;
+        if (nempty) {
+            // a cluster is empty: move the farthest samples into the empty
+            // clusters and redo the update with those labels (every row of
+            // nxt is rewritten); an iteration without one pays only the check
+            e = launch_relocate(labels, best_dist, n, k, F.reloc, w, s);
+            if (e == cudaSuccess) e = launch_update(X, labels, cur, nxt, cnt, n, k, d, U, w, false, s);
+            if (e != cudaSuccess) break;
+        }
         if (inertia_history) inertia_history[it - 1] = inertia;
         float *t = cur;
         cur = nxt;
@@ -374,6 +402,21 @@ int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int3
     // the last update wrote `cur`; the caller's C must hold it
     if (e == cudaSuccess && cur != C) e = cudaMemcpyAsync(C, cur, (size_t)(k * d) * sizeof(float), cudaMemcpyDeviceToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_status(e);
+}
+
+int kmeans_relocate_empty(int64_t *labels, const float *best_dist, int64_t n, int64_t k, void *ws, size_t ws_bytes,
+                          void *stream) {
+    if (!labels || !best_dist) return KMEANS_ERR_INVALID_ARG;
+    if (!sizes_ok(n, k, 1)) return KMEANS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(labels) & 7u) || !aligned4(best_dist)) return KMEANS_ERR_INVALID_ARG;
+    const RelocLayout R = reloc_layout(k, sizeof(WsHeader));
+    const int wst = check_ws(ws, ws_bytes, (size_t)R.end);
+    if (wst != KMEANS_OK) return wst;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    cudaError_t e = cudaMemsetAsync(w, 0, sizeof(WsHeader), s);  // this call's status word
+    if (e == cudaSuccess) e = launch_relocate(labels, best_dist, n, k, R, w, s);
     return cuda_status(e);
 }
 

@@ -21,6 +21,8 @@
  *      the comparison; ||c||^2 is computed once per centroid and reused.
  *  [K] same page, section "k-means++": greedy D^2 seeding with
  *      2 + log(n_clusters) candidate trials per new center.
+ *  [L] same page, section "Cython timing": the Lloyd step measured there
+ *      also relocates empty clusters (the page gives no rule).
  *
  * Conventions shared by every entry point
  *  - Layout: X is (n, d) float32 row-major, C is (k, d) float32 row-major,
@@ -80,13 +82,19 @@ enum {
     KMEANS_OP_KMEANSPP = 4,
     KMEANS_OP_FIT = 5,
     KMEANS_OP_ASSIGN_3XTF32 = 6,
-    KMEANS_OP_LLOYD_FUSED = 7
+    KMEANS_OP_LLOYD_FUSED = 7,
+    KMEANS_OP_RELOCATE = 8
 };
 
 /* Initialisation of kmeans_fit. */
 enum {
     KMEANS_INIT_GIVEN = 0,    /* start from the centroids in C            */
     KMEANS_INIT_KMEANSPP = 1  /* greedy k-means++ seeding (kmeanspp_init) */
+};
+
+/* Options of kmeans_fit, or-ed into its `init` argument. */
+enum {
+    KMEANS_FIT_RELOCATE_EMPTY = 0x100  /* kmeans_relocate_empty before each update */
 };
 
 /* Bytes of device workspace the operation needs for these sizes (0 when the
@@ -204,6 +212,23 @@ int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, f
                            int64_t n, int64_t k, int64_t d, int slices, int flags,
                            void *ws, size_t ws_bytes, void *stream, void *copy_stream);
 
+/* Empty-cluster relocation [L] (the rule is this library's reading; the
+ * page names the step only).  With m clusters that no label names, the m
+ * samples with the largest best_dist (equal distances: the lower sample
+ * index first) are moved: taken in increasing sample index, their labels
+ * become the empty clusters taken in increasing cluster index.  A cluster
+ * whose every member moves is empty afterwards (kmeans_update then keeps
+ * its centroid).  Nothing changes when no cluster is empty.
+ * labels (device int64, n): in/out, values in [0, k).  best_dist (device
+ * float32, n): each sample's squared distance to its assigned centroid, as
+ * kmeans_assign writes it (no NaN; -0 counts as 0); read only.
+ * A label outside [0, k) leaves every label as it was and sets
+ * KMEANS_ERR_DEVICE_LABEL in the status word.  Cost: a counting pass over
+ * the labels, then, only while a cluster is empty, six passes over best_dist
+ * by one thread block.  Workspace KMEANS_OP_RELOCATE (d is ignored). */
+int kmeans_relocate_empty(int64_t *labels, const float *best_dist, int64_t n, int64_t k,
+                          void *ws, size_t ws_bytes, void *stream);
+
 /* Greedy k-means++ seeding [K].
  * indices (device int64, k) receives the chosen sample indices, centers
  * (device float32 (k, d), may be NULL) the chosen rows of X.
@@ -224,7 +249,13 @@ int kmeanspp_init(const float *X, int64_t n, int64_t d, int64_t k, int n_trials,
  * pages fix no stopping rule; this is the plain one).  With
  * init == KMEANS_INIT_KMEANSPP, C is first seeded by kmeanspp_init with the
  * default trial count and `seed`; with KMEANS_INIT_GIVEN, C holds the
- * starting centroids.  Iteration t assigns X to C_t (inertia_t) and updates
+ * starting centroids.  With KMEANS_FIT_RELOCATE_EMPTY or-ed into init, the
+ * labels of every iteration pass through kmeans_relocate_empty before the
+ * update (best_dist and the inertia stay the assignment's); without it an
+ * empty cluster keeps its centroid.  (The fit checks the update's counts for
+ * an empty cluster, and only then relocates and updates again: an iteration
+ * that empties no cluster pays one small kernel.)
+ * Iteration t assigns X to C_t (inertia_t) and updates
  * to C_{t+1}; the fit stops after iteration t when
  * inertia_t >= (1 - tol) * inertia_{t-1} (relative improvement at most tol;
  * tol = 0 runs to a fixed point, where the inertia no longer drops), or after

@@ -98,14 +98,35 @@ def test_lloyd_workspace_is_the_larger_of_its_steps(km):
 
 
 def test_fit_workspace_is_the_shared_scratch_plus_a_centroid_buffer(km):
-    import math
+    # the shared scratch, a second centroid buffer, the seeding's indices, the
+    # inertia and the relocation's two k-long int32 arrays
     for n, k, d in [(4096, 256, 512), (65536, 1024, 2048), (131072, 8192, 8192)]:
         lloyd = km.kmeans_workspace_bytes(km.OP_LLOYD, n, k, d)
         fit = km.kmeans_workspace_bytes(km.OP_FIT, n, k, d)
         extra = fit - lloyd
-        assert k * d * 4 <= extra <= k * d * 4 + k * 8 + 8 + 4 * 1024 + \
+        assert k * d * 4 + k * 16 <= extra <= k * d * 4 + k * 16 + 8 + 6 * 1024 + \
             max(0, km.kmeans_workspace_bytes(km.OP_KMEANSPP, n, k, d) - lloyd)
         assert fit < n * k * 4
+
+
+def test_relocate_workspace_and_argument_checks(km):
+    lib = _lib(km)
+    for n, k in [(10, 1), (4096, 256), (131072, 8192)]:
+        b = km.kmeans_workspace_bytes(km.OP_RELOCATE, n, k, 1)
+        assert 256 + 8 * k <= b <= 256 + 8 * k + 512      # header, counts, empty list
+        assert b == km.kmeans_workspace_bytes(km.OP_RELOCATE, 2 * n, k, 7)  # independent of n and d
+    need = km.kmeans_workspace_bytes(km.OP_RELOCATE, 100, 10, 1)
+    rel = lambda labels, best, n, k, ws=FAKE_WS, wsb=need: lib.kmeans_relocate_empty(labels, best, n, k, ws, wsb,
+                                                                                      None)
+    assert rel(None, FAKE, 100, 10) == km.KMEANS_ERR_INVALID_ARG
+    assert rel(FAKE, None, 100, 10) == km.KMEANS_ERR_INVALID_ARG
+    assert rel(FAKE, FAKE, 100, 101) == km.KMEANS_ERR_INVALID_ARG       # k > n
+    assert rel(FAKE, FAKE, 0, 0) == km.KMEANS_ERR_INVALID_ARG
+    assert rel(FAKE, FAKE, 2**31, 10) == km.KMEANS_ERR_INVALID_ARG
+    assert rel(ctypes.c_void_p(0x10004), FAKE, 100, 10) == km.KMEANS_ERR_INVALID_ARG   # labels not 8-aligned
+    assert rel(FAKE, ctypes.c_void_p(0x10002), 100, 10) == km.KMEANS_ERR_INVALID_ARG   # best not 4-aligned
+    assert rel(FAKE, FAKE, 100, 10, wsb=need - 1) == km.KMEANS_ERR_WORKSPACE
+    assert rel(FAKE, FAKE, 100, 10, ws=ctypes.c_void_p(0x100010)) == km.KMEANS_ERR_WORKSPACE
 
 
 def test_workspace_far_below_the_distance_matrix_at_every_workload(km):
