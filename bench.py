@@ -267,7 +267,7 @@ def time_kmeanspp(km, synth, dev, stream, barrier):
     km.kmeans_trace_stop()
     moved = 4.0 * w.n * w.d * w.k  # one read of X per center
     # one distance pass: X once, plus its (slice, trial, sample) float2 partial sums
-    slices = (w.d + 2047) // 2048
+    slices = (w.d + km.KPP_SLICE_FEATURES - 1) // km.KPP_SLICE_FEATURES
     pass_bytes = 4.0 * w.n * w.d + 8.0 * slices * T * w.n
     t_pass = dist_ms / 1e3 / max(dist_timed, 1)
     return {"workload": f"n={w.n} d={w.d} k={w.k} trials={T}", "ms": 1e3 * t, "gbs": moved / t / 1e9,

@@ -51,6 +51,9 @@ KERNEL_KMEANSPP_DIST = 2
 TRACE_MAX_CAPACITY = 65536
 HOST_MAX_SLICES = 64
 HOST_OVERLAP_PREVIOUS = 1
+# Features per slice of the k-means++ distance pass: each pass writes one
+# float2 partial sum per (slice, trial, sample), ceil(d / 4096) slices.
+KPP_SLICE_FEATURES = 4096
 
 # Every symbol the header declares (the ABI test checks the library exports them).
 EXPORTS = (

@@ -218,7 +218,7 @@ inline UpdateLayout update_layout(int64_t n, int64_t k, int64_t d) {
 constexpr int kKppScanBlock = 1024;   // samples per scan / potential block
 constexpr int kKppMaxTrials = 32;
 constexpr int kKppGroupTrials = 8;    // trial candidates per pass over X
-constexpr int kKppSliceFloats = 2048; // features of the 8 candidates a CTA keeps in shared memory (64 KiB)
+constexpr int kKppSliceFloats = 4096; // features of the 8 candidates a CTA keeps in shared memory (128 KiB)
 
 struct KppLayout {
     int T;

@@ -152,16 +152,24 @@ __global__ void kpp_pick_kernel(const double *__restrict__ bsum, int64_t n_block
 namespace kd {
 constexpr int KT = kKppGroupTrials;  // trial candidates per pass over X
 constexpr int ROWS = 2;              // samples per warp at a time
-constexpr int MIN_BLOCKS = 3;        // resident blocks per SM (64 KiB of candidates each)
-constexpr int WARPS = 8;
+constexpr int MIN_BLOCKS = 1;        // one block per SM: 128 KiB of candidates, 16 warps of up to 128 registers
+constexpr int WARPS = 16;
 constexpr int THREADS = WARPS * 32;
 constexpr int GROUP = WARPS * ROWS;
 }  // namespace kd
 
-__device__ __forceinline__ void kahan(float &s, float &c, float v) {
-    const float y = v - c;
-    const float t = s + y;
-    c = (t - s) - y;
+// Kahan's compensated sum (y = v - c, t = s + y, c = (t - s) - y, s = t) on two
+// independent sums at once (row 0 in .x, row 1 in .y) with the packed
+// two-float instructions.  cm holds the negated compensation, so no negation
+// is needed: t - s is fma(s, -1, t) and the new -c is fma(t - s, -1, y).  Each
+// step rounds exactly as the scalar form does, so each half carries the bits
+// of a scalar Kahan sum.
+__device__ __forceinline__ void kahan2(float2 &s, float2 &cm, float2 v) {
+    const float2 m1 = make_float2(-1.f, -1.f);
+    const float2 y = __fadd2_rn(v, cm);      // v - c
+    const float2 t = __fadd2_rn(s, y);
+    const float2 ts = __ffma2_rn(s, m1, t);  // t - s
+    cm = __ffma2_rn(ts, m1, y);              // y - (t - s) = -c
     s = t;
 }
 
@@ -228,7 +236,8 @@ __device__ __forceinline__ void load4x2(const float *__restrict__ p, int avail, 
 // The block stages its slice of the candidates (negated) in shared memory once
 // and then streams its share of the samples, each sample read exactly once.
 // Differences and squares use the packed two-float instructions; each run of
-// a lane's 8 features of a step is added to a compensated per-lane sum.
+// a lane's 8 features of a step is added to a compensated per-lane sum, the
+// two rows' sums paired in one packed compensated add.
 template <bool VEC>
 __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand, int T,
@@ -252,27 +261,35 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     const int64_t n_groups = (n + kd::GROUP - 1) / kd::GROUP;
     for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x) {
         const int64_t r0 = g * kd::GROUP + warp * kd::ROWS;
-        float s[kd::ROWS][kd::KT], c[kd::ROWS][kd::KT];
+        static_assert(kd::ROWS == 2, "the two rows' sums are paired in float2");
+        float2 s2[kd::KT], cm2[kd::KT];  // .x row 0, .y row 1; cm2 = -(compensation)
 #pragma unroll
-        for (int r = 0; r < kd::ROWS; ++r)
-#pragma unroll
-            for (int t = 0; t < kd::KT; ++t) s[r][t] = c[r][t] = 0.f;
-        // no register prefetch of the next step: with it the kernel spills and
-        // runs slower; the other resident warps hide the load latency
-        float2 x[kd::ROWS][4];
+        for (int t = 0; t < kd::KT; ++t) s2[t] = cm2[t] = make_float2(0.f, 0.f);
         // a lane owns features f .. f+3 and f+128 .. f+131 of each 256-feature
         // step, so every 16-byte load of the warp (global and shared) covers
-        // 512 contiguous bytes
+        // 512 contiguous bytes.  The next step's rows are loaded while this
+        // step is computed (xn): one block of 16 warps per SM leaves each
+        // thread the registers for it, where three blocks of 8 warps spilled.
+        float2 x[kd::ROWS][4], xn[kd::ROWS][4];
+#pragma unroll
+        for (int r = 0; r < kd::ROWS; ++r) {
+            if (r0 + r < n) {
+                load4x2<VEC>(X + (r0 + r) * (int64_t)d + fb + lane * 4, width - lane * 4, xn[r]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) xn[r][e] = make_float2(0.f, 0.f);
+            }
+        }
         for (int f0 = 0; f0 < width; f0 += 256) {
             const int f = f0 + lane * 4;
 #pragma unroll
-            for (int r = 0; r < kd::ROWS; ++r) {
-                const float *xp = X + (r0 + r) * (int64_t)d + fb + f;
-                if (r0 + r < n) {
-                    load4x2<VEC>(xp, width - f, x[r]);
-                } else {
+            for (int r = 0; r < kd::ROWS; ++r)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) x[r][e] = make_float2(0.f, 0.f);
+                for (int e = 0; e < 4; ++e) x[r][e] = xn[r][e];
+            if (f0 + 256 < width) {
+#pragma unroll
+                for (int r = 0; r < kd::ROWS; ++r) {
+                    if (r0 + r < n) load4x2<VEC>(X + (r0 + r) * (int64_t)d + fb + f + 256, width - f - 256, xn[r]);
                 }
             }
 #pragma unroll
@@ -281,6 +298,7 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
                 const float4 cb = *reinterpret_cast<const float4 *>(&cs[t * W + f + 128]);
                 const float2 nc[4] = {make_float2(ca.x, ca.y), make_float2(ca.z, ca.w), make_float2(cb.x, cb.y),
                                       make_float2(cb.z, cb.w)};
+                float rs[kd::ROWS];
 #pragma unroll
                 for (int r = 0; r < kd::ROWS; ++r) {
                     const float2 e0 = __fadd2_rn(x[r][0], nc[0]);
@@ -290,8 +308,9 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
                         const float2 de = __fadd2_rn(x[r][e], nc[e]);
                         run = __ffma2_rn(de, de, run);
                     }
-                    kahan(s[r][t], c[r][t], run.x + run.y);
+                    rs[r] = run.x + run.y;
                 }
+                kahan2(s2[t], cm2[t], make_float2(rs[0], rs[1]));
             }
         }
         // lanes -> one partial per (row, trial), as double-float values in
@@ -308,8 +327,8 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
         for (int r = 0; r < kd::ROWS; ++r)
 #pragma unroll
             for (int t = 0; t < kd::KT; ++t) {
-                hi[r * kd::KT + t] = s[r][t];
-                lo[r * kd::KT + t] = -c[r][t];
+                hi[r * kd::KT + t] = r == 0 ? s2[t].x : s2[t].y;
+                lo[r * kd::KT + t] = r == 0 ? cm2[t].x : cm2[t].y;
             }
         reduce_scatter_level<NS, NS / 2>(hi, lo, lane, 16);
         reduce_scatter_level<NS, NS / 4>(hi, lo, lane, 8);
@@ -476,7 +495,8 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t groups = (n + kd::GROUP - 1) / kd::GROUP;
-    int64_t gx = (3 * (int64_t)(sms > 0 ? sms : 1) + L.S - 1) / L.S;  // about three blocks per SM in total
+    // one resident block per SM over all slices
+    int64_t gx = (kd::MIN_BLOCKS * (int64_t)(sms > 0 ? sms : 1) + L.S - 1) / L.S;
     if (gx > groups) gx = groups;
     const dim3 dgrid((unsigned)(gx < 1 ? 1 : gx), (unsigned)L.S);
 

@@ -109,6 +109,16 @@ def test_fit_workspace_is_the_shared_scratch_plus_a_centroid_buffer(km):
         assert fit < n * k * 4
 
 
+def test_kmeanspp_slice_width_matches_the_library(km):
+    # the workspace holds one float2 per (slice, 8 trials, sample): one more
+    # feature than a whole slice adds exactly one slice of partial sums
+    n, k, s = 65536, 1024, km.KPP_SLICE_FEATURES
+    for d in (s, 2 * s):
+        grow = km.kmeans_workspace_bytes(km.OP_KMEANSPP, n, k, d + 1) - km.kmeans_workspace_bytes(km.OP_KMEANSPP, n, k, d)
+        assert grow == 8 * 8 * n
+    assert km.kmeans_workspace_bytes(km.OP_KMEANSPP, n, k, s) == km.kmeans_workspace_bytes(km.OP_KMEANSPP, n, k, s - 1)
+
+
 def test_relocate_workspace_and_argument_checks(km):
     lib = _lib(km)
     for n, k in [(10, 1), (4096, 256), (131072, 8192)]:
