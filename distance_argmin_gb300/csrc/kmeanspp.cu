@@ -80,12 +80,16 @@ __device__ __forceinline__ double warp_incl_scan(double v, int lane) {
 
 // The running sum at sample i is (sum of the block sums before its block) +
 // (the in-block prefix up to i); the block-sum prefix is the same for every
-// trial, so all trials see one consistent running sum.
-__global__ void kpp_pick_kernel(const double *__restrict__ bsum, int64_t n_blocks, const double *__restrict__ D2,
-                                int64_t n, uint64_t seed, uint64_t draw_base, int T, int64_t *__restrict__ cand) {
+// trial, so all trials see one consistent running sum.  One warp per trial,
+// each in a block of its own: the scans are float64, and this part's float64
+// pipe is narrow enough (about two FMAs per clock per SM) that eight trials
+// sharing one SM took 14 us.
+__global__ void __launch_bounds__(32)
+    kpp_pick_kernel(const double *__restrict__ bsum, int64_t n_blocks, const double *__restrict__ D2, int64_t n,
+                    uint64_t seed, uint64_t draw_base, int T, int64_t *__restrict__ cand) {
     griddep_wait();
-    const int lane = threadIdx.x & 31;
-    const int t = threadIdx.x >> 5;
+    const int lane = threadIdx.x;
+    const int t = blockIdx.x;
     if (t >= T) return;
     // total of D^2
     double total = 0.0;
@@ -527,7 +531,7 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
         chain(launch_kernel(true, kpp_update_kernel, dim3((unsigned)L.n_blocks), dim3(kBsThreads), 0, s,
                             (const double *)dist, (const double *)bpot, T, n, L.n_blocks, (const int64_t *)cand, indices,
                             c - 1, c == 1 ? 1 : 0, D2, bsum));
-        chain(launch_kernel(true, kpp_pick_kernel, dim3(1), dim3(32 * T), 0, s, (const double *)bsum, L.n_blocks,
+        chain(launch_kernel(true, kpp_pick_kernel, dim3((unsigned)T), dim3(32), 0, s, (const double *)bsum, L.n_blocks,
                             (const double *)D2, n, seed, 1 + (uint64_t)(c - 1) * (uint64_t)T, T, cand));
         dist_pass(T, D2);
     }
