@@ -196,7 +196,13 @@ def test_status_ok_after_assign(gpu_lib):
 
 # ------------------------------------------------------------- k-means++
 @pytest.mark.parametrize("case", [(3000, 64, 40, 0, 42), (3000, 64, 40, 1, 7), (500, 33, 60, 3, 123),
-                                  (2048, 128, 32, 8, 2024), (1000, 4, 1000, 2, 5)],
+                                  (2048, 128, 32, 8, 2024), (1000, 4, 1000, 2, 5),
+                                  # several 256-feature steps (the register prefetch), ragged last step
+                                  (1500, 700, 12, 4, 11),
+                                  # two feature slices, the second ragged
+                                  (1200, 4100, 6, 3, 12),
+                                  # odd d: scalar loads, several steps
+                                  (900, 1027, 8, 2, 13)],
                          ids=lambda c: "n%d_d%d_k%d_T%d_s%d" % c)
 def test_kmeanspp_indices_match_oracle(gpu_lib, case):
     n, d, k, T, seed = case
