@@ -617,16 +617,13 @@ static bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, int elem_byte
 }
 
 int device_sm_count() {
-    static int cached[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (cached[dev] == 0) {
-        int v = 0;
+    static std::atomic<int> cached[kMaxDevices];
+    return cached_per_device(cached, [] {
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = v > 0 ? v : 1;
-    }
-    return cached[dev];
+        return v > 0 ? v : 1;
+    });
 }
 
 int assign_tc_smem_bytes() { return tc::Fmt<false>::SMEM_BYTES; }
@@ -634,11 +631,8 @@ int assign_tc_smem_bytes() { return tc::Fmt<false>::SMEM_BYTES; }
 // CTA pairs that can be resident at once (the persistent grid never exceeds
 // it, so no pair waits for another to finish).
 static int resident_pairs() {
-    static int cached[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (cached[dev] == 0) {
+    static std::atomic<int> cached[kMaxDevices];
+    return cached_per_device(cached, [] {
         int clusters = 0;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
@@ -656,9 +650,8 @@ static int resident_pairs() {
             cudaGetLastError();  // clear
             clusters = device_sm_count() / 2;
         }
-        cached[dev] = clusters < 1 ? 1 : clusters;
-    }
-    return cached[dev];
+        return clusters < 1 ? 1 : clusters;
+    });
 }
 
 template <bool DB, bool TF32>
@@ -669,18 +662,30 @@ static cudaError_t set_smem_limit() {
 
 cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
                              uint8_t *ws, cudaStream_t stream, bool chained, bool tf32, const FusedUpdate *fused) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = set_smem_limit<true, false>();
-        if (attr_err == cudaSuccess) attr_err = set_smem_limit<false, false>();
-        if (attr_err == cudaSuccess) attr_err = set_smem_limit<true, true>();
-        if (attr_err == cudaSuccess) attr_err = set_smem_limit<false, true>();
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(assign_tc_kernel<true, false, true>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Fmt<false>::SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    // the shared-memory opt-in, once per device; a failure is kept and
+    // returned by every later launch on that device
+    static std::once_flag attr_once[kMaxDevices];
+    static std::atomic<int> attr_err[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
+    auto set_all = [] {
+        cudaError_t e = set_smem_limit<true, false>();
+        if (e == cudaSuccess) e = set_smem_limit<false, false>();
+        if (e == cudaSuccess) e = set_smem_limit<true, true>();
+        if (e == cudaSuccess) e = set_smem_limit<false, true>();
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(assign_tc_kernel<true, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     tc::Fmt<false>::SMEM_BYTES);
+        return e;
+    };
+    if (dev < 0) {
+        const cudaError_t e = set_all();
+        if (e != cudaSuccess) return e;
+    } else {
+        std::call_once(attr_once[dev], [&] { attr_err[dev].store((int)set_all(), std::memory_order_release); });
+        const cudaError_t e = (cudaError_t)attr_err[dev].load(std::memory_order_acquire);
+        if (e != cudaSuccess) return e;
+    }
 
     // C hi / lo: bf16 (64-byte swizzle) or, for 3xTF32, fp32 (128-byte swizzle)
     CUtensorMap tmX, tmChi, tmClo;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
 #include <utility>
 
 #include "../../include/kmeans_gb300.h"
@@ -42,6 +44,38 @@ inline cudaError_t launch_kernel(bool chained, void (*kernel)(KArgs...), dim3 gr
     cfg.attrs = chained ? attr : nullptr;
     cfg.numAttrs = chained ? 1u : 0u;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------------------------
+// Host: one-time setup per device.  Function attributes (the shared-memory
+// opt-in) are per device, and the cached launch limits differ per device, so
+// both are kept per device index and set up safely from any host thread.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+// Runs fn() once for the current device (every time for a device index
+// beyond kMaxDevices, which has no slot).
+template <typename Fn>
+inline void once_per_device(std::once_flag (&flags)[kMaxDevices], Fn &&fn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices)
+        std::call_once(flags[dev], std::forward<Fn>(fn));
+    else
+        fn();
+}
+
+// cache[device] = compute() the first time it is asked for on a device (a
+// positive value; races compute the same value twice).
+template <typename Fn>
+inline int cached_per_device(std::atomic<int> (&cache)[kMaxDevices], Fn &&compute) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return compute();
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        v = compute();
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
 }
 
 // ---------------------------------------------------------------------------

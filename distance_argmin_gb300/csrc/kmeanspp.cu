@@ -484,16 +484,13 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
     const bool vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(X) & 15) == 0;
     const size_t smem = (size_t)kd::KT * L.W * sizeof(float);
     {
-        static bool attr_set[64] = {false};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        static std::once_flag attr_once[kMaxDevices];
+        once_per_device(attr_once, [] {
             cudaFuncSetAttribute(kpp_dist_part_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(kd::KT * kKppSliceFloats * sizeof(float)));
             cudaFuncSetAttribute(kpp_dist_part_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(kd::KT * kKppSliceFloats * sizeof(float)));
-            attr_set[dev] = true;
-        }
+        });
     }
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);

@@ -24,7 +24,7 @@ namespace {
 // Every GPU that loads this library holds this array until the process ends.
 __device__ __align__(256) static unsigned char g_noalloc_scratch[KMEANS_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+using km::kMaxDevices;
 std::mutex g_setup_mutex;
 void *g_scratch_ptr[kMaxDevices] = {nullptr};
 

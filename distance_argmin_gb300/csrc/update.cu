@@ -674,15 +674,15 @@ cudaError_t launch_fused_mean(const float *sums, const int32_t *cnt, const float
 // counting path above the 48 KiB default.
 static void set_counting_smem_limits(int64_t k) {
     if (k * 4 <= 48 * 1024) return;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || attr_set[dev]) return;
-    cudaFuncSetAttribute(upd_tile_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kCountingMaxK * 4));
-    cudaFuncSetAttribute(fin_tile_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kCountingMaxK * 4));
-    cudaFuncSetAttribute(upd_tile_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)(kCountingMaxK * 4));
-    attr_set[dev] = true;
+    static std::once_flag attr_once[kMaxDevices];
+    once_per_device(attr_once, [] {
+        cudaFuncSetAttribute(upd_tile_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kCountingMaxK * 4));
+        cudaFuncSetAttribute(fin_tile_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kCountingMaxK * 4));
+        cudaFuncSetAttribute(upd_tile_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kCountingMaxK * 4));
+    });
 }
 
 static int radix_passes(int64_t k) {
