@@ -118,7 +118,7 @@ struct FusedLayout {
 
 FusedLayout fused_layout(int64_t n, int64_t k, int64_t d) {
     FusedLayout F{};
-    F.A = assign_layout(n, k, d, true);
+    F.A = assign_layout(n, k, d, true, 2, false);  // the fused kernel never splits K
     int64_t o = align_up(F.A.bytes, 1024);
     F.off_sums = o; o = align_up(o + k * d * 4, 256);
     F.off_cnt = o; o = align_up(o + k * 4, 256);

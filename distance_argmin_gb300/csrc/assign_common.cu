@@ -40,10 +40,26 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 h) {
 // columns d .. d_pad-1 of the copies are zeroed.
 constexpr int kPrepThreads = 128;
 
+// Per call, before the tensor-core pass: every key to "none yet"; with the
+// K-split area, every ||x||^2 to 0 (the two halves of a split tile add their
+// partial norms into it) and the split tickets and tags to 0.
+__device__ __forceinline__ void reset_for_assign(unsigned long long *__restrict__ keys, int n,
+                                                 float *__restrict__ xnorm_zero, uint32_t *__restrict__ ksync,
+                                                 int ksync_words) {
+    const int stride = gridDim.x * blockDim.x;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        keys[i] = kEmptyKey;
+        if (xnorm_zero) xnorm_zero[i] = 0.f;
+    }
+    if (ksync)
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ksync_words; i += stride) ksync[i] = 0u;
+}
+
 __global__ void __launch_bounds__(kPrepThreads)
     prep_split_kernel(const float *__restrict__ C, int k, int d, int d_pad, __nv_bfloat16 *__restrict__ chi,
                       __nv_bfloat16 *__restrict__ clo, float *__restrict__ cnorm,
-                      unsigned long long *__restrict__ keys, int n, WsHeader *hdr) {
+                      unsigned long long *__restrict__ keys, int n, WsHeader *hdr, float *__restrict__ xnorm_zero,
+                      uint32_t *__restrict__ ksync, int ksync_words) {
     __shared__ float red[kPrepThreads / 32];
     griddep_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -92,8 +108,7 @@ __global__ void __launch_bounds__(kPrepThreads)
         }
         __syncthreads();
     }
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
-        keys[i] = kEmptyKey;
+    reset_for_assign(keys, n, xnorm_zero, ksync, ksync_words);
 }
 
 __device__ __forceinline__ float tf32_bits_trunc(float v) {
@@ -107,7 +122,8 @@ __device__ __forceinline__ float tf32_bits_trunc(float v) {
 __global__ void __launch_bounds__(kPrepThreads)
     prep_split_tf32_kernel(const float *__restrict__ C, int k, int d, int d_pad, float *__restrict__ chi,
                            float *__restrict__ clo, float *__restrict__ cnorm,
-                           unsigned long long *__restrict__ keys, int n, WsHeader *hdr) {
+                           unsigned long long *__restrict__ keys, int n, WsHeader *hdr, float *__restrict__ xnorm_zero,
+                      uint32_t *__restrict__ ksync, int ksync_words) {
     __shared__ float red[kPrepThreads / 32];
     griddep_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -144,8 +160,7 @@ __global__ void __launch_bounds__(kPrepThreads)
         }
         __syncthreads();
     }
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
-        keys[i] = kEmptyKey;
+    reset_for_assign(keys, n, xnorm_zero, ksync, ksync_words);
 }
 
 // Norms only (any d, any 4-byte alignment).
@@ -240,20 +255,26 @@ static int prep_grid(int64_t k, int64_t n) {
 
 cudaError_t launch_prep_split(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
                               uint8_t *ws, cudaStream_t s) {
+    const bool ks = L.off_ksync != 0;
     prep_split_kernel<<<prep_grid(k, n), kPrepThreads, 0, s>>>(
         C, (int)k, (int)d, (int)L.d_pad, reinterpret_cast<__nv_bfloat16 *>(ws + L.off_chi),
         reinterpret_cast<__nv_bfloat16 *>(ws + L.off_clo), reinterpret_cast<float *>(ws + L.off_cnorm),
-        reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws));
+        reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws),
+        ks ? reinterpret_cast<float *>(ws + L.off_xnorm) : nullptr,
+        ks ? reinterpret_cast<uint32_t *>(ws + L.off_ksync) : nullptr, ks ? kKSplitSlots * kKSplitSyncWords : 0);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prep_split_tf32(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
                                    uint8_t *ws, cudaStream_t s) {
     if (L.split_elem_bytes != 4) return cudaErrorInvalidValue;
+    const bool ks = L.off_ksync != 0;
     prep_split_tf32_kernel<<<prep_grid(k, n), kPrepThreads, 0, s>>>(
         C, (int)k, (int)d, (int)L.d_pad, reinterpret_cast<float *>(ws + L.off_chi),
         reinterpret_cast<float *>(ws + L.off_clo), reinterpret_cast<float *>(ws + L.off_cnorm),
-        reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws));
+        reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws),
+        ks ? reinterpret_cast<float *>(ws + L.off_xnorm) : nullptr,
+        ks ? reinterpret_cast<uint32_t *>(ws + L.off_ksync) : nullptr, ks ? kKSplitSlots * kKSplitSyncWords : 0);
     return cudaGetLastError();
 }
 

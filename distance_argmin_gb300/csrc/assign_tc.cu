@@ -100,6 +100,8 @@ constexpr int SINGLE_ACC_MAX_D_TF32 = 2048;
 constexpr int GROUP_M = 8;                     // pair sample blocks per raster band
 constexpr uint16_t PAIR_MASK = 0x3;
 static_assert(SPLIT_WARPS % 4 == 0 && WARP_EPI % 4 == 0, "epilogue warps start on a lane-quarter boundary");
+static_assert(kKSplitSlotBytes == 2 * BM * BN * 4 && kKSplitSyncWords == 2 * EPI_WARPS * 2,
+              "the K-split parking area matches the tile and the epilogue warps");
 
 // What depends on the operand format.
 //  bf16x3: hi = bf16(v), lo = bf16(v - hi), both written by the split warps
@@ -147,6 +149,14 @@ struct TcParams {
     uint32_t *status;
     int test_starve;  // test hook: the producer issues no loads, so the pipeline waits run out
     FusedUpdate fu;   // the update fused into the epilogue (kmeans_lloyd_iter_fused), else all null
+    // K split of the last round: units [0, num_full) are whole tiles; unit
+    // num_full + 2 s + h is half h of tile num_full + s (h = 0: k-blocks
+    // [0, kb_half), h = 1: [kb_half, num_kb)).  Without a split num_units =
+    // num_full = num_tiles.
+    int num_units, num_full, kb_half;
+    uint32_t epoch;   // this launch's ready tag: nonzero, unlike any tag left in ksync
+    float *kacc;      // parked accumulators [slot][CTA][BM rows][BN columns]
+    uint32_t *ksync;  // [slot][CTA][epilogue warp] {ticket, ready tag}
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb) {
@@ -156,6 +166,17 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
     const int r = tile - band * tc::GROUP_M * num_n;
     mb = first + r % gs;
     nb = r / gs;
+}
+
+struct KUnit {
+    int tile, kb0, kb1, half;  // half -1: a whole tile
+};
+
+__device__ __forceinline__ KUnit unit_at(const TcParams &p, int u) {
+    if (u < p.num_full) return {u, 0, p.num_kb, -1};
+    const int v = u - p.num_full;
+    const int h = v & 1;
+    return {p.num_full + (v >> 1), h ? p.kb_half : 0, h ? p.num_kb : p.kb_half, h};
 }
 
 __device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 h) {
@@ -348,14 +369,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
         const int t = threadIdx.x;  // 0 .. SPLIT_THREADS-1
         int it = 0;
         bool ok = true;
-        for (int tile = pair; tile < p.num_tiles && ok; tile += num_pairs) {
+        for (int unit = pair; unit < p.num_units && ok; unit += num_pairs) {
+            const KUnit un = unit_at(p, unit);
             int mb, nb;
-            tile_coords(tile, p.num_m, p.num_n, mb, nb);
+            tile_coords(un.tile, p.num_m, p.num_n, mb, nb);
             const int m0 = mb * (2 * tc::BM) + (int)rank * tc::BM;
             float acc[tc::ROWS_PER_SPLIT_THREAD], comp[tc::ROWS_PER_SPLIT_THREAD];
 #pragma unroll
             for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) acc[i] = comp[i] = 0.f;
-            for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+            for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
                 const int s = it % F::SXB;
                 const int as = it % F::SA;
                 if (!mbar_wait_warp(bar(F::XB_FULL + s), (it / F::SXB) & 1, p.status) ||
@@ -389,7 +411,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 float v = acc[0] - comp[0];
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
                 const int row = m0 + (t >> 1);
-                if (nb == 0 && (t & 1) == 0 && row < p.n) p.xnorm[row] = v;
+                if (nb == 0 && (t & 1) == 0 && row < p.n) {
+                    // the two K halves of a split tile each add their part (onto 0)
+                    if (un.half < 0) p.xnorm[row] = v;
+                    else atomicAdd(p.xnorm + row, v);
+                }
             } else {
 #pragma unroll
                 for (int i = 0; i < tc::ROWS_PER_SPLIT_THREAD; ++i) {
@@ -397,7 +423,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                     v += __shfl_xor_sync(0xffffffffu, v, 1);
                     v += __shfl_xor_sync(0xffffffffu, v, 2);
                     const int row = m0 + tc::SPLIT_ROW_STRIDE * i + t / tc::SPLIT_GROUPS;
-                    if (nb == 0 && (t & (tc::SPLIT_GROUPS - 1)) == 0 && row < p.n) p.xnorm[row] = v;
+                    if (nb == 0 && (t & (tc::SPLIT_GROUPS - 1)) == 0 && row < p.n) {
+                        if (un.half < 0) p.xnorm[row] = v;
+                        else atomicAdd(p.xnorm + row, v);  // a K half of a split tile, onto 0
+                    }
                 }
             }
         }
@@ -406,15 +435,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
         const int q = warp & 3;              // tensor-memory lane quarter this warp may read
         const int part = (warp - tc::WARP_EPI) >> 2;  // which EPI_COLS of the tile's 256 columns
         int tile_iter = 0;
-        for (int tile = pair; tile < p.num_tiles; tile += num_pairs, ++tile_iter) {
+        for (int unit = pair; unit < p.num_units; unit += num_pairs, ++tile_iter) {
+            const KUnit un = unit_at(p, unit);
             int mb, nb;
-            tile_coords(tile, p.num_m, p.num_n, mb, nb);
+            tile_coords(un.tile, p.num_m, p.num_n, mb, nb);
             const int buf = DB ? (tile_iter & 1) : 0;
             const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (tile_iter & 1);
             if (!mbar_wait_warp(bar(F::T_FULL + buf), phase, p.status)) break;
             tc_fence_after();
             const uint32_t acc_base = tmem_base + (DB ? (uint32_t)(buf * tc::BN) : (uint32_t)tc::ACC_MAIN);
             const int n0 = nb * tc::BN + part * tc::EPI_COLS;
+            const float *parked = nullptr;  // the other K half's accumulator, to add before the argmin
+            if constexpr (DB && !FUSED) {
+                if (un.half >= 0) {
+                    // The two K halves of a split tile meet here, warp by warp.
+                    // The first to take a ticket parks its raw accumulator and
+                    // tags it; the second waits for the tag (the first is
+                    // running and only storing) and adds the parked part to its
+                    // own.  float addition commutes, so the sum does not depend
+                    // on which half came first.
+                    const int slot = un.tile - p.num_full;
+                    uint32_t *sync = p.ksync + (((size_t)slot * 2 + rank) * tc::EPI_WARPS + (warp - tc::WARP_EPI)) * 2;
+                    // this warp's 32 rows x EPI_COLS columns, interleaved so that
+                    // every 16-byte access of the warp covers 512 contiguous
+                    // bytes: float4 u4 of chunk ch of lane l at (ch * 8 + u4) * 32 + l
+                    float *park = p.kacc + ((((size_t)slot * 2 + rank) * tc::EPI_WARPS + (warp - tc::WARP_EPI)) *
+                                                (32 * tc::EPI_COLS)) + (size_t)lane * 4;
+                    uint32_t ticket = 0;
+                    if (lane == 0) ticket = atomicAdd(sync, 1u);
+                    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+                    if (ticket == 0) {
+                        const uint32_t lanes = (uint32_t)(q * 32) << 16;
+#pragma unroll 1
+                        for (int ch = 0; ch < tc::EPI_COLS / tc::EPI_CHUNK; ++ch) {
+                            if (n0 + ch * tc::EPI_CHUNK >= p.k) break;
+                            float vm[tc::EPI_CHUNK];
+                            tmem_ld_one<tc::EPI_CHUNK>(
+                                acc_base + lanes + (uint32_t)(part * tc::EPI_COLS + ch * tc::EPI_CHUNK), vm);
+                            float4 *dst = reinterpret_cast<float4 *>(park) + ch * (tc::EPI_CHUNK / 4) * 32;
+#pragma unroll
+                            for (int u4 = 0; u4 < tc::EPI_CHUNK / 4; ++u4)
+                                dst[u4 * 32] = make_float4(vm[4 * u4], vm[4 * u4 + 1], vm[4 * u4 + 2], vm[4 * u4 + 3]);
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(F::T_EMPTY + buf), 0));
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0) st_release_gpu(sync + 1, p.epoch);
+                        continue;
+                    }
+                    if (!flag_wait_warp(sync + 1, p.epoch, p.status)) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(F::T_EMPTY + buf), 0));
+                        break;
+                    }
+                    __threadfence();
+                    if (lane == 0) sync[0] = 0u;  // the next launch starts from ticket 0
+                    parked = park;
+                }
+            }
             float best = __int_as_float(0x7f800000);  // +inf
             int arg = -1;
 #pragma unroll 1
@@ -427,6 +508,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 float vm[tc::EPI_CHUNK], vc[tc::EPI_CHUNK];
                 if constexpr (DB) {
                     tmem_ld_one<tc::EPI_CHUNK>(acc_base + lanes + col, vm);
+                    if constexpr (!FUSED) {
+                        if (parked) {
+                            const float4 *src = reinterpret_cast<const float4 *>(parked) + ch * (tc::EPI_CHUNK / 4) * 32;
+#pragma unroll
+                            for (int u4 = 0; u4 < tc::EPI_CHUNK / 4; ++u4) {
+                                const float4 pv = __ldcg(src + u4 * 32);
+                                vm[4 * u4] += pv.x;
+                                vm[4 * u4 + 1] += pv.y;
+                                vm[4 * u4 + 2] += pv.z;
+                                vm[4 * u4 + 3] += pv.w;
+                            }
+                        }
+                    }
                 } else {
                     tmem_ld_pair<tc::EPI_CHUNK>(acc_base + lanes + col, tmem_base + lanes + tc::ACC_CORR + col, vm, vc);
 #pragma unroll
@@ -484,12 +578,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             tma_prefetch_desc(&tmClo);
             int it = 0;
             bool ok = true;
-            for (int tile = pair; tile < p.num_tiles && ok; tile += num_pairs) {
+            for (int unit = pair; unit < p.num_units && ok; unit += num_pairs) {
+                const KUnit un = unit_at(p, unit);
                 int mb, nb;
-                tile_coords(tile, p.num_m, p.num_n, mb, nb);
+                tile_coords(un.tile, p.num_m, p.num_n, mb, nb);
                 const int m0 = mb * (2 * tc::BM) + (int)rank * tc::BM;
                 const int c0 = nb * tc::BN + (int)rank * tc::BN_CTA;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
                     const int s = it % F::SXB;
                     if (!mbar_wait(bar(F::XB_EMPTY + s), ((it / F::SXB) & 1) ^ 1, p.status)) {
                         ok = false;
@@ -517,56 +612,106 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             const uint32_t d_corr = tmem_base + tc::ACC_CORR;
             int it = 0, tile_iter = 0;
             bool ok = true;
-            for (int tile = pair; tile < p.num_tiles && ok; tile += num_pairs, ++tile_iter) {
+            for (int unit = pair; unit < p.num_units && ok; unit += num_pairs, ++tile_iter) {
                 const int buf = DB ? (tile_iter & 1) : 0;
                 const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (tile_iter & 1);
                 if (!mbar_wait_cluster(bar(F::T_EMPTY + buf), phase ^ 1, p.status)) break;
                 tc_fence_after();
                 const uint32_t dm = DB ? tmem_base + (uint32_t)(buf * tc::BN) : d_main;
                 const uint32_t dc = DB ? dm : d_corr;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const int s = it % F::SXB;
-                    const int as = it % F::SA;
-                    // operands of this stage: bf16 hi and lo of X in the A stage;
-                    // 3xTF32 hi of X in place in the fp32 tile, lo in the A stage
-                    const uint32_t xb = sbase + s * F::XB_STAGE;
-                    const uint32_t bhi = xb + tc::X_BYTES;
-                    const uint32_t blo = bhi + F::B_BYTES;
-                    const uint32_t ast = sbase + F::A_BASE + as * F::A_STAGE;
-                    const uint32_t ahi = TF32 ? xb : ast;
-                    const uint32_t alo = TF32 ? ast : ast + F::A_LO;
-                    // descriptors first: once the split stage lands, only the
-                    // MMAs remain between it and the tensor pipe (measured: the
-                    // issue latency here is on the critical path)
-                    uint64_t dah[F::K_STEPS], dal[F::K_STEPS], dbh[F::K_STEPS], dbl[F::K_STEPS];
-#pragma unroll
-                    for (int kk = 0; kk < F::K_STEPS; ++kk) {
-                        dah[kk] = umma_smem_desc(ahi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                        dal[kk] = umma_smem_desc(alo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                        dbh[kk] = umma_smem_desc(bhi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                        dbl[kk] = umma_smem_desc(blo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                    }
-                    // both CTAs' split warps have seen their X and C stage land
-                    if (!mbar_wait_cluster(bar(F::A_FULL + as), (it / F::SA) & 1, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < F::K_STEPS; ++kk) {
-                        const uint32_t first = (kb | kk) != 0 ? 1u : 0u;
-                        if constexpr (TF32) {
-                            mma_tf32_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
-                            mma_tf32_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
-                            mma_tf32_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
-                        } else {
-                            mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
-                            mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
-                            mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                // whole tiles keep a loop of their own: any per-unit logic in it
+                // measured 1.3% on the whole kernel
+                if (unit < p.num_full) {
+                    for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                        const int s = it % F::SXB;
+                        const int as = it % F::SA;
+                        // operands of this stage: bf16 hi and lo of X in the A stage;
+                        // 3xTF32 hi of X in place in the fp32 tile, lo in the A stage
+                        const uint32_t xb = sbase + s * F::XB_STAGE;
+                        const uint32_t bhi = xb + tc::X_BYTES;
+                        const uint32_t blo = bhi + F::B_BYTES;
+                        const uint32_t ast = sbase + F::A_BASE + as * F::A_STAGE;
+                        const uint32_t ahi = TF32 ? xb : ast;
+                        const uint32_t alo = TF32 ? ast : ast + F::A_LO;
+                        // descriptors first: once the split stage lands, only the
+                        // MMAs remain between it and the tensor pipe (measured: the
+                        // issue latency here is on the critical path)
+                        uint64_t dah[F::K_STEPS], dal[F::K_STEPS], dbh[F::K_STEPS], dbl[F::K_STEPS];
+    #pragma unroll
+                        for (int kk = 0; kk < F::K_STEPS; ++kk) {
+                            dah[kk] = umma_smem_desc(ahi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            dal[kk] = umma_smem_desc(alo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            dbh[kk] = umma_smem_desc(bhi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            dbl[kk] = umma_smem_desc(blo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
                         }
+                        // both CTAs' split warps have seen their X and C stage land
+                        if (!mbar_wait_cluster(bar(F::A_FULL + as), (it / F::SA) & 1, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+    #pragma unroll
+                        for (int kk = 0; kk < F::K_STEPS; ++kk) {
+                            const uint32_t first = (kb | kk) != 0 ? 1u : 0u;
+                            if constexpr (TF32) {
+                                mma_tf32_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
+                                mma_tf32_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
+                                mma_tf32_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                            } else {
+                                mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
+                                mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
+                                mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                            }
+                        }
+                        mma_commit_pair_multicast(bar(F::XB_EMPTY + s), tc::PAIR_MASK);
+                        mma_commit_pair_multicast(bar(F::A_EMPTY + as), tc::PAIR_MASK);
                     }
-                    mma_commit_pair_multicast(bar(F::XB_EMPTY + s), tc::PAIR_MASK);
-                    mma_commit_pair_multicast(bar(F::A_EMPTY + as), tc::PAIR_MASK);
+                } else {
+                    const KUnit un = unit_at(p, unit);
+                    for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
+                        const int s = it % F::SXB;
+                        const int as = it % F::SA;
+                        // operands of this stage: bf16 hi and lo of X in the A stage;
+                        // 3xTF32 hi of X in place in the fp32 tile, lo in the A stage
+                        const uint32_t xb = sbase + s * F::XB_STAGE;
+                        const uint32_t bhi = xb + tc::X_BYTES;
+                        const uint32_t blo = bhi + F::B_BYTES;
+                        const uint32_t ast = sbase + F::A_BASE + as * F::A_STAGE;
+                        const uint32_t ahi = TF32 ? xb : ast;
+                        const uint32_t alo = TF32 ? ast : ast + F::A_LO;
+                        // descriptors first: once the split stage lands, only the
+                        // MMAs remain between it and the tensor pipe (measured: the
+                        // issue latency here is on the critical path)
+                        uint64_t dah[F::K_STEPS], dal[F::K_STEPS], dbh[F::K_STEPS], dbl[F::K_STEPS];
+    #pragma unroll
+                        for (int kk = 0; kk < F::K_STEPS; ++kk) {
+                            dah[kk] = umma_smem_desc(ahi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            dal[kk] = umma_smem_desc(alo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            dbh[kk] = umma_smem_desc(bhi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            dbl[kk] = umma_smem_desc(blo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                        }
+                        // both CTAs' split warps have seen their X and C stage land
+                        if (!mbar_wait_cluster(bar(F::A_FULL + as), (it / F::SA) & 1, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+    #pragma unroll
+                        for (int kk = 0; kk < F::K_STEPS; ++kk) {
+                            const uint32_t first = (kb != un.kb0 || kk != 0) ? 1u : 0u;
+                            if constexpr (TF32) {
+                                mma_tf32_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
+                                mma_tf32_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
+                                mma_tf32_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                            } else {
+                                mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
+                                mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
+                                mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                            }
+                        }
+                        mma_commit_pair_multicast(bar(F::XB_EMPTY + s), tc::PAIR_MASK);
+                        mma_commit_pair_multicast(bar(F::A_EMPTY + as), tc::PAIR_MASK);
+                    }
                 }
                 if (!ok) break;
                 mma_commit_pair_multicast(bar(F::T_FULL + buf), tc::PAIR_MASK);
@@ -654,6 +799,18 @@ static int resident_pairs() {
     });
 }
 
+// Ready tags of K-split tiles: one per launch, never 0 (the value the prologue
+// leaves), so a tag from an earlier launch on the same workspace never reads
+// as ready.
+static uint32_t next_ksplit_epoch() {
+    static std::atomic<uint32_t> counter{0};
+    uint32_t e;
+    do {
+        e = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    } while (e == 0u);
+    return e;
+}
+
 template <bool DB, bool TF32>
 static cudaError_t set_smem_limit() {
     return cudaFuncSetAttribute(assign_tc_kernel<DB, TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -723,8 +880,27 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     const int max_pairs = resident_pairs();
     const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
     const int grid = 2 * (pairs > 0 ? pairs : 1);
-    trace_mark(kTraceAssignTc, false, stream);
     const bool db = d <= (tf32 ? tc::SINGLE_ACC_MAX_D_TF32 : tc::SINGLE_ACC_MAX_D);
+    // K split of a last round that is at most half full (double-buffered
+    // accumulators only, not the fused update): its tiles run as two K halves
+    // on two pairs each, about half a round instead of a whole one
+    p.num_units = p.num_full = p.num_tiles;
+    p.kb_half = p.num_kb / 2;
+    p.epoch = 0;
+    p.kacc = nullptr;
+    p.ksync = nullptr;
+    if (db && !fused && L.off_kacc != 0 && p.num_kb >= 2 && p.num_tiles > pairs) {
+        const int rounds = (p.num_tiles + pairs - 1) / pairs;
+        const int tail = p.num_tiles - (rounds - 1) * pairs;
+        if (2 * tail <= pairs && tail <= kKSplitSlots) {
+            p.num_full = p.num_tiles - tail;
+            p.num_units = p.num_full + 2 * tail;
+            p.kacc = reinterpret_cast<float *>(ws + L.off_kacc);
+            p.ksync = reinterpret_cast<uint32_t *>(ws + L.off_ksync);
+            p.epoch = next_ksplit_epoch();
+        }
+    }
+    trace_mark(kTraceAssignTc, false, stream);
     const dim3 g(grid), b(tc::THREADS);
     cudaError_t e;
     if (fused) {

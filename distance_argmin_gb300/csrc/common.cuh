@@ -150,12 +150,31 @@ struct AssignLayout {
     int64_t off_clo;     // k x d_pad bf16 lo part of C
     int64_t off_partial; // kMaxReduceBlocks x f64 inertia partial sums
     int64_t split_elem_bytes;  // 2: bf16 hi / lo of C; 4: fp32 (3xTF32) hi / lo
+    int64_t off_kacc;    // K-split tiles: kKSplitSlots x kKSplitSlotBytes parked accumulators (0: none)
+    int64_t off_ksync;   // K-split tiles: kKSplitSlots x kKSplitSyncWords tickets and ready tags
     int64_t bytes;
 };
 
 constexpr int kMaxReduceBlocks = 1024;
 
-inline AssignLayout assign_layout(int64_t n, int64_t k, int64_t d, bool split, int split_elem_bytes = 2) {
+// The tensor-core assignment runs a persistent schedule of 256 x 256 tiles
+// over its CTA pairs.  When the last round is at most half full, its tiles
+// run as two halves of K each on two pairs; the half that finishes first
+// parks its raw accumulator (one CTA: 128 rows x 256 columns of float32) for
+// the other.  The parking area exists only for problems with more than
+// kKSplitMinTiles tiles (below that there are no more tiles than pairs), and
+// is sized for at most kKSplitSlots split tiles.
+constexpr int kKSplitSlots = 40;
+constexpr int64_t kKSplitMinTiles = 64;
+constexpr int64_t kKSplitSlotBytes = 2 * 128 * 256 * 4;  // both CTAs of a pair
+constexpr int kKSplitSyncWords = 2 * 8 * 2;              // CTA x epilogue warp x (ticket, tag)
+
+inline int64_t assign_tiles(int64_t n, int64_t k) { return ((n + 255) / 256) * ((k + 255) / 256); }
+
+// `tail_split`: reserve the K-split parking area (tensor-core paths that may
+// split their last round; not the built-in scratch or the fused update).
+inline AssignLayout assign_layout(int64_t n, int64_t k, int64_t d, bool split, int split_elem_bytes = 2,
+                                  bool tail_split = true) {
     AssignLayout L{};
     L.d_pad = align_up(d, 64);
     L.split_elem_bytes = split ? split_elem_bytes : 0;
@@ -170,6 +189,11 @@ inline AssignLayout assign_layout(int64_t n, int64_t k, int64_t d, bool split, i
         L.off_chi = L.off_clo = 0;
     }
     o = align_up(o, 1024); L.off_partial = o; o += kMaxReduceBlocks * 8;
+    L.off_kacc = L.off_ksync = 0;
+    if (split && tail_split && assign_tiles(n, k) > kKSplitMinTiles) {
+        o = align_up(o, 1024); L.off_kacc = o; o += kKSplitSlots * kKSplitSlotBytes;
+        o = align_up(o, 1024); L.off_ksync = o; o += kKSplitSlots * kKSplitSyncWords * 4;
+    }
     L.bytes = align_up(o, 1024);
     return L;
 }

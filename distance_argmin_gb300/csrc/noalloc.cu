@@ -58,7 +58,7 @@ extern "C" int kmeans_assign_noalloc(const float *X, const float *C, int64_t n, 
     if ((reinterpret_cast<uintptr_t>(X) & 3u) || (reinterpret_cast<uintptr_t>(C) & 3u)) return KMEANS_ERR_INVALID_ARG;
     if (d % 4 != 0 || (reinterpret_cast<uintptr_t>(X) & 15u) || (reinterpret_cast<uintptr_t>(C) & 15u))
         return KMEANS_ERR_UNSUPPORTED;
-    const km::AssignLayout L = km::assign_layout(n, k, d, true);
+    const km::AssignLayout L = km::assign_layout(n, k, d, true, 2, false);  // no K-split area in the scratch
     if ((uint64_t)L.bytes > (uint64_t)KMEANS_NOALLOC_SCRATCH_BYTES) return KMEANS_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;
     const int st = scratch_address(&scratch);

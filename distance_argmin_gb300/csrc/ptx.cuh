@@ -92,6 +92,51 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, ui
     }
 }
 
+// ---------------------------------------------------------------------------
+// Flags in global memory shared between CTA pairs of one grid.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Whole warp: wait until *flag == want (lane 0 polls with acquire loads).
+// False once the status word holds an error or the wait ran out of time
+// (which it then records).
+__device__ __forceinline__ bool flag_wait_warp(const uint32_t *flag, uint32_t want, uint32_t *status) {
+    int result = 0;  // 1 ready, -1 gave up
+    if (lane_id() == 0) {
+        uint64_t t0 = 0;
+        for (uint32_t spins = 0;; ++spins) {
+            if (ld_acquire_gpu(flag) == want) {
+                result = 1;
+                break;
+            }
+            if ((spins & 63u) == 63u) {
+                const uint64_t now = globaltimer_ns();
+                if (t0 == 0) t0 = now;
+                if (error_raised(status)) {
+                    result = -1;
+                    break;
+                }
+                if (now - t0 > kWaitLimitNs) {
+                    flag_error(status, kFlagTimeout);
+                    result = -1;
+                    break;
+                }
+            }
+        }
+    }
+    result = __shfl_sync(0xffffffffu, result, 0);
+    __syncwarp();
+    return result > 0;
+}
+
 // Bounded wait used while winding down after an error: ignores the error
 // flag (the point is to let in-flight work land) but keeps the time limit.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {

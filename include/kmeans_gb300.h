@@ -109,6 +109,13 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d);
  * inertia: output (device, one double), may be NULL.
  * Extra requirement of this tensor-core path: d % 4 == 0 and X, C 16-byte
  * aligned (KMEANS_ERR_UNSUPPORTED otherwise; kmeans_assign_ffma has none).
+ * Schedule: pairs of SMs work through 256 x 256 tiles of (samples,
+ * centroids) in rounds; when the last round is at most half full (and d <=
+ * 4096), each of its tiles is computed as two halves of the features on two
+ * pairs and the halves' sums are added at the end.  Those tiles' distances
+ * carry a different (no larger) float32 accumulation error than a single
+ * pass would, within the accuracy stated above; the results are the same
+ * from run to run on a given GPU.
  * seed: unused (kept for a uniform signature). */
 int kmeans_assign(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
                   int64_t *labels, float *best_dist, double *inertia,
@@ -164,8 +171,10 @@ int kmeans_lloyd_iter(const float *X, const float *C_old, float *C_new, int64_t 
  * samples, the epilogue warp that merged last adds those samples' rows
  * (still in L2) into their clusters' sums with float atomics; a last pass
  * divides.  No sorted member list and no second pass over X in HBM.
- * Labels, best_dist and *inertia are kmeans_lloyd_iter's bit for bit.
- * C_new differs: the sums are plain float32 in an order that varies from run
+ * Labels, best_dist and *inertia are kmeans_lloyd_iter's bit for bit, except
+ * where kmeans_lloyd_iter computes a tile as two K halves (see kmeans_assign):
+ * there best_dist and *inertia differ within the distance accuracy (labels
+ * only at ties that close).  C_new differs: the sums are plain float32 in an order that varies from run
  * to run (not reproducible bit for bit), so a cluster of m members carries a
  * relative error up to about m * 2^-24 (within 1e-5 up to some 150 members
  * per cluster); empty clusters keep C_old bit for bit.  counts (may be NULL)
@@ -196,8 +205,12 @@ int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, in
  * `copy_stream`; on `stream` the centroids are copied and split once, and
  * each slice's tensor-core pass starts as soon as its rows have landed, so
  * the copies and the assignment overlap.  Finalize and the mean update then
- * run on `stream` exactly as in kmeans_lloyd_iter, whose outputs (C_new,
- * labels, best_dist, *inertia, counts) these are, bit for bit.  Finally
+ * run on `stream` exactly as in kmeans_lloyd_iter.  With slices = 1 the
+ * outputs (C_new, labels, best_dist, *inertia, counts) are kmeans_lloyd_iter's
+ * bit for bit; with more, each slice's pass may compute other tiles as two K
+ * halves than the single call does (see kmeans_assign), so best_dist and
+ * *inertia may differ within the distance accuracy (and labels, C_new and
+ * counts only at ties that close).  Finally
  * C_new, the labels and *inertia are copied to C_new_host, labels_host and
  * *inertia_host (each may be NULL; inertia_host needs inertia).
  * The copies into X wait for the work enqueued on `stream` before the call

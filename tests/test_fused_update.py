@@ -1,9 +1,12 @@
 """kmeans_lloyd_iter_fused: the update fused into the assignment's epilogue.
 
 The assignment half is the same kernel, so labels, distances and inertia must
-equal kmeans_lloyd_iter's bit for bit; the counts are exact; the centroids
-are float32 sums in a varying order, checked against the oracle's mean of the
-same labels within the centroid tolerance, with empty clusters bit for bit."""
+equal kmeans_lloyd_iter's bit for bit while no tile is split (no more tiles
+than CTA pairs); kmeans_lloyd_iter may run a partly filled last round as two
+K halves per tile, whose sum carries a different float32 accumulation error
+(within the distance tolerance), and the fused kernel never does.  The counts are exact; the centroids are float32
+sums in a varying order, checked against the oracle's mean of the same labels
+within the centroid tolerance, with empty clusters bit for bit."""
 import ctypes
 
 import numpy as np
@@ -11,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from parity import check_centroids
+from parity import DIST_RTOL, check_centroids
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -35,9 +38,16 @@ def test_fused_iteration_matches_the_sorted_one_and_the_oracle(gpu_lib, shape):
     ref = gpu_lib.kmeans_lloyd_iter(Xd, Cd)
     got = gpu_lib.kmeans_lloyd_iter_fused(Xd, Cd)
     labels = _host(got[1])
-    np.testing.assert_array_equal(labels, _host(ref[1]))
-    assert _host(got[2]).tobytes() == _host(ref[2]).tobytes()
-    assert float(got[3].item()) == float(ref[3].item())
+    np.testing.assert_array_equal(labels, _host(ref[1]))  # planted blobs: no near ties
+    tiles = ((n + 255) // 256) * ((k + 255) // 256)
+    if tiles <= 76:  # no more tiles than a GB300 has CTA pairs: nothing splits
+        assert _host(got[2]).tobytes() == _host(ref[2]).tobytes()
+        assert float(got[3].item()) == float(ref[3].item())
+    else:
+        scale = (X.astype(np.float64) ** 2).sum(1) + (C0.astype(np.float64) ** 2).sum(1)[labels]
+        diff = np.abs(_host(got[2]).astype(np.float64) - _host(ref[2]).astype(np.float64))
+        assert (diff <= DIST_RTOL * scale).all()
+        assert abs(float(got[3].item()) - float(ref[3].item())) <= DIST_RTOL * scale.sum()
     np.testing.assert_array_equal(_host(got[4]), _host(ref[4]))
     o_C, o_cnt = oracle.update(X, labels, C0)
     check_centroids(_host(got[0]), o_C, what=f"fused {shape}")

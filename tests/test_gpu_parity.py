@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from parity import check_assign, check_centroids, sq_norms
+from parity import DIST_RTOL, check_assign, check_centroids, sq_norms
 
 pytestmark = pytest.mark.gpu
 
@@ -323,10 +323,22 @@ def test_starved_pipeline_times_out_and_reports(gpu_lib, monkeypatch):
     check_assign(X, C, host(labels), host(best), o_l, o_b, o_s, what="after timeout")
 
 
+def _same_distances(best, ref_best, X, C, labels):
+    # each slice runs its own tensor-core pass, whose schedule may split a
+    # partly filled last round into K halves differently from the single
+    # call: a different float32 accumulation error, within the tolerance
+    scale = sq_norms(X) + sq_norms(C)[labels]
+    diff = np.abs(np.asarray(best, np.float64) - np.asarray(ref_best, np.float64))
+    assert (diff <= DIST_RTOL * scale).all()
+    return scale.sum()
+
+
 def test_lloyd_iteration_from_host_buffers_matches_device_call(gpu_lib):
     # the host-input iteration (row slices assigned as they land) gives the
-    # device-resident call's labels, centroids, counts and inertia bit for bit;
-    # 5 slices of 6144 rows over 30000 samples leave a ragged last slice
+    # device-resident call's labels, centroids and counts bit for bit, and its
+    # distances and inertia bit for bit in one slice, within the tolerance in
+    # several; 5 slices of 6144 rows over 30000 samples leave a ragged last
+    # slice
     w = synth.Workload("t", 30000, 300, 132, 300, 1, 51, 52, "")
     X, C0, _ = synth.workload_inputs(w)
     n, k, d = w.n, w.k, w.d
@@ -347,16 +359,20 @@ def test_lloyd_iteration_from_host_buffers_matches_device_call(gpu_lib):
         done.synchronize()
         np.testing.assert_array_equal(lab_h.numpy(), host(ref[1]))
         assert C_out_h.numpy().tobytes() == host(ref[0]).tobytes()
-        assert host(best).tobytes() == host(ref[2]).tobytes()
-        assert float(in_h[0]) == float(ref[3].item())
         np.testing.assert_array_equal(host(counts), host(ref[4]))
+        if slices == 1:
+            assert host(best).tobytes() == host(ref[2]).tobytes()
+            assert float(in_h[0]) == float(ref[3].item())
+        else:
+            total = _same_distances(host(best), host(ref[2]), X, C0, host(ref[1]))
+            assert abs(float(in_h[0]) - float(ref[3].item())) <= DIST_RTOL * total
         assert Xd.cpu().numpy().tobytes() == X.tobytes()
 
 
 def test_back_to_back_host_iterations_overlapping_their_copies(gpu_lib):
     # two alternating device buffer sets with the overlap flag: each call's
     # copies may run beside the previous call's update; every call must still
-    # give the device call's results
+    # give the device call's results (the inertia within the tolerance)
     w = synth.Workload("t", 20000, 200, 64, 200, 1, 53, 54, "")
     X, C0, _ = synth.workload_inputs(w)
     n, k, d = w.n, w.k, w.d
@@ -380,10 +396,11 @@ def test_back_to_back_host_iterations_overlapping_their_copies(gpu_lib):
         done[slot] = gpu_lib.kmeans_lloyd_iter_host(Xh, Ch, Xd[slot], Cd[slot], C_new, labels, best, counts, C_h,
                                                     lab_h, in_h, slices=4, copy_stream=cs, overlap_previous=True)
     torch.cuda.synchronize()
+    total = (sq_norms(X) + sq_norms(C0)[host(ref[1])]).sum()
     for C_h, lab_h, in_h in outs:
         np.testing.assert_array_equal(lab_h.numpy(), host(ref[1]))
         assert C_h.numpy().tobytes() == host(ref[0]).tobytes()
-        assert float(in_h[0]) == float(ref[3].item())
+        assert abs(float(in_h[0]) - float(ref[3].item())) <= DIST_RTOL * total  # four slices: see above
 
 
 def test_lloyd_iteration_from_host_buffers_rejects_bad_arguments(gpu_lib):

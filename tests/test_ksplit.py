@@ -1,0 +1,85 @@
+"""The tensor-core assignment's K split of a partly filled last round.
+
+The assignment runs a persistent schedule of 256 x 256 tiles over the GPU's
+CTA pairs (76 on a GB300).  When its last round is at most half full, those
+tiles run as two K halves on two pairs each; the half that finishes first
+parks its raw accumulator, the other adds it before the argmin, and both add
+their part of ||x||^2 for tiles of the first centroid block.  These shapes
+have more tiles than a GB300 has pairs, and their last rounds split."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import check_assign, check_centroids, sq_norms
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+SPLIT = [
+    # (n, k, d) -> tiles = ceil(n / 256) * ceil(k / 256)
+    (25600, 200, 256),  # 100 tiles in one centroid block: every split tile also reports ||x||^2
+    (5000, 1000, 260),  # 80 tiles; ragged n, k and K halves (4 and 5 k-blocks)
+    (40000, 600, 128),  # 471 tiles: a last round of 15 after six full ones
+]
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _inputs(n, k, d):
+    X, _, _ = synth.planted_blobs(n, d, k, seed=n + k + d)
+    C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=d + 1)])
+    return X, C
+
+
+@pytest.mark.parametrize("shape", SPLIT, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("impl", ["kmeans_assign", "kmeans_assign_3xtf32"])
+def test_split_tiles_match_the_oracle_and_repeat_bit_for_bit(gpu_lib, shape, impl):
+    n, k, d = shape
+    X, C = _inputs(n, k, d)
+    fn = getattr(gpu_lib, impl)
+    Xd, Cd = _dev(X), _dev(C)
+    labels, best, inertia = fn(Xd, Cd)
+    o_l, o_b, o_s, o_in = oracle.assign(X, C)
+    check_assign(X, C, labels.cpu().numpy(), best.cpu().numpy(), o_l, o_b, o_s, what=f"{impl} {shape}")
+    scale = (sq_norms(X) + sq_norms(C)[o_l]).sum()
+    assert abs(float(inertia.item()) - o_in) <= 1e-4 * scale
+    # which half parks is a race; the sum is not
+    labels2, best2, inertia2 = fn(Xd, Cd)
+    assert labels2.cpu().numpy().tobytes() == labels.cpu().numpy().tobytes()
+    assert best2.cpu().numpy().tobytes() == best.cpu().numpy().tobytes()
+    assert float(inertia2.item()) == float(inertia.item())
+
+
+def test_the_split_runs_on_a_gb300(gpu_lib):
+    # the built-in scratch of kmeans_assign_noalloc has no parking area, so
+    # it never splits: on a GB300 the split tiles' sums round differently
+    # (the K halves add at the end), while the labels agree
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the split schedule is sized for 152 SMs")
+    n, k, d = SPLIT[0]
+    X, C = _inputs(n, k, d)
+    Xd, Cd = _dev(X), _dev(C)
+    l_split, b_split, _ = gpu_lib.kmeans_assign(Xd, Cd)
+    l_whole = torch.empty(n, dtype=torch.int64, device="cuda")
+    b_whole = torch.empty(n, dtype=torch.float32, device="cuda")
+    gpu_lib.kmeans_assign_noalloc(Xd, Cd, l_whole, b_whole)
+    assert np.array_equal(l_split.cpu().numpy(), l_whole.cpu().numpy())
+    differ = b_split.cpu().numpy() != b_whole.cpu().numpy()
+    assert differ.any()
+    # 100 tiles over 76 pairs: the last 24 tiles (rows 76 * 256 onwards) split
+    assert not differ[:76 * 256].any()
+
+
+def test_lloyd_iteration_with_split_tiles(gpu_lib):
+    n, k, d = SPLIT[1]
+    X, C = _inputs(n, k, d)
+    C1, labels, best, inertia, counts = gpu_lib.kmeans_lloyd_iter(_dev(X), _dev(C))
+    o_l, o_b, o_s, _ = oracle.assign(X, C)
+    lab = labels.cpu().numpy()
+    check_assign(X, C, lab, best.cpu().numpy(), o_l, o_b, o_s, what="lloyd with split tiles")
+    o_C, o_cnt = oracle.update(X, lab, C)
+    check_centroids(C1.cpu().numpy(), o_C, what="lloyd with split tiles")
+    assert np.array_equal(counts.cpu().numpy().astype(np.int64), o_cnt)
