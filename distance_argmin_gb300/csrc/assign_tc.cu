@@ -46,6 +46,12 @@
 //                accumulator(s) (two warps per lane quarter, 128 columns
 //                each), score = ||c||^2 - 2 x.c, row min / argmin, atomicMin
 //                into the per-sample key
+// The tiles go to the pairs in rounds.  A last round at most half full would
+// leave most pairs idle for a whole tile; its tiles run instead as two halves
+// of the k-blocks on two pairs (work units, see unit_at).  In the epilogue the
+// half that takes the first ticket parks its raw accumulator in the workspace
+// and tags it; the other waits for the tag and adds the parked part to its
+// own before the argmin.  Whole tiles keep an MMA issue loop of their own.
 // Every wait is bounded; a timeout raises a flag in the status word and both
 // CTAs wind down without hanging.
 #include <cuda.h>
