@@ -98,7 +98,9 @@ enum {
 };
 
 /* Bytes of device workspace the operation needs for these sizes (0 when the
- * sizes are invalid).  Linear in n, in k*d and in n/4096; never in n*k. */
+ * sizes are invalid).  Linear in n, in k*d and in n/4096; never in n*k.  The
+ * tensor-core assignment adds a constant 10 MiB (40 parked 256 x 256 float32
+ * tile halves) once the problem has more than 64 tiles of 256 x 256. */
 size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d);
 
 /* Assignment [G][R][S].
