@@ -53,6 +53,20 @@ def test_split_tiles_match_the_oracle_and_repeat_bit_for_bit(gpu_lib, shape, imp
     assert float(inertia2.item()) == float(inertia.item())
 
 
+@pytest.mark.parametrize("shape,impl", [
+    ((25600, 200, 4), "kmeans_assign"),            # one k-block: nothing to split
+    ((20480, 200, 2052), "kmeans_assign_3xtf32"),  # 3xTF32 past its single-accumulator limit: never split
+], ids=["one_kblock", "tf32_separate_accumulators"])
+def test_many_tiles_without_a_split(gpu_lib, shape, impl):
+    n, k, d = shape
+    X, C = _inputs(n, k, d)
+    labels, best, inertia = getattr(gpu_lib, impl)(_dev(X), _dev(C))
+    o_l, o_b, o_s, o_in = oracle.assign(X, C)
+    check_assign(X, C, labels.cpu().numpy(), best.cpu().numpy(), o_l, o_b, o_s, what=f"{impl} {shape}")
+    scale = (sq_norms(X) + sq_norms(C)[o_l]).sum()
+    assert abs(float(inertia.item()) - o_in) <= 1e-4 * scale
+
+
 def test_the_split_runs_on_a_gb300(gpu_lib):
     # the built-in scratch of kmeans_assign_noalloc has no parking area, so
     # it never splits: on a GB300 the split tiles' sums round differently
