@@ -62,3 +62,20 @@ def test_fit_honours_max_iter_and_rejects_bad_arguments(gpu_lib):
     assert lib.kmeans_fit(*args(0, 0, 0.0)) == gpu_lib.KMEANS_ERR_INVALID_ARG
     assert lib.kmeans_fit(*args(0, 10, -1.0)) == gpu_lib.KMEANS_ERR_INVALID_ARG
     assert lib.kmeans_fit(*args(0, 10, float("nan"))) == gpu_lib.KMEANS_ERR_INVALID_ARG
+
+
+def test_fit_on_a_shape_whose_assignment_splits_its_last_round(gpu_lib):
+    # 20480 samples x 256 centroids: 80 tiles of 256 x 256 over a GB300's 76
+    # CTA pairs, so every assignment of the fit runs its last round as K
+    # halves.  Starting from the planted centers moved by N(0, 0.3^2) keeps
+    # every decision on the way clear of a tie (smallest margin 0.27 of
+    # ||x||^2 + ||c||^2), so both fits take the same path.
+    X, centers, _ = synth.planted_blobs(20480, 64, 256, seed=91)
+    C0 = np.ascontiguousarray(centers + synth.gaussian(centers.shape, seed=93) * np.float32(0.3), dtype=np.float32)
+    C, labels, best, counts, hist, n_iter = gpu_lib.kmeans_fit(_dev(X), C=_dev(C0), init="given", max_iter=50,
+                                                                tol=0.0)
+    o_C, o_labels, _, o_hist, o_n = oracle.fit(X, C0, max_iter=50, tol=0.0)
+    assert n_iter == o_n
+    np.testing.assert_array_equal(labels.cpu().numpy(), o_labels)
+    check_centroids(C.cpu().numpy(), o_C, what="fit with split assignment rounds")
+    np.testing.assert_allclose(hist, o_hist, rtol=1e-4)
