@@ -49,7 +49,11 @@
  *    the workspace, which each call clears when it starts; read it with
  *    kmeans_device_status().
  *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
- *    default stream).
+ *    default stream).  A call may be captured into a CUDA graph and
+ *    replayed (each replay redoes the whole call), except kmeans_fit, which
+ *    synchronises, and the first kmeans_assign_noalloc call on a device.
+ *    Make one ordinary call on the device before capturing, so that the
+ *    one-time per-device set-up has run.
  */
 #ifndef KMEANS_GB300_H
 #define KMEANS_GB300_H
