@@ -154,6 +154,7 @@ struct TcParams {
     unsigned long long *keys;
     uint32_t *status;
     int test_starve;  // test hook: the producer issues no loads, so the pipeline waits run out
+    int test_hold_tag;  // test hook: K-split halves park but never tag, so the other halves' waits run out
     FusedUpdate fu;   // the update fused into the epilogue (kmeans_lloyd_iter_fused), else all null
     // K split of the last round: units [0, num_full) are whole tiles; unit
     // num_full + 2 s + h is half h of tile num_full + s (h = 0: k-blocks
@@ -488,7 +489,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                         if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(F::T_EMPTY + buf), 0));
                         __threadfence();
                         __syncwarp();
-                        if (lane == 0) st_release_gpu(sync + 1, p.epoch);
+                        if (lane == 0 && !p.test_hold_tag) st_release_gpu(sync + 1, p.epoch);
                         continue;
                     }
                     if (!flag_wait_warp(sync + 1, p.epoch, p.status)) {
@@ -883,6 +884,11 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     // status word reports KMEANS_ERR_DEVICE_TIMEOUT and the outputs hold -1.
     const char *starve = getenv("KMEANS_GB300_TEST_STARVE_PIPELINE");
     p.test_starve = (starve != nullptr && starve[0] == '1') ? 1 : 0;
+    // Test-only, likewise: the first K half of a split tile parks its
+    // accumulator but never tags it, so the second half's bounded wait runs
+    // out and the call reports KMEANS_ERR_DEVICE_TIMEOUT.
+    const char *hold = getenv("KMEANS_GB300_TEST_HOLD_KSPLIT_TAG");
+    p.test_hold_tag = (hold != nullptr && hold[0] == '1') ? 1 : 0;
     const int max_pairs = resident_pairs();
     const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
     const int grid = 2 * (pairs > 0 ? pairs : 1);

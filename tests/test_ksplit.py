@@ -97,3 +97,25 @@ def test_lloyd_iteration_with_split_tiles(gpu_lib):
     o_C, o_cnt = oracle.update(X, lab, C)
     check_centroids(C1.cpu().numpy(), o_C, what="lloyd with split tiles")
     assert np.array_equal(counts.cpu().numpy().astype(np.int64), o_cnt)
+
+
+def test_a_withheld_ready_tag_times_out_and_reports(gpu_lib, monkeypatch):
+    # Fault injection on the host side: with the test switch set, the first
+    # K half of every split tile parks its accumulator but never tags it.
+    # Every second half's bounded wait (2 s) runs out, the kernel winds down,
+    # the status word says so, and the next call on the same workspace is
+    # correct again.  No trap, no fault, no unbounded spin.
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the split schedule is sized for 152 SMs")
+    n, k, d = SPLIT[0]
+    X, C = _inputs(n, k, d)
+    Xd, Cd = _dev(X), _dev(C)
+    ws = gpu_lib.workspace(gpu_lib.OP_ASSIGN, n, k, d)
+    monkeypatch.setenv("KMEANS_GB300_TEST_HOLD_KSPLIT_TAG", "1")
+    gpu_lib.kmeans_assign(Xd, Cd, ws=ws)
+    assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_ERR_DEVICE_TIMEOUT
+    monkeypatch.delenv("KMEANS_GB300_TEST_HOLD_KSPLIT_TAG")
+    labels, best, _ = gpu_lib.kmeans_assign(Xd, Cd, ws=ws)
+    assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_OK
+    o_l, o_b, o_s, _ = oracle.assign(X, C)
+    check_assign(X, C, labels.cpu().numpy(), best.cpu().numpy(), o_l, o_b, o_s, what="after a withheld tag")
