@@ -442,7 +442,9 @@ def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_o
     ``copy_stream`` and assigns each slice on ``stream`` as soon as it has
     landed; the update follows, and C_new, the labels and the inertia come
     back to ``C_out_h``, ``labels_h`` and ``inertia_h`` (one float64).  The
-    device outputs equal kmeans_lloyd_iter's bit for bit.  Returns an event
+    device outputs are kmeans_lloyd_iter's: bit for bit with one slice; with
+    more, the distances and inertia within the distance tolerance (each
+    slice's pass may split other tiles along K).  Returns an event
     recorded on ``stream`` after the last copy.  ``overlap_previous``: the
     copies may overlap earlier work on ``stream`` (the caller guarantees that
     ``Xd`` and ``Cd`` are not in use, e.g. by alternating two sets).

@@ -119,3 +119,38 @@ def test_a_withheld_ready_tag_times_out_and_reports(gpu_lib, monkeypatch):
     assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_OK
     o_l, o_b, o_s, _ = oracle.assign(X, C)
     check_assign(X, C, labels.cpu().numpy(), best.cpu().numpy(), o_l, o_b, o_s, what="after a withheld tag")
+
+
+def test_host_iteration_whose_slices_each_split(gpu_lib):
+    # kmeans_lloyd_iter_host with two slices launches the tensor-core pass
+    # twice in one call, and on a GB300 each launch splits its last round
+    # (320 tiles each: a last round of 16).  The second launch reuses the
+    # tickets and tags without a prologue in between: its distinct epoch and
+    # the reset by each first launch's second halves must keep it correct.
+    n, k, d = 40960, 1024, 128
+    X, C = _inputs(n, k, d)
+    ref = gpu_lib.kmeans_lloyd_iter(_dev(X), _dev(C))
+    Xh = torch.from_numpy(X).pin_memory()
+    Ch = torch.from_numpy(C).pin_memory()
+    Xd, Cd = torch.empty_like(Xh, device="cuda"), torch.empty_like(Ch, device="cuda")
+    C_new = torch.empty_like(Cd)
+    labels = torch.empty(n, dtype=torch.int64, device="cuda")
+    best = torch.empty(n, device="cuda")
+    counts = torch.empty(k, dtype=torch.int32, device="cuda")
+    C_out_h = torch.empty((k, d), dtype=torch.float32).pin_memory()
+    lab_h = torch.empty(n, dtype=torch.int64).pin_memory()
+    in_h = torch.empty(1, dtype=torch.float64).pin_memory()
+    ws = gpu_lib.workspace(gpu_lib.OP_LLOYD, n, k, d)
+    for _ in range(2):  # twice on one workspace: the tickets left by the first call are clean
+        done = gpu_lib.kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best, counts, C_out_h, lab_h, in_h,
+                                              slices=2, ws=ws)
+        done.synchronize()
+        assert gpu_lib.kmeans_device_status(ws) == gpu_lib.KMEANS_OK
+        lab = labels.cpu().numpy()
+        np.testing.assert_array_equal(lab, ref[1].cpu().numpy())
+        assert C_new.cpu().numpy().tobytes() == ref[0].cpu().numpy().tobytes()
+        scale = sq_norms(X) + sq_norms(C)[lab]
+        assert (np.abs(best.cpu().numpy().astype(np.float64) - ref[2].cpu().numpy()) <= 1e-4 * scale).all()
+    rows = np.sort(np.random.default_rng(5).choice(n, 2048, replace=False))
+    o_l, o_b, o_s, _ = oracle.assign(X[rows], C)
+    check_assign(X[rows], C, lab, best.cpu().numpy(), o_l, o_b, o_s, rows=rows, what="two splitting slices")
