@@ -195,6 +195,14 @@ def test_status_ok_after_assign(gpu_lib):
 
 
 # ------------------------------------------------------------- k-means++
+def _record_margins(record_property, margins):
+    # how close each D^2 draw came to a running-sum boundary (fraction of
+    # the total): the closer, the more exactly the distances must agree
+    record_property("draws", int(len(margins)))
+    record_property("min_margin", float(margins.min()))
+    record_property("draws_below_1e-7", int((margins < 1e-7).sum()))
+
+
 @pytest.mark.parametrize("case", [(3000, 64, 40, 0, 42), (3000, 64, 40, 1, 7), (500, 33, 60, 3, 123),
                                   (2048, 128, 32, 8, 2024), (1000, 4, 1000, 2, 5),
                                   # several 256-feature steps (the register prefetch), ragged last step
@@ -204,11 +212,12 @@ def test_status_ok_after_assign(gpu_lib):
                                   # odd d: scalar loads, several steps
                                   (900, 1027, 8, 2, 13)],
                          ids=lambda c: "n%d_d%d_k%d_T%d_s%d" % c)
-def test_kmeanspp_indices_match_oracle(gpu_lib, case):
+def test_kmeanspp_indices_match_oracle(gpu_lib, case, record_property):
     n, d, k, T, seed = case
     X, _, _ = synth.planted_blobs(n, d, max(1, k // 2), seed=n + d)
     idx, centers = gpu_lib.kmeanspp_init(dev_tensor(X), k, seed, n_trials=T)
     o_idx, margins, _ = oracle.kmeanspp(X, k, seed, n_trials=T)
+    _record_margins(record_property, margins)
     got = host(idx)
     assert np.array_equal(got, o_idx), f"first mismatch at {np.argmax(got != o_idx)}"
     assert host(centers).tobytes() == np.ascontiguousarray(X[o_idx]).tobytes()
@@ -293,7 +302,7 @@ def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d, impl):
 
 
 @pytest.mark.slow
-def test_kmeanspp_workload_prefix(gpu_lib):
+def test_kmeanspp_workload_prefix(gpu_lib, record_property):
     w = synth.KMEANSPP
     X, _, _ = synth.planted_blobs(w.n, w.d, w.blobs, w.data_seed)
     T = oracle.n_trials_for(w.k)
@@ -301,6 +310,7 @@ def test_kmeanspp_workload_prefix(gpu_lib):
     got = host(idx)
     assert len(np.unique(got)) == w.k  # D^2 sampling never repeats a chosen sample
     o_idx, margins, _ = oracle.kmeanspp(X, 12, w.init_seed, n_trials=T)
+    _record_margins(record_property, margins)
     assert np.array_equal(got[:12], o_idx), f"first mismatch at {np.argmax(got[:12] != o_idx)}"
 
 
