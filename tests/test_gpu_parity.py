@@ -3,6 +3,8 @@ the same seeded inputs.  Small shapes are compared on every row; full-size
 workloads on a seeded sample of rows (assignment) and on every row (update,
 with the GPU's own labels so near-tie flips do not cascade)."""
 import ctypes
+import hashlib
+import os
 
 import numpy as np
 import pytest
@@ -312,6 +314,43 @@ def test_kmeanspp_workload_prefix(gpu_lib, record_property):
     o_idx, margins, _ = oracle.kmeanspp(X, 12, w.init_seed, n_trials=T)
     _record_margins(record_property, margins)
     assert np.array_equal(got[:12], o_idx), f"first mismatch at {np.argmax(got[:12] != o_idx)}"
+
+
+def _read_kmeanspp_golden():
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "kmeanspp_workload_indices.txt")
+    meta, idx = {}, []
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#"):
+                for tok in line[1:].split():
+                    if "=" in tok:
+                        key, val = tok.split("=", 1)
+                        meta[key] = val
+            elif line.strip():
+                idx.append(int(line))
+    return meta, np.array(idx, dtype=np.int64)
+
+
+@pytest.mark.slow
+def test_kmeanspp_workload_every_center(gpu_lib, record_property):
+    # All 1024 centers of the full seeding against the oracle's, written ahead
+    # of time by tests/golden/make_kmeanspp_workload.py (the oracle needs
+    # about 8 minutes for them).  The stored SHA-256 of the samples makes sure
+    # the input generator gave this machine the bytes the oracle saw.
+    w = synth.KMEANSPP
+    meta, o_idx = _read_kmeanspp_golden()
+    assert (int(meta["n"]), int(meta["d"]), int(meta["k"]), int(meta["seed"])) == (w.n, w.d, w.k, w.init_seed)
+    X, _, _ = synth.planted_blobs(w.n, w.d, w.blobs, w.data_seed)
+    assert hashlib.sha256(X.tobytes()).hexdigest() == meta["x_sha256"], \
+        f"the input generator gave different samples here than on the {meta.get('machine')} host the oracle ran on"
+    T = int(meta["trials"])
+    assert T == oracle.n_trials_for(w.k) and len(o_idx) == w.k
+    idx, centers = gpu_lib.kmeanspp_init(dev_tensor(X), w.k, w.init_seed, n_trials=T)
+    got = host(idx)
+    record_property("draws", int(meta["draws"]))
+    record_property("min_margin", float(meta["smallest_margin"]))
+    assert np.array_equal(got, o_idx), f"first mismatch at center {np.argmax(got != o_idx)}"
+    assert host(centers).tobytes() == np.ascontiguousarray(X[o_idx]).tobytes()
 
 
 def test_starved_pipeline_times_out_and_reports(gpu_lib, monkeypatch):
