@@ -76,15 +76,13 @@ int run_assign(AssignPath path, const float *X, const float *C, int64_t n, int64
 }
 
 // kmeans_fit's workspace: the Lloyd / k-means++ scratch at the base (so the
-// status word sits where kmeans_device_status looks), then the second
-// centroid buffer of the ping-pong, the seeding's indices, the inertia and
-// the relocation's scratch.
+// status word, and beside it the fit's inertia and empty count, sit in the
+// header where kmeans_device_status looks), then the second centroid buffer
+// of the ping-pong, the seeding's indices and the relocation's scratch.
 struct FitLayout {
     int64_t shared;       // max(Lloyd, k-means++) scratch
     int64_t off_calt;     // k x d f32
     int64_t off_indices;  // k x i64
-    int64_t off_inertia;  // f64
-    int64_t off_nempty;   // u32 number of empty clusters after an update
     RelocLayout reloc;    // counts and empty list, 2 x k x i32
     int64_t bytes;
 };
@@ -99,8 +97,6 @@ FitLayout fit_layout(int64_t n, int64_t k, int64_t d) {
     int64_t o = align_up(F.shared, 1024);
     F.off_calt = o; o = align_up(o + k * d * 4, 1024);
     F.off_indices = o; o = align_up(o + k * 8, 1024);
-    F.off_inertia = o;
-    F.off_nempty = o + 8; o = align_up(o + 16, 1024);
     F.reloc = reloc_layout(k, o);
     F.bytes = align_up(F.reloc.end, 1024);
     return F;
@@ -347,7 +343,8 @@ int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int3
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *w = static_cast<uint8_t *>(ws);
     float *calt = reinterpret_cast<float *>(w + F.off_calt);
-    double *inertia_d = reinterpret_cast<double *>(w + F.off_inertia);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
+    double *inertia_d = &hdr->fit_inertia;
     *n_iter = 0;
     cudaError_t e = cudaSuccess;
     if (init == KMEANS_INIT_KMEANSPP) {
@@ -363,7 +360,7 @@ int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int3
     // the relocation itself rewrites only after they have been read
     int32_t *cnt = counts;
     if (relocate && !cnt) cnt = reinterpret_cast<int32_t *>(w + F.reloc.off_counts);
-    uint32_t *nempty_d = reinterpret_cast<uint32_t *>(w + F.off_nempty);
+    uint32_t *nempty_d = &hdr->fit_nempty;
     float *cur = C, *nxt = calt;
     double prev = 0.0;
     int it = 0;
@@ -372,13 +369,15 @@ int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int3
         if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, A, w, s);
         if (e == cudaSuccess) e = lloyd_finish(X, cur, nxt, labels, best_dist, inertia_d, cnt, n, k, d, A, w, s);
         if (e == cudaSuccess && relocate) e = launch_count_empty(cnt, k, nempty_d, s);
-        double inertia = 0.0;
-        uint32_t flags = 0, nempty = 0;
-        if (e == cudaSuccess) e = cudaMemcpyAsync(&inertia, inertia_d, sizeof(double), cudaMemcpyDeviceToHost, s);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(&flags, w, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
-        if (e == cudaSuccess && relocate) e = cudaMemcpyAsync(&nempty, nempty_d, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+        // status word, inertia and empty count in one read (each small
+        // pageable copy costs a round trip while the GPU waits)
+        WsHeader rec{};
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&rec, w, kFitRecordBytes, cudaMemcpyDeviceToHost, s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) break;
+        const double inertia = rec.fit_inertia;
+        const uint32_t flags = rec.status;
+        const uint32_t nempty = relocate ? rec.fit_nempty : 0u;
         ++it;
         *n_iter = it;
         if (flags & kFlagTimeout) return KMEANS_ERR_DEVICE_TIMEOUT;

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <cstddef>
 
 #include <atomic>
 #include <mutex>
@@ -91,8 +92,15 @@ enum : uint32_t {
 struct WsHeader {
     uint32_t status;          // device status flags
     uint32_t done_blocks;     // "last block" counter of the inertia reduction
-    uint32_t pad[62];
+    double fit_inertia;       // kmeans_fit: the last iteration's inertia
+    uint32_t fit_nempty;      // kmeans_fit: clusters left empty by the last update
+    uint32_t pad[59];
 };
+// kmeans_fit reads the status word, the inertia and the empty count back in
+// one copy of the header's first bytes.
+constexpr size_t kFitRecordBytes = 20;
+static_assert(offsetof(WsHeader, fit_inertia) == 8 && offsetof(WsHeader, fit_nempty) + 4 == kFitRecordBytes,
+              "the fit's record is the header's first bytes");
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 // Wall-clock limit of one pipeline wait.  A wait that legitimately takes this
