@@ -265,6 +265,27 @@ def test_lloyd10_workload_ten_iterations(gpu_lib):
 
 
 @pytest.mark.slow
+def test_lloyd10_first_iteration_every_row(gpu_lib, record_property):
+    # the assignment of all 65536 samples against the 1024 initial centroids,
+    # row by row against the oracle (2.7e11 float64 multiply-adds: seconds on
+    # a many-core host), then the update on the GPU's labels
+    w = synth.WORKLOADS["lloyd10"]
+    X, C0, _ = synth.workload_inputs(w)
+    C1, labels, best, inertia, counts = gpu_lib.kmeans_lloyd_iter(dev_tensor(X), dev_tensor(C0))
+    lab = host(labels)
+    o_l, o_b, o_s, o_in = oracle.assign(X, C0)
+    flips, worst = check_assign(X, C0, lab, host(best), o_l, o_b, o_s, what="lloyd10 every row")
+    record_property("near_tie_flips", flips)
+    record_property("worst_rel_distance_error", worst)
+    print(f"lloyd10 iteration 1, all {w.n} rows: worst relative distance error {worst:.3e}, near-tie flips {flips}")
+    scale = (sq_norms(X) + sq_norms(C0)[o_l]).sum()
+    assert abs(float(inertia.item()) - o_in) <= 1e-4 * scale
+    o_C1, o_cnt = oracle.update(X, lab, C0)
+    check_centroids(host(C1), o_C1, what="lloyd10 iteration 1 update")
+    assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+
+
+@pytest.mark.slow
 @pytest.mark.parametrize("name", ["sample_heavy", "centroid_heavy", "feature_heavy"])
 def test_large_workload_one_iteration(gpu_lib, name):
     w = synth.WORKLOADS[name]

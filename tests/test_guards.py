@@ -62,14 +62,21 @@ def _all_intact(*bufs):
     return all(b.intact() for b in bufs)
 
 
+def _clean(km, *workspaces):
+    # no bounded device wait ran out and no label was out of range
+    return all(km.kmeans_device_status(w) == km.KMEANS_OK for w in workspaces)
+
+
 @pytest.mark.parametrize("name,op", [("kmeans_assign", "OP_ASSIGN"), ("kmeans_assign_3xtf32", "OP_ASSIGN_3XTF32"),
                                      ("kmeans_assign_ffma", "OP_ASSIGN_FFMA")])
 def test_assignment_stays_inside_its_buffers(gpu_lib, name, op):
     X, C = _inputs()
     fn = getattr(gpu_lib, name)
-    ref = fn(X, C)
+    wsr = gpu_lib.workspace(getattr(gpu_lib, op), N, K, D)
+    ref = fn(X, C, ws=wsr)
     ws, out = _ws(gpu_lib, getattr(gpu_lib, op)), _outputs()
     got = fn(X, C, labels=out["labels"].t, best_dist=out["best"].t, inertia=out["inertia"].t, ws=ws.t)
+    assert _clean(gpu_lib, wsr, ws.t)
     assert _all_intact(ws, out["labels"], out["best"], out["inertia"])
     assert not torch.isnan(out["best"].t).any() and not torch.isnan(out["inertia"].t).any()
     for a, b in zip(got, ref):
@@ -78,11 +85,15 @@ def test_assignment_stays_inside_its_buffers(gpu_lib, name, op):
 
 def test_update_stays_inside_its_buffers(gpu_lib):
     X, C = _inputs()
-    labels, _, _ = gpu_lib.kmeans_assign(X, C)
+    wsa = gpu_lib.workspace(gpu_lib.OP_ASSIGN, N, K, D)
+    labels, _, _ = gpu_lib.kmeans_assign(X, C, ws=wsa)
+    assert _clean(gpu_lib, wsa)
     labels[labels == 3] = 4  # cluster 3 empty: its row comes from C_old
-    ref = gpu_lib.kmeans_update(X, labels, C)
+    wsr = gpu_lib.workspace(gpu_lib.OP_UPDATE, N, K, D)
+    ref = gpu_lib.kmeans_update(X, labels, C, ws=wsr)
     ws, out = _ws(gpu_lib, gpu_lib.OP_UPDATE), _outputs()
     got = gpu_lib.kmeans_update(X, labels, C, C_new=out["C_new"].t, counts=out["counts"].t, ws=ws.t)
+    assert _clean(gpu_lib, wsr, ws.t)
     assert _all_intact(ws, out["C_new"], out["counts"])
     assert not torch.isnan(out["C_new"].t).any() and int(out["counts"].t.sum()) == N
     for a, b in zip(got, ref):
@@ -93,10 +104,12 @@ def test_update_stays_inside_its_buffers(gpu_lib):
 def test_lloyd_iteration_stays_inside_its_buffers(gpu_lib, name, op):
     X, C = _inputs()
     fn = getattr(gpu_lib, name)
-    ref = fn(X, C)
+    wsr = gpu_lib.workspace(getattr(gpu_lib, op), N, K, D)
+    ref = fn(X, C, ws=wsr)
     ws, out = _ws(gpu_lib, getattr(gpu_lib, op)), _outputs()
     got = fn(X, C, C_new=out["C_new"].t, labels=out["labels"].t, best_dist=out["best"].t,
              inertia=out["inertia"].t, counts=out["counts"].t, ws=ws.t)
+    assert _clean(gpu_lib, wsr, ws.t)
     assert _all_intact(ws, *out.values())
     assert not torch.isnan(out["C_new"].t).any() and not torch.isnan(out["best"].t).any()
     assert int(out["counts"].t.sum()) == N
@@ -110,23 +123,29 @@ def test_lloyd_iteration_stays_inside_its_buffers(gpu_lib, name, op):
 
 def test_kmeanspp_stays_inside_its_buffers(gpu_lib):
     X, _ = _inputs()
-    ref_idx, ref_cen = gpu_lib.kmeanspp_init(X, K, 17)
-    ws = Guarded((gpu_lib.kmeans_workspace_bytes(gpu_lib.OP_KMEANSPP, N, K, D),), torch.uint8, 0xFF)
+    wsr = gpu_lib.workspace(gpu_lib.OP_KMEANSPP, N, K, D)
+    ref_idx, ref_cen = gpu_lib.kmeanspp_init(X, K, 17, ws=wsr)
+    ws = _ws(gpu_lib, gpu_lib.OP_KMEANSPP)
     idx, cen = Guarded((K,), torch.int64, -7), Guarded((K, D), torch.float32, float("nan"))
     gpu_lib.kmeanspp_init(X, K, 17, centers=cen.t, indices=idx.t, ws=ws.t)
+    assert _clean(gpu_lib, wsr, ws.t)
     assert _all_intact(ws, idx, cen)
     assert _same(idx.t, ref_idx) and _same(cen.t, ref_cen)
 
 
 def test_relocation_stays_inside_its_buffers(gpu_lib):
     X, C = _inputs()
-    labels, best, _ = gpu_lib.kmeans_assign(X, C)
+    wsa = gpu_lib.workspace(gpu_lib.OP_ASSIGN, N, K, D)
+    labels, best, _ = gpu_lib.kmeans_assign(X, C, ws=wsa)
+    assert _clean(gpu_lib, wsa)
     labels[labels % 2 == 1] = 0  # every odd cluster empty
-    ref = gpu_lib.kmeans_relocate_empty(labels.clone(), best, K)
+    wsr = gpu_lib.workspace(gpu_lib.OP_RELOCATE, N, K, 1)
+    ref = gpu_lib.kmeans_relocate_empty(labels.clone(), best, K, ws=wsr)
     ws = Guarded((gpu_lib.kmeans_workspace_bytes(gpu_lib.OP_RELOCATE, N, K, 1),), torch.uint8, 0xFF)
     lab = Guarded((N,), torch.int64, 0)
     lab.t.copy_(labels)
     gpu_lib.kmeans_relocate_empty(lab.t, best, K, ws=ws.t)
+    assert _clean(gpu_lib, wsr, ws.t)
     assert _all_intact(ws, lab)
     assert _same(lab.t, ref)
 
