@@ -14,8 +14,9 @@
 //            potentials sum_i min(D^2_i, dist_ti)
 //
 // Distances: float32 differences, squared and summed in runs of 8 features,
-// runs added with compensation, lanes and slices combined in float64.  Running
-// sums and potentials are float64.  Every reduction has a fixed order.
+// a lane's runs added in float32, lanes and slices combined in double-float,
+// then float64.  Running sums and potentials are float64.  Every reduction
+// has a fixed order.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -156,26 +157,11 @@ __global__ void __launch_bounds__(32)
 namespace kd {
 constexpr int KT = kKppGroupTrials;  // trial candidates per pass over X
 constexpr int ROWS = 2;              // samples per warp at a time
-constexpr int MIN_BLOCKS = 1;        // one block per SM: 128 KiB of candidates, 16 warps of up to 128 registers
-constexpr int WARPS = 16;
+constexpr int MIN_BLOCKS = 1;        // one block per SM: 128 KiB of candidates, 24 warps of up to 85 registers
+constexpr int WARPS = 24;
 constexpr int THREADS = WARPS * 32;
 constexpr int GROUP = WARPS * ROWS;
 }  // namespace kd
-
-// Kahan's compensated sum (y = v - c, t = s + y, c = (t - s) - y, s = t) on two
-// independent sums at once (row 0 in .x, row 1 in .y) with the packed
-// two-float instructions.  cm holds the negated compensation, so no negation
-// is needed: t - s is fma(s, -1, t) and the new -c is fma(t - s, -1, y).  Each
-// step rounds exactly as the scalar form does, so each half carries the bits
-// of a scalar Kahan sum.
-__device__ __forceinline__ void kahan2(float2 &s, float2 &cm, float2 v) {
-    const float2 m1 = make_float2(-1.f, -1.f);
-    const float2 y = __fadd2_rn(v, cm);      // v - c
-    const float2 t = __fadd2_rn(s, y);
-    const float2 ts = __ffma2_rn(s, m1, t);  // t - s
-    cm = __ffma2_rn(ts, m1, y);              // y - (t - s) = -c
-    s = t;
-}
 
 // Error-free sum: s + e == a + b exactly (Knuth's TwoSum).
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
@@ -240,8 +226,9 @@ __device__ __forceinline__ void load4x2(const float *__restrict__ p, int avail, 
 // The block stages its slice of the candidates (negated) in shared memory once
 // and then streams its share of the samples, each sample read exactly once.
 // Differences and squares use the packed two-float instructions; each run of
-// a lane's 8 features of a step is added to a compensated per-lane sum, the
-// two rows' sums paired in one packed compensated add.
+// a lane's 8 features of a step is added to a per-lane sum, the two rows'
+// sums paired in one packed add.  A lane adds at most W / 256 runs (16 for a
+// 4096-feature slice); lanes and slices are combined in double-float.
 template <bool VEC>
 __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand, int T,
@@ -266,14 +253,15 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x) {
         const int64_t r0 = g * kd::GROUP + warp * kd::ROWS;
         static_assert(kd::ROWS == 2, "the two rows' sums are paired in float2");
-        float2 s2[kd::KT], cm2[kd::KT];  // .x row 0, .y row 1; cm2 = -(compensation)
+        float2 s2[kd::KT];  // .x row 0, .y row 1
 #pragma unroll
-        for (int t = 0; t < kd::KT; ++t) s2[t] = cm2[t] = make_float2(0.f, 0.f);
+        for (int t = 0; t < kd::KT; ++t) s2[t] = make_float2(0.f, 0.f);
         // a lane owns features f .. f+3 and f+128 .. f+131 of each 256-feature
         // step, so every 16-byte load of the warp (global and shared) covers
         // 512 contiguous bytes.  The next step's rows are loaded while this
-        // step is computed (xn): one block of 16 warps per SM leaves each
-        // thread the registers for it, where three blocks of 8 warps spilled.
+        // step is computed (xn).  One block of 24 warps per SM fits it in 85
+        // registers a thread; more resident warps hide more of the loads (16,
+        // 20, 24 and 28 warps measured 397, 375, 363 and 386 us a pass).
         float2 x[kd::ROWS][4], xn[kd::ROWS][4];
 #pragma unroll
         for (int r = 0; r < kd::ROWS; ++r) {
@@ -314,7 +302,7 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
                     }
                     rs[r] = run.x + run.y;
                 }
-                kahan2(s2[t], cm2[t], make_float2(rs[0], rs[1]));
+                s2[t] = __fadd2_rn(s2[t], make_float2(rs[0], rs[1]));
             }
         }
         // lanes -> one partial per (row, trial), as double-float values in
@@ -332,7 +320,7 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
 #pragma unroll
             for (int t = 0; t < kd::KT; ++t) {
                 hi[r * kd::KT + t] = r == 0 ? s2[t].x : s2[t].y;
-                lo[r * kd::KT + t] = r == 0 ? cm2[t].x : cm2[t].y;
+                lo[r * kd::KT + t] = 0.f;
             }
         reduce_scatter_level<NS, NS / 2>(hi, lo, lane, 16);
         reduce_scatter_level<NS, NS / 4>(hi, lo, lane, 8);

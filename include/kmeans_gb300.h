@@ -258,8 +258,9 @@ int kmeans_relocate_empty(int64_t *labels, const float *best_dist, int64_t n, in
  * takes the first sample whose running sum of D^2 exceeds uniform * sum(D^2)
  * (the last sample if none does); the trial with the lowest potential
  * sum_i min(D^2_i, ||x_i - cand||^2) wins (lowest trial on ties).
- * Distances are float32 differences squared with compensated summation;
- * running sums and potentials are float64. */
+ * Distances are float32 differences, squared and summed in float32 over
+ * runs of at most 8 x 16 features per thread, the runs combined in
+ * double-float; running sums and potentials are float64. */
 int kmeanspp_init(const float *X, int64_t n, int64_t d, int64_t k, int n_trials,
                   uint64_t seed, float *centers, int64_t *indices,
                   void *ws, size_t ws_bytes, void *stream);
