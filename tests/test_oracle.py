@@ -444,3 +444,156 @@ def test_blob_generator_statistics_and_determinism():
     assert abs(noise.std() - 0.5) < 0.01
     assert abs(centers.std() - 1.0) < 0.05
     assert (blob == np.arange(4096) % 16).all()
+
+
+# --------------------------------------------------------------------------
+# k-means++: the greedy choice among trials and the draw numbering
+# ("004 — tile sizes, a Cython Lloyd step, and k-means++", section
+# "k-means++": each new center is the best of 2 + log(n_clusters) D^2-drawn
+# candidates, the best being the one that leaves the smallest potential)
+# --------------------------------------------------------------------------
+def _d2_pick(D2, u):
+    """Plain loop: the first sample whose running sum of D^2 exceeds
+    u * sum(D^2); the last sample when none does."""
+    total = 0.0
+    for v in D2:
+        total += v
+    target = u * total
+    run = 0.0
+    for i, v in enumerate(D2):
+        run += v
+        if run > target:
+            return i
+    return len(D2) - 1
+
+
+def _kmeanspp_loops(X, k, seed, T, rule="lowest", numbering="paper"):
+    """Greedy k-means++ restated with plain Python loops, for tiny inputs of
+    small integers (every distance, sum and potential is then exact in
+    binary64).  ``rule`` and ``numbering`` select deliberately wrong variants,
+    so a test can show that the oracle's answers tell them apart."""
+    n = len(X)
+
+    def sq(a, b):
+        return float(sum((float(p) - float(q)) ** 2 for p, q in zip(a, b)))
+
+    idx = [min(int(math.floor(oracle.uniform(seed, 0) * n)), n - 1)]
+    D2 = [sq(X[i], X[idx[0]]) for i in range(n)]
+    for c in range(1, k):
+        cands = []
+        for t in range(T):
+            draw = 1 + (c - 1) * T + t if numbering == "paper" else c * T + t
+            cands.append(_d2_pick(D2, oracle.uniform(seed, draw)))
+        pots = [sum(min(D2[i], sq(X[i], X[j])) for i in range(n)) for j in cands]
+        if rule == "lowest":          # smallest potential, lowest trial on ties
+            bt = min(range(T), key=lambda t: (pots[t], t))
+        elif rule == "highest":
+            bt = max(range(T), key=lambda t: (pots[t], -t))
+        elif rule == "first":
+            bt = 0
+        elif rule == "last":
+            bt = T - 1
+        else:                         # smallest potential, lowest index on ties
+            bt = min(range(T), key=lambda t: (pots[t], cands[t]))
+        best = cands[bt]
+        idx.append(best)
+        D2 = [min(D2[i], sq(X[i], X[best])) for i in range(n)]
+    return idx
+
+
+def test_kmeanspp_hand_worked_best_trial_is_the_middle_one():
+    # 1-D points 0, 2, 5, 9, 14; k = 2 with T = 3 trials.  With seed 103:
+    #   u0 = 0.0252 -> first center floor(0.0252 * 5) = sample 0 (x = 0);
+    #   D^2 = 0, 4, 25, 81, 196 (total 306), running sums 0, 4, 29, 110, 306;
+    #   trial 0: u = 0.0592, target 18.1 -> sample 2 (x = 5);
+    #   trial 1: u = 0.2165, target 66.3 -> sample 3 (x = 9);
+    #   trial 2: u = 0.8702, target 266.3 -> sample 4 (x = 14).
+    # Potentials sum_i min(D^2_i, (x_i - x_cand)^2):
+    #   x = 5:  0 + 4 + 0 + 16 + 81 = 101
+    #   x = 9:  0 + 4 + 16 + 0 + 25 = 45   <- smallest: the middle trial
+    #   x = 14: 0 + 4 + 25 + 25 + 0 = 54
+    # A first-trial rule gives sample 2, a last-trial rule sample 4 and a
+    # largest-potential rule sample 2.  Seed 594 draws the same three
+    # candidates in the reverse order (4, 3, 2) and must give sample 3 too.
+    X = np.array([[0.0], [2.0], [5.0], [9.0], [14.0]], np.float32)
+    for seed, us in ((103, (0.0252, 0.0592, 0.2165, 0.8702)), (594, (0.0328, 0.8765, 0.2855, 0.0236))):
+        for draw, want in enumerate(us):
+            assert abs(oracle.uniform(seed, draw) - want) < 5e-5
+        idx, _, pots = oracle.kmeanspp(X, 2, seed, n_trials=3)
+        assert idx.tolist() == [0, 3]
+        assert pots.tolist() == [306.0, 45.0]
+
+
+@pytest.mark.parametrize("seed,want", [(0, 2), (2, 0)])
+def test_kmeanspp_equal_potentials_go_to_the_lowest_trial(seed, want):
+    # 1-D points -1, 0, 1; the first center is sample 1 (u0 in [1/3, 2/3) for
+    # both seeds), so D^2 = 1, 0, 1 and a draw picks sample 0 when u < 1/2,
+    # sample 2 otherwise.  Either candidate leaves potential 1: an exact tie.
+    # Seed 0 draws (sample 2, sample 0), seed 2 draws (sample 0, sample 2); the
+    # lowest trial wins, so a lowest-index or last-trial rule fails one of them.
+    X = np.array([[-1.0], [0.0], [1.0]], np.float32)
+    u = [oracle.uniform(seed, i) for i in range(3)]
+    assert 1 / 3 <= u[0] < 2 / 3
+    assert (u[1] >= 0.5) == (want == 2) and (u[2] >= 0.5) == (want == 0)
+    idx, _, pots = oracle.kmeanspp(X, 2, seed, n_trials=2)
+    assert idx.tolist() == [1, want]
+    assert pots.tolist() == [2.0, 1.0]
+
+
+def test_kmeanspp_draw_numbering_with_several_trials():
+    # Scaled one-hot rows: every pair of distinct samples is 2 s^2 apart, so
+    # every unchosen sample carries the same D^2 and every candidate leaves
+    # the same potential.  The lowest trial then always wins, and center c is
+    # the candidate of draw 1 + (c - 1) T (trial 0): the floor(u m)-th of the
+    # m samples not yet chosen, in index order.  A numbering that used draw
+    # c T + t, or (c - 1) T + t, gives another sequence for this seed.
+    n, k, T, s = 9, 6, 3, 2.0
+    X = (s * np.eye(n)).astype(np.float32)
+
+    def closed_form(draw_of):
+        chosen = [min(int(math.floor(oracle.uniform(5, 0) * n)), n - 1)]
+        for c in range(1, k):
+            free = [i for i in range(n) if i not in chosen]
+            chosen.append(free[int(math.floor(oracle.uniform(5, draw_of(c)) * len(free)))])
+        return chosen
+
+    want = closed_form(lambda c: 1 + (c - 1) * T)
+    idx, _, pots = oracle.kmeanspp(X, k, 5, n_trials=T)
+    assert idx.tolist() == want
+    assert pots.tolist() == [2 * s * s * (n - 1 - c) for c in range(k)]
+    assert closed_form(lambda c: c * T) != want
+    assert closed_form(lambda c: (c - 1) * T) != want
+
+
+def test_kmeanspp_matches_plain_loops_and_not_the_wrong_rules():
+    # Tiny integer point sets over many seeds: the oracle picks exactly what
+    # the loop restatement picks, index by index, and each wrong rule (largest
+    # potential, first trial, last trial, lowest index on equal potentials,
+    # draws numbered c T + t) disagrees with the oracle somewhere.
+    rng = np.random.default_rng(2024)
+    wrong = {"highest": 0, "first": 0, "last": 0, "lowest_index": 0, "numbering": 0}
+    middle_wins = 0
+    for case in range(120):
+        n = int(rng.integers(3, 13))
+        d = int(rng.integers(1, 4))
+        X = rng.integers(-6, 7, size=(n, d)).astype(np.float32)
+        k = int(rng.integers(2, n + 1))
+        T = int(rng.integers(2, 5))
+        seed = int(rng.integers(0, 2**63))
+        o_idx, _, _ = oracle.kmeanspp(X, k, seed, n_trials=T)
+        got = o_idx.tolist()
+        assert got == _kmeanspp_loops(X, k, seed, T), f"case {case}"
+        for rule in ("highest", "first", "last", "lowest_index"):
+            wrong[rule] += got != _kmeanspp_loops(X, k, seed, T, rule=rule)
+        wrong["numbering"] += got != _kmeanspp_loops(X, k, seed, T, numbering="shifted")
+        if T >= 3:
+            # does the strictly best trial sit strictly inside the trial list?
+            idx0 = got[0]
+            D2 = [float(((X[i].astype(np.float64) - X[idx0]) ** 2).sum()) for i in range(n)]
+            cands = [_d2_pick(D2, oracle.uniform(seed, 1 + t)) for t in range(T)]
+            pots = [sum(min(D2[i], float(((X[i].astype(np.float64) - X[j]) ** 2).sum())) for i in range(n))
+                    for j in cands]
+            bt = min(range(T), key=lambda t: (pots[t], t))
+            middle_wins += 0 < bt < T - 1 and pots[bt] < min(pots[0], pots[-1])
+    assert all(v > 0 for v in wrong.values()), wrong
+    assert middle_wins > 0
