@@ -1,10 +1,12 @@
 #!/usr/bin/env python3
 """Benchmark: one k-means Lloyd iteration (assign + mean update) per step.
 
-Workload (default ``lloyd10``): n = 65536 samples, k = 1024 centroids,
-d = 2048 features, float32 planted Gaussian blobs (1024 centers ~ N(0, 1),
-noise sigma 0.5), initial centroids = seeded random rows of X.  Each step is
-one Lloyd iteration whose output centroids feed the next step.
+Workload (default ``sample_heavy``, the largest of the five shapes): n =
+131072 samples, k = 8192 centroids, d = 8192 features, float32 planted
+Gaussian blobs (8192 centers ~ N(0, 1), noise sigma 0.5), initial centroids =
+seeded random rows of X.  Each step is one Lloyd iteration whose output
+centroids feed the next step.  ``--workload`` selects another shape (probe,
+lloyd10, centroid_heavy, feature_heavy).
 
 Printed JSON line (rank 0):
 * ``value``: whole-job throughput in TFLOP/s, 2 n k d per Lloyd iteration
@@ -14,7 +16,10 @@ Printed JSON line (rank 0):
   fraction of the fp32-accurate tensor roofline; ``roofline`` describes it;
 * ``e2e``: the same metric through the public API with the step's inputs
   copied from pinned host memory and its results copied back, every step;
-* ``cpu_baseline``: the CPU oracle on a bounded sample of the same workload.
+* ``cpu_baseline``: the CPU oracle on a bounded sample of the same workload;
+* ``parity``: the GPU assignment and update against the oracle outputs of
+  that same leg (sampled rows; the update on every row), and the k-means++
+  indices against the stored oracle indices.
 
 ``--impl reference`` times the CPU oracle alone (the reference arm).
 Under torchrun every rank runs its own replica of the workload (the update
@@ -40,7 +45,8 @@ sys.path.insert(0, ROOT)
 
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "assign_tc_kernel_lloyd10.md")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "assign_tc_kernel_traffic.json")
+KMEANSPP_GOLDEN = os.path.join(ROOT, "tests", "golden", "kmeanspp_workload_indices.txt")
 KERNEL_SOURCE = os.path.join(ROOT, "distance_argmin_gb300", "csrc", "assign_tc.cu")
 METRIC = "Lloyd iter time & assign TFLOP/s (2nkd/t) at 1 GB300, % of fp32-accurate roofline"
 SPLIT_PRODUCTS = 3  # bf16x3: hi*hi + hi*lo + lo*hi per fp32 product
@@ -50,10 +56,10 @@ TF32_NOMINAL_TFLOPS = 1100.0  # dense, per GPU (context; no measured TF32 peak)
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", default="lloyd10")
+    ap.add_argument("--workload", default="sample_heavy")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kmeanspp", action="store_true")
@@ -77,20 +83,21 @@ def code_sha256(path):
     return hashlib.sha256("\n".join(l for l in lines if l.strip()).encode()).hexdigest()
 
 
-def recorded_traffic():
-    """Per-launch DRAM bytes of the assign kernel from the committed ncu
-    summary, if it was taken on the current kernel code; else None."""
-    if not os.path.exists(PROFILE_SUMMARY):
+def recorded_traffic(workload):
+    """Per-launch DRAM bytes (read + write) of the assign kernel on this
+    workload, from the committed ncu record, if it was taken on the current
+    kernel code; else None."""
+    if not os.path.exists(TRAFFIC_RECORD):
         return None
-    sha = code_sha256(KERNEL_SOURCE)
-    rec_sha, traffic = None, None
-    for line in open(PROFILE_SUMMARY):
-        line = line.strip().strip("`")
-        if line.startswith("code_sha256:"):
-            rec_sha = line.split(":", 1)[1].strip()
-        elif line.startswith("traffic_bytes_per_launch:"):
-            traffic = float(line.split(":", 1)[1].strip())
-    return traffic if (rec_sha == sha and traffic is not None) else None
+    with open(TRAFFIC_RECORD) as f:
+        rec = json.load(f).get("records", {}).get(workload)
+    if not rec or rec.get("code_sha256") != code_sha256(KERNEL_SOURCE):
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+def gib(nbytes):
+    return f"{nbytes / 2**30:.3g} GiB" if nbytes >= 2**30 else f"{nbytes / 2**20:.3g} MiB"
 
 
 def launches_per_lloyd_step(k: int) -> int:
@@ -183,28 +190,80 @@ def whole_job_tflops(flop_per_rank, world, seconds):
 
 def oracle_sample_step(oracle, X, C, rows):
     """One bounded-sample Lloyd step of the oracle: assign the sampled rows,
-    then the mean update over those rows.  Returns seconds."""
+    then the mean update over those rows.  Returns (seconds, the assignment's
+    (labels, best, second))."""
     t0 = time.perf_counter()
-    labels, _, _, _ = oracle.assign(X[rows], C)
-    oracle.update(X[rows], labels, C)
-    return time.perf_counter() - t0
+    o_l, o_b, o_s, _ = oracle.assign(X[rows], C)
+    oracle.update(X[rows], o_l, C)
+    return time.perf_counter() - t0, (o_l, o_b, o_s)
 
 
-def cpu_baseline(oracle, w, X, C0, budget_s=20.0):
+DIST_RTOL = 1e-4      # best distance, relative to ||x||^2 + ||c_best||^2
+CENTROID_RTOL = 1e-5  # centroid row, relative to the row's largest magnitude
+
+
+def sq_norms(A):
+    import numpy as np
+    A64 = A.astype(np.float64)
+    return np.einsum("ij,ij->i", A64, A64)
+
+
+def assign_parity(X, C, rows, labels, best, o_l, o_b, o_s):
+    """The GPU's labels and best distances on ``rows`` against the oracle's:
+    the worst relative distance error, label mismatches where the oracle's
+    winner is clear (must be 0) and near-tie flips (allowed, counted)."""
+    import numpy as np
+    lab = labels[rows]
+    scale = sq_norms(X[rows]) + sq_norms(C)[o_l]
+    rel = np.abs(best[rows].astype(np.float64) - o_b) / scale
+    clear = (o_s - o_b) > DIST_RTOL * scale
+    return {"rows_checked": int(len(rows)), "worst_rel_distance_error": float(rel.max()),
+            "distances_within_tolerance": bool((rel <= DIST_RTOL).all()),
+            "clear_label_mismatches": int((clear & (lab != o_l)).sum()),
+            "near_tie_flips": int((~clear & (lab != o_l)).sum()),
+            "near_ties": int((~clear).sum())}
+
+
+def centroid_parity(C_gpu, counts_gpu, o_C, o_counts):
+    """Per centroid row: max |gpu - oracle| over max |oracle row|."""
+    import numpy as np
+    got = C_gpu.astype(np.float64)
+    want = o_C.astype(np.float64)
+    row_scale = np.maximum(np.abs(want).max(axis=1), np.finfo(np.float32).tiny)
+    rel = np.abs(got - want).max(axis=1) / row_scale
+    return {"worst_centroid_row_error": float(rel.max()),
+            "centroids_within_tolerance": bool((rel <= CENTROID_RTOL).all()),
+            "counts_equal": bool(np.array_equal(counts_gpu.astype(np.int64), o_counts))}
+
+
+def cpu_baseline(oracle, w, X, C0, gpu=None, budget_s=20.0):
     """Time the oracle (as it stands, all host cores) on seeded row samples
     of the workload; TFLOP/s = 2 * rows * k * d / time (the per-row cost of
-    the full iteration is the same for every row)."""
+    the full iteration is the same for every row).
+
+    ``gpu`` (labels, best, C_new, counts of the GPU's assignment of every row
+    to C0 and its update on those labels) is compared, after the timing, with
+    the oracle outputs of the timed sample and with the oracle's update of
+    every row on the GPU's labels (so near-tie flips do not cascade)."""
     import numpy as np
     rng = np.random.default_rng(7)
     rows = np.sort(rng.choice(w.n, size=min(w.n, 256), replace=False))
-    t = oracle_sample_step(oracle, X, C0, rows)  # calibrate
+    t, _ = oracle_sample_step(oracle, X, C0, rows)  # calibrate
     m = int(min(w.n, max(256, 256 * budget_s / max(t, 1e-3) * 0.8)))
     rows = np.sort(rng.choice(w.n, size=m, replace=False))
-    t = oracle_sample_step(oracle, X, C0, rows)
-    return {"value": 2.0 * m * w.k * w.d / t / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+    t, (o_l, o_b, o_s) = oracle_sample_step(oracle, X, C0, rows)
+    base = {"value": 2.0 * m * w.k * w.d / t / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
             "kind": "oracle", "sample": f"{m} of {w.n} seeded rows: binary64 brute-force assign of the rows "
-                                        f"against all {w.k} centroids + mean update of those rows; {t:.1f} s",
-            "seconds": t}
+                                        f"against all {w.k} centroids + mean update of those rows; {t:.1f} s"}
+    parity = None
+    if gpu is not None:
+        labels, best, C_new, counts = gpu
+        parity = assign_parity(X, C0, rows, labels, best, o_l, o_b, o_s)
+        parity["rows"] = "the cpu_baseline leg's seeded sample, assigned to the initial centroids"
+        o_C, o_cnt = oracle.update(X, labels, C0)
+        parity.update(centroid_parity(C_new, counts, o_C, o_cnt))
+        parity["update"] = "every row, on the GPU's labels"
+    return base, parity
 
 
 # ------------------------------------------------------------ reference arm
@@ -225,7 +284,7 @@ def run_reference(args):
         oracle_sample_step(oracle, X, C0, samples[i])
     t = 0.0
     for i in range(args.steps):
-        t += oracle_sample_step(oracle, X, C0, samples[args.warmup + i])
+        t += oracle_sample_step(oracle, X, C0, samples[args.warmup + i])[0]
     ms_per_step = 1e3 * t / args.steps
     value = 2.0 * rows_per_step * w.k * w.d / (t / args.steps) / 1e12
     line = {
@@ -243,6 +302,26 @@ def run_reference(args):
 
 
 # -------------------------------------------------------------- GB300 arm
+def kmeanspp_matches_stored_oracle(X, w, T, got):
+    """The seeding's indices against the oracle's, stored with the SHA-256 of
+    the samples it saw: True/False, or None when this host's generator gave
+    other samples (the stored answer then does not apply)."""
+    import numpy as np
+    if not os.path.exists(KMEANSPP_GOLDEN):
+        return None
+    meta, want = {}, []
+    for line in open(KMEANSPP_GOLDEN):
+        if line.startswith("#"):
+            meta.update(tok.split("=", 1) for tok in line[1:].split() if "=" in tok)
+        elif line.strip():
+            want.append(int(line))
+    if ((int(meta.get("n", -1)), int(meta.get("d", -1)), int(meta.get("k", -1)), int(meta.get("seed", -1)),
+         int(meta.get("trials", -1))) != (w.n, w.d, w.k, w.init_seed, T)
+            or hashlib.sha256(X.tobytes()).hexdigest() != meta.get("x_sha256")):
+        return None
+    return bool(np.array_equal(np.asarray(got), np.asarray(want, dtype=np.int64)))
+
+
 def time_kmeanspp(km, synth, dev, stream, barrier):
     """Greedy k-means++ on its own workload (65536 x 8192, 1024 centers,
     8 trials): one timed call after a short warm-up call."""
@@ -272,6 +351,7 @@ def time_kmeanspp(km, synth, dev, stream, barrier):
 
     t = seed_once(False)
     first = idx.clone()
+    match = kmeanspp_matches_stored_oracle(X, w, T, first.cpu().numpy())
     t_traced = seed_once(True)
     dist_ms, dist_timed, dist_seen = km.kmeans_trace_read(km.KERNEL_KMEANSPP_DIST)
     km.kmeans_trace_stop()
@@ -282,7 +362,7 @@ def time_kmeanspp(km, synth, dev, stream, barrier):
     pass_bytes = 4.0 * w.n * w.d + 8.0 * slices * T * w.n
     t_pass = dist_ms / 1e3 / max(dist_timed, 1)
     return {"workload": f"n={w.n} d={w.d} k={w.k} trials={T}", "ms": 1e3 * t, "gbs": moved / t / 1e9,
-            "ms_per_center": 1e3 * t / w.k,
+            "ms_per_center": 1e3 * t / w.k, "indices_match_oracle": match,
             "distance_pass": {"kernel": "kpp_dist_part_kernel", "launches": dist_seen, "us": 1e6 * t_pass,
                               "bytes_per_launch": pass_bytes, "gbs": pass_bytes / t_pass / 1e9,
                               "share_of_call": dist_ms / 1e3 / t_traced,
@@ -398,10 +478,13 @@ def run_gb300(args):
     ev1.record(stream)
     barrier()
     t_update = ev0.elapsed_time(ev1) / 1e3 / steps
+    # the assignment of every row to C0 and the update on those labels, kept
+    # for the parity check against the oracle (after all timed regions)
+    gpu_c0 = (labels.cpu().numpy(), best.cpu().numpy(), C_upd.cpu().numpy(), counts.cpu().numpy())
 
     # the FFMA comparator on the same workload (fewer calls: it is ~10x slower)
     ws_f = km.workspace(km.OP_ASSIGN_FFMA, n, k, d, dev)
-    f_steps = max(1, min(steps, 20))
+    f_steps = max(1, min(steps, 20, int(4e13 / flop)))  # about 10x the tensor path's time
     km.kmeans_assign_ffma(Xd, C0d, labels, best, inertia_a, ws=ws_f, stream=stream)
     barrier()
     ev0.record(stream)
@@ -528,6 +611,7 @@ def run_gb300(args):
 
     peaks, peaks_src = load_peaks()
     r_peak = peaks["bf16_tflops"] / SPLIT_PRODUCTS
+    r_sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) / SPLIT_PRODUCTS
     assign_tflops = flop / t_assign / 1e12
     tc_tflops = flop / t_tc / 1e12
     upd_bytes = 4.0 * n * d + 8.0 * n + 4.0 * k * d
@@ -547,7 +631,7 @@ def run_gb300(args):
         "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "n": n, "k": k, "d": d, "blobs": w.blobs,
-                   "init": "seeded random rows of X", "l2": "inputs larger than L2 (X 512 MiB)",
+                   "init": "seeded random rows of X", "l2": f"inputs larger than L2 (X {gib(X.nbytes)})",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "assign": {"ms": 1e3 * t_assign, "tflops": assign_tflops, "frac_of_R": assign_tflops / r_peak,
                    "R_tflops": r_peak, "R": f"fp32-accurate roofline = bf16 dense peak ({peaks_src}, burst) / 3 "
@@ -575,7 +659,8 @@ def run_gb300(args):
                                    "restores the labels first (a device copy of n int64, in the time)"},
         "lloyd_frac_of_roofline": (flop / (r_peak * 1e12) + upd_bytes / (peaks["hbm_gbs"] * 1e9)) / t_lloyd,
         "roofline": {"bound": "tensor", "achieved": tc_tflops, "peak": r_peak, "unit": "TFLOP/s",
-                     "frac": tc_tflops / r_peak, "traffic": recorded_traffic(),
+                     "frac": tc_tflops / r_peak, "traffic": recorded_traffic(w.name),
+                     "peak_sustained": r_sustained, "frac_sustained": tc_tflops / r_sustained,
                      "kernel": "assign_tc_kernel",
                      "kernel_us": 1e6 * t_tc, "kernel_share_of_step": t_tc / t_lloyd_traced,
                      "timing": "CUDA events the library records around each launch on the launch stream, in "
@@ -584,7 +669,11 @@ def run_gb300(args):
                                f"{1e3 * t_lloyd:.4f} without: each record holds the next chained launch back "
                                "until the kernel has drained, so the kernel time includes its own ramp-up)",
                      "algorithmic": "2 n k d flops per launch",
-                     "peak_source": f"{peaks_src} bf16 burst {peaks['bf16_tflops']} / 3"},
+                     "peak_source": f"{peaks_src} bf16 burst {peaks['bf16_tflops']} / 3; peak_sustained: "
+                                    f"{peaks_src} sustained {peaks.get('bf16_tflops_sustained')} / 3",
+                     "algorithmic_bytes": 4.0 * n * d + 4.0 * k * d + 12.0 * n,
+                     "traffic_source": "profiles/assign_tc_kernel_traffic.json (ncu dram__bytes_read.sum + "
+                                       "dram__bytes_write.sum, one launch on this workload)"},
         "inertia_first10": [float(v) for v in inertia_hist[:10]],
         "gpu_launches": steps * launches_per_lloyd_step(k),
         "clocks": clocks,
@@ -597,8 +686,9 @@ def run_gb300(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        line["cpu_baseline"] = cpu_baseline(oracle, w, X, C0)
-        line["cpu_baseline"].pop("seconds", None)
+        line["cpu_baseline"], line["parity"] = cpu_baseline(oracle, w, X, C0, gpu=gpu_c0)
+        if kpp:
+            line["parity"]["kmeanspp_indices_match"] = kpp["indices_match_oracle"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -1,17 +1,20 @@
 """GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
-the same seeded inputs.  Small shapes are compared on every row; full-size
-workloads on a seeded sample of rows (assignment) and on every row (update,
-with the GPU's own labels so near-tie flips do not cascade)."""
+the same seeded inputs.  Small shapes are compared on every row.  The three
+large workloads' assignments are compared on every row with stored oracle
+results, lloyd10's first iteration with the oracle run live, and its ten
+iterations on a seeded sample of rows; updates on every row, with the GPU's
+own labels so near-tie flips do not cascade."""
 import ctypes
 import hashlib
 import os
+import sys
 
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from parity import DIST_RTOL, check_assign, check_centroids, sq_norms
+from parity import DIST_RTOL, check_assign, check_assign_every_row, check_centroids, sq_norms
 
 pytestmark = pytest.mark.gpu
 
@@ -285,25 +288,44 @@ def test_lloyd10_first_iteration_every_row(gpu_lib, record_property):
     assert np.array_equal(host(counts).astype(np.int64), o_cnt)
 
 
+def _large_golden(name):
+    sys.path.insert(0, os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden"))
+    import make_large_assign
+    return make_large_assign.load(name)
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["sample_heavy", "centroid_heavy", "feature_heavy"])
-def test_large_workload_one_iteration(gpu_lib, name):
+def test_large_workload_one_iteration(gpu_lib, name, record_property):
+    # Every row of the assignment against the oracle's, which
+    # tests/golden/make_large_assign.py stored ahead of time (the brute-force
+    # argmin takes the oracle minutes per workload).  The stored SHA-256 of the
+    # samples and centroids makes sure the input generator gave this machine
+    # the bytes the oracle saw.  Then the update on the GPU's labels, every
+    # row, against the oracle run live.
     w = synth.WORKLOADS[name]
+    o_l, near_rows, near_best, near_second, o_inertia, meta = _large_golden(name)
+    assert (meta["n"], meta["k"], meta["d"]) == (w.n, w.k, w.d)
     X, C0, _ = synth.workload_inputs(w)
+    assert hashlib.sha256(X.tobytes()).hexdigest() == meta["x_sha256"], \
+        f"the input generator gave different samples here than on the {meta['machine']} host the oracle ran on"
+    assert hashlib.sha256(C0.tobytes()).hexdigest() == meta["c_sha256"]
     Xd, Cd = dev_tensor(X), dev_tensor(C0)
     C1, labels, best, inertia, counts = gpu_lib.kmeans_lloyd_iter(Xd, Cd)
     lab, bd = host(labels), host(best)
     del Xd
     torch.cuda.empty_cache()
-    rows = _sample_rows(w.n, 512, 17)
-    o_l, o_b, o_s, _ = oracle.assign(X[rows], C0)
-    flips, worst = check_assign(X[rows], C0, lab, bd, o_l, o_b, o_s, rows=rows, what=name)
-    print(f"{name}: worst relative distance error {worst:.3e}, near-tie flips {flips} of {len(rows)}")
+    flips, worst, near = check_assign_every_row(X, C0, lab, bd, o_l, near_rows, near_best, near_second, what=name)
+    record_property("rows", w.n)
+    record_property("near_ties", near)
+    record_property("near_tie_flips", flips)
+    record_property("worst_rel_distance_error", worst)
+    print(f"{name}, all {w.n} rows: worst relative distance error {worst:.3e}, {near} near ties, {flips} flips")
+    scale = (sq_norms(X) + sq_norms(C0)[o_l]).sum()
+    assert abs(float(inertia.item()) - o_inertia) <= DIST_RTOL * scale
     o_C1, o_cnt = oracle.update(X, lab, C0)
     check_centroids(host(C1), o_C1, what=name + " update")
     assert np.array_equal(host(counts).astype(np.int64), o_cnt)
-    # every label is a valid index and every distance finite and non-negative
-    assert lab.min() >= 0 and lab.max() < w.k
     assert np.isfinite(bd).all() and (bd >= 0).all()
 
 
