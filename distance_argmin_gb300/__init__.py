@@ -9,7 +9,10 @@ streams.  There is no CPU path: without the built library every call fails.
 
 Names follow the C ABI: ``kmeans_assign``, ``kmeans_assign_ffma``,
 ``kmeans_update``, ``kmeans_lloyd_iter``, ``kmeanspp_init``,
-``kmeans_workspace_bytes``, ``kmeans_device_status``, ``kmeans_status_string``.
+``kmeans_workspace_bytes``, ``kmeans_device_status``, ``kmeans_status_string``,
+and the shard entry points (``kmeans_lloyd_iter_partial``,
+``kmeans_reduce_partials``, ``kmeanspp_shard_*``) that ``sharded.py`` drives
+across processes.
 """
 from __future__ import annotations
 
@@ -29,6 +32,7 @@ KMEANS_ERR_CUDA = 4
 KMEANS_ERR_DEVICE_TIMEOUT = 5
 KMEANS_ERR_DEVICE_LABEL = 6
 KMEANS_ERR_SCRATCH_LIMIT = 7
+KMEANS_ERR_DEVICE_EXCHANGE = 8
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 OP_ASSIGN = 0
@@ -40,6 +44,9 @@ OP_FIT = 5
 OP_ASSIGN_3XTF32 = 6
 OP_LLOYD_FUSED = 7
 OP_RELOCATE = 8
+OP_KMEANSPP_SHARD = 9
+OP_LLOYD_PARTIAL = 10
+OP_UPDATE_PARTIAL = 11
 
 INIT_GIVEN = 0
 INIT_KMEANSPP = 1
@@ -61,7 +68,9 @@ EXPORTS = (
     "kmeans_lloyd_iter", "kmeanspp_init", "kmeans_device_status", "kmeans_status_string",
     "kmeans_build_info", "kmeans_assign_noalloc", "kmeans_trace_start", "kmeans_trace_read",
     "kmeans_trace_stop", "kmeans_lloyd_iter_host", "kmeans_fit", "kmeans_assign_3xtf32",
-    "kmeans_lloyd_iter_fused", "kmeans_relocate_empty",
+    "kmeans_lloyd_iter_fused", "kmeans_relocate_empty", "kmeans_update_partial", "kmeans_lloyd_iter_partial",
+    "kmeans_reduce_partials", "kmeanspp_shard_exchange_bytes", "kmeanspp_shard_first", "kmeanspp_shard_pick",
+    "kmeanspp_shard_dist", "kmeanspp_shard_commit",
 )
 
 _lock = threading.Lock()
@@ -125,6 +134,22 @@ def load(path: str | None = None):
         lib.kmeans_relocate_empty.restype = INT
         lib.kmeans_trace_stop.argtypes = []
         lib.kmeans_trace_stop.restype = INT
+        lib.kmeans_update_partial.argtypes = [P, P, I64, I64, I64, P, P, P, SZ, U64, P]
+        lib.kmeans_update_partial.restype = INT
+        lib.kmeans_lloyd_iter_partial.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, P, SZ, U64, P]
+        lib.kmeans_lloyd_iter_partial.restype = INT
+        lib.kmeans_reduce_partials.argtypes = [P, P, P, INT, I64, I64, P, P, P, P, P]
+        lib.kmeans_reduce_partials.restype = INT
+        lib.kmeanspp_shard_exchange_bytes.argtypes = [INT, I64]
+        lib.kmeanspp_shard_exchange_bytes.restype = SZ
+        lib.kmeanspp_shard_first.argtypes = [P, I64, I64, I64, I64, INT, U64, P, P, SZ, P]
+        lib.kmeanspp_shard_first.restype = INT
+        lib.kmeanspp_shard_pick.argtypes = [P, I64, I64, I64, INT, U64, I64, P, INT, INT, P, P, SZ, P]
+        lib.kmeanspp_shard_pick.restype = INT
+        lib.kmeanspp_shard_dist.argtypes = [P, I64, I64, INT, INT, P, INT, P, P, SZ, P]
+        lib.kmeanspp_shard_dist.restype = INT
+        lib.kmeanspp_shard_commit.argtypes = [I64, I64, INT, INT, P, INT, I64, P, P, P, P, SZ, P]
+        lib.kmeanspp_shard_commit.restype = INT
         _lib = lib
         return lib
 
@@ -481,3 +506,112 @@ def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_o
     done = torch.cuda.Event()
     done.record(stream)
     return done
+
+
+# ------------------------------------------------- samples split across GPUs
+def kmeans_update_partial(X, labels, k: int, sums=None, counts=None, ws=None, seed=0, stream=None):
+    """One shard's cluster sums (zeros for an empty cluster) and counts ->
+    ``(sums (k, d), counts (k,))``."""
+    torch = _torch()
+    _check(X, "X", torch.float32)
+    n, d = X.shape
+    _check(labels, "labels", torch.int64, (n,), X.device)
+    k = int(k)
+    if sums is None:
+        sums = torch.empty((k, d), dtype=torch.float32, device=X.device)
+    if counts is None:
+        counts = torch.empty(k, dtype=torch.int32, device=X.device)
+    _check(sums, "sums", torch.float32, (k, d), X.device)
+    _check(counts, "counts", torch.int32, (k,), X.device)
+    ws = _ws(ws, OP_UPDATE_PARTIAL, n, k, d, X.device)
+    st = load().kmeans_update_partial(_ptr(X), _ptr(labels), n, k, d, _ptr(sums), _ptr(counts), _ptr(ws), ws.numel(),
+                                      seed & (2**64 - 1), _stream_handle(stream))
+    _raise(st, "kmeans_update_partial")
+    return sums, counts
+
+
+def kmeans_lloyd_iter_partial(X, C, labels=None, best_dist=None, inertia=None, sums=None, counts=None, ws=None,
+                              seed=0, stream=None):
+    """One shard's part of a Lloyd iteration -> ``(sums, counts, labels,
+    best_dist, inertia)`` (the shard's assignment and its cluster sums)."""
+    torch = _torch()
+    _check(X, "X", torch.float32)
+    n, d = X.shape
+    _check(C, "C", torch.float32, device=X.device)
+    k = C.shape[0]
+    if C.dim() != 2 or C.shape[1] != d:
+        raise ValueError("C must be (k, d) with the same d as X")
+    labels = torch.empty(n, dtype=torch.int64, device=X.device) if labels is None else labels
+    best_dist = torch.empty(n, dtype=torch.float32, device=X.device) if best_dist is None else best_dist
+    inertia = torch.empty(1, dtype=torch.float64, device=X.device) if inertia is None else inertia
+    sums = torch.empty((k, d), dtype=torch.float32, device=X.device) if sums is None else sums
+    counts = torch.empty(k, dtype=torch.int32, device=X.device) if counts is None else counts
+    _check(labels, "labels", torch.int64, (n,), X.device)
+    _check(best_dist, "best_dist", torch.float32, (n,), X.device)
+    _check(inertia, "inertia", torch.float64, (1,), X.device)
+    _check(sums, "sums", torch.float32, (k, d), X.device)
+    _check(counts, "counts", torch.int32, (k,), X.device)
+    ws = _ws(ws, OP_LLOYD_PARTIAL, n, k, d, X.device)
+    st = load().kmeans_lloyd_iter_partial(_ptr(X), _ptr(C), _ptr(labels), _ptr(best_dist), _ptr(inertia), _ptr(sums),
+                                          _ptr(counts), n, k, d, _ptr(ws), ws.numel(), seed & (2**64 - 1),
+                                          _stream_handle(stream))
+    _raise(st, "kmeans_lloyd_iter_partial")
+    return sums, counts, labels, best_dist, inertia
+
+
+def kmeans_reduce_partials(parts, part_counts, C_old, C_new=None, counts=None, part_inertia=None, inertia=None,
+                           stream=None):
+    """Rank-order sum of ``parts`` (world, rows, d) over the summed
+    ``part_counts`` (world, rows); C_old's row where no rank has a member ->
+    ``(C_new, counts, inertia)``."""
+    torch = _torch()
+    _check(parts, "parts", torch.float32)
+    world, rows, d = parts.shape
+    dev = parts.device
+    _check(part_counts, "part_counts", torch.int32, (world, rows), dev)
+    _check(C_old, "C_old", torch.float32, (rows, d), dev)
+    C_new = torch.empty_like(C_old) if C_new is None else C_new
+    counts = torch.empty(rows, dtype=torch.int32, device=dev) if counts is None else counts
+    _check(C_new, "C_new", torch.float32, (rows, d), dev)
+    _check(counts, "counts", torch.int32, (rows,), dev)
+    if part_inertia is not None:
+        _check(part_inertia, "part_inertia", torch.float64, (world,), dev)
+        inertia = torch.empty(1, dtype=torch.float64, device=dev) if inertia is None else inertia
+        _check(inertia, "inertia", torch.float64, (1,), dev)
+    st = load().kmeans_reduce_partials(_ptr(parts), _ptr(part_counts), _ptr(part_inertia), world, rows, d,
+                                       _ptr(C_old), _ptr(C_new), _ptr(counts),
+                                       _ptr(inertia if part_inertia is not None else None), _stream_handle(stream))
+    _raise(st, "kmeans_reduce_partials")
+    return C_new, counts, inertia
+
+
+def kmeanspp_shard_exchange_bytes(n_trials: int, d: int) -> int:
+    return int(load().kmeanspp_shard_exchange_bytes(int(n_trials), int(d)))
+
+
+def kmeanspp_shard_first(X, row_offset: int, n_global: int, n_trials: int, seed: int, send, ws, stream=None):
+    st = load().kmeanspp_shard_first(_ptr(X), X.shape[0], X.shape[1], int(row_offset), int(n_global), int(n_trials),
+                                     int(seed) & (2**64 - 1), _ptr(send), _ptr(ws), ws.numel(), _stream_handle(stream))
+    _raise(st, "kmeanspp_shard_first")
+
+
+def kmeanspp_shard_pick(X, row_offset: int, n_trials: int, seed: int, c: int, totals, rank: int, send, ws,
+                        stream=None):
+    st = load().kmeanspp_shard_pick(_ptr(X), X.shape[0], X.shape[1], int(row_offset), int(n_trials),
+                                    int(seed) & (2**64 - 1), int(c), _ptr(totals), totals.numel(), int(rank),
+                                    _ptr(send), _ptr(ws), ws.numel(), _stream_handle(stream))
+    _raise(st, "kmeanspp_shard_pick")
+
+
+def kmeanspp_shard_dist(X, n_trials: int, first: bool, recv, world: int, pot, ws, stream=None):
+    st = load().kmeanspp_shard_dist(_ptr(X), X.shape[0], X.shape[1], int(n_trials), 1 if first else 0, _ptr(recv),
+                                    int(world), _ptr(pot), _ptr(ws), ws.numel(), _stream_handle(stream))
+    _raise(st, "kmeanspp_shard_dist")
+
+
+def kmeanspp_shard_commit(n: int, d: int, n_trials: int, first: bool, pots, world: int, c: int, indices, centers,
+                          total, ws, stream=None):
+    st = load().kmeanspp_shard_commit(int(n), int(d), int(n_trials), 1 if first else 0, _ptr(pots), int(world), int(c),
+                                      _ptr(indices), _ptr(centers), _ptr(total), _ptr(ws), ws.numel(),
+                                      _stream_handle(stream))
+    _raise(st, "kmeanspp_shard_commit")

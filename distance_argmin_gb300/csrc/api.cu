@@ -23,6 +23,11 @@ bool sizes_ok(int64_t n, int64_t k, int64_t d) {
     return n >= 1 && k >= 1 && k <= n && d >= 1 && n <= kMaxIndex && k <= kMaxIndex && d <= kMaxIndex;
 }
 
+// A shard of the samples may hold fewer samples than there are centroids.
+bool shard_sizes_ok(int64_t n, int64_t k, int64_t d) {
+    return n >= 1 && k >= 1 && d >= 1 && n <= kMaxIndex && k <= kMaxIndex && d <= kMaxIndex;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -128,15 +133,23 @@ FusedLayout fused_layout(int64_t n, int64_t k, int64_t d) {
 // the mean update.  The update reuses the assignment's workspace: its scratch
 // is dead once the labels are written, and the count table and the fused
 // finalize's block sums lie above the keys and norms that finalize still reads.
+// With `sums_only` (a shard of the samples) C_new receives the clusters'
+// sums instead of their means (see launch_update).
 cudaError_t lloyd_finish(const float *X, const float *C_old, float *C_new, int64_t *labels, float *best_dist,
                          double *inertia, int32_t *counts, int64_t n, int64_t k, int64_t d, const AssignLayout &A,
-                         uint8_t *w, cudaStream_t s) {
+                         uint8_t *w, cudaStream_t s, bool sums_only = false) {
     const UpdateLayout U = update_layout(n, k, d);
     const bool fused = U.counting && U.off_table >= A.off_xnorm + n * 4 && U.off_table >= A.off_keys + n * 8;
     cudaError_t e = fused ? launch_finalize_counting(n, k, A, U, w, labels, best_dist, inertia, s)
                           : launch_finalize(n, A, w, labels, best_dist, inertia, s);
-    if (e == cudaSuccess) e = launch_update(X, labels, C_old, C_new, counts, n, k, d, U, w, false, s, fused);
+    if (e == cudaSuccess) e = launch_update(X, labels, C_old, C_new, counts, n, k, d, U, w, false, s, fused, sums_only);
     return e;
+}
+
+int64_t lloyd_ws_bytes(int64_t n, int64_t k, int64_t d) {
+    const int64_t a = assign_layout(n, k, d, true).bytes;
+    const int64_t u = update_layout(n, k, d).bytes;
+    return a > u ? a : u;
 }
 
 }  // namespace
@@ -144,6 +157,13 @@ cudaError_t lloyd_finish(const float *X, const float *C_old, float *C_new, int64
 extern "C" {
 
 size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
+    // the shard operations accept more centroids than samples
+    if (op == KMEANS_OP_LLOYD_PARTIAL || op == KMEANS_OP_UPDATE_PARTIAL || op == KMEANS_OP_KMEANSPP_SHARD) {
+        if (!shard_sizes_ok(n, k, d)) return 0;
+        if (op == KMEANS_OP_LLOYD_PARTIAL) return (size_t)lloyd_ws_bytes(n, k, d);
+        if (op == KMEANS_OP_UPDATE_PARTIAL) return (size_t)update_layout(n, k, d).bytes;
+        return (size_t)kpp_shard_layout(n, d).bytes;
+    }
     if (!sizes_ok(n, k, d)) return 0;
     switch (op) {
         case KMEANS_OP_ASSIGN:
@@ -154,11 +174,8 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
             return (size_t)assign_layout(n, k, d, true, 4).bytes;
         case KMEANS_OP_UPDATE:
             return (size_t)update_layout(n, k, d).bytes;
-        case KMEANS_OP_LLOYD: {
-            const int64_t a = assign_layout(n, k, d, true).bytes;
-            const int64_t u = update_layout(n, k, d).bytes;
-            return (size_t)(a > u ? a : u);
-        }
+        case KMEANS_OP_LLOYD:
+            return (size_t)lloyd_ws_bytes(n, k, d);
         case KMEANS_OP_KMEANSPP:
             return (size_t)kpp_layout(n, d, kKppMaxTrials).bytes;
         case KMEANS_OP_FIT:
@@ -404,6 +421,124 @@ int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int3
     return cuda_status(e);
 }
 
+int kmeans_update_partial(const float *X, const int64_t *labels, int64_t n, int64_t k, int64_t d, float *sums,
+                          int32_t *counts, void *ws, size_t ws_bytes, uint64_t seed, void *stream) {
+    (void)seed;
+    if (!X || !labels || !sums || !counts) return KMEANS_ERR_INVALID_ARG;
+    if (!shard_sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    if (!aligned4(X) || !aligned4(sums) || !aligned4(counts) || (reinterpret_cast<uintptr_t>(labels) & 7u))
+        return KMEANS_ERR_INVALID_ARG;
+    const UpdateLayout L = update_layout(n, k, d);
+    const int wst = check_ws(ws, ws_bytes, (size_t)L.bytes);
+    if (wst != KMEANS_OK) return wst;
+    return cuda_status(launch_update(X, labels, nullptr, sums, counts, n, k, d, L, static_cast<uint8_t *>(ws), true,
+                                     static_cast<cudaStream_t>(stream), false, true));
+}
+
+int kmeans_lloyd_iter_partial(const float *X, const float *C, int64_t *labels, float *best_dist, double *inertia,
+                              float *sums, int32_t *counts, int64_t n, int64_t k, int64_t d, void *ws,
+                              size_t ws_bytes, uint64_t seed, void *stream) {
+    (void)seed;
+    if (!X || !C || !labels || !best_dist || !sums || !counts) return KMEANS_ERR_INVALID_ARG;
+    if (!shard_sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
+    if (!aligned4(sums) || !aligned4(counts) || (reinterpret_cast<uintptr_t>(labels) & 7u))
+        return KMEANS_ERR_INVALID_ARG;
+    const int st = tc_path_ok(X, C, d);
+    if (st != KMEANS_OK) return st;
+    const int wst = check_ws(ws, ws_bytes, (size_t)lloyd_ws_bytes(n, k, d));
+    if (wst != KMEANS_OK) return wst;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    const AssignLayout A = assign_layout(n, k, d, true);
+    cudaError_t e = launch_prep_split(C, n, k, d, A, w, s);
+    if (e == cudaSuccess) e = launch_assign_tc(X, n, k, d, A, w, s);
+    if (e == cudaSuccess) e = lloyd_finish(X, nullptr, sums, labels, best_dist, inertia, counts, n, k, d, A, w, s, true);
+    return cuda_status(e);
+}
+
+int kmeans_reduce_partials(const float *parts, const int32_t *part_counts, const double *part_inertia, int world,
+                           int64_t rows, int64_t d, const float *C_old, float *C_new, int32_t *counts, double *inertia,
+                           void *stream) {
+    if (world < 1 || world > 65536 || rows < 0 || d < 1 || d > kMaxIndex) return KMEANS_ERR_INVALID_ARG;
+    if ((part_inertia == nullptr) != (inertia == nullptr)) return KMEANS_ERR_INVALID_ARG;
+    if (rows > 0 && (!parts || !part_counts || !C_old || !C_new)) return KMEANS_ERR_INVALID_ARG;
+    if (rows == 0 && !inertia) return KMEANS_OK;
+    if (!aligned4(parts) || !aligned4(part_counts) || !aligned4(C_old) || !aligned4(C_new) || !aligned4(counts) ||
+        (reinterpret_cast<uintptr_t>(part_inertia) & 7u) || (reinterpret_cast<uintptr_t>(inertia) & 7u))
+        return KMEANS_ERR_INVALID_ARG;
+    return cuda_status(launch_reduce_partials(parts, part_counts, part_inertia, world, rows, d, C_old, C_new, counts,
+                                              inertia, static_cast<cudaStream_t>(stream)));
+}
+
+size_t kmeanspp_shard_exchange_bytes(int n_trials, int64_t d) {
+    if (n_trials < 1 || n_trials > kKppMaxTrials || d < 1 || d > kMaxIndex) return 0;
+    return (size_t)kpp_exchange_bytes(n_trials, d);
+}
+
+namespace {
+int kpp_shard_check(const float *X, int64_t n, int64_t d, int T, const void *ws, size_t ws_bytes, KppShardLayout &L) {
+    if (n < 1 || d < 1 || n > kMaxIndex || d > kMaxIndex) return KMEANS_ERR_INVALID_ARG;
+    if (T < 1 || T > kKppMaxTrials) return KMEANS_ERR_INVALID_ARG;
+    if (X && !aligned4(X)) return KMEANS_ERR_INVALID_ARG;
+    L = kpp_shard_layout(n, d);
+    return check_ws(ws, ws_bytes, (size_t)L.bytes);
+}
+}  // namespace
+
+int kmeanspp_shard_first(const float *X, int64_t n, int64_t d, int64_t row_offset, int64_t n_global, int n_trials,
+                         uint64_t seed, void *send, void *ws, size_t ws_bytes, void *stream) {
+    if (!X || !send || !aligned16(send)) return KMEANS_ERR_INVALID_ARG;
+    if (row_offset < 0 || n_global < 1 || row_offset + n > n_global) return KMEANS_ERR_INVALID_ARG;
+    KppShardLayout L;
+    const int st = kpp_shard_check(X, n, d, n_trials, ws, ws_bytes, L);
+    if (st != KMEANS_OK) return st;
+    return cuda_status(launch_kpp_shard_first(X, n, d, row_offset, n_global, n_trials, seed,
+                                              static_cast<uint8_t *>(send), static_cast<uint8_t *>(ws),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+int kmeanspp_shard_pick(const float *X, int64_t n, int64_t d, int64_t row_offset, int n_trials, uint64_t seed,
+                        int64_t c, const double *totals, int world, int rank, void *send, void *ws, size_t ws_bytes,
+                        void *stream) {
+    if (!X || !totals || !send || !aligned16(send) || (reinterpret_cast<uintptr_t>(totals) & 7u))
+        return KMEANS_ERR_INVALID_ARG;
+    if (world < 1 || world > 65536 || rank < 0 || rank >= world || c < 1 || row_offset < 0)
+        return KMEANS_ERR_INVALID_ARG;
+    KppShardLayout L;
+    const int st = kpp_shard_check(X, n, d, n_trials, ws, ws_bytes, L);
+    if (st != KMEANS_OK) return st;
+    return cuda_status(launch_kpp_shard_pick(X, n, d, row_offset, n_trials, seed, c, totals, world, rank,
+                                             static_cast<uint8_t *>(send), L, static_cast<uint8_t *>(ws),
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int kmeanspp_shard_dist(const float *X, int64_t n, int64_t d, int n_trials, int first, const void *recv, int world,
+                        double *pot, void *ws, size_t ws_bytes, void *stream) {
+    if (!X || !recv || !aligned16(recv) || (!first && !pot) || (reinterpret_cast<uintptr_t>(pot) & 7u))
+        return KMEANS_ERR_INVALID_ARG;
+    if (world < 1 || world > 65536 || (first != 0 && first != 1)) return KMEANS_ERR_INVALID_ARG;
+    KppShardLayout L;
+    const int st = kpp_shard_check(X, n, d, n_trials, ws, ws_bytes, L);
+    if (st != KMEANS_OK) return st;
+    return cuda_status(launch_kpp_shard_dist(X, n, d, n_trials, first != 0, static_cast<const uint8_t *>(recv), world,
+                                             pot, L, static_cast<uint8_t *>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+int kmeanspp_shard_commit(int64_t n, int64_t d, int n_trials, int first, const double *pots, int world, int64_t c,
+                          int64_t *indices, float *centers, double *total, void *ws, size_t ws_bytes, void *stream) {
+    if (!indices || (!first && !pots) || (first != 0 && first != 1) || c < 0 || (first && c != 0))
+        return KMEANS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(indices) & 7u) || (reinterpret_cast<uintptr_t>(pots) & 7u) ||
+        (reinterpret_cast<uintptr_t>(total) & 7u) || (centers && !aligned4(centers)))
+        return KMEANS_ERR_INVALID_ARG;
+    if (world < 1 || world > 65536) return KMEANS_ERR_INVALID_ARG;
+    KppShardLayout L;
+    const int st = kpp_shard_check(nullptr, n, d, n_trials, ws, ws_bytes, L);
+    if (st != KMEANS_OK) return st;
+    return cuda_status(launch_kpp_shard_commit(n, d, n_trials, first != 0, pots, world, c, indices, centers, total, L,
+                                               static_cast<uint8_t *>(ws), static_cast<cudaStream_t>(stream)));
+}
+
 int kmeans_relocate_empty(int64_t *labels, const float *best_dist, int64_t n, int64_t k, void *ws, size_t ws_bytes,
                           void *stream) {
     if (!labels || !best_dist) return KMEANS_ERR_INVALID_ARG;
@@ -441,6 +576,7 @@ int kmeans_device_status(const void *ws, void *stream) {
     if (cudaMemcpy(&st, ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return KMEANS_ERR_CUDA;
     if (st & kFlagTimeout) return KMEANS_ERR_DEVICE_TIMEOUT;
     if (st & kFlagBadLabel) return KMEANS_ERR_DEVICE_LABEL;
+    if (st & kFlagExchange) return KMEANS_ERR_DEVICE_EXCHANGE;
     return KMEANS_OK;
 }
 
@@ -456,15 +592,18 @@ const char *kmeans_status_string(int status) {
         case KMEANS_ERR_SCRATCH_LIMIT:
             return "problem too large for the built-in scratch of kmeans_assign_noalloc "
                    "(use kmeans_assign with a workspace)";
+        case KMEANS_ERR_DEVICE_EXCHANGE: return "sharded k-means++: no rank's exchange block held a trial's candidate";
         default: return "unknown status";
     }
 }
 
 const char *kmeans_build_info(void) {
     return "kmeans_gb300 sm_103a: assign = tcgen05 cta_group::2 CTA pairs, 256x256 tile, bf16x3 split "
-           "(hi.hi and corrections in separate f32 accumulators), BK 32, X/C ring 4, split ring 6, "
-           "8 split warps; comparator = FFMA 128x128; update = LSD radix member list + compensated "
-           "segmented mean; k-means++ = Philox4x32-10 greedy D^2";
+           "(one double-buffered f32 accumulator up to d = 4096, separate hi.hi and correction accumulators "
+           "above), BK 32, X/C ring 4, split ring 6, 8 split warps; comparator = FFMA 128x128; update = "
+           "counting-scatter member list (k <= 32768; LSD radix above) + compensated segmented mean; "
+           "sharded update = per-rank sums reduced in rank order; k-means++ = Philox4x32-10 greedy D^2 "
+           "(single GPU or sharded steps)";
 }
 
 }  // extern "C"

@@ -87,6 +87,7 @@ inline int cached_per_device(std::atomic<int> (&cache)[kMaxDevices], Fn &&comput
 enum : uint32_t {
     kFlagTimeout = 1u,   // a pipeline wait ran out of time
     kFlagBadLabel = 2u,  // update saw a label outside [0, k)
+    kFlagExchange = 4u,  // sharded k-means++: no rank's exchange block owned a trial
 };
 
 struct WsHeader {
@@ -321,5 +322,30 @@ inline KppLayout kpp_layout(int64_t n, int64_t d, int T) {
     L.bytes = align_up(o, 1024);
     return L;
 }
+
+// k-means++ on one shard of the samples: the seeding's scratch for the
+// shard's rows (room for the largest trial count), then the current
+// candidates' rows and global indices, gathered from the ranks' exchange
+// blocks.
+struct KppShardLayout {
+    KppLayout K;
+    int64_t off_crow;   // kKppMaxTrials x d f32 candidate rows
+    int64_t off_cglob;  // kKppMaxTrials x i64 candidate global sample indices
+    int64_t bytes;
+};
+
+inline KppShardLayout kpp_shard_layout(int64_t n_local, int64_t d) {
+    KppShardLayout L{};
+    L.K = kpp_layout(n_local, d, kKppMaxTrials);
+    int64_t o = align_up(L.K.bytes, 1024);
+    L.off_crow = o; o += (int64_t)kKppMaxTrials * d * 4;
+    o = align_up(o, 1024); L.off_cglob = o; o += (int64_t)kKppMaxTrials * 8;
+    L.bytes = align_up(o, 1024);
+    return L;
+}
+
+// One rank's exchange block: T int64 indices, then T rows of d float32.
+inline int64_t kpp_exchange_idx_bytes(int T) { return align_up((int64_t)T * 8, 16); }
+inline int64_t kpp_exchange_bytes(int T, int64_t d) { return align_up(kpp_exchange_idx_bytes(T) + (int64_t)T * d * 4, 16); }
 
 }  // namespace km

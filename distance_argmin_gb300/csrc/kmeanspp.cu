@@ -79,29 +79,29 @@ __device__ __forceinline__ double warp_incl_scan(double v, int lane) {
     return v;
 }
 
-// The running sum at sample i is (sum of the block sums before its block) +
-// (the in-block prefix up to i); the block-sum prefix is the same for every
-// trial, so all trials see one consistent running sum.  One warp per trial,
-// each in a block of its own: the scans are float64, and this part's float64
-// pipe is narrow enough (about two FMAs per clock per SM) that eight trials
-// sharing one SM took 14 us.
-__global__ void __launch_bounds__(32)
-    kpp_pick_kernel(const double *__restrict__ bsum, int64_t n_blocks, const double *__restrict__ D2, int64_t n,
-                    uint64_t seed, uint64_t draw_base, int T, int64_t *__restrict__ cand) {
-    griddep_wait();
-    const int lane = threadIdx.x;
-    const int t = blockIdx.x;
-    if (t >= T) return;
-    // total of D^2
+// Total of D^2 from its block sums, in chunks of 32 (one warp; every lane
+// gets the same value).  The shard path computes its shard's total the same
+// way, so one shard sees the single-GPU total bit for bit.
+__device__ __forceinline__ double d2_total(const double *__restrict__ bsum, int64_t n_blocks, int lane) {
     double total = 0.0;
     for (int64_t b0 = 0; b0 < n_blocks; b0 += 32) {
         const double v = (b0 + lane < n_blocks) ? bsum[b0 + lane] : 0.0;
         const double incl = warp_incl_scan(v, lane);
         total += __shfl_sync(0xffffffffu, incl, 31);
     }
-    const double target = philox_uniform(seed, draw_base + (uint64_t)t) * total;
+    return total;
+}
+
+// The D^2 draw (one warp): the first sample i whose running sum base + D2[0]
+// + ... + D2[i] exceeds `target`, or n - 1 when none does.  The running sum
+// at sample i is base + (sum of the block sums before its block) + (the
+// in-block prefix up to i); the block-sum prefix is the same for every
+// trial, so all trials see one consistent running sum.  `base` is 0 on one
+// GPU and the sum of the earlier shards' totals on a shard.  Lane-uniform.
+__device__ int64_t d2_search(const double *__restrict__ bsum, int64_t n_blocks, const double *__restrict__ D2,
+                             int64_t n, double target, double base, int lane) {
     // first block whose inclusive prefix exceeds the target
-    double before = 0.0;  // sum of block sums before the current chunk
+    double before = base;  // running sum before the current chunk of blocks
     int64_t blk = -1;
     double blk_before = 0.0;
     for (int64_t b0 = 0; b0 < n_blocks && blk < 0; b0 += 32) {
@@ -150,6 +150,22 @@ __global__ void __launch_bounds__(32)
         }
         run = __shfl_sync(0xffffffffu, incl, 31);
     }
+    return pick;
+}
+
+// One warp per trial, each in a block of its own: the scans are float64, and
+// this part's float64 pipe is narrow enough (about two FMAs per clock per SM)
+// that eight trials sharing one SM took 14 us.
+__global__ void __launch_bounds__(32)
+    kpp_pick_kernel(const double *__restrict__ bsum, int64_t n_blocks, const double *__restrict__ D2, int64_t n,
+                    uint64_t seed, uint64_t draw_base, int T, int64_t *__restrict__ cand) {
+    griddep_wait();
+    const int lane = threadIdx.x;
+    const int t = blockIdx.x;
+    if (t >= T) return;
+    const double total = d2_total(bsum, n_blocks, lane);
+    const double target = philox_uniform(seed, draw_base + (uint64_t)t) * total;
+    const int64_t pick = d2_search(bsum, n_blocks, D2, n, target, 0.0, lane);
     if (lane == 0) cand[t] = pick;
 }
 
@@ -223,6 +239,8 @@ __device__ __forceinline__ void load4x2(const float *__restrict__ p, int avail, 
 
 // Partial distances over one feature slice (blockIdx.y) to trials
 // [t0, t0 + nt): dpart[slice][t][i] = sum over the slice of (x_if - cand_tf)^2.
+// The candidates are the rows cand[] of X, or the rows of `crows` when it is
+// given (the shard path, whose candidates may live on other GPUs).
 // The block stages its slice of the candidates (negated) in shared memory once
 // and then streams its share of the samples, each sample read exactly once.
 // Differences and squares use the packed two-float instructions; each run of
@@ -231,8 +249,8 @@ __device__ __forceinline__ void load4x2(const float *__restrict__ p, int avail, 
 // 4096-feature slice); lanes and slices are combined in double-float.
 template <bool VEC>
 __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
-    kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand, int T,
-                         int t0, int W, float2 *__restrict__ dpart) {
+    kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand,
+                         const float *__restrict__ crows, int T, int t0, int W, float2 *__restrict__ dpart) {
     griddep_wait();
     extern __shared__ __align__(16) float cs[];  // [KT][W], negated
     const int lane = threadIdx.x & 31;
@@ -244,7 +262,9 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     for (int e = threadIdx.x; e < kd::KT * W; e += kd::THREADS) {
         const int t = e / W, f = e - t * W;
         float v = 0.f;
-        if (t < nt && f < width) v = -__ldg(X + cand[t0 + t] * (int64_t)d + fb + f);
+        // the candidates are rows of X, or (a shard) rows of the exchange buffer
+        if (t < nt && f < width)
+            v = -__ldg((crows ? crows + (int64_t)(t0 + t) * d : X + cand[t0 + t] * (int64_t)d) + fb + f);
         cs[e] = v;
     }
     __syncthreads();
@@ -385,16 +405,24 @@ __global__ void __launch_bounds__(kBsThreads)
 
 // The winning trial of the previous center: lowest total potential (lowest
 // trial on ties), every block computing the same sums in the same order.
+// Potential of trial t (one warp, every lane gets it): its block
+// potentials summed lane-strided, then a butterfly.
+__device__ __forceinline__ double trial_potential(const double *__restrict__ bpot, int t, int64_t n_blocks,
+                                                  int lane) {
+    double v = 0.0;
+    for (int64_t b = lane; b < n_blocks; b += 32) v += bpot[(int64_t)t * n_blocks + b];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
 __device__ int select_best_trial(const double *__restrict__ bpot, int T, int64_t n_blocks) {
     __shared__ int best_s;
     __shared__ double pot_s[kKppMaxTrials];
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     for (int t = w; t < T; t += blockDim.x / 32) {
-        double v = 0.0;
-        for (int64_t b = lane; b < n_blocks; b += 32) v += bpot[(int64_t)t * n_blocks + b];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        const double v = trial_potential(bpot, t, n_blocks, lane);
         if (lane == 0) pot_s[t] = v;
     }
     __syncthreads();
@@ -460,16 +488,16 @@ __global__ void gather_rows_kernel(const float *__restrict__ X, const int64_t *_
     }
 }
 
-cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int T, uint64_t seed, float *centers,
-                            int64_t *indices, const KppLayout &L, uint8_t *ws, cudaStream_t s) {
-    WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
-    double *D2 = reinterpret_cast<double *>(ws + L.off_d2);
+// One pass over X for the candidates of trials [0, Tn): the per-slice
+// partial distances, then their combination (with D2: and the block
+// potentials).  Candidates: rows cand[] of X, or the rows of `crows`.
+static cudaError_t kpp_dist_pass(const float *X, int64_t n, int64_t d, const KppLayout &L, uint8_t *ws, int Tn,
+                                 const int64_t *cand, const float *crows, const double *d2, bool chained_first,
+                                 cudaStream_t s) {
     double *dist = reinterpret_cast<double *>(ws + L.off_dist);
     float2 *dpart = reinterpret_cast<float2 *>(ws + L.off_dpart);
-    double *bsum = reinterpret_cast<double *>(ws + L.off_bsum);
     double *bpot = reinterpret_cast<double *>(ws + L.off_bpot);
-    int64_t *cand = reinterpret_cast<int64_t *>(ws + L.off_cand);
-    const bool vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(X) & 15) == 0;
+    const bool vec = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(crows)) & 15) == 0;
     const size_t smem = (size_t)kd::KT * L.W * sizeof(float);
     {
         static std::once_flag attr_once[kMaxDevices];
@@ -480,14 +508,43 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
                                  (int)(kd::KT * kKppSliceFloats * sizeof(float)));
         });
     }
-    int sms = 0, dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    static std::atomic<int> sm_cache[kMaxDevices];
+    const int sms = cached_per_device(sm_cache, [] {
+        int v = 0, dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        return v > 0 ? v : 1;
+    });
     const int64_t groups = (n + kd::GROUP - 1) / kd::GROUP;
     // one resident block per SM over all slices
-    int64_t gx = (kd::MIN_BLOCKS * (int64_t)(sms > 0 ? sms : 1) + L.S - 1) / L.S;
+    int64_t gx = (kd::MIN_BLOCKS * (int64_t)sms + L.S - 1) / L.S;
     if (gx > groups) gx = groups;
     const dim3 dgrid((unsigned)(gx < 1 ? 1 : gx), (unsigned)L.S);
+    cudaError_t e = cudaSuccess;
+    for (int t0 = 0; t0 < Tn && e == cudaSuccess; t0 += kd::KT) {
+        const bool chained = chained_first || t0 > 0;
+        trace_mark(kTraceKppDist, false, s);
+        e = vec ? launch_kernel(chained, kpp_dist_part_kernel<true>, dgrid, dim3(kd::THREADS), smem, s, X, n, (int)d,
+                                cand, crows, Tn, t0, L.W, dpart)
+                : launch_kernel(chained, kpp_dist_part_kernel<false>, dgrid, dim3(kd::THREADS), smem, s, X, n, (int)d,
+                                cand, crows, Tn, t0, L.W, dpart);
+        trace_mark(kTraceKppDist, true, s);
+        const int nt = Tn - t0 < kd::KT ? Tn - t0 : kd::KT;
+        if (e == cudaSuccess)
+            e = launch_kernel(true, kpp_combine_kernel, dim3((unsigned)L.n_blocks, (unsigned)nt), dim3(kBsThreads), 0,
+                              s, (const float2 *)dpart, L.S, n, t0, d2, dist, bpot, L.n_blocks);
+    }
+    return e;
+}
+
+cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int T, uint64_t seed, float *centers,
+                            int64_t *indices, const KppLayout &L, uint8_t *ws, cudaStream_t s) {
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+    double *D2 = reinterpret_cast<double *>(ws + L.off_d2);
+    double *dist = reinterpret_cast<double *>(ws + L.off_dist);
+    double *bsum = reinterpret_cast<double *>(ws + L.off_bsum);
+    double *bpot = reinterpret_cast<double *>(ws + L.off_bpot);
+    int64_t *cand = reinterpret_cast<int64_t *>(ws + L.off_cand);
 
     // every kernel after the first is chained to the one before it (see
     // launch_kernel); each waits for its predecessor before touching memory
@@ -495,30 +552,18 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
     auto chain = [&](cudaError_t r) {
         if (e == cudaSuccess) e = r;
     };
-    auto dist_pass = [&](int Tn, const double *d2) {
-        for (int t0 = 0; t0 < Tn; t0 += kd::KT) {
-            trace_mark(kTraceKppDist, false, s);
-            chain(vec ? launch_kernel(true, kpp_dist_part_kernel<true>, dgrid, dim3(kd::THREADS), smem, s, X, n,
-                                      (int)d, (const int64_t *)cand, Tn, t0, L.W, dpart)
-                      : launch_kernel(true, kpp_dist_part_kernel<false>, dgrid, dim3(kd::THREADS), smem, s, X, n,
-                                      (int)d, (const int64_t *)cand, Tn, t0, L.W, dpart));
-            trace_mark(kTraceKppDist, true, s);
-            const int nt = Tn - t0 < kd::KT ? Tn - t0 : kd::KT;
-            chain(launch_kernel(true, kpp_combine_kernel, dim3((unsigned)L.n_blocks, (unsigned)nt), dim3(kBsThreads), 0,
-                                s, (const float2 *)dpart, L.S, n, t0, d2, dist, bpot, L.n_blocks));
-        }
-    };
 
     kpp_first_kernel<<<1, 1, 0, s>>>(n, seed, cand, indices, hdr);
     chain(cudaGetLastError());
-    dist_pass(1, nullptr);  // distances to the first center
+    // distances to the first center
+    if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, 1, cand, nullptr, nullptr, true, s));
     for (int64_t c = 1; c < k && e == cudaSuccess; ++c) {
         chain(launch_kernel(true, kpp_update_kernel, dim3((unsigned)L.n_blocks), dim3(kBsThreads), 0, s,
                             (const double *)dist, (const double *)bpot, T, n, L.n_blocks, (const int64_t *)cand, indices,
                             c - 1, c == 1 ? 1 : 0, D2, bsum));
         chain(launch_kernel(true, kpp_pick_kernel, dim3((unsigned)T), dim3(32), 0, s, (const double *)bsum, L.n_blocks,
                             (const double *)D2, n, seed, 1 + (uint64_t)(c - 1) * (uint64_t)T, T, cand));
-        dist_pass(T, D2);
+        if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, T, cand, nullptr, D2, true, s));
     }
     if (k > 1)
         chain(launch_kernel(true, kpp_select_last_kernel, dim3(1), dim3(256), 0, s, (const double *)bpot, T,
@@ -529,6 +574,227 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
                             centers));
     }
     return e;
+}
+
+// ------------------------------------------------------------- shard path
+// Greedy k-means++ over samples split by rows across ranks.  Each rank holds
+// its shard's D^2 and calls the steps below in turn; between them the caller
+// all-gathers small buffers (candidate blocks, potentials, shard totals).
+// Every rank makes the same decisions from the same gathered values, summed
+// in rank order.  Exchange block of one rank: T int64 global sample indices
+// (-1: the trial's candidate is not in this shard), then T rows of d
+// float32 (the candidates this shard owns).
+
+__global__ void kpp_shard_first_kernel(const float *__restrict__ X, int64_t n_local, int d, int64_t row_offset,
+                                       int64_t n_global, uint64_t seed, int T, uint8_t *__restrict__ send,
+                                       int64_t idx_bytes, WsHeader *hdr) {
+    if (threadIdx.x == 0) {
+        hdr->status = 0u;
+        hdr->done_blocks = 0u;
+    }
+    const double u = philox_uniform(seed, 0);
+    int64_t g = static_cast<int64_t>(u * static_cast<double>(n_global));  // u >= 0: truncation is floor
+    if (g > n_global - 1) g = n_global - 1;
+    const int64_t loc = g - row_offset;
+    const bool mine = loc >= 0 && loc < n_local;
+    int64_t *idx = reinterpret_cast<int64_t *>(send);
+    float *rows = reinterpret_cast<float *>(send + idx_bytes);
+    for (int t = threadIdx.x; t < T; t += blockDim.x) idx[t] = (t == 0 && mine) ? g : -1;
+    if (mine)
+        for (int f = threadIdx.x; f < d; f += blockDim.x) rows[f] = X[loc * (int64_t)d + f];
+}
+
+// Trial t's candidate comes from the first rank whose block owns it (exactly
+// one does; none sets the exchange flag and leaves a zero row).
+__global__ void kpp_shard_gather_kernel(const uint8_t *__restrict__ recv, int world, int64_t blk_bytes,
+                                        int64_t idx_bytes, int d, float *__restrict__ crow,
+                                        int64_t *__restrict__ cglob, uint32_t *status) {
+    __shared__ int owner_s;
+    const int t = blockIdx.x;
+    if (threadIdx.x == 0) {
+        int owner = -1;
+        int64_t g = -1;
+        for (int r = 0; r < world && owner < 0; ++r) {
+            const int64_t v = reinterpret_cast<const int64_t *>(recv + (int64_t)r * blk_bytes)[t];
+            if (v >= 0) {
+                owner = r;
+                g = v;
+            }
+        }
+        if (owner < 0) flag_error(status, kFlagExchange);
+        cglob[t] = g;
+        owner_s = owner;
+    }
+    __syncthreads();
+    const int owner = owner_s;
+    const float *src = owner < 0 ? nullptr
+                                 : reinterpret_cast<const float *>(recv + (int64_t)owner * blk_bytes + idx_bytes) +
+                                       (int64_t)t * d;
+    for (int f = threadIdx.x; f < d; f += blockDim.x) crow[(int64_t)t * d + f] = src ? src[f] : 0.f;
+}
+
+// This shard's potential of every trial (the same sums as one GPU's choice).
+__global__ void kpp_shard_potentials_kernel(const double *__restrict__ bpot, int T, int64_t n_blocks,
+                                            double *__restrict__ pot_out) {
+    griddep_wait();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int t = w; t < T; t += blockDim.x / 32) {
+        const double v = trial_potential(bpot, t, n_blocks, lane);
+        if (lane == 0) pot_out[t] = v;
+    }
+}
+
+// The winner of center c: the trial whose potential, summed over the ranks
+// in rank order, is lowest (lowest trial on ties; trial 0 for the first
+// center).  indices[c] and centers[c] take its global index and row; D^2 is
+// lowered by its distances and the shard's block sums rewritten.
+__global__ void __launch_bounds__(kBsThreads)
+    kpp_shard_commit_kernel(const double *__restrict__ dist, const double *__restrict__ recv_pot, int world, int T,
+                            int first, int64_t n, const int64_t *__restrict__ cglob, const float *__restrict__ crow,
+                            int d, int64_t c, int64_t *__restrict__ indices, float *__restrict__ centers,
+                            double *__restrict__ D2, double *__restrict__ bsum, int64_t n_blocks) {
+    griddep_wait();
+    __shared__ double red[kBsThreads];
+    __shared__ int best_s;
+    if (threadIdx.x == 0) {
+        int best = 0;
+        if (!first) {
+            double bp = 0.0;
+            for (int t = 0; t < T; ++t) {
+                double p = recv_pot[t];
+                for (int r = 1; r < world; ++r) p += recv_pot[(int64_t)r * T + t];
+                if (t == 0 || p < bp) {
+                    bp = p;
+                    best = t;
+                }
+            }
+        }
+        best_s = best;
+    }
+    __syncthreads();
+    const int best = best_s;
+    if (blockIdx.x == 0) {
+        if (threadIdx.x == 0) indices[c] = cglob[best];
+        if (centers)
+            for (int f = threadIdx.x; f < d; f += kBsThreads)
+                centers[c * (int64_t)d + f] = crow[(int64_t)best * d + f];
+    }
+    if (blockIdx.x >= n_blocks) return;
+    const double *db = dist + (int64_t)best * n;
+    const int64_t base = (int64_t)blockIdx.x * kKppScanBlock;
+    double sum = 0.0;
+#pragma unroll
+    for (int q = 0; q < kKppScanBlock / kBsThreads; ++q) {
+        const int64_t i = base + threadIdx.x + (int64_t)q * kBsThreads;
+        if (i < n) {
+            const double v = db[i];
+            const double nd = first ? v : fmin(D2[i], v);
+            D2[i] = nd;
+            sum += nd;
+        }
+    }
+    red[threadIdx.x] = sum;
+    __syncthreads();
+    for (int w = kBsThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) bsum[blockIdx.x] = red[0];
+}
+
+__global__ void kpp_shard_total_kernel(const double *__restrict__ bsum, int64_t n_blocks, double *__restrict__ out) {
+    griddep_wait();
+    const double t = d2_total(bsum, n_blocks, threadIdx.x);
+    if (threadIdx.x == 0) *out = t;
+}
+
+// The draws of center c on a shard (one warp per trial).  From the ranks'
+// totals, in rank order: the global sum S, target = u * S, and the owner,
+// the first rank whose running total exceeds the target (the last rank's
+// last sample when none does, as on one GPU).  The owner searches its shard
+// with the earlier ranks' total as the running sum's start and fills its
+// exchange slot; the other ranks mark the slot -1.
+__global__ void __launch_bounds__(32)
+    kpp_shard_pick_kernel(const double *__restrict__ bsum, int64_t n_blocks, const double *__restrict__ D2,
+                          int64_t n_local, const float *__restrict__ X, int d, int64_t row_offset, uint64_t seed,
+                          uint64_t draw_base, int T, const double *__restrict__ totals, int world, int rank,
+                          uint8_t *__restrict__ send, int64_t idx_bytes) {
+    const int lane = threadIdx.x;
+    const int t = blockIdx.x;
+    if (t >= T) return;
+    double S = totals[0];
+    for (int r = 1; r < world; ++r) S += totals[r];
+    const double target = philox_uniform(seed, draw_base + (uint64_t)t) * S;
+    int owner = world - 1;
+    bool clip = true;
+    double base = 0.0, run = 0.0;
+    for (int r = 0; r < world; ++r) {
+        const double next = r == 0 ? totals[0] : run + totals[r];
+        if (next > target) {
+            owner = r;
+            base = run;
+            clip = false;
+            break;
+        }
+        run = next;
+    }
+    int64_t *idx = reinterpret_cast<int64_t *>(send);
+    if (owner != rank) {
+        if (lane == 0) idx[t] = -1;
+        return;
+    }
+    const int64_t pick = clip ? n_local - 1 : d2_search(bsum, n_blocks, D2, n_local, target, base, lane);
+    if (lane == 0) idx[t] = row_offset + pick;
+    float *row = reinterpret_cast<float *>(send + idx_bytes) + (int64_t)t * d;
+    for (int f = lane; f < d; f += 32) row[f] = X[pick * (int64_t)d + f];
+}
+
+cudaError_t launch_kpp_shard_first(const float *X, int64_t n_local, int64_t d, int64_t row_offset, int64_t n_global,
+                                   int T, uint64_t seed, uint8_t *send, uint8_t *ws, cudaStream_t s) {
+    kpp_shard_first_kernel<<<1, 256, 0, s>>>(X, n_local, (int)d, row_offset, n_global, seed, T, send,
+                                             kpp_exchange_idx_bytes(T), reinterpret_cast<WsHeader *>(ws));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kpp_shard_dist(const float *X, int64_t n_local, int64_t d, int T, bool first, const uint8_t *recv,
+                                  int world, double *pot_out, const KppShardLayout &L, uint8_t *ws, cudaStream_t s) {
+    const int Tn = first ? 1 : T;
+    float *crow = reinterpret_cast<float *>(ws + L.off_crow);
+    int64_t *cglob = reinterpret_cast<int64_t *>(ws + L.off_cglob);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+    kpp_shard_gather_kernel<<<Tn, 256, 0, s>>>(recv, world, kpp_exchange_bytes(T, d), kpp_exchange_idx_bytes(T),
+                                               (int)d, crow, cglob, &hdr->status);
+    cudaError_t e = cudaGetLastError();
+    const double *D2 = first ? nullptr : reinterpret_cast<const double *>(ws + L.K.off_d2);
+    if (e == cudaSuccess) e = kpp_dist_pass(X, n_local, d, L.K, ws, Tn, nullptr, crow, D2, true, s);
+    if (e == cudaSuccess && !first)
+        e = launch_kernel(true, kpp_shard_potentials_kernel, dim3(1), dim3(256), 0, s,
+                          (const double *)(ws + L.K.off_bpot), T, L.K.n_blocks, pot_out);
+    return e;
+}
+
+cudaError_t launch_kpp_shard_commit(int64_t n_local, int64_t d, int T, bool first, const double *recv_pot, int world,
+                                    int64_t c, int64_t *indices, float *centers, double *total_out,
+                                    const KppShardLayout &L, uint8_t *ws, cudaStream_t s) {
+    double *bsum = reinterpret_cast<double *>(ws + L.K.off_bsum);
+    cudaError_t e = launch_kernel(false, kpp_shard_commit_kernel, dim3((unsigned)L.K.n_blocks), dim3(kBsThreads), 0, s,
+                                  (const double *)(ws + L.K.off_dist), recv_pot, world, T, first ? 1 : 0, n_local,
+                                  (const int64_t *)(ws + L.off_cglob), (const float *)(ws + L.off_crow), (int)d, c,
+                                  indices, centers, reinterpret_cast<double *>(ws + L.K.off_d2), bsum, L.K.n_blocks);
+    if (e == cudaSuccess && total_out)
+        e = launch_kernel(true, kpp_shard_total_kernel, dim3(1), dim3(32), 0, s, (const double *)bsum, L.K.n_blocks,
+                          total_out);
+    return e;
+}
+
+cudaError_t launch_kpp_shard_pick(const float *X, int64_t n_local, int64_t d, int64_t row_offset, int T, uint64_t seed,
+                                  int64_t c, const double *totals, int world, int rank, uint8_t *send,
+                                  const KppShardLayout &L, uint8_t *ws, cudaStream_t s) {
+    kpp_shard_pick_kernel<<<T, 32, 0, s>>>(reinterpret_cast<const double *>(ws + L.K.off_bsum), L.K.n_blocks,
+                                           reinterpret_cast<const double *>(ws + L.K.off_d2), n_local, X, (int)d,
+                                           row_offset, seed, 1 + (uint64_t)(c - 1) * (uint64_t)T, T, totals, world,
+                                           rank, send, kpp_exchange_idx_bytes(T));
+    return cudaGetLastError();
 }
 
 }  // namespace km

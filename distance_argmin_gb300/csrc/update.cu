@@ -3,10 +3,17 @@
 // its members).  No (n, k) one-hot matrix: the labels are sorted into a member
 // list and each centroid's members are summed as one contiguous segment.
 //
-//   1. count members per cluster and clear the digit histograms
-//   2. stable LSD radix sort of (label, sample index), 8-bit digits
-//      (ceil(bits(k-1) / 8) passes: hist -> scan -> stable scatter)
-//   3. exclusive scan of the counts -> segment offsets
+// The member list, for k <= 32768 (the counting path):
+//   1. per-cluster member counts of 256 fixed sample tiles (in a Lloyd
+//      iteration the finalize of the assignment does this)
+//   2. per-cluster prefixes over the tiles and the exclusive scan of the
+//      totals -> segment offsets
+//   3. one warp per tile scatters its samples in index order -> a stable
+//      member list ordered by (label, sample index)
+// For larger k: a stable LSD radix sort of (label, sample index) with 8-bit
+// digits (ceil(bits(k-1) / 8) passes: hist -> scan -> stable scatter), then
+// the exclusive scan of the counts.
+// Then, on both paths:
 //   4. segmented sum over fixed chunks of the member list: a CTA owns one
 //      chunk x one 512-column slice, sums each segment in member order with
 //      compensated float32 additions and writes the mean when the segment is
@@ -14,6 +21,11 @@
 //   5. fix-up: segments that crossed chunks add their partials in chunk order;
 //      empty clusters keep their old row bit for bit
 // Every step has a fixed order, so C_new is bitwise reproducible.
+//
+// The same kernels also serve a shard of the samples (the sample-sharded
+// iteration): in sums mode steps 4 and 5 write each cluster's unnormalised
+// sum, and zeros for an empty cluster, and reduce_partials_kernel later adds
+// the shards' sums in rank order and divides.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -421,7 +433,8 @@ constexpr int kMeanThreads = 128;
 
 // One CTA = one chunk of the member list x one slice of columns.
 // VEC: 4 columns per thread with 16-byte loads (d % 4 == 0, X aligned).
-template <bool VEC>
+// MEAN: a segment inside the chunk writes its mean; otherwise its sum.
+template <bool VEC, bool MEAN>
 __global__ void __launch_bounds__(kMeanThreads)
     segmented_mean_kernel(const float *__restrict__ X, const int32_t *__restrict__ perm,
                           const uint32_t *__restrict__ sorted_labels, const int32_t *__restrict__ offsets,
@@ -512,7 +525,7 @@ __global__ void __launch_bounds__(kMeanThreads)
             dst = tail + (size_t)c * d + col;
             if (tailc && blockIdx.y == 0 && threadIdx.x == 0) tailc[c] = (int32_t)j;
         }
-        if (mean) {
+        if (MEAN && mean) {
             const float cnt = (float)(seg1 - seg0);
             if (VEC) *reinterpret_cast<float4 *>(dst) = make_float4(tot.x / cnt, tot.y / cnt, tot.z / cnt, tot.w / cnt);
             else *dst = tot.x / cnt;
@@ -525,17 +538,21 @@ __global__ void __launch_bounds__(kMeanThreads)
 }
 
 // Segments that crossed chunk boundaries, empty clusters, and the counts.
+// With `mean` 0 (sums mode) crossing segments write their sum and empty
+// clusters zeros.
 __global__ void __launch_bounds__(kMeanThreads)
     mean_fixup_kernel(const int32_t *__restrict__ offsets, const float *__restrict__ head,
                       const float *__restrict__ tail, const float *__restrict__ C_old, float *__restrict__ C_new,
-                      int32_t *__restrict__ counts_out, int k, int d, int chunk) {
+                      int32_t *__restrict__ counts_out, int k, int d, int chunk, int mean) {
     for (int j = blockIdx.x; j < k; j += gridDim.x) {
         const int seg0 = offsets[j];
         const int seg1 = offsets[j + 1];
         const int cnt = seg1 - seg0;
         if (counts_out && threadIdx.x == 0) counts_out[j] = cnt;
         if (cnt == 0) {
-            if (C_new != C_old)
+            if (!mean)
+                for (int f = threadIdx.x; f < d; f += kMeanThreads) C_new[(size_t)j * d + f] = 0.f;
+            else if (C_new != C_old)
                 for (int f = threadIdx.x; f < d; f += kMeanThreads) C_new[(size_t)j * d + f] = C_old[(size_t)j * d + f];
             continue;
         }
@@ -551,7 +568,7 @@ __global__ void __launch_bounds__(kMeanThreads)
                 cmp = (t - s) - y;
                 s = t;
             }
-            C_new[(size_t)j * d + f] = (s - cmp) / (float)cnt;
+            C_new[(size_t)j * d + f] = mean ? (s - cmp) / (float)cnt : s - cmp;
         }
     }
 }
@@ -564,7 +581,7 @@ __global__ void __launch_bounds__(kMeanThreads)
 constexpr int kFixThreads = 256;
 constexpr int kFixUnroll = 4;
 
-template <bool VEC>
+template <bool VEC, bool MEAN>
 __global__ void __launch_bounds__(kFixThreads)
     mean_fixup_chunks_kernel(const int32_t *__restrict__ offsets, const int32_t *__restrict__ totals,
                              const float *__restrict__ head, const float *__restrict__ tail,
@@ -624,7 +641,7 @@ __global__ void __launch_bounds__(kFixThreads)
                 V r;
                 float *rf = reinterpret_cast<float *>(&r);
 #pragma unroll
-                for (int e = 0; e < W; ++e) rf[e] = (s[u][e] - cmp[u][e]) / cnt;
+                for (int e = 0; e < W; ++e) rf[e] = MEAN ? (s[u][e] - cmp[u][e]) / cnt : s[u][e] - cmp[u][e];
                 out[g] = r;
             }
         }
@@ -632,7 +649,9 @@ __global__ void __launch_bounds__(kFixThreads)
     for (int j = blockIdx.x; j < k; j += gridDim.x) {
         const int cnt = totals[j];
         if (counts_out && threadIdx.x == 0) counts_out[j] = cnt;
-        if (cnt == 0 && C_new != C_old)
+        if (cnt == 0 && !MEAN)
+            for (int f = threadIdx.x; f < d; f += kFixThreads) C_new[(size_t)j * d + f] = 0.f;
+        else if (cnt == 0 && C_new != C_old)
             for (int f = threadIdx.x; f < d; f += kFixThreads) C_new[(size_t)j * d + f] = C_old[(size_t)j * d + f];
     }
 }
@@ -670,6 +689,76 @@ cudaError_t launch_fused_mean(const float *sums, const int32_t *cnt, const float
                          reinterpret_cast<const float4 *>(sums), cnt, C_old, C_new, counts_out, (int)k, (int)(d / 4));
 }
 
+// The sample-sharded iteration's reduction of one slice of centroid rows:
+// every rank's partial sum of row j, added in rank order in float64 (the
+// first rank's value taken as it is, so one rank gives the same bits as the
+// single-GPU mean), divided once by the summed count and rounded to float32;
+// the old row when no rank has a member.  The inertia is the rank-order sum
+// of the ranks' inertias.
+template <bool VEC>
+__global__ void __launch_bounds__(256)
+    reduce_partials_kernel(const float *__restrict__ parts, const int32_t *__restrict__ pcounts,
+                           const double *__restrict__ pinertia, int world, int64_t rows, int d,
+                           const float *__restrict__ C_old, float *__restrict__ C_new,
+                           int32_t *__restrict__ counts_out, double *__restrict__ inertia_out) {
+    using V = typename std::conditional<VEC, float4, float>::type;
+    constexpr int W = VEC ? 4 : 1;
+    const int64_t dv = d / W;
+    const int64_t total = rows * dv;
+    const int64_t plane = rows * (int64_t)d;  // floats per rank
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < total;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t j = g / dv;
+        const int64_t off = j * d + (g - j * dv) * W;
+        int64_t cnt = 0;
+        for (int r = 0; r < world; ++r) cnt += pcounts[(int64_t)r * rows + j];
+        if (cnt == 0) {
+            *reinterpret_cast<V *>(C_new + off) = *reinterpret_cast<const V *>(C_old + off);
+        } else if constexpr (VEC) {
+            float4 v = *reinterpret_cast<const float4 *>(parts + off);
+            double a0 = v.x, a1 = v.y, a2 = v.z, a3 = v.w;
+            for (int r = 1; r < world; ++r) {
+                v = *reinterpret_cast<const float4 *>(parts + (int64_t)r * plane + off);
+                a0 += v.x;
+                a1 += v.y;
+                a2 += v.z;
+                a3 += v.w;
+            }
+            const double c = (double)cnt;
+            *reinterpret_cast<float4 *>(C_new + off) =
+                make_float4((float)(a0 / c), (float)(a1 / c), (float)(a2 / c), (float)(a3 / c));
+        } else {
+            double a = parts[off];
+            for (int r = 1; r < world; ++r) a += parts[(int64_t)r * plane + off];
+            C_new[off] = (float)(a / (double)cnt);
+        }
+        if (counts_out && off == j * d) counts_out[j] = (int32_t)cnt;
+    }
+    if (inertia_out && blockIdx.x == 0 && threadIdx.x == 0) {
+        double acc = pinertia[0];
+        for (int r = 1; r < world; ++r) acc += pinertia[r];
+        *inertia_out = acc;
+    }
+}
+
+cudaError_t launch_reduce_partials(const float *parts, const int32_t *part_counts, const double *part_inertia,
+                                   int world, int64_t rows, int64_t d, const float *C_old, float *C_new,
+                                   int32_t *counts_out, double *inertia_out, cudaStream_t s) {
+    const bool vec = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(parts) | reinterpret_cast<uintptr_t>(C_old) |
+                                       reinterpret_cast<uintptr_t>(C_new)) & 15) == 0;
+    const int64_t total = rows * (vec ? d / 4 : d);
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    if (vec)
+        reduce_partials_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(parts, part_counts, part_inertia, world, rows,
+                                                                      (int)d, C_old, C_new, counts_out, inertia_out);
+    else
+        reduce_partials_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(parts, part_counts, part_inertia, world, rows,
+                                                                       (int)d, C_old, C_new, counts_out, inertia_out);
+    return cudaGetLastError();
+}
+
 // Per device, once: allow the per-cluster shared-memory counters of the
 // counting path above the 48 KiB default.
 static void set_counting_smem_limits(int64_t k) {
@@ -694,7 +783,7 @@ static int radix_passes(int64_t k) {
 
 cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_old, float *C_new,
                           int32_t *counts_out, int64_t n, int64_t k, int64_t d, const UpdateLayout &L,
-                          uint8_t *ws, bool clear_header, cudaStream_t s, bool tile_counts_ready) {
+                          uint8_t *ws, bool clear_header, cudaStream_t s, bool tile_counts_ready, bool sums_only) {
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
     int32_t *counts = reinterpret_cast<int32_t *>(ws + L.off_counts);
     int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.off_offsets);
@@ -711,6 +800,13 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
     const int cols_per_cta = kMeanThreads * (vec ? 4 : 1);
     const dim3 mgrid((unsigned)L.n_chunks, (unsigned)((d + cols_per_cta - 1) / cols_per_cta));
     const size_t msmem = (size_t)L.chunk * 8;
+    // sums mode (a shard of the samples): sums instead of means, zeros for an
+    // empty cluster
+    const bool mean = !sums_only;
+    auto *mean_k = vec ? (mean ? segmented_mean_kernel<true, true> : segmented_mean_kernel<true, false>)
+                       : (mean ? segmented_mean_kernel<false, true> : segmented_mean_kernel<false, false>);
+    auto *fix_k = vec ? (mean ? mean_fixup_chunks_kernel<true, true> : mean_fixup_chunks_kernel<true, false>)
+                      : (mean ? mean_fixup_chunks_kernel<false, true> : mean_fixup_chunks_kernel<false, false>);
 
     if (L.counting) {
         int32_t *table = reinterpret_cast<int32_t *>(ws + L.off_table);
@@ -733,23 +829,16 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
                               (int)L.utile, (const int32_t *)table, (const int32_t *)offsets, perm, slab, status);
         trace_mark(kTraceUpdateMean, false, s);
         if (e == cudaSuccess)
-            e = vec ? launch_kernel(true, segmented_mean_kernel<true>, mgrid, dim3(kMeanThreads), msmem, s, X,
-                                    (const int32_t *)perm, (const uint32_t *)slab, (const int32_t *)offsets, (int)n,
-                                    (int)d, (int)L.chunk, C_new, head, tail, tailc)
-                    : launch_kernel(true, segmented_mean_kernel<false>, mgrid, dim3(kMeanThreads), msmem, s, X,
-                                    (const int32_t *)perm, (const uint32_t *)slab, (const int32_t *)offsets, (int)n,
-                                    (int)d, (int)L.chunk, C_new, head, tail, tailc);
+            e = launch_kernel(true, mean_k, mgrid, dim3(kMeanThreads), msmem, s, X, (const int32_t *)perm,
+                              (const uint32_t *)slab, (const int32_t *)offsets, (int)n, (int)d, (int)L.chunk, C_new,
+                              head, tail, tailc);
         trace_mark(kTraceUpdateMean, true, s);
         const int fgrid = (int)(L.n_chunks > 256 ? L.n_chunks : 256);
         if (e == cudaSuccess)
-            e = vec ? launch_kernel(true, mean_fixup_chunks_kernel<true>, dim3(fgrid), dim3(kFixThreads), 0, s,
-                                    (const int32_t *)offsets, (const int32_t *)counts, (const float *)head,
-                                    (const float *)tail, (const int32_t *)tailc, (int)L.n_chunks, C_old, C_new,
-                                    counts_out, (int)k, (int)d, (int)L.chunk)
-                    : launch_kernel(true, mean_fixup_chunks_kernel<false>, dim3(fgrid), dim3(kFixThreads), 0, s,
-                                    (const int32_t *)offsets, (const int32_t *)counts, (const float *)head,
-                                    (const float *)tail, (const int32_t *)tailc, (int)L.n_chunks, C_old, C_new,
-                                    counts_out, (int)k, (int)d, (int)L.chunk);
+            e = launch_kernel(true, fix_k, dim3(fgrid), dim3(kFixThreads), 0, s, (const int32_t *)offsets,
+                              (const int32_t *)counts, (const float *)head, (const float *)tail,
+                              (const int32_t *)tailc, (int)L.n_chunks, C_old, C_new, counts_out, (int)k, (int)d,
+                              (int)L.chunk);
         return e;
     }
 
@@ -775,16 +864,12 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
     exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, offsets, k, offsets + k);
 
     trace_mark(kTraceUpdateMean, false, s);
-    if (vec)
-        segmented_mean_kernel<true><<<mgrid, kMeanThreads, msmem, s>>>(X, vin, kin, offsets, (int)n, (int)d,
-                                                                       (int)L.chunk, C_new, head, tail, nullptr);
-    else
-        segmented_mean_kernel<false><<<mgrid, kMeanThreads, msmem, s>>>(X, vin, kin, offsets, (int)n, (int)d,
-                                                                        (int)L.chunk, C_new, head, tail, nullptr);
+    mean_k<<<mgrid, kMeanThreads, msmem, s>>>(X, vin, kin, offsets, (int)n, (int)d, (int)L.chunk, C_new, head, tail,
+                                              nullptr);
     trace_mark(kTraceUpdateMean, true, s);
     const int fix_grid = (int)(k < 4096 ? k : 4096);
     mean_fixup_kernel<<<fix_grid, kMeanThreads, 0, s>>>(offsets, head, tail, C_old, C_new, counts_out, (int)k,
-                                                       (int)d, (int)L.chunk);
+                                                       (int)d, (int)L.chunk, mean ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -8,9 +8,21 @@
 
 namespace km {
 
+// `sums_only`: write each cluster's unnormalised sum (zeros for an empty
+// cluster) to C_new instead of its mean; C_old is then not read.
 cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_old, float *C_new,
                           int32_t *counts_out, int64_t n, int64_t k, int64_t d, const UpdateLayout &L,
-                          uint8_t *ws, bool clear_header, cudaStream_t s, bool tile_counts_ready = false);
+                          uint8_t *ws, bool clear_header, cudaStream_t s, bool tile_counts_ready = false,
+                          bool sums_only = false);
+
+// Sample-sharded iteration: C_new[j] = (sum over ranks of parts[r][j], in
+// rank order, in float64) / (sum over ranks of part_counts[r][j]), or C_old[j]
+// when that count is 0; counts_out (nullable) the summed counts; inertia_out
+// (nullable) the rank-order sum of part_inertia.  parts: world x rows x d
+// float32, rank-major.
+cudaError_t launch_reduce_partials(const float *parts, const int32_t *part_counts, const double *part_inertia,
+                                   int world, int64_t rows, int64_t d, const float *C_old, float *C_new,
+                                   int32_t *counts_out, double *inertia_out, cudaStream_t s);
 
 // Assignment finalize fused with the update's per-tile cluster counts (one
 // block per counting tile); used by the Lloyd iteration when the counting

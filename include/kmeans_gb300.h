@@ -73,8 +73,10 @@ typedef enum {
     KMEANS_ERR_CUDA = 4,            /* a CUDA runtime call failed                */
     KMEANS_ERR_DEVICE_TIMEOUT = 5,  /* a device pipeline wait ran out of time    */
     KMEANS_ERR_DEVICE_LABEL = 6,    /* kmeans_update saw a label outside [0, k)  */
-    KMEANS_ERR_SCRATCH_LIMIT = 7    /* kmeans_assign_noalloc: the problem needs more
+    KMEANS_ERR_SCRATCH_LIMIT = 7,   /* kmeans_assign_noalloc: the problem needs more
                                        than KMEANS_NOALLOC_SCRATCH_BYTES of scratch */
+    KMEANS_ERR_DEVICE_EXCHANGE = 8  /* kmeanspp_shard_dist: no rank's exchange block
+                                       held a trial's candidate */
 } kmeans_status;
 
 /* Operation codes for kmeans_workspace_bytes. */
@@ -87,7 +89,10 @@ enum {
     KMEANS_OP_FIT = 5,
     KMEANS_OP_ASSIGN_3XTF32 = 6,
     KMEANS_OP_LLOYD_FUSED = 7,
-    KMEANS_OP_RELOCATE = 8
+    KMEANS_OP_RELOCATE = 8,
+    KMEANS_OP_KMEANSPP_SHARD = 9,  /* n = the shard's samples                   */
+    KMEANS_OP_LLOYD_PARTIAL = 10,  /* kmeans_lloyd_iter_partial (k may exceed n) */
+    KMEANS_OP_UPDATE_PARTIAL = 11  /* kmeans_update_partial (k may exceed n)     */
 };
 
 /* Initialisation of kmeans_fit. */
@@ -230,6 +235,114 @@ int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, f
                            float *C_new_host, int64_t *labels_host, double *inertia_host,
                            int64_t n, int64_t k, int64_t d, int slices, int flags,
                            void *ws, size_t ws_bytes, void *stream, void *copy_stream);
+
+/* ---------------------------------------------------------------------------
+ * Samples split by rows across GPUs (one process per GPU).  The update [U]
+ * needs every member of a cluster, so the shards' unnormalised sums and
+ * counts are combined before the divide; the collectives are the caller's
+ * (e.g. NCCL through torch.distributed) and only move bytes, while every
+ * addition across ranks happens in the library in rank order, so the result
+ * does not depend on how the collective is scheduled.  One iteration:
+ *   1. each rank: kmeans_lloyd_iter_partial on its rows (or kmeans_assign +
+ *      kmeans_update_partial) -> sums (k, d), counts (k), its inertia;
+ *   2. all-to-all: rank q receives every rank's rows [q*m, q*m + m) of the
+ *      sums and counts (m = ceil(k / world), zero rows past k);
+ *   3. each rank: kmeans_reduce_partials on its slice -> C_new rows, counts;
+ *   4. all-gather of the C_new slices (and counts) -> C_new on every rank.
+ * --------------------------------------------------------------------------- */
+
+/* The mean update's sums [U] over one shard of the samples: sums[j] = the
+ * sum of the rows X[i] with labels[i] == j (compensated float32 in a fixed
+ * order, as kmeans_update sums before it divides), zeros for a cluster with
+ * no member here; counts[j] (required) the member count.  X (n, d) and
+ * labels (n) are this shard's; k is the global number of centroids (it may
+ * exceed n).  Workspace KMEANS_OP_UPDATE_PARTIAL; requirements and label
+ * checking as kmeans_update.  seed: unused. */
+int kmeans_update_partial(const float *X, const int64_t *labels, int64_t n, int64_t k, int64_t d,
+                          float *sums, int32_t *counts,
+                          void *ws, size_t ws_bytes, uint64_t seed, void *stream);
+
+/* One shard's part of a Lloyd iteration [U]: kmeans_assign of the shard's X
+ * (n, d) against C (k, d, all centroids), then kmeans_update_partial of
+ * those labels.  labels, best_dist, *inertia (the shard's, may be NULL) as
+ * kmeans_assign; sums (k, d) and counts (k, required) as
+ * kmeans_update_partial.  Requirements as kmeans_lloyd_iter, except that k
+ * may exceed the shard's n; workspace KMEANS_OP_LLOYD_PARTIAL.  seed: unused. */
+int kmeans_lloyd_iter_partial(const float *X, const float *C, int64_t *labels, float *best_dist,
+                              double *inertia, float *sums, int32_t *counts,
+                              int64_t n, int64_t k, int64_t d,
+                              void *ws, size_t ws_bytes, uint64_t seed, void *stream);
+
+/* The divide of the sharded update [U] for `rows` centroid rows.
+ * parts (world, rows, d) float32 and part_counts (world, rows) int32 hold
+ * every rank's sums and counts of those rows, rank-major.  For each row j:
+ * count = sum over ranks of part_counts[r][j]; if count > 0, C_new[j] =
+ * (sum over r of parts[r][j], added in rank order in float64, the first
+ * rank's value as it is) / count, rounded once to float32; otherwise
+ * C_new[j] = C_old[j].  With world = 1 this gives kmeans_update's bits.
+ * counts (rows, may be NULL) receives the summed counts (the global count
+ * of a cluster must be below 2^31).  part_inertia (world doubles) and
+ * inertia (one double) are both NULL or both given: *inertia = the rank-order
+ * sum of part_inertia.  C_new may alias C_old.  rows >= 0, 1 <= world <= 65536,
+ * d >= 1.  One kernel, no workspace. */
+int kmeans_reduce_partials(const float *parts, const int32_t *part_counts, const double *part_inertia,
+                           int world, int64_t rows, int64_t d, const float *C_old, float *C_new,
+                           int32_t *counts, double *inertia, void *stream);
+
+/* Greedy k-means++ [K] over samples split by rows across ranks: the same
+ * seeding as kmeanspp_init over the concatenated shards (rank order), as a
+ * sequence of steps between which the caller all-gathers small buffers.
+ * Rank r holds rows [row_offset, row_offset + n) of the n_global samples
+ * (n >= 1; the offsets are the shards' sizes summed in rank order).
+ * Exchange block: kmeanspp_shard_exchange_bytes(n_trials, d) bytes per rank
+ * (16-byte aligned device memory): n_trials int64 global sample indices
+ * (-1: not this rank's), then n_trials rows of d float32.
+ * Workspace KMEANS_OP_KMEANSPP_SHARD with n = this shard's samples; it holds
+ * the shard's D^2 between the steps, and its status word collects device
+ * faults over the whole seeding (cleared by kmeanspp_shard_first).
+ *   kmeanspp_shard_first   draw 0 picks the first center (uniform over
+ *                          n_global); its owner fills slot 0 of `send`.
+ *   (all-gather `send` of every rank -> recv, world blocks, rank order)
+ *   kmeanspp_shard_dist    first = 1: distances to that center.
+ *   kmeanspp_shard_commit  first = 1, c = 0: indices[0], centers[0], D^2,
+ *                          and this shard's total of D^2 -> *total.
+ *   (all-gather the totals -> world doubles, rank order)
+ *   for c = 1 .. k-1:
+ *     kmeanspp_shard_pick   draws 1 + (c-1)*n_trials + t: each trial's
+ *                           target = u * (sum of the totals, rank order);
+ *                           its owner is the first rank whose running total
+ *                           exceeds it (the last rank's last sample when none
+ *                           does), which finds the sample by its running sum
+ *                           started at the earlier ranks' total and fills
+ *                           the trial's slot of `send`.
+ *     (all-gather `send`)
+ *     kmeanspp_shard_dist   first = 0: distances to the n_trials candidates
+ *                           and this shard's potentials -> pot (n_trials
+ *                           doubles, device).
+ *     (all-gather pot -> world x n_trials doubles)
+ *     kmeanspp_shard_commit first = 0: the trial with the lowest potential
+ *                           summed over ranks in rank order (lowest trial on
+ *                           ties) becomes center c: indices[c] (device int64,
+ *                           k), centers[c] (device float32 (k, d), may be
+ *                           NULL), D^2 lowered; *total for the next draws
+ *                           (total may be NULL after the last center).
+ *     (all-gather the totals)
+ * Every rank ends with the same indices and centers.  With world = 1 the
+ * indices are kmeanspp_init's bit for bit.  Distances and sums as
+ * kmeanspp_init.  kmeanspp_shard_dist sets KMEANS_ERR_DEVICE_EXCHANGE in the
+ * status word if no block held a trial's candidate (inconsistent inputs).
+ * n_trials: 1 .. 32 (use 2 + floor(ln k) for kmeanspp_init's default). */
+size_t kmeanspp_shard_exchange_bytes(int n_trials, int64_t d);
+int kmeanspp_shard_first(const float *X, int64_t n, int64_t d, int64_t row_offset, int64_t n_global,
+                         int n_trials, uint64_t seed, void *send, void *ws, size_t ws_bytes, void *stream);
+int kmeanspp_shard_pick(const float *X, int64_t n, int64_t d, int64_t row_offset, int n_trials, uint64_t seed,
+                        int64_t c, const double *totals, int world, int rank, void *send,
+                        void *ws, size_t ws_bytes, void *stream);
+int kmeanspp_shard_dist(const float *X, int64_t n, int64_t d, int n_trials, int first, const void *recv,
+                        int world, double *pot, void *ws, size_t ws_bytes, void *stream);
+int kmeanspp_shard_commit(int64_t n, int64_t d, int n_trials, int first, const double *pots, int world,
+                          int64_t c, int64_t *indices, float *centers, double *total,
+                          void *ws, size_t ws_bytes, void *stream);
 
 /* Empty-cluster relocation [L] (the rule is this library's reading; the
  * page names the step only).  With m clusters that no label names, the m

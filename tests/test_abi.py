@@ -163,3 +163,20 @@ def test_probe_byte_counts_from_the_page(km):
     assert vals["one_centroid_difference_nd"] * MiB == n * d * 4
     assert round(n * 8 / MiB, 3) == vals["labels_n_int64"]
     assert km.kmeans_workspace_bytes(km.OP_ASSIGN, n, k, d) < vals["distance_nk"] * MiB
+
+
+def test_update_workspace_holds_every_chunks_partials(km):
+    # The segmented mean cuts the member list into chunks sized for one wave
+    # of 512-column slices (152 SMs x 12 blocks), at least 16 members, a
+    # multiple of 16, at most 4096; every chunk keeps a head and a tail
+    # partial row of d floats.  Small n with large d gives many short chunks.
+    def chunk(n, d):
+        slices = (d + 511) // 512
+        chunks = (152 * 12 + slices - 1) // slices
+        c = max(16, (n + chunks - 1) // chunks)
+        return min(4096, (c + 15) // 16 * 16)
+
+    for n, k, d in ((4096, 4, 8192), (65536, 1024, 2048), (1000, 10, 16384), (300, 3, 64)):
+        n_chunks = (n + chunk(n, d) - 1) // chunk(n, d)
+        assert km.kmeans_workspace_bytes(km.OP_UPDATE, n, k, d) >= 2 * n_chunks * d * 4 + 16 * n
+    assert chunk(4096, 8192) == 48  # 86 chunks: one cluster of 4050 members crosses 85 of them

@@ -126,6 +126,21 @@ def test_update_single_cluster_and_skewed_sizes(gpu_lib):
     check_centroids(host(C_new), o_C, what="skewed")
 
 
+def test_update_one_cluster_across_many_small_chunks(gpu_lib):
+    # small n, large d: the member list is cut into chunks of a few dozen
+    # members (one wave of 512-column slices), so cluster 0's ~4050 members
+    # cross some 85 chunk boundaries and are finished by the chunk fix-up
+    n, k, d = 4096, 4, 8192
+    X = synth.gaussian((n, d), seed=44, scale=1.5)
+    labels = np.zeros(n, np.int64)
+    labels[::97] = np.arange(len(labels[::97])) % 3 + 1
+    C_old = synth.gaussian((k, d), seed=45)
+    C_new, counts = gpu_lib.kmeans_update(dev_tensor(X), dev_tensor(labels), dev_tensor(C_old))
+    o_C, o_cnt = oracle.update(X, labels, C_old)
+    assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+    check_centroids(host(C_new), o_C, what="one cluster over many chunks")
+
+
 def test_update_in_place(gpu_lib):
     n, k, d = 3000, 50, 64
     X = synth.gaussian((n, d), seed=8)

@@ -95,3 +95,61 @@ def test_noalloc_leaves_device_memory_untouched(gpu_lib):
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0
+
+
+# With n and k multiples of 256 and d = 64, the scratch is exactly 12 n + 4 k
+# + 4 k * 64 bytes plus 9 KiB (a 1 KiB header region and the 8 KiB of inertia
+# block sums): (1386240, 512, 64) needs exactly 16 MiB, (1391872, 256, 64)
+# exactly 16 MiB + 1 KiB.
+AT_LIMIT = (1386240, 512, 64)
+ONE_KIB_OVER = (1391872, 256, 64)
+
+
+def test_noalloc_scratch_limit_boundary(gpu_lib):
+    lib = gpu_lib.load()
+    fake = ctypes.c_void_p(0x10000)  # validation fails before any pointer is used
+    n, k, d = ONE_KIB_OVER
+    assert lib.kmeans_assign_noalloc(fake, fake, n, k, d, fake, fake, None, 0, None) == \
+        gpu_lib.KMEANS_ERR_SCRATCH_LIMIT
+    # the problem that fills the scratch exactly runs, and gives kmeans_assign's answer
+    n, k, d = AT_LIMIT
+    X, _, _ = synth.planted_blobs(n, d, k, seed=81)
+    C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=82)])
+    Xd, Cd = _dev(X), _dev(C)
+    got, ref = _outputs(n), _outputs(n)
+    assert _assign_noalloc(lib, Xd, Cd, *got) == gpu_lib.KMEANS_OK
+    assert _assign_with_workspace(gpu_lib, lib, Xd, Cd, *ref) == gpu_lib.KMEANS_OK
+    torch.cuda.synchronize()
+    # with a workspace this many tiles split their last round along K (the
+    # built-in scratch never does): distances agree within the tolerance, and
+    # a label may differ only where its own distance is that close too
+    g_lab, r_lab = got[0].cpu().numpy(), ref[0].cpu().numpy()
+    g_best, r_best = got[1].cpu().numpy().astype(np.float64), ref[1].cpu().numpy().astype(np.float64)
+    scale = sq_norms(X) + sq_norms(C)[r_lab]
+    assert np.all(np.abs(g_best - r_best) <= DIST_RTOL * scale)
+    for i in np.flatnonzero(g_lab != r_lab):
+        diff = X[i].astype(np.float64) - C[g_lab[i]].astype(np.float64)
+        assert abs(float(diff @ diff) - r_best[i]) <= DIST_RTOL * scale[i]
+
+
+def test_noalloc_timeout_leaves_minus_one_then_recovers(gpu_lib, monkeypatch):
+    # The bounded pipeline waits of the built-in scratch's call run out when
+    # the producer is starved on purpose (a host-side switch; no fault): the
+    # call returns, its labels hold -1, and the next call resets the shared
+    # scratch's status word and gives kmeans_assign's answer again.
+    lib = gpu_lib.load()
+    X, C, _ = synth.workload_inputs(synth.WORKLOADS["probe"])
+    Xd, Cd = _dev(X), _dev(C)
+    n = X.shape[0]
+    outs = _outputs(n)
+    monkeypatch.setenv("KMEANS_GB300_TEST_STARVE_PIPELINE", "1")
+    assert _assign_noalloc(lib, Xd, Cd, *outs) == gpu_lib.KMEANS_OK
+    torch.cuda.synchronize()
+    assert (outs[0].cpu().numpy() == -1).all()
+    monkeypatch.delenv("KMEANS_GB300_TEST_STARVE_PIPELINE")
+    ref = _outputs(n)
+    assert _assign_noalloc(lib, Xd, Cd, *outs) == gpu_lib.KMEANS_OK
+    assert _assign_with_workspace(gpu_lib, lib, Xd, Cd, *ref) == gpu_lib.KMEANS_OK
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(outs[0].cpu().numpy(), ref[0].cpu().numpy())
+    assert outs[1].cpu().numpy().tobytes() == ref[1].cpu().numpy().tobytes()
