@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="sample_heavy")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="keep only the workload's first ROWS samples (a smaller case of the same shape for "
+                         "profiler captures; the JSON line names it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kmeanspp", action="store_true")
@@ -389,6 +392,12 @@ def run_gb300(args):
 
     w = synth.WORKLOADS[args.workload]
     X, C0, _ = synth.workload_inputs(w)
+    if 0 < args.rows < w.n:
+        if args.rows < w.k:
+            raise SystemExit(f"--rows {args.rows} is below k = {w.k}")
+        X = np.ascontiguousarray(X[:args.rows])
+        w = synth.Workload(f"{w.name}_rows{args.rows}", args.rows, w.k, w.d, w.blobs, w.iters, w.data_seed,
+                           w.init_seed, w.note + f"; first {args.rows} samples only")
     n, k, d = w.n, w.k, w.d
     flop = 2.0 * n * k * d
     Xd = torch.from_numpy(X).to(dev)

@@ -251,7 +251,6 @@ template <bool VEC>
 __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand,
                          const float *__restrict__ crows, int T, int t0, int W, float2 *__restrict__ dpart) {
-    griddep_wait();
     extern __shared__ __align__(16) float cs[];  // [KT][W], negated
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -259,39 +258,65 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     const int slice = blockIdx.y;
     const int fb = slice * W;
     const int width = min(W, d - fb);
-    for (int e = threadIdx.x; e < kd::KT * W; e += kd::THREADS) {
-        const int t = e / W, f = e - t * W;
-        float v = 0.f;
-        // the candidates are rows of X, or (a shard) rows of the exchange buffer
-        if (t < nt && f < width)
-            v = -__ldg((crows ? crows + (int64_t)(t0 + t) * d : X + cand[t0 + t] * (int64_t)d) + fb + f);
-        cs[e] = v;
-    }
-    __syncthreads();
-
     const int64_t n_groups = (n + kd::GROUP - 1) / kd::GROUP;
-    for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x) {
-        const int64_t r0 = g * kd::GROUP + warp * kd::ROWS;
-        static_assert(kd::ROWS == 2, "the two rows' sums are paired in float2");
-        float2 s2[kd::KT];  // .x row 0, .y row 1
-#pragma unroll
-        for (int t = 0; t < kd::KT; ++t) s2[t] = make_float2(0.f, 0.f);
-        // a lane owns features f .. f+3 and f+128 .. f+131 of each 256-feature
-        // step, so every 16-byte load of the warp (global and shared) covers
-        // 512 contiguous bytes.  The next step's rows are loaded while this
-        // step is computed (xn).  One block of 24 warps per SM fits it in 85
-        // registers a thread; more resident warps hide more of the loads (16,
-        // 20, 24 and 28 warps measured 397, 375, 363 and 386 us a pass).
-        float2 x[kd::ROWS][4], xn[kd::ROWS][4];
+    static_assert(kd::ROWS == 2, "the two rows' sums are paired in float2");
+
+    // A lane owns features f .. f+3 and f+128 .. f+131 of each 256-feature
+    // step, so every 16-byte load of the warp (global and shared) covers 512
+    // contiguous bytes.  The next step's rows are loaded while this step is
+    // computed (xn), and the last step of a group loads the first step of the
+    // block's next group, so a group starts without waiting for memory.  One
+    // block of 24 warps per SM fits it in 85 registers a thread; more resident
+    // warps hide more of the loads (16, 20, 24 and 28 warps measured 397, 375,
+    // 363 and 386 us a pass).
+    float2 x[kd::ROWS][4], xn[kd::ROWS][4];
+    auto load_first_step = [&](int64_t gg) {
+        const int64_t rr = gg * kd::GROUP + warp * kd::ROWS;
 #pragma unroll
         for (int r = 0; r < kd::ROWS; ++r) {
-            if (r0 + r < n) {
-                load4x2<VEC>(X + (r0 + r) * (int64_t)d + fb + lane * 4, width - lane * 4, xn[r]);
+            if (rr + r < n) {  // a group past the last one has every row past n
+                load4x2<VEC>(X + (rr + r) * (int64_t)d + fb + lane * 4, width - lane * 4, xn[r]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) xn[r][e] = make_float2(0.f, 0.f);
             }
         }
+    };
+    // X is an input of the whole entry point, never written by a kernel of
+    // the chain, so its first rows are requested before the wait for the
+    // kernel that chose the candidates
+    load_first_step(blockIdx.x);
+    griddep_wait();
+    // the candidates are rows of X, or (a shard) rows of the exchange buffer
+    if (VEC) {
+        // W and width are multiples of 4: a 16-byte group never straddles a
+        // trial or the slice's end
+        for (int e = threadIdx.x * 4; e < kd::KT * W; e += kd::THREADS * 4) {
+            const int t = e / W, f = e - t * W;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < nt && f < width) {
+                const float *src = crows ? crows + (int64_t)(t0 + t) * d : X + cand[t0 + t] * (int64_t)d;
+                v = __ldg(reinterpret_cast<const float4 *>(src + fb + f));
+                v = make_float4(-v.x, -v.y, -v.z, -v.w);
+            }
+            *reinterpret_cast<float4 *>(&cs[e]) = v;
+        }
+    } else {
+        for (int e = threadIdx.x; e < kd::KT * W; e += kd::THREADS) {
+            const int t = e / W, f = e - t * W;
+            float v = 0.f;
+            if (t < nt && f < width)
+                v = -__ldg((crows ? crows + (int64_t)(t0 + t) * d : X + cand[t0 + t] * (int64_t)d) + fb + f);
+            cs[e] = v;
+        }
+    }
+    __syncthreads();
+
+    for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x) {
+        const int64_t r0 = g * kd::GROUP + warp * kd::ROWS;
+        float2 s2[kd::KT];  // .x row 0, .y row 1
+#pragma unroll
+        for (int t = 0; t < kd::KT; ++t) s2[t] = make_float2(0.f, 0.f);
         for (int f0 = 0; f0 < width; f0 += 256) {
             const int f = f0 + lane * 4;
 #pragma unroll
@@ -303,6 +328,8 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
                 for (int r = 0; r < kd::ROWS; ++r) {
                     if (r0 + r < n) load4x2<VEC>(X + (r0 + r) * (int64_t)d + fb + f + 256, width - f - 256, xn[r]);
                 }
+            } else {
+                load_first_step(g + gridDim.x);
             }
 #pragma unroll
             for (int t = 0; t < kd::KT; ++t) {
