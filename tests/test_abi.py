@@ -180,3 +180,64 @@ def test_update_workspace_holds_every_chunks_partials(km):
         n_chunks = (n + chunk(n, d) - 1) // chunk(n, d)
         assert km.kmeans_workspace_bytes(km.OP_UPDATE, n, k, d) >= 2 * n_chunks * d * 4 + 16 * n
     assert chunk(4096, 8192) == 48  # 86 chunks: one cluster of 4050 members crosses 85 of them
+
+
+def test_shard_entry_points_validate_on_the_host(km):
+    lib = _lib(km)
+    F, W = FAKE, FAKE_WS
+    # shard workspaces accept more centroids than samples; the others do not
+    assert km.kmeans_workspace_bytes(km.OP_LLOYD_PARTIAL, 300, 700, 36) > 0
+    assert km.kmeans_workspace_bytes(km.OP_UPDATE_PARTIAL, 300, 700, 36) > 0
+    assert km.kmeans_workspace_bytes(km.OP_KMEANSPP_SHARD, 300, 700, 36) > 0
+    assert km.kmeans_workspace_bytes(km.OP_LLOYD, 300, 700, 36) == 0
+    n, k, d = 300, 700, 36
+    need = km.kmeans_workspace_bytes(km.OP_UPDATE_PARTIAL, n, k, d)
+    up = lambda sums, counts, labels=F, wsb=need: lib.kmeans_update_partial(F, labels, n, k, d, sums, counts, W, wsb,
+                                                                            0, None)
+    assert up(None, F) == km.KMEANS_ERR_INVALID_ARG
+    assert up(F, None) == km.KMEANS_ERR_INVALID_ARG               # the counts are required
+    assert up(F, F, labels=ctypes.c_void_p(0x10004)) == km.KMEANS_ERR_INVALID_ARG
+    assert up(F, F, wsb=need - 1) == km.KMEANS_ERR_WORKSPACE       # k > n passed the size checks
+    need = km.kmeans_workspace_bytes(km.OP_LLOYD_PARTIAL, n, k, d)
+    lp = lambda dd, counts=F, wsb=need: lib.kmeans_lloyd_iter_partial(F, F, F, F, None, F, counts, n, k, dd, W, wsb,
+                                                                      0, None)
+    assert lp(34) == km.KMEANS_ERR_UNSUPPORTED                     # d % 4
+    assert lp(d, counts=None) == km.KMEANS_ERR_INVALID_ARG
+    assert lp(d, wsb=need - 1) == km.KMEANS_ERR_WORKSPACE
+    rp = lambda pin, world, rows, parts=F, inertia=None: lib.kmeans_reduce_partials(parts, F, pin, world, rows, 8, F,
+                                                                                    F, None, inertia, None)
+    assert rp(None, 0, 4) == km.KMEANS_ERR_INVALID_ARG             # world 0
+    assert rp(None, 2, -1) == km.KMEANS_ERR_INVALID_ARG
+    assert rp(F, 2, 4) == km.KMEANS_ERR_INVALID_ARG                # part inertia without an output
+    assert rp(None, 2, 4, inertia=F) == km.KMEANS_ERR_INVALID_ARG  # and the reverse
+    assert rp(None, 2, 4, parts=None) == km.KMEANS_ERR_INVALID_ARG
+    assert rp(None, 2, 0) == km.KMEANS_OK                          # nothing to reduce, nothing enqueued
+
+
+def test_kmeanspp_shard_steps_validate_on_the_host(km):
+    lib = _lib(km)
+    F, W = FAKE, FAKE_WS
+    assert km.kmeanspp_shard_exchange_bytes(8, 8192) == 64 + 8 * 8192 * 4
+    assert km.kmeanspp_shard_exchange_bytes(3, 5) == 32 + 64       # indices and rows, each rounded to 16 bytes
+    assert km.kmeanspp_shard_exchange_bytes(0, 8) == 0 and km.kmeanspp_shard_exchange_bytes(33, 8) == 0
+    n, d, T = 1000, 64, 8
+    need = km.kmeans_workspace_bytes(km.OP_KMEANSPP_SHARD, n, 10, d)
+    first = lambda off, ng, send=F, T=T: lib.kmeanspp_shard_first(F, n, d, off, ng, T, 0, send, W, need, None)
+    assert first(500, 1499) == km.KMEANS_ERR_INVALID_ARG           # the shard runs past n_global
+    assert first(-1, 5000) == km.KMEANS_ERR_INVALID_ARG
+    assert first(0, 5000, send=ctypes.c_void_p(0x10008)) == km.KMEANS_ERR_INVALID_ARG  # send not 16-aligned
+    assert first(0, 5000, T=0) == km.KMEANS_ERR_INVALID_ARG
+    assert first(0, 5000, T=33) == km.KMEANS_ERR_INVALID_ARG
+    assert lib.kmeanspp_shard_first(F, n, d, 0, 5000, T, 0, F, W, need - 1, None) == km.KMEANS_ERR_WORKSPACE
+    pick = lambda c, world, rank: lib.kmeanspp_shard_pick(F, n, d, 0, T, 0, c, F, world, rank, F, W, need, None)
+    assert pick(0, 2, 0) == km.KMEANS_ERR_INVALID_ARG              # center 0 is the first step's
+    assert pick(1, 2, 2) == km.KMEANS_ERR_INVALID_ARG              # rank outside the world
+    assert pick(1, 0, 0) == km.KMEANS_ERR_INVALID_ARG
+    dist = lambda first, pot: lib.kmeanspp_shard_dist(F, n, d, T, first, F, 2, pot, W, need, None)
+    assert dist(0, None) == km.KMEANS_ERR_INVALID_ARG              # potentials needed after the first center
+    assert dist(2, F) == km.KMEANS_ERR_INVALID_ARG
+    commit = lambda first, pots, c: lib.kmeanspp_shard_commit(n, d, T, first, pots, 2, c, F, None, None, W, need, None)
+    assert commit(1, None, 3) == km.KMEANS_ERR_INVALID_ARG         # the first center is center 0
+    assert commit(0, None, 3) == km.KMEANS_ERR_INVALID_ARG
+    assert commit(0, F, -1) == km.KMEANS_ERR_INVALID_ARG
+    assert "exchange block" in km.kmeans_status_string(km.KMEANS_ERR_DEVICE_EXCHANGE)
