@@ -168,3 +168,29 @@ def kmeanspp_init_sharded(X, k: int, seed: int, ex: Exchange, n_trials: int = 0,
         km.kmeanspp_shard_commit(n, d, T, False, pots, world, c, indices, centers, None if last else total, ws,
                                  stream=stream)
     return indices, centers
+
+
+def fit_sharded(X, C0, ex: Exchange, max_iter: int = 300, tol: float = 1e-4, ws=None, ops=None, stream=None):
+    """Lloyd iterations over samples split by rows across the ranks of
+    ``ex``, from the centroids C0 (the same on every rank), with the stopping
+    rule of kmeans_fit: stop after iteration t when inertia_t >=
+    (1 - tol) * inertia_{t-1}, or after max_iter iterations.  Every rank reads
+    the same global inertia, so every rank stops at the same iteration.
+    Returns ``(C (k, d), labels, best_dist, counts, inertia_history,
+    n_iter)``: C, counts and the history global, labels and best_dist this
+    rank's rows of the last iteration."""
+    import numpy as np
+    km = ops or _default_ops()
+    n, d = X.shape
+    k = C0.shape[0]
+    if ws is None:
+        ws = km.workspace(km.OP_LLOYD_PARTIAL, n, k, d, X.device)
+    C = C0
+    hist = []
+    labels = best = counts = None
+    for it in range(int(max_iter)):
+        C, counts, labels, best, inertia = lloyd_iter_sharded(X, C, ex, ws=ws, ops=ops, stream=stream)
+        hist.append(float(inertia.reshape(-1)[0].item()))
+        if it > 0 and hist[-1] >= hist[-2] * (1.0 - tol):
+            break
+    return C, labels, best, counts, np.array(hist), len(hist)

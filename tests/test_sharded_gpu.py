@@ -128,6 +128,22 @@ def test_one_rank_seeding_steps_are_kmeanspp_init(gpu_lib, case):
     assert host(cen).tobytes() == host(ref_cen).tobytes()
 
 
+def test_one_rank_sharded_fit_is_kmeans_fit(gpu_lib):
+    # the same iterations, so the same bits, history and stopping point
+    from distance_argmin_gb300 import sharded
+    X, C0, _ = synth.workload_inputs(synth.Workload("t", 6000, 40, 36, 40, 1, 81, 82, ""))
+    Xd = dev_tensor(X)
+    C_ref = dev_tensor(C0)
+    C_ref, lab_ref, best_ref, cnt_ref, hist_ref, it_ref = gpu_lib.kmeans_fit(Xd, C=C_ref, init="given", max_iter=30,
+                                                                             tol=0.0)
+    C, labels, best, counts, hist, n_iter = sharded.fit_sharded(Xd, dev_tensor(C0), OneRank(), max_iter=30, tol=0.0)
+    assert n_iter == it_ref and n_iter > 2
+    np.testing.assert_array_equal(hist, hist_ref)
+    assert host(C).tobytes() == host(C_ref).tobytes()
+    np.testing.assert_array_equal(host(labels), host(lab_ref))
+    np.testing.assert_array_equal(host(counts), host(cnt_ref))
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))

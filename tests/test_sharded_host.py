@@ -221,3 +221,50 @@ def test_slices_cover_every_centroid_row_once():
             full = [q * m + i for q in range(world) for i in range(m)]
             kept = [q * m + i for q in range(world) for i in range(rows[q])]
             assert kept == full[:k]
+
+
+def _fit_rank_main(rank, world, port, q):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import synth
+    from distance_argmin_gb300 import sharded
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        X, C0, _ = synth.workload_inputs(synth.Workload("t", 900, 9, 6, 9, 1, 63, 64, ""))
+        b = [0, 250, 600, 900]
+        Xl = torch.from_numpy(np.ascontiguousarray(X[b[rank]:b[rank + 1]]))
+        C, labels, best, counts, hist, n_iter = sharded.fit_sharded(Xl, torch.from_numpy(C0), sharded.Exchange(),
+                                                                    max_iter=50, tol=0.0, ops=FakeOps())
+        q.put((rank, C.numpy().copy(), labels.numpy().copy(), hist, n_iter))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sharded_fit_stops_where_the_oracle_fit_stops():
+    import torch.multiprocessing as mp
+    sys.path.insert(0, ROOT)
+    import oracle
+    import synth
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_fit_rank_main, args=(r, 3, port, q)) for r in range(3)]
+    for p in procs:
+        p.start()
+    got = dict((res[0], res[1:]) for res in (q.get(timeout=300) for _ in procs))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    X, C0, _ = synth.workload_inputs(synth.Workload("t", 900, 9, 6, 9, 1, 63, 64, ""))
+    o_C, o_lab, _, o_hist, o_iter = oracle.fit(X, C0, 50, 0.0)
+    b = [0, 250, 600, 900]
+    for r in range(3):
+        C, labels, hist, n_iter = got[r]
+        assert n_iter == o_iter and n_iter > 2
+        # the partial sums are float32, so later centroids (and inertias) carry ~1e-8 relative rounding
+        np.testing.assert_allclose(hist, o_hist, rtol=1e-6)
+        np.testing.assert_array_equal(labels, o_lab[b[r]:b[r + 1]])
+        assert (np.abs(C - o_C) <= 1e-5 * np.abs(o_C).max(axis=1, keepdims=True)).all()
