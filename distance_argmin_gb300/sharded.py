@@ -23,10 +23,14 @@ calls the C ABI through the binding and calls torch.distributed.
 
 ``ops`` (default: the binding) is the object whose functions are called; the
 host-side tests pass a stand-in with the same functions to run the exchange
-logic on CPU ranks.
+logic on CPU ranks.  ``stream`` (optional, every entry): the CUDA stream the
+whole sequence runs on; it is made the current stream for the duration, so the
+collectives and the kernels between them stay in order.
 """
 from __future__ import annotations
 
+import contextlib
+import functools
 import math
 
 
@@ -38,6 +42,23 @@ def _torch():
 def _default_ops():
     import distance_argmin_gb300 as km
     return km
+
+
+def _on_stream(fn):
+    """Run ``fn`` with its ``stream`` argument as the current CUDA stream, so
+    that the library's kernels and the torch.distributed collectives between
+    them are ordered on one stream; the library calls inside then take the
+    current stream."""
+    @functools.wraps(fn)
+    def wrapped(*args, stream=None, **kwargs):
+        ctx = contextlib.nullcontext()
+        if stream is not None:
+            torch = _torch()
+            ctx = torch.cuda.stream(stream if isinstance(stream, torch.cuda.Stream)
+                                    else torch.cuda.ExternalStream(int(stream)))
+        with ctx:
+            return fn(*args, **kwargs)
+    return wrapped
 
 
 class Exchange:
@@ -89,7 +110,8 @@ def slice_rows(k: int, world: int):
     return m, [max(0, min(m, k - q * m)) for q in range(world)]
 
 
-def lloyd_iter_sharded(X, C_old, ex: Exchange, ws=None, ops=None, stream=None):
+@_on_stream
+def lloyd_iter_sharded(X, C_old, ex: Exchange, ws=None, ops=None):
     """One Lloyd iteration over samples split by rows across the ranks of
     ``ex``.  X: this rank's (n_local, d) rows; C_old: the (k, d) centroids,
     the same on every rank.  Returns ``(C_new (k, d), counts (k,), labels,
@@ -104,7 +126,7 @@ def lloyd_iter_sharded(X, C_old, ex: Exchange, ws=None, ops=None, stream=None):
     world, rank = ex.world, ex.rank
     if ws is None:
         ws = km.workspace(km.OP_LLOYD_PARTIAL, n, k, d, dev)
-    sums, counts, labels, best, inertia = km.kmeans_lloyd_iter_partial(X, C_old, ws=ws, stream=stream)
+    sums, counts, labels, best, inertia = km.kmeans_lloyd_iter_partial(X, C_old, ws=ws)
     m, rows = slice_rows(k, world)
     mine = rows[rank]
     # every rank's sums and counts of this rank's centroid rows, rank-major
@@ -116,7 +138,7 @@ def lloyd_iter_sharded(X, C_old, ex: Exchange, ws=None, ops=None, stream=None):
     cnt_slice = torch.zeros(m, dtype=torch.int32, device=dev)
     total = torch.empty(1, dtype=torch.float64, device=dev)
     km.kmeans_reduce_partials(parts, part_counts, C_old[lo:lo + mine], C_new=C_slice[:mine],
-                              counts=cnt_slice[:mine], part_inertia=part_inertia, inertia=total, stream=stream)
+                              counts=cnt_slice[:mine], part_inertia=part_inertia, inertia=total)
     # rank q's slice holds rows [q m, q m + rows[q]); only the last slices
     # are short, so the gathered slices' first k rows are C_new in order
     C_new = ex.all_gather(C_slice).view(world * m, d)[:k]
@@ -132,7 +154,8 @@ def shard_offsets(n_local: int, ex: Exchange, device):
     return int(sum(sizes[:ex.rank])), int(sum(sizes))
 
 
-def kmeanspp_init_sharded(X, k: int, seed: int, ex: Exchange, n_trials: int = 0, ws=None, ops=None, stream=None):
+@_on_stream
+def kmeanspp_init_sharded(X, k: int, seed: int, ex: Exchange, n_trials: int = 0, ws=None, ops=None):
     """Greedy k-means++ seeding of k centers over the samples split by rows
     across the ranks of ``ex`` (rank order = sample order).  Returns
     ``(indices (k,) global sample indices, centers (k, d))``, the same on
@@ -154,23 +177,23 @@ def kmeanspp_init_sharded(X, k: int, seed: int, ex: Exchange, n_trials: int = 0,
     indices = torch.empty(k, dtype=torch.int64, device=dev)
     centers = torch.empty((k, d), dtype=torch.float32, device=dev)
 
-    km.kmeanspp_shard_first(X, row_offset, n_global, T, seed, send, ws, stream=stream)
+    km.kmeanspp_shard_first(X, row_offset, n_global, T, seed, send, ws)
     recv = ex.all_gather(send)
-    km.kmeanspp_shard_dist(X, T, True, recv, world, None, ws, stream=stream)
-    km.kmeanspp_shard_commit(n, d, T, True, None, world, 0, indices, centers, total, ws, stream=stream)
+    km.kmeanspp_shard_dist(X, T, True, recv, world, None, ws)
+    km.kmeanspp_shard_commit(n, d, T, True, None, world, 0, indices, centers, total, ws)
     for c in range(1, k):
         totals = ex.all_gather(total).view(world)
-        km.kmeanspp_shard_pick(X, row_offset, T, seed, c, totals, rank, send, ws, stream=stream)
+        km.kmeanspp_shard_pick(X, row_offset, T, seed, c, totals, rank, send, ws)
         recv = ex.all_gather(send)
-        km.kmeanspp_shard_dist(X, T, False, recv, world, pot, ws, stream=stream)
+        km.kmeanspp_shard_dist(X, T, False, recv, world, pot, ws)
         pots = ex.all_gather(pot).view(world * T)
         last = c == k - 1
-        km.kmeanspp_shard_commit(n, d, T, False, pots, world, c, indices, centers, None if last else total, ws,
-                                 stream=stream)
+        km.kmeanspp_shard_commit(n, d, T, False, pots, world, c, indices, centers, None if last else total, ws)
     return indices, centers
 
 
-def fit_sharded(X, C0, ex: Exchange, max_iter: int = 300, tol: float = 1e-4, ws=None, ops=None, stream=None):
+@_on_stream
+def fit_sharded(X, C0, ex: Exchange, max_iter: int = 300, tol: float = 1e-4, ws=None, ops=None):
     """Lloyd iterations over samples split by rows across the ranks of
     ``ex``, from the centroids C0 (the same on every rank), with the stopping
     rule of kmeans_fit: stop after iteration t when inertia_t >=
@@ -189,7 +212,7 @@ def fit_sharded(X, C0, ex: Exchange, max_iter: int = 300, tol: float = 1e-4, ws=
     hist = []
     labels = best = counts = None
     for it in range(int(max_iter)):
-        C, counts, labels, best, inertia = lloyd_iter_sharded(X, C, ex, ws=ws, ops=ops, stream=stream)
+        C, counts, labels, best, inertia = lloyd_iter_sharded(X, C, ex, ws=ws, ops=ops)
         hist.append(float(inertia.reshape(-1)[0].item()))
         if it > 0 and hist[-1] >= hist[-2] * (1.0 - tol):
             break

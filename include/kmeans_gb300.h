@@ -243,8 +243,9 @@ int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, f
  * (e.g. NCCL through torch.distributed) and only move bytes, while every
  * addition across ranks happens in the library in rank order, so the result
  * does not depend on how the collective is scheduled.  One iteration:
- *   1. each rank: kmeans_lloyd_iter_partial on its rows (or kmeans_assign +
- *      kmeans_update_partial) -> sums (k, d), counts (k), its inertia;
+ *   1. each rank: kmeans_lloyd_iter_partial on its rows (or, when the shard
+ *      has at least k samples, kmeans_assign + kmeans_update_partial) ->
+ *      sums (k, d), counts (k), its inertia;
  *   2. all-to-all: rank q receives every rank's rows [q*m, q*m + m) of the
  *      sums and counts (m = ceil(k / world), zero rows past k);
  *   3. each rank: kmeans_reduce_partials on its slice -> C_new rows, counts;

@@ -65,6 +65,13 @@ def test_one_rank_partial_then_reduce_is_the_lloyd_iteration(gpu_lib, shape):
     assert host(best).tobytes() == ref[2].tobytes()
     assert float(inertia.item()) == float(ref[3][0])
     np.testing.assert_array_equal(host(counts), ref[4])
+    # on a stream of its own (the library's kernels and the collectives all
+    # run on it), the same bits
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    C2, counts2, _, _, inertia2 = sharded.lloyd_iter_sharded(Xd, Cd, OneRank(), stream=side)
+    side.synchronize()
+    assert host(C2).tobytes() == ref[0].tobytes() and float(inertia2.item()) == float(ref[3][0])
 
 
 @pytest.mark.parametrize("shape", [(3000, 50, 64), (2000, 513, 132), (300, 700, 36), (100000, 20, 12),
@@ -181,7 +188,8 @@ def _rank_main(rank, world, port, case, q):
     (6000, 300, 132, (3000, 3000), (30, 4, 7)),
     (1000, 700, 64, (400, 600), (20, 3, 9)),   # more centroids than either shard has samples
     (20000, 1024, 256, (9000, 11000), (64, 0, 11)),
-], ids=["k300", "k700_more_than_a_shard", "k1024"])
+    (3000, 1, 64, (1000, 2000), (1, 2, 3)),   # one centroid: rank 1 reduces no row
+], ids=["k300", "k700_more_than_a_shard", "k1024", "k1"])
 def test_two_ranks_sharing_this_gpu(gpu_lib, case):
     import torch.multiprocessing as mp
     n, k, d, splits, (kk, T, seed) = case

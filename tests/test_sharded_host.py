@@ -175,7 +175,8 @@ def _rank_main(rank, world, port, case, q):
     (500, 5, 6, (120, 200, 180)),  # three ranks, unequal shards; the last rank reduces one row
     (240, 3, 4, (100, 140)),       # fewer centroids than ranks x 2
     (90, 40, 5, (30, 30, 30)),     # more centroids than any shard has samples
-], ids=["k7_w2", "k5_w3", "k3_w2", "k40_w3"])
+    (60, 2, 3, (20, 25, 15)),      # fewer centroids than ranks: the last rank reduces no row
+], ids=["k7_w2", "k5_w3", "k3_w2", "k40_w3", "k2_w3"])
 def test_sharded_iteration_and_seeding_match_the_oracle(case):
     import torch.multiprocessing as mp
     sys.path.insert(0, ROOT)
