@@ -269,3 +269,52 @@ def test_sharded_fit_stops_where_the_oracle_fit_stops():
         np.testing.assert_allclose(hist, o_hist, rtol=1e-6)
         np.testing.assert_array_equal(labels, o_lab[b[r]:b[r + 1]])
         assert (np.abs(C - o_C) <= 1e-5 * np.abs(o_C).max(axis=1, keepdims=True)).all()
+
+
+class FailingOps(FakeOps):
+    """The stand-in, except that this rank's shard step raises (a rank that
+    fails before the exchange)."""
+
+    def kmeans_lloyd_iter_partial(self, X, C, ws=None, stream=None):
+        raise RuntimeError("planted failure of this rank's shard step")
+
+
+def _failing_rank_main(rank, world, port, q):
+    import datetime
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import synth
+    from distance_argmin_gb300 import sharded
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=10))
+    X, C0, _ = synth.workload_inputs(synth.Workload("t", 400, 5, 8, 5, 1, 65, 66, ""))
+    Xl = torch.from_numpy(np.ascontiguousarray(X[rank * 200:(rank + 1) * 200]))
+    ops = FailingOps() if rank == 1 else FakeOps()
+    try:
+        sharded.lloyd_iter_sharded(Xl, torch.from_numpy(C0), sharded.Exchange(), ops=ops)
+        q.put((rank, "finished"))
+    except Exception as e:  # the failing rank's own error, or the survivor's collective error
+        q.put((rank, type(e).__name__ + ": " + str(e)[:200]))
+    # no destroy_process_group: the peer is gone
+
+
+def test_a_failing_rank_ends_the_others_collective_with_an_error():
+    # Rank 1 raises before its first collective and leaves; rank 0's
+    # all-to-all must end with an error (the peer closed, or the process
+    # group's 10 s timeout), not hang.
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_failing_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        if p.is_alive():
+            p.kill()
+    assert "planted failure" in got[1]
+    assert got[0] != "finished", got[0]
