@@ -15,11 +15,14 @@
 // lo_x.lo_c term.  The tensor cores add each 16-wide partial product into the
 // float32 accumulator with a truncating add, so every MMA into an accumulator
 // of magnitude |x.c| costs up to one unit in its last place, always in the
-// same direction.  Two accumulator modes (template DB):
+// same direction.  Three accumulator modes (templates DB, WIDE):
 //   d <= 4096  the three products share one accumulator per tile, and two
 //              such accumulators are double-buffered in tensor memory, so the
 //              epilogue of one tile overlaps the MMAs of the next;
-//   d >  4096  hi.hi gets an accumulator of its own and the two small
+//   d <= 8192  (WIDE) a CTA pair computes two adjacent 256-column tiles at
+//              once, each with one accumulator, single-buffered: every X
+//              k-block is split once for 512 centroids instead of 256;
+//   d >  8192  hi.hi gets an accumulator of its own and the two small
 //              correction products another (only d/16 truncating adds act at
 //              the magnitude of x.c, not 3 d/16; the corrections stay about
 //              2^8 smaller), added in float32 in the epilogue, single-buffered.
@@ -96,13 +99,26 @@ constexpr int TMEM_COLS = 2 * BN;              // either main + corrections, or 
 // tile and the accumulators are double-buffered, so the epilogue of one tile
 // overlaps the MMAs of the next.  The tensor cores' truncating float32
 // accumulation then costs about 6e-9 * d relative (measured 1.01e-4 at
-// d = 16384); beyond this size the correction products keep their own
-// accumulator (single-buffered), which is about 3x more accurate.
+// d = 16384); the wide units below extend the one accumulator to d = 8192,
+// and beyond that the correction products keep their own accumulator
+// (single-buffered), which is about 3x more accurate.
 constexpr int SINGLE_ACC_MAX_D = 4096;
 // 3xTF32 issues an MMA per 8 features instead of 16, twice the truncating
 // adds (measured 8.4e-5 relative with one accumulator at d = 4096, against
 // 2.7e-5 for bf16x3), so its single-accumulator limit is half as large.
 constexpr int SINGLE_ACC_MAX_D_TF32 = 2048;
+// Above SINGLE_ACC_MAX_D and up to this many features, bf16x3 runs wide
+// units: a CTA pair computes 256 samples x 512 centroids (two 256-column
+// tiles), each tile's three products in one accumulator, the two filling the
+// 512 tensor-memory columns (single-buffered).  Every split of an X k-block
+// then feeds twice the MMAs: at the power cap the X split costs energy the
+// tensor cores could use (halving its work measured about 5% on the
+// sample-heavy shape; the wide units as a whole ran that shape's assignment
+// 12.5% faster).  One accumulator at d = 8192 carries about twice the
+// truncation error of d = 4096 (about 6e-9 * d; measured 5.6e-5 over every
+// row of the sample- and centroid-heavy shapes), inside the 1e-4 bound; above
+// this size the separate accumulators are needed.
+constexpr int WIDE_MAX_D = 8192;
 constexpr int GROUP_M = 8;                     // pair sample blocks per raster band
 constexpr uint16_t PAIR_MASK = 0x3;
 static_assert(SPLIT_WARPS % 4 == 0 && WARP_EPI % 4 == 0, "epilogue warps start on a lane-quarter boundary");
@@ -119,14 +135,17 @@ static_assert(kKSplitSlotBytes == 2 * BM * BN * 4 && kKSplitSyncWords == 2 * EPI
 //          hi) and write lo beside it, the prologue writes C's hi and lo as
 //          fp32; everything keeps the 128-byte-swizzled K-major layout of
 //          the fp32 tiles, and an MMA covers K = 8.
-template <bool TF32>
+template <bool TF32, bool WIDE = false>
 struct Fmt {
+    static constexpr int NT = WIDE ? 2 : 1;                        // centroid tiles per work unit
     static constexpr int B_BYTES = BN_CTA * BK * (TF32 ? 4 : 2);  // one C part per CTA
     static constexpr int A_STAGE = TF32 ? BM * BK * 4 : 2 * BM * BK * 2;  // lo (tf32) or hi + lo (bf16)
     static constexpr int A_LO = TF32 ? 0 : BM * BK * 2;                   // offset of lo in an A stage
-    static constexpr int XB_STAGE = X_BYTES + 2 * B_BYTES;
-    static constexpr int SXB = TF32 ? 3 : 4;   // X + C stages (TMA ring)
-    static constexpr int SA = TF32 ? 4 : 6;    // split-X stages
+    static constexpr int XB_STAGE = X_BYTES + 2 * NT * B_BYTES;  // X, then hi and lo of each centroid tile
+    // X + C stages (TMA ring) and split-X stages; a wide stage carries twice
+    // the MMA work, so fewer stages cover as much time
+    static constexpr int SXB = TF32 ? 3 : (WIDE ? 3 : 4);
+    static constexpr int SA = TF32 ? 4 : (WIDE ? 5 : 6);
     static constexpr int A_BASE = SXB * XB_STAGE;
     static constexpr int BAR_BASE = A_BASE + SA * A_STAGE;
     static constexpr int SMEM_BYTES = BAR_BASE + BAR_BYTES + 1024;  // + alignment slack
@@ -324,12 +343,16 @@ __device__ __forceinline__ void fused_accumulate_rows(const TcParams &p, int row
 }
 
 // DB: one accumulator per tile, double-buffered (d <= SINGLE_ACC_MAX_D); TF32:
-// the 3xTF32 operand split instead of bf16x3 (see Fmt)
-template <bool DB, bool TF32, bool FUSED = false>
+// the 3xTF32 operand split instead of bf16x3 (see Fmt); WIDE: 256 x 512
+// units, one accumulator per 256-column tile, single-buffered (bf16x3,
+// SINGLE_ACC_MAX_D < d <= WIDE_MAX_D)
+template <bool DB, bool TF32, bool FUSED = false, bool WIDE = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     assign_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmChi,
                      const __grid_constant__ CUtensorMap tmClo, const TcParams p) {
-    using F = tc::Fmt<TF32>;
+    using F = tc::Fmt<TF32, WIDE>;
+    static_assert(!WIDE || (!DB && !TF32 && !FUSED), "wide units: bf16x3, single-buffered, no fused update");
+    constexpr int UNIT_N = F::NT * tc::BN;  // centroid columns of one work unit
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -451,7 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             if (!mbar_wait_warp(bar(F::T_FULL + buf), phase, p.status)) break;
             tc_fence_after();
             const uint32_t acc_base = tmem_base + (DB ? (uint32_t)(buf * tc::BN) : (uint32_t)tc::ACC_MAIN);
-            const int n0 = nb * tc::BN + part * tc::EPI_COLS;
+            const int n0 = nb * UNIT_N + part * tc::EPI_COLS;
             const float *parked = nullptr;  // the other K half's accumulator, to add before the argmin
             if constexpr (DB && !FUSED) {
                 if (un.half >= 0) {
@@ -505,15 +528,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
             }
             float best = __int_as_float(0x7f800000);  // +inf
             int arg = -1;
+            // the unit's tiles in column order (one, or two when wide), so that
+            // the strict comparison keeps the lowest index on ties
+#pragma unroll 1
+            for (int t2 = 0; t2 < F::NT; ++t2) {
 #pragma unroll 1
             for (int ch = 0; ch < tc::EPI_COLS / tc::EPI_CHUNK; ++ch) {
-                const int j0 = n0 + ch * tc::EPI_CHUNK;
+                const int j0 = n0 + t2 * tc::BN + ch * tc::EPI_CHUNK;
                 if (j0 >= p.k) break;
-                const uint32_t col = (uint32_t)(part * tc::EPI_COLS + ch * tc::EPI_CHUNK);
+                const uint32_t col = (uint32_t)(t2 * tc::BN + part * tc::EPI_COLS + ch * tc::EPI_CHUNK);
                 const uint32_t lanes = (uint32_t)(q * 32) << 16;
                 // x.c of this chunk's columns: one accumulator, or main + corrections
                 float vm[tc::EPI_CHUNK], vc[tc::EPI_CHUNK];
-                if constexpr (DB) {
+                if constexpr (DB || WIDE) {
                     tmem_ld_one<tc::EPI_CHUNK>(acc_base + lanes + col, vm);
                     if constexpr (!FUSED) {
                         if (parked) {
@@ -557,6 +584,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                     }
                 }
             }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(F::T_EMPTY + buf), 0));
@@ -590,7 +618,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 int mb, nb;
                 tile_coords(un.tile, p.num_m, p.num_n, mb, nb);
                 const int m0 = mb * (2 * tc::BM) + (int)rank * tc::BM;
-                const int c0 = nb * tc::BN + (int)rank * tc::BN_CTA;
+                const int c0 = nb * UNIT_N + (int)rank * tc::BN_CTA;
                 for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
                     const int s = it % F::SXB;
                     if (!mbar_wait(bar(F::XB_EMPTY + s), ((it / F::SXB) & 1) ^ 1, p.status)) {
@@ -602,6 +630,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                     tma_load_2d(st, &tmX, bar(F::XB_FULL + s), kb * tc::BK, m0);
                     tma_load_2d(st + tc::X_BYTES, &tmChi, bar(F::XB_FULL + s), kb * tc::BK, c0);
                     tma_load_2d(st + tc::X_BYTES + F::B_BYTES, &tmClo, bar(F::XB_FULL + s), kb * tc::BK, c0);
+                    if constexpr (WIDE) {  // the unit's second centroid tile (zero rows past k)
+                        tma_load_2d(st + tc::X_BYTES + 2 * F::B_BYTES, &tmChi, bar(F::XB_FULL + s), kb * tc::BK,
+                                    c0 + tc::BN);
+                        tma_load_2d(st + tc::X_BYTES + 3 * F::B_BYTES, &tmClo, bar(F::XB_FULL + s), kb * tc::BK,
+                                    c0 + tc::BN);
+                    }
                 }
             }
             if (!ok) {
@@ -625,7 +659,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 if (!mbar_wait_cluster(bar(F::T_EMPTY + buf), phase ^ 1, p.status)) break;
                 tc_fence_after();
                 const uint32_t dm = DB ? tmem_base + (uint32_t)(buf * tc::BN) : d_main;
-                const uint32_t dc = DB ? dm : d_corr;
+                const uint32_t dc = (DB || WIDE) ? dm : d_corr;  // one accumulator per tile, or main + corrections
+                const uint32_t dw = tmem_base + tc::BN;           // wide: the second tile's accumulator
                 // whole tiles keep a loop of their own: any per-unit logic in it
                 // measured 1.3% on the whole kernel
                 if (unit < p.num_full) {
@@ -644,12 +679,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                         // MMAs remain between it and the tensor pipe (measured: the
                         // issue latency here is on the critical path)
                         uint64_t dah[F::K_STEPS], dal[F::K_STEPS], dbh[F::K_STEPS], dbl[F::K_STEPS];
+                        uint64_t dwh[F::K_STEPS], dwl[F::K_STEPS];  // wide: the second tile's hi and lo
     #pragma unroll
                         for (int kk = 0; kk < F::K_STEPS; ++kk) {
                             dah[kk] = umma_smem_desc(ahi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
                             dal[kk] = umma_smem_desc(alo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
                             dbh[kk] = umma_smem_desc(bhi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
                             dbl[kk] = umma_smem_desc(blo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            if constexpr (WIDE) {
+                                dwh[kk] = umma_smem_desc(blo + F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                                dwl[kk] = umma_smem_desc(blo + 2 * F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            }
                         }
                         // both CTAs' split warps have seen their X and C stage land
                         if (!mbar_wait_cluster(bar(F::A_FULL + as), (it / F::SA) & 1, p.status)) {
@@ -666,8 +706,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                                 mma_tf32_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
                             } else {
                                 mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
-                                mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
+                                mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, (DB || WIDE) ? 1u : first);
                                 mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                                if constexpr (WIDE) {
+                                    mma_bf16_ss_pair(dw, dah[kk], dwh[kk], idesc, first);
+                                    mma_bf16_ss_pair(dw, dal[kk], dwh[kk], idesc, 1u);
+                                    mma_bf16_ss_pair(dw, dah[kk], dwl[kk], idesc, 1u);
+                                }
                             }
                         }
                         mma_commit_pair_multicast(bar(F::XB_EMPTY + s), tc::PAIR_MASK);
@@ -690,12 +735,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                         // MMAs remain between it and the tensor pipe (measured: the
                         // issue latency here is on the critical path)
                         uint64_t dah[F::K_STEPS], dal[F::K_STEPS], dbh[F::K_STEPS], dbl[F::K_STEPS];
+                        uint64_t dwh[F::K_STEPS], dwl[F::K_STEPS];  // wide: the second tile's hi and lo
     #pragma unroll
                         for (int kk = 0; kk < F::K_STEPS; ++kk) {
                             dah[kk] = umma_smem_desc(ahi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
                             dal[kk] = umma_smem_desc(alo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
                             dbh[kk] = umma_smem_desc(bhi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
                             dbl[kk] = umma_smem_desc(blo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            if constexpr (WIDE) {
+                                dwh[kk] = umma_smem_desc(blo + F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                                dwl[kk] = umma_smem_desc(blo + 2 * F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                            }
                         }
                         // both CTAs' split warps have seen their X and C stage land
                         if (!mbar_wait_cluster(bar(F::A_FULL + as), (it / F::SA) & 1, p.status)) {
@@ -712,8 +762,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                                 mma_tf32_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
                             } else {
                                 mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
-                                mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
+                                mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, (DB || WIDE) ? 1u : first);
                                 mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                                if constexpr (WIDE) {
+                                    mma_bf16_ss_pair(dw, dah[kk], dwh[kk], idesc, first);
+                                    mma_bf16_ss_pair(dw, dal[kk], dwh[kk], idesc, 1u);
+                                    mma_bf16_ss_pair(dw, dah[kk], dwl[kk], idesc, 1u);
+                                }
                             }
                         }
                         mma_commit_pair_multicast(bar(F::XB_EMPTY + s), tc::PAIR_MASK);
@@ -840,6 +895,9 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(assign_tc_kernel<true, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      tc::Fmt<false>::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(assign_tc_kernel<false, false, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Fmt<false, true>::SMEM_BYTES);
         return e;
     };
     if (dev < 0) {
@@ -867,12 +925,17 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
                    cswz))
         return cudaErrorInvalidValue;
 
+    // accumulator mode: one double-buffered accumulator per tile up to
+    // SINGLE_ACC_MAX_D; above, bf16x3 runs wide units (two tiles, one
+    // accumulator each) up to WIDE_MAX_D and separate accumulators beyond
+    const bool db = d <= (tf32 ? tc::SINGLE_ACC_MAX_D_TF32 : tc::SINGLE_ACC_MAX_D);
+    const bool wide = !db && !tf32 && !fused && d <= tc::WIDE_MAX_D;
     TcParams p{};
     p.n = (int)n;
     p.k = (int)k;
     p.d = (int)d;
     p.num_m = (int)((n + 2 * tc::BM - 1) / (2 * tc::BM));
-    p.num_n = (int)((k + tc::BN - 1) / tc::BN);
+    p.num_n = (int)((k + (wide ? 2 : 1) * tc::BN - 1) / ((wide ? 2 : 1) * tc::BN));  // work-unit columns
     p.num_kb = (int)((d + tc::BK - 1) / tc::BK);
     p.num_tiles = p.num_m * p.num_n;
     p.cnorm = reinterpret_cast<const float *>(ws + L.off_cnorm);
@@ -892,7 +955,6 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     const int max_pairs = resident_pairs();
     const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
     const int grid = 2 * (pairs > 0 ? pairs : 1);
-    const bool db = d <= (tf32 ? tc::SINGLE_ACC_MAX_D_TF32 : tc::SINGLE_ACC_MAX_D);
     // K split of a last round that is at most half full (double-buffered
     // accumulators only, not the fused update): its tiles run as two K halves
     // on two pairs each, about half a round instead of a whole one
@@ -926,11 +988,15 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
                                tmClo, p)
                : launch_kernel(chained, assign_tc_kernel<false, true>, g, b, tc::Fmt<true>::SMEM_BYTES, stream, tmX,
                                tmChi, tmClo, p);
+    else if (db)
+        e = launch_kernel(chained, assign_tc_kernel<true, false>, g, b, tc::Fmt<false>::SMEM_BYTES, stream, tmX, tmChi,
+                          tmClo, p);
+    else if (wide)
+        e = launch_kernel(chained, assign_tc_kernel<false, false, false, true>, g, b, tc::Fmt<false, true>::SMEM_BYTES,
+                          stream, tmX, tmChi, tmClo, p);
     else
-        e = db ? launch_kernel(chained, assign_tc_kernel<true, false>, g, b, tc::Fmt<false>::SMEM_BYTES, stream, tmX,
-                               tmChi, tmClo, p)
-               : launch_kernel(chained, assign_tc_kernel<false, false>, g, b, tc::Fmt<false>::SMEM_BYTES, stream, tmX,
-                               tmChi, tmClo, p);
+        e = launch_kernel(chained, assign_tc_kernel<false, false>, g, b, tc::Fmt<false>::SMEM_BYTES, stream, tmX, tmChi,
+                          tmClo, p);
     trace_mark(kTraceAssignTc, true, stream);
     return e;
 }

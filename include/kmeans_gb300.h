@@ -31,9 +31,9 @@
  *  - Precision: inputs must be finite.  The assignment contraction runs on the
  *    tensor cores as three bf16 products of an error-compensated split of
  *    each float32 operand (hi = bf16(v), lo = bf16(v - hi)) with float32
- *    accumulation (up to d = 4096 the three products share one accumulator;
- *    above, the two correction products keep their own, which is about three
- *    times more accurate); the reported distance is within
+ *    accumulation (up to d = 8192 the three products share one accumulator
+ *    per tile; above, the two correction products keep their own, which is
+ *    about three times more accurate); the reported distance is within
  *    1e-4 * (||x||^2 + ||c||^2) of the exact one for d up to about 16384 (the
  *    error of the float32 tensor-core accumulation grows about linearly with
  *    d).  Ties between centroids go to the lowest index.
@@ -121,7 +121,8 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d);
  * Extra requirement of this tensor-core path: d % 4 == 0 and X, C 16-byte
  * aligned (KMEANS_ERR_UNSUPPORTED otherwise; kmeans_assign_ffma has none).
  * Schedule: pairs of SMs work through 256 x 256 tiles of (samples,
- * centroids) in rounds; when the last round is at most half full (and d <=
+ * centroids), or 256 x 512 units of two such tiles for 4096 < d <= 8192,
+ * in rounds; when the last round is at most half full (and d <=
  * 4096), each of its tiles is computed as two halves of the features on two
  * pairs and the halves' sums are added at the end.  Those tiles' distances
  * carry a different (no larger) float32 accumulation error than a single
