@@ -16,22 +16,26 @@
 // float32 accumulator with a truncating add, so every MMA into an accumulator
 // of magnitude |x.c| costs up to one unit in its last place, always in the
 // same direction.  Three accumulator modes (templates DB, WIDE):
-//   d <= 4096  the three products share one accumulator per tile, and two
-//              such accumulators are double-buffered in tensor memory, so the
-//              epilogue of one tile overlaps the MMAs of the next;
-//   d <= 8192  (WIDE) a CTA pair computes two adjacent 256-column tiles at
-//              once, each with one accumulator, single-buffered: every X
-//              k-block is split once for 512 centroids instead of 256;
-//   d >  8192  hi.hi gets an accumulator of its own and the two small
-//              correction products another (only d/16 truncating adds act at
-//              the magnitude of x.c, not 3 d/16; the corrections stay about
-//              2^8 smaller), added in float32 in the epilogue, single-buffered.
+//   DB    d < 2048 (and up to 4096 where wide units do not apply: k <= 256,
+//         the fused update, 3xTF32 up to 2048): the three products share one
+//         accumulator per tile, and two such accumulators are double-buffered
+//         in tensor memory, so the epilogue of one tile overlaps the MMAs of
+//         the next;
+//   WIDE  2048 <= d <= 8192: a CTA pair computes two adjacent 256-column
+//         tiles at once, each with one accumulator, single-buffered: every X
+//         k-block is split once for 512 centroids instead of 256;
+//   else  (d > 8192, or 3xTF32 above 2048): hi.hi gets an accumulator of its
+//         own and the two small correction products another (only d/16
+//         truncating adds act at the magnitude of x.c, not 3 d/16; the
+//         corrections stay about 2^8 smaller), added in float32 in the
+//         epilogue, single-buffered.
 // Template TF32 swaps the split for 3xTF32 (see Fmt), a comparator; template
 // FUSED adds the mean update's accumulation to the epilogue
 // (kmeans_lloyd_iter_fused), another comparator.
 //
 // Structure: CTA pairs (clusters of 2, tcgen05 cta_group::2), persistent over
-// a grouped tile order.  A pair owns a 256-sample x 256-centroid tile: each
+// a grouped tile order.  A pair owns a 256-sample x 256-centroid tile (two
+// side by side when wide; below, one tile): each
 // CTA holds 128 samples (its half of A, the rows of its tensor memory) and
 // 128 centroids (its half of B); the even CTA issues the M = 256 MMAs for both.
 //   warp 16      TMA producer (each CTA): its X rows (fp32) and its C rows
@@ -95,22 +99,23 @@ constexpr int BAR_BYTES = 256;
 constexpr int ACC_MAIN = 0;                    // tensor-memory columns (separate accumulators)
 constexpr int ACC_CORR = BN;
 constexpr int TMEM_COLS = 2 * BN;              // either main + corrections, or two single accumulators
-// Up to this many features the three products share one accumulator per
-// tile and the accumulators are double-buffered, so the epilogue of one tile
-// overlaps the MMAs of the next.  The tensor cores' truncating float32
-// accumulation then costs about 6e-9 * d relative (measured 1.01e-4 at
-// d = 16384); the wide units below extend the one accumulator to d = 8192,
-// and beyond that the correction products keep their own accumulator
-// (single-buffered), which is about 3x more accurate.
+// Where wide units (below) do not apply, up to this many features the three
+// products share one accumulator per tile and the accumulators are
+// double-buffered, so the epilogue of one tile overlaps the MMAs of the next.
+// The tensor cores' truncating float32 accumulation then costs about
+// 6e-9 * d relative (measured 1.01e-4 at d = 16384); the wide units keep one
+// accumulator up to d = 8192, and beyond that the correction products keep
+// their own accumulator (single-buffered), which is about 3x more accurate.
 constexpr int SINGLE_ACC_MAX_D = 4096;
 // 3xTF32 issues an MMA per 8 features instead of 16, twice the truncating
 // adds (measured 8.4e-5 relative with one accumulator at d = 4096, against
 // 2.7e-5 for bf16x3), so its single-accumulator limit is half as large.
 constexpr int SINGLE_ACC_MAX_D_TF32 = 2048;
-// Above SINGLE_ACC_MAX_D and up to this many features, bf16x3 runs wide
-// units: a CTA pair computes 256 samples x 512 centroids (two 256-column
-// tiles), each tile's three products in one accumulator, the two filling the
-// 512 tensor-memory columns (single-buffered).  Every split of an X k-block
+// From WIDE_MIN_D up to this many features, with more than one tile of
+// centroids, bf16x3 runs wide units: a CTA pair computes 256 samples x 512
+// centroids (two 256-column tiles), each tile's three products in one
+// accumulator, the two filling the 512 tensor-memory columns
+// (single-buffered).  Every split of an X k-block
 // then feeds twice the MMAs: at the power cap the X split costs energy the
 // tensor cores could use (halving its work measured about 5% on the
 // sample-heavy shape; the wide units as a whole ran that shape's assignment
@@ -119,6 +124,12 @@ constexpr int SINGLE_ACC_MAX_D_TF32 = 2048;
 // row of the sample- and centroid-heavy shapes), inside the 1e-4 bound; above
 // this size the separate accumulators are needed.
 constexpr int WIDE_MAX_D = 8192;
+// Wide units pay off from this many features (and more than one tile of
+// centroids): on lloyd10 (d = 2048) they ran 3.7% faster than the
+// double-buffered single tiles, whose overlapped epilogue matters less than
+// halving the split; with fewer features the epilogue's share grows, and the
+// double-buffered tiles (with their K split of a short last round) stay.
+constexpr int WIDE_MIN_D = 2048;
 constexpr int GROUP_M = 8;                     // pair sample blocks per raster band
 constexpr uint16_t PAIR_MASK = 0x3;
 static_assert(SPLIT_WARPS % 4 == 0 && WARP_EPI % 4 == 0, "epilogue warps start on a lane-quarter boundary");
@@ -925,11 +936,12 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
                    cswz))
         return cudaErrorInvalidValue;
 
-    // accumulator mode: one double-buffered accumulator per tile up to
-    // SINGLE_ACC_MAX_D; above, bf16x3 runs wide units (two tiles, one
-    // accumulator each) up to WIDE_MAX_D and separate accumulators beyond
-    const bool db = d <= (tf32 ? tc::SINGLE_ACC_MAX_D_TF32 : tc::SINGLE_ACC_MAX_D);
-    const bool wide = !db && !tf32 && !fused && d <= tc::WIDE_MAX_D;
+    // accumulator mode: bf16x3 runs wide units (two tiles, one accumulator
+    // each) for WIDE_MIN_D <= d <= WIDE_MAX_D when there is more than one
+    // tile of centroids; otherwise one double-buffered accumulator per tile
+    // up to SINGLE_ACC_MAX_D, and separate accumulators beyond
+    const bool wide = !tf32 && !fused && d >= tc::WIDE_MIN_D && d <= tc::WIDE_MAX_D && k > tc::BN;
+    const bool db = !wide && d <= (tf32 ? tc::SINGLE_ACC_MAX_D_TF32 : tc::SINGLE_ACC_MAX_D);
     TcParams p{};
     p.n = (int)n;
     p.k = (int)k;

@@ -121,10 +121,10 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d);
  * Extra requirement of this tensor-core path: d % 4 == 0 and X, C 16-byte
  * aligned (KMEANS_ERR_UNSUPPORTED otherwise; kmeans_assign_ffma has none).
  * Schedule: pairs of SMs work through 256 x 256 tiles of (samples,
- * centroids), or 256 x 512 units of two such tiles for 4096 < d <= 8192,
- * in rounds; when the last round is at most half full (and d <=
- * 4096), each of its tiles is computed as two halves of the features on two
- * pairs and the halves' sums are added at the end.  Those tiles' distances
+ * centroids), or 256 x 512 units of two such tiles for 2048 <= d <= 8192
+ * with k > 256, in rounds; when the last round of single tiles is at most
+ * half full (d <= 4096), each of its tiles is computed as two halves of the
+ * features on two pairs and the halves' sums are added at the end.  Those tiles' distances
  * carry a different (no larger) float32 accumulation error than a single
  * pass would, within the accuracy stated above; the results are the same
  * from run to run on a given GPU.

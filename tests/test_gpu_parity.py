@@ -353,6 +353,24 @@ def test_large_workload_one_iteration(gpu_lib, name, record_property):
     assert np.isfinite(bd).all() and (bd >= 0).all()
 
 
+@pytest.mark.parametrize("shape", [(3000, 300, 2048), (5000, 700, 4100), (2600, 257, 8192), (9000, 1100, 2052)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_wide_units_with_ragged_centroid_columns(gpu_lib, shape):
+    # wide units (two 256-column tiles per CTA pair) where the second tile
+    # is partly or, in the last unit column, entirely past k; ragged rows
+    n, k, d = shape
+    X, _, _ = synth.planted_blobs(n, d, max(1, k // 3), seed=n + d)
+    C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=k)])
+    C1, labels, best, inertia, counts = gpu_lib.kmeans_lloyd_iter(dev_tensor(X), dev_tensor(C))
+    o_l, o_b, o_s, o_in = oracle.assign(X, C)
+    check_assign(X, C, host(labels), host(best), o_l, o_b, o_s, what=f"wide {shape}")
+    scale = (sq_norms(X) + sq_norms(C)[o_l]).sum()
+    assert abs(float(inertia.item()) - o_in) <= DIST_RTOL * scale
+    o_C1, o_cnt = oracle.update(X, host(labels), C)
+    check_centroids(host(C1), o_C1, what=f"wide {shape} update")
+    assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+
+
 @pytest.mark.parametrize("impl,d", [("tc", 4096), ("tc", 4100), ("tf32", 2048), ("tf32", 2052), ("tf32", 8192)])
 def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d, impl):
     # up to 4096 features (bf16x3; 2048 for 3xTF32) the three split products
