@@ -250,7 +250,7 @@ __device__ __forceinline__ void load4x2(const float *__restrict__ p, int avail, 
 template <bool VEC>
 __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand,
-                         const float *__restrict__ crows, int T, int t0, int W, float2 *__restrict__ dpart) {
+                         const float *__restrict__ crows, int T, int t0, int W, int rev, float2 *__restrict__ dpart) {
     extern __shared__ __align__(16) float cs[];  // [KT][W], negated
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -269,12 +269,17 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     // block of 24 warps per SM fits it in 85 registers a thread; more resident
     // warps hide more of the loads (16, 20, 24 and 28 warps measured 397, 375,
     // 363 and 386 us a pass).
+    //
+    // With `rev` set the block visits its groups from the top of X down: the
+    // pass then starts on the rows the previous pass read last, which are
+    // still in L2.  The i-th group a block visits is group(i) either way.
     float2 x[kd::ROWS][4], xn[kd::ROWS][4];
-    auto load_first_step = [&](int64_t gg) {
-        const int64_t rr = gg * kd::GROUP + warp * kd::ROWS;
+    auto group = [&](int64_t i) { return rev ? n_groups - 1 - i : i; };
+    auto load_first_step = [&](int64_t i) {
+        const int64_t rr = (i < n_groups ? group(i) : n_groups) * kd::GROUP + warp * kd::ROWS;
 #pragma unroll
         for (int r = 0; r < kd::ROWS; ++r) {
-            if (rr + r < n) {  // a group past the last one has every row past n
+            if (rr + r < n) {  // past the last group every row is past n
                 load4x2<VEC>(X + (rr + r) * (int64_t)d + fb + lane * 4, width - lane * 4, xn[r]);
             } else {
 #pragma unroll
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     __syncthreads();
 
     for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x) {
-        const int64_t r0 = g * kd::GROUP + warp * kd::ROWS;
+        const int64_t r0 = group(g) * kd::GROUP + warp * kd::ROWS;
         float2 s2[kd::KT];  // .x row 0, .y row 1
 #pragma unroll
         for (int t = 0; t < kd::KT; ++t) s2[t] = make_float2(0.f, 0.f);
@@ -520,7 +525,7 @@ __global__ void gather_rows_kernel(const float *__restrict__ X, const int64_t *_
 // potentials).  Candidates: rows cand[] of X, or the rows of `crows`.
 static cudaError_t kpp_dist_pass(const float *X, int64_t n, int64_t d, const KppLayout &L, uint8_t *ws, int Tn,
                                  const int64_t *cand, const float *crows, const double *d2, bool chained_first,
-                                 cudaStream_t s) {
+                                 bool rev, cudaStream_t s) {
     double *dist = reinterpret_cast<double *>(ws + L.off_dist);
     float2 *dpart = reinterpret_cast<float2 *>(ws + L.off_dpart);
     double *bpot = reinterpret_cast<double *>(ws + L.off_bpot);
@@ -552,9 +557,9 @@ static cudaError_t kpp_dist_pass(const float *X, int64_t n, int64_t d, const Kpp
         const bool chained = chained_first || t0 > 0;
         trace_mark(kTraceKppDist, false, s);
         e = vec ? launch_kernel(chained, kpp_dist_part_kernel<true>, dgrid, dim3(kd::THREADS), smem, s, X, n, (int)d,
-                                cand, crows, Tn, t0, L.W, dpart)
+                                cand, crows, Tn, t0, L.W, (int)rev, dpart)
                 : launch_kernel(chained, kpp_dist_part_kernel<false>, dgrid, dim3(kd::THREADS), smem, s, X, n, (int)d,
-                                cand, crows, Tn, t0, L.W, dpart);
+                                cand, crows, Tn, t0, L.W, (int)rev, dpart);
         trace_mark(kTraceKppDist, true, s);
         const int nt = Tn - t0 < kd::KT ? Tn - t0 : kd::KT;
         if (e == cudaSuccess)
@@ -583,14 +588,15 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
     kpp_first_kernel<<<1, 1, 0, s>>>(n, seed, cand, indices, hdr);
     chain(cudaGetLastError());
     // distances to the first center
-    if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, 1, cand, nullptr, nullptr, true, s));
+    if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, 1, cand, nullptr, nullptr, true, false, s));
     for (int64_t c = 1; c < k && e == cudaSuccess; ++c) {
         chain(launch_kernel(true, kpp_update_kernel, dim3((unsigned)L.n_blocks), dim3(kBsThreads), 0, s,
                             (const double *)dist, (const double *)bpot, T, n, L.n_blocks, (const int64_t *)cand, indices,
                             c - 1, c == 1 ? 1 : 0, D2, bsum));
         chain(launch_kernel(true, kpp_pick_kernel, dim3((unsigned)T), dim3(32), 0, s, (const double *)bsum, L.n_blocks,
                             (const double *)D2, n, seed, 1 + (uint64_t)(c - 1) * (uint64_t)T, T, cand));
-        if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, T, cand, nullptr, D2, true, s));
+        // successive passes run in opposite directions over X (see the kernel)
+        if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, T, cand, nullptr, D2, true, (c & 1) != 0, s));
     }
     if (k > 1)
         chain(launch_kernel(true, kpp_select_last_kernel, dim3(1), dim3(256), 0, s, (const double *)bpot, T,
@@ -793,7 +799,7 @@ cudaError_t launch_kpp_shard_dist(const float *X, int64_t n_local, int64_t d, in
                                                (int)d, crow, cglob, &hdr->status);
     cudaError_t e = cudaGetLastError();
     const double *D2 = first ? nullptr : reinterpret_cast<const double *>(ws + L.K.off_d2);
-    if (e == cudaSuccess) e = kpp_dist_pass(X, n_local, d, L.K, ws, Tn, nullptr, crow, D2, true, s);
+    if (e == cudaSuccess) e = kpp_dist_pass(X, n_local, d, L.K, ws, Tn, nullptr, crow, D2, true, false, s);
     if (e == cudaSuccess && !first)
         e = launch_kernel(true, kpp_shard_potentials_kernel, dim3(1), dim3(256), 0, s,
                           (const double *)(ws + L.K.off_bpot), T, L.K.n_blocks, pot_out);
