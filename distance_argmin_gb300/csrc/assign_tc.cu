@@ -15,20 +15,26 @@
 // lo_x.lo_c term.  The tensor cores add each 16-wide partial product into the
 // float32 accumulator with a truncating add, so every MMA into an accumulator
 // of magnitude |x.c| costs up to one unit in its last place, always in the
-// same direction.  Three accumulator modes (templates DB, WIDE):
+// same direction.  Accumulator modes (templates DB, WIDE, CHUNKED):
 //   DB    d < 2048 (and up to 4096 where wide units do not apply: k <= 256,
 //         the fused update, 3xTF32 up to 2048): the three products share one
 //         accumulator per tile, and two such accumulators are double-buffered
 //         in tensor memory, so the epilogue of one tile overlaps the MMAs of
 //         the next;
-//   WIDE  2048 <= d <= 8192: a CTA pair computes two adjacent 256-column
+//   WIDE  d >= 2048 with k > 256: a CTA pair computes two adjacent 256-column
 //         tiles at once, each with one accumulator, single-buffered: every X
-//         k-block is split once for 512 centroids instead of 256;
-//   else  (d > 8192, or 3xTF32 above 2048): hi.hi gets an accumulator of its
-//         own and the two small correction products another (only d/16
-//         truncating adds act at the magnitude of x.c, not 3 d/16; the
-//         corrections stay about 2^8 smaller), added in float32 in the
-//         epilogue, single-buffered.
+//         k-block is split once for 512 centroids instead of 256.  Above
+//         8192 features (CHUNKED) K runs in chunks of at most 8192: after
+//         each chunk but the last the epilogue adds the raw accumulator into
+//         a running sum the CTA keeps in the workspace and hands the
+//         accumulator back, and the last chunk's epilogue adds the running
+//         sum before the argmin.  The truncation error is then that of one
+//         chunk, as at d = 8192, at any d;
+//   else  (d > 4096 with k <= 256, the built-in scratch above 8192, or 3xTF32
+//         above 2048): hi.hi gets an accumulator of its own and the two small
+//         correction products another (only d/16 truncating adds act at the
+//         magnitude of x.c, not 3 d/16; the corrections stay about 2^8
+//         smaller), added in float32 in the epilogue, single-buffered.
 // Template TF32 swaps the split for 3xTF32 (see Fmt), a comparator; template
 // FUSED adds the mean update's accumulation to the epilogue
 // (kmeans_lloyd_iter_fused), another comparator.
@@ -58,7 +64,8 @@
 // of the k-blocks on two pairs (work units, see unit_at).  In the epilogue the
 // half that takes the first ticket parks its raw accumulator in the workspace
 // and tags it; the other waits for the tag and adds the parked part to its
-// own before the argmin.  Whole tiles keep an MMA issue loop of their own.
+// own before the argmin.  Whole tiles, split tiles and chunked units each
+// keep an MMA issue loop of their own around one inlined k-block step.
 // Every wait is bounded; a timeout raises a flag in the status word and both
 // CTAs wind down without hanging.
 #include <cuda.h>
@@ -111,18 +118,17 @@ constexpr int SINGLE_ACC_MAX_D = 4096;
 // adds (measured 8.4e-5 relative with one accumulator at d = 4096, against
 // 2.7e-5 for bf16x3), so its single-accumulator limit is half as large.
 constexpr int SINGLE_ACC_MAX_D_TF32 = 2048;
-// From WIDE_MIN_D up to this many features, with more than one tile of
-// centroids, bf16x3 runs wide units: a CTA pair computes 256 samples x 512
-// centroids (two 256-column tiles), each tile's three products in one
-// accumulator, the two filling the 512 tensor-memory columns
-// (single-buffered).  Every split of an X k-block
-// then feeds twice the MMAs: at the power cap the X split costs energy the
-// tensor cores could use (halving its work measured about 5% on the
-// sample-heavy shape; the wide units as a whole ran that shape's assignment
-// 12.5% faster).  One accumulator at d = 8192 carries about twice the
-// truncation error of d = 4096 (about 6e-9 * d; measured 5.6e-5 over every
-// row of the sample- and centroid-heavy shapes), inside the 1e-4 bound; above
-// this size the separate accumulators are needed.
+// From WIDE_MIN_D features, with more than one tile of centroids, bf16x3
+// runs wide units: a CTA pair computes 256 samples x 512 centroids (two
+// 256-column tiles), each tile's three products in one accumulator, the two
+// filling the 512 tensor-memory columns (single-buffered).  Every split of an
+// X k-block then feeds twice the MMAs: at the power cap the X split costs
+// energy the tensor cores could use (halving its work measured about 5% on
+// the sample-heavy shape; the wide units as a whole ran that shape's
+// assignment 12.5% faster).  One accumulator over this many features carries
+// about twice the truncation error of d = 4096 (about 6e-9 * d; measured
+// 5.6e-5 over every row of the sample- and centroid-heavy shapes), inside the
+// 1e-4 bound; above it the wide units run K in chunks of at most this size.
 constexpr int WIDE_MAX_D = 8192;
 // Wide units pay off from this many features (and more than one tile of
 // centroids): on lloyd10 (d = 2048) they ran 3.7% faster than the
@@ -194,6 +200,11 @@ struct TcParams {
     uint32_t epoch;   // this launch's ready tag: nonzero, unlike any tag left in ksync
     float *kacc;      // parked accumulators [slot][CTA][BM rows][BN columns]
     uint32_t *ksync;  // [slot][CTA][epilogue warp] {ticket, ready tag}
+    // Chunked wide units: K runs in chunks of kb_chunk k-blocks, and each CTA
+    // keeps the running sum of its finished chunks in park (kChunkParkCtaBytes
+    // per CTA, indexed by blockIdx.x).
+    int kb_chunk;
+    float *park;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb) {
@@ -356,14 +367,17 @@ __device__ __forceinline__ void fused_accumulate_rows(const TcParams &p, int row
 // DB: one accumulator per tile, double-buffered (d <= SINGLE_ACC_MAX_D); TF32:
 // the 3xTF32 operand split instead of bf16x3 (see Fmt); WIDE: 256 x 512
 // units, one accumulator per 256-column tile, single-buffered (bf16x3,
-// SINGLE_ACC_MAX_D < d <= WIDE_MAX_D)
-template <bool DB, bool TF32, bool FUSED = false, bool WIDE = false>
+// d >= WIDE_MIN_D, k > 256); CHUNKED: wide units whose K runs in chunks of
+// p.kb_chunk k-blocks with a running sum per CTA (d > WIDE_MAX_D)
+template <bool DB, bool TF32, bool FUSED = false, bool WIDE = false, bool CHUNKED = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
     assign_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmChi,
                      const __grid_constant__ CUtensorMap tmClo, const TcParams p) {
     using F = tc::Fmt<TF32, WIDE>;
     static_assert(!WIDE || (!DB && !TF32 && !FUSED), "wide units: bf16x3, single-buffered, no fused update");
+    static_assert(!CHUNKED || WIDE, "K chunks are a form of the wide units");
     constexpr int UNIT_N = F::NT * tc::BN;  // centroid columns of one work unit
+    constexpr int EPI_CHUNKS = tc::EPI_COLS / tc::EPI_CHUNK;  // tensor-memory loads per tile and epilogue warp
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -475,18 +489,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;              // tensor-memory lane quarter this warp may read
         const int part = (warp - tc::WARP_EPI) >> 2;  // which EPI_COLS of the tile's 256 columns
+        const uint32_t lanes = (uint32_t)(q * 32) << 16;
         int tile_iter = 0;
+        int acc_use = 0;  // single-buffered accumulator: hand-overs so far (one per K chunk of a unit)
+        // chunked wide units: this warp's rows and columns of the CTA's running
+        // sum, interleaved like the K-split parking area below (float4 u4 of
+        // load ch of tile t2 of lane l at ((t2 * EPI_CHUNKS + ch) * 8 + u4) * 32 + l)
+        static_assert(kChunkParkCtaBytes == tc::EPI_WARPS * 32 * 2 * tc::EPI_COLS * 4, "one CTA's running sum");
+        float *const csum = CHUNKED ? p.park + (size_t)blockIdx.x * (kChunkParkCtaBytes / 4) +
+                                          (size_t)(warp - tc::WARP_EPI) * (32 * F::NT * tc::EPI_COLS) + lane * 4
+                                    : nullptr;
         for (int unit = pair; unit < p.num_units; unit += num_pairs, ++tile_iter) {
             const KUnit un = unit_at(p, unit);
             int mb, nb;
             tile_coords(un.tile, p.num_m, p.num_n, mb, nb);
             const int buf = DB ? (tile_iter & 1) : 0;
-            const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (tile_iter & 1);
+            const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (acc_use & 1);
             if (!mbar_wait_warp(bar(F::T_FULL + buf), phase, p.status)) break;
             tc_fence_after();
+            if constexpr (!DB) ++acc_use;
             const uint32_t acc_base = tmem_base + (DB ? (uint32_t)(buf * tc::BN) : (uint32_t)tc::ACC_MAIN);
             const int n0 = nb * UNIT_N + part * tc::EPI_COLS;
-            const float *parked = nullptr;  // the other K half's accumulator, to add before the argmin
+            const float *parked = nullptr;  // the rest of K (other half or earlier chunks), to add before the argmin
+            if constexpr (CHUNKED) {
+                // every K chunk but the last: add the accumulator into the
+                // running sum (the first chunk stores it) and hand it back for
+                // the next chunk
+                bool ok = true;
+                for (int kb = p.kb_chunk; kb < p.num_kb; kb += p.kb_chunk) {
+#pragma unroll 1
+                    for (int t2 = 0; t2 < F::NT; ++t2) {
+#pragma unroll 1
+                        for (int ch = 0; ch < EPI_CHUNKS; ++ch) {
+                            if (n0 + t2 * tc::BN + ch * tc::EPI_CHUNK >= p.k) break;
+                            float vm[tc::EPI_CHUNK];
+                            tmem_ld_one<tc::EPI_CHUNK>(
+                                acc_base + lanes + (uint32_t)(t2 * tc::BN + part * tc::EPI_COLS + ch * tc::EPI_CHUNK),
+                                vm);
+                            float4 *dst = reinterpret_cast<float4 *>(csum) + (t2 * EPI_CHUNKS + ch) * (tc::EPI_CHUNK / 4) * 32;
+#pragma unroll
+                            for (int u4 = 0; u4 < tc::EPI_CHUNK / 4; ++u4) {
+                                float4 v = make_float4(vm[4 * u4], vm[4 * u4 + 1], vm[4 * u4 + 2], vm[4 * u4 + 3]);
+                                if (kb > p.kb_chunk) {
+                                    const float4 o = __ldcg(dst + u4 * 32);
+                                    v = make_float4(v.x + o.x, v.y + o.y, v.z + o.z, v.w + o.w);
+                                }
+                                dst[u4 * 32] = v;
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(F::T_EMPTY), 0));
+                    if (!mbar_wait_warp(bar(F::T_FULL), acc_use & 1, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    ++acc_use;
+                    tc_fence_after();
+                }
+                if (!ok) break;
+                if (p.num_kb > p.kb_chunk) parked = csum;
+            }
             if constexpr (DB && !FUSED) {
                 if (un.half >= 0) {
                     // The two K halves of a split tile meet here, warp by warp.
@@ -506,9 +570,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                     if (lane == 0) ticket = atomicAdd(sync, 1u);
                     ticket = __shfl_sync(0xffffffffu, ticket, 0);
                     if (ticket == 0) {
-                        const uint32_t lanes = (uint32_t)(q * 32) << 16;
 #pragma unroll 1
-                        for (int ch = 0; ch < tc::EPI_COLS / tc::EPI_CHUNK; ++ch) {
+                        for (int ch = 0; ch < EPI_CHUNKS; ++ch) {
                             if (n0 + ch * tc::EPI_CHUNK >= p.k) break;
                             float vm[tc::EPI_CHUNK];
                             tmem_ld_one<tc::EPI_CHUNK>(
@@ -544,18 +607,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
 #pragma unroll 1
             for (int t2 = 0; t2 < F::NT; ++t2) {
 #pragma unroll 1
-            for (int ch = 0; ch < tc::EPI_COLS / tc::EPI_CHUNK; ++ch) {
+            for (int ch = 0; ch < EPI_CHUNKS; ++ch) {
                 const int j0 = n0 + t2 * tc::BN + ch * tc::EPI_CHUNK;
                 if (j0 >= p.k) break;
                 const uint32_t col = (uint32_t)(t2 * tc::BN + part * tc::EPI_COLS + ch * tc::EPI_CHUNK);
-                const uint32_t lanes = (uint32_t)(q * 32) << 16;
                 // x.c of this chunk's columns: one accumulator, or main + corrections
                 float vm[tc::EPI_CHUNK], vc[tc::EPI_CHUNK];
                 if constexpr (DB || WIDE) {
                     tmem_ld_one<tc::EPI_CHUNK>(acc_base + lanes + col, vm);
                     if constexpr (!FUSED) {
                         if (parked) {
-                            const float4 *src = reinterpret_cast<const float4 *>(parked) + ch * (tc::EPI_CHUNK / 4) * 32;
+                            const float4 *src =
+                                reinterpret_cast<const float4 *>(parked) + (t2 * EPI_CHUNKS + ch) * (tc::EPI_CHUNK / 4) * 32;
 #pragma unroll
                             for (int u4 = 0; u4 < tc::EPI_CHUNK / 4; ++u4) {
                                 const float4 pv = __ldcg(src + u4 * 32);
@@ -662,128 +725,111 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 TF32 ? umma_idesc_tf32_f32(2 * tc::BM, tc::BN) : umma_idesc_bf16_f32(2 * tc::BM, tc::BN);
             const uint32_t d_main = tmem_base + tc::ACC_MAIN;
             const uint32_t d_corr = tmem_base + tc::ACC_CORR;
+            const uint32_t dw = tmem_base + tc::BN;  // wide: the second tile's accumulator
+            // One k-block (pipeline step `it`): the stage's MMAs into dm (hi.hi)
+            // and dc (the corrections), the first of them onto a cleared
+            // accumulator unless `acc_kb`, then the commits that free the
+            // stages.  False when the wait for the split stage ran out.
+            auto kblock = [&](int it, uint32_t dm, uint32_t dc, bool acc_kb) -> bool {
+                const int s = it % F::SXB;
+                const int as = it % F::SA;
+                // operands of this stage: bf16 hi and lo of X in the A stage;
+                // 3xTF32 hi of X in place in the fp32 tile, lo in the A stage
+                const uint32_t xb = sbase + s * F::XB_STAGE;
+                const uint32_t bhi = xb + tc::X_BYTES;
+                const uint32_t blo = bhi + F::B_BYTES;
+                const uint32_t ast = sbase + F::A_BASE + as * F::A_STAGE;
+                const uint32_t ahi = TF32 ? xb : ast;
+                const uint32_t alo = TF32 ? ast : ast + F::A_LO;
+                // descriptors first: once the split stage lands, only the
+                // MMAs remain between it and the tensor pipe (measured: the
+                // issue latency here is on the critical path)
+                uint64_t dah[F::K_STEPS], dal[F::K_STEPS], dbh[F::K_STEPS], dbl[F::K_STEPS];
+                uint64_t dwh[F::K_STEPS], dwl[F::K_STEPS];  // wide: the second tile's hi and lo
+#pragma unroll
+                for (int kk = 0; kk < F::K_STEPS; ++kk) {
+                    dah[kk] = umma_smem_desc(ahi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                    dal[kk] = umma_smem_desc(alo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                    dbh[kk] = umma_smem_desc(bhi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                    dbl[kk] = umma_smem_desc(blo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                    if constexpr (WIDE) {
+                        dwh[kk] = umma_smem_desc(blo + F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                        dwl[kk] = umma_smem_desc(blo + 2 * F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                    }
+                }
+                // both CTAs' split warps have seen their X and C stage land
+                if (!mbar_wait_cluster(bar(F::A_FULL + as), (it / F::SA) & 1, p.status)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < F::K_STEPS; ++kk) {
+                    const uint32_t acc = (acc_kb || kk != 0) ? 1u : 0u;
+                    if constexpr (TF32) {
+                        mma_tf32_ss_pair(dm, dah[kk], dbh[kk], idesc, acc);
+                        mma_tf32_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : acc);
+                        mma_tf32_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                    } else {
+                        mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, acc);
+                        mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, (DB || WIDE) ? 1u : acc);
+                        mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
+                        if constexpr (WIDE) {
+                            mma_bf16_ss_pair(dw, dah[kk], dwh[kk], idesc, acc);
+                            mma_bf16_ss_pair(dw, dal[kk], dwh[kk], idesc, 1u);
+                            mma_bf16_ss_pair(dw, dah[kk], dwl[kk], idesc, 1u);
+                        }
+                    }
+                }
+                mma_commit_pair_multicast(bar(F::XB_EMPTY + s), tc::PAIR_MASK);
+                mma_commit_pair_multicast(bar(F::A_EMPTY + as), tc::PAIR_MASK);
+                return true;
+            };
             int it = 0, tile_iter = 0;
+            int acc_use = 0;  // single-buffered accumulator: hand-overs so far (one per K chunk of a unit)
             bool ok = true;
             for (int unit = pair; unit < p.num_units && ok; unit += num_pairs, ++tile_iter) {
                 const int buf = DB ? (tile_iter & 1) : 0;
-                const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (tile_iter & 1);
+                const uint32_t phase = DB ? ((tile_iter >> 1) & 1) : (acc_use & 1);
                 if (!mbar_wait_cluster(bar(F::T_EMPTY + buf), phase ^ 1, p.status)) break;
                 tc_fence_after();
+                if constexpr (!DB) ++acc_use;
                 const uint32_t dm = DB ? tmem_base + (uint32_t)(buf * tc::BN) : d_main;
                 const uint32_t dc = (DB || WIDE) ? dm : d_corr;  // one accumulator per tile, or main + corrections
-                const uint32_t dw = tmem_base + tc::BN;           // wide: the second tile's accumulator
-                // whole tiles keep a loop of their own: any per-unit logic in it
-                // measured 1.3% on the whole kernel
-                if (unit < p.num_full) {
-                    for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                        const int s = it % F::SXB;
-                        const int as = it % F::SA;
-                        // operands of this stage: bf16 hi and lo of X in the A stage;
-                        // 3xTF32 hi of X in place in the fp32 tile, lo in the A stage
-                        const uint32_t xb = sbase + s * F::XB_STAGE;
-                        const uint32_t bhi = xb + tc::X_BYTES;
-                        const uint32_t blo = bhi + F::B_BYTES;
-                        const uint32_t ast = sbase + F::A_BASE + as * F::A_STAGE;
-                        const uint32_t ahi = TF32 ? xb : ast;
-                        const uint32_t alo = TF32 ? ast : ast + F::A_LO;
-                        // descriptors first: once the split stage lands, only the
-                        // MMAs remain between it and the tensor pipe (measured: the
-                        // issue latency here is on the critical path)
-                        uint64_t dah[F::K_STEPS], dal[F::K_STEPS], dbh[F::K_STEPS], dbl[F::K_STEPS];
-                        uint64_t dwh[F::K_STEPS], dwl[F::K_STEPS];  // wide: the second tile's hi and lo
-    #pragma unroll
-                        for (int kk = 0; kk < F::K_STEPS; ++kk) {
-                            dah[kk] = umma_smem_desc(ahi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                            dal[kk] = umma_smem_desc(alo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                            dbh[kk] = umma_smem_desc(bhi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                            dbl[kk] = umma_smem_desc(blo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                            if constexpr (WIDE) {
-                                dwh[kk] = umma_smem_desc(blo + F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                                dwl[kk] = umma_smem_desc(blo + 2 * F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
+                if constexpr (CHUNKED) {
+                    for (int c0 = 0; c0 < p.num_kb && ok; c0 += p.kb_chunk) {
+                        if (c0 > 0) {
+                            // the epilogue adds this chunk to the running sum
+                            // and hands the accumulator back
+                            mma_commit_pair_multicast(bar(F::T_FULL), tc::PAIR_MASK);
+                            if (!mbar_wait_cluster(bar(F::T_EMPTY), (acc_use & 1) ^ 1, p.status)) {
+                                ok = false;
+                                break;
+                            }
+                            ++acc_use;
+                            tc_fence_after();
+                        }
+                        const int c1 = min(c0 + p.kb_chunk, p.num_kb);
+                        for (int kb = c0; kb < c1; ++kb, ++it) {
+                            if (!kblock(it, dm, dc, kb != c0)) {
+                                ok = false;
+                                break;
                             }
                         }
-                        // both CTAs' split warps have seen their X and C stage land
-                        if (!mbar_wait_cluster(bar(F::A_FULL + as), (it / F::SA) & 1, p.status)) {
+                    }
+                } else if (unit < p.num_full) {
+                    // whole tiles keep a loop of their own: any per-unit logic in
+                    // it measured 1.3% on the whole kernel
+                    for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                        if (!kblock(it, dm, dc, kb != 0)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-    #pragma unroll
-                        for (int kk = 0; kk < F::K_STEPS; ++kk) {
-                            const uint32_t first = (kb | kk) != 0 ? 1u : 0u;
-                            if constexpr (TF32) {
-                                mma_tf32_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
-                                mma_tf32_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
-                                mma_tf32_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
-                            } else {
-                                mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
-                                mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, (DB || WIDE) ? 1u : first);
-                                mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
-                                if constexpr (WIDE) {
-                                    mma_bf16_ss_pair(dw, dah[kk], dwh[kk], idesc, first);
-                                    mma_bf16_ss_pair(dw, dal[kk], dwh[kk], idesc, 1u);
-                                    mma_bf16_ss_pair(dw, dah[kk], dwl[kk], idesc, 1u);
-                                }
-                            }
-                        }
-                        mma_commit_pair_multicast(bar(F::XB_EMPTY + s), tc::PAIR_MASK);
-                        mma_commit_pair_multicast(bar(F::A_EMPTY + as), tc::PAIR_MASK);
                     }
                 } else {
                     const KUnit un = unit_at(p, unit);
                     for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
-                        const int s = it % F::SXB;
-                        const int as = it % F::SA;
-                        // operands of this stage: bf16 hi and lo of X in the A stage;
-                        // 3xTF32 hi of X in place in the fp32 tile, lo in the A stage
-                        const uint32_t xb = sbase + s * F::XB_STAGE;
-                        const uint32_t bhi = xb + tc::X_BYTES;
-                        const uint32_t blo = bhi + F::B_BYTES;
-                        const uint32_t ast = sbase + F::A_BASE + as * F::A_STAGE;
-                        const uint32_t ahi = TF32 ? xb : ast;
-                        const uint32_t alo = TF32 ? ast : ast + F::A_LO;
-                        // descriptors first: once the split stage lands, only the
-                        // MMAs remain between it and the tensor pipe (measured: the
-                        // issue latency here is on the critical path)
-                        uint64_t dah[F::K_STEPS], dal[F::K_STEPS], dbh[F::K_STEPS], dbl[F::K_STEPS];
-                        uint64_t dwh[F::K_STEPS], dwl[F::K_STEPS];  // wide: the second tile's hi and lo
-    #pragma unroll
-                        for (int kk = 0; kk < F::K_STEPS; ++kk) {
-                            dah[kk] = umma_smem_desc(ahi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                            dal[kk] = umma_smem_desc(alo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                            dbh[kk] = umma_smem_desc(bhi + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                            dbl[kk] = umma_smem_desc(blo + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                            if constexpr (WIDE) {
-                                dwh[kk] = umma_smem_desc(blo + F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                                dwl[kk] = umma_smem_desc(blo + 2 * F::B_BYTES + kk * F::K_STEP_BYTES, F::SBO, F::LAYOUT);
-                            }
-                        }
-                        // both CTAs' split warps have seen their X and C stage land
-                        if (!mbar_wait_cluster(bar(F::A_FULL + as), (it / F::SA) & 1, p.status)) {
+                        if (!kblock(it, dm, dc, kb != un.kb0)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-    #pragma unroll
-                        for (int kk = 0; kk < F::K_STEPS; ++kk) {
-                            const uint32_t first = (kb != un.kb0 || kk != 0) ? 1u : 0u;
-                            if constexpr (TF32) {
-                                mma_tf32_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
-                                mma_tf32_ss_pair(dc, dal[kk], dbh[kk], idesc, DB ? 1u : first);
-                                mma_tf32_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
-                            } else {
-                                mma_bf16_ss_pair(dm, dah[kk], dbh[kk], idesc, first);
-                                mma_bf16_ss_pair(dc, dal[kk], dbh[kk], idesc, (DB || WIDE) ? 1u : first);
-                                mma_bf16_ss_pair(dc, dah[kk], dbl[kk], idesc, 1u);
-                                if constexpr (WIDE) {
-                                    mma_bf16_ss_pair(dw, dah[kk], dwh[kk], idesc, first);
-                                    mma_bf16_ss_pair(dw, dal[kk], dwh[kk], idesc, 1u);
-                                    mma_bf16_ss_pair(dw, dah[kk], dwl[kk], idesc, 1u);
-                                }
-                            }
-                        }
-                        mma_commit_pair_multicast(bar(F::XB_EMPTY + s), tc::PAIR_MASK);
-                        mma_commit_pair_multicast(bar(F::A_EMPTY + as), tc::PAIR_MASK);
                     }
                 }
                 if (!ok) break;
@@ -909,6 +955,9 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(assign_tc_kernel<false, false, false, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Fmt<false, true>::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(assign_tc_kernel<false, false, false, true, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Fmt<false, true>::SMEM_BYTES);
         return e;
     };
     if (dev < 0) {
@@ -937,10 +986,14 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
         return cudaErrorInvalidValue;
 
     // accumulator mode: bf16x3 runs wide units (two tiles, one accumulator
-    // each) for WIDE_MIN_D <= d <= WIDE_MAX_D when there is more than one
-    // tile of centroids; otherwise one double-buffered accumulator per tile
-    // up to SINGLE_ACC_MAX_D, and separate accumulators beyond
-    const bool wide = !tf32 && !fused && d >= tc::WIDE_MIN_D && d <= tc::WIDE_MAX_D && k > tc::BN;
+    // each) from WIDE_MIN_D features when there is more than one tile of
+    // centroids, above WIDE_MAX_D in K chunks of at most WIDE_MAX_D features
+    // (where the workspace holds the running sums); otherwise one
+    // double-buffered accumulator per tile up to SINGLE_ACC_MAX_D, and
+    // separate accumulators beyond
+    static_assert(tc::WIDE_MAX_D == kWideChunkD, "the workspace reserves the running sums above WIDE_MAX_D");
+    const bool chunked = !tf32 && !fused && d > tc::WIDE_MAX_D && k > tc::BN && L.off_park != 0;
+    const bool wide = chunked || (!tf32 && !fused && d >= tc::WIDE_MIN_D && d <= tc::WIDE_MAX_D && k > tc::BN);
     const bool db = !wide && d <= (tf32 ? tc::SINGLE_ACC_MAX_D_TF32 : tc::SINGLE_ACC_MAX_D);
     TcParams p{};
     p.n = (int)n;
@@ -964,7 +1017,8 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     // out and the call reports KMEANS_ERR_DEVICE_TIMEOUT.
     const char *hold = getenv("KMEANS_GB300_TEST_HOLD_KSPLIT_TAG");
     p.test_hold_tag = (hold != nullptr && hold[0] == '1') ? 1 : 0;
-    const int max_pairs = resident_pairs();
+    int max_pairs = resident_pairs();
+    if (chunked && max_pairs > kChunkParkCtas / 2) max_pairs = kChunkParkCtas / 2;  // one running sum per CTA
     const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
     const int grid = 2 * (pairs > 0 ? pairs : 1);
     // K split of a last round that is at most half full (double-buffered
@@ -975,6 +1029,15 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     p.epoch = 0;
     p.kacc = nullptr;
     p.ksync = nullptr;
+    // K chunks of at most WIDE_MAX_D features, balanced
+    p.kb_chunk = p.num_kb;
+    p.park = nullptr;
+    if (chunked) {
+        const int max_kb = tc::WIDE_MAX_D / tc::BK;
+        const int chunks = (p.num_kb + max_kb - 1) / max_kb;
+        p.kb_chunk = (p.num_kb + chunks - 1) / chunks;
+        p.park = reinterpret_cast<float *>(ws + L.off_park);
+    }
     if (db && !fused && L.off_kacc != 0 && p.num_kb >= 2 && p.num_tiles > pairs) {
         const int rounds = (p.num_tiles + pairs - 1) / pairs;
         const int tail = p.num_tiles - (rounds - 1) * pairs;
@@ -1003,6 +1066,9 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     else if (db)
         e = launch_kernel(chained, assign_tc_kernel<true, false>, g, b, tc::Fmt<false>::SMEM_BYTES, stream, tmX, tmChi,
                           tmClo, p);
+    else if (chunked)
+        e = launch_kernel(chained, assign_tc_kernel<false, false, false, true, true>, g, b,
+                          tc::Fmt<false, true>::SMEM_BYTES, stream, tmX, tmChi, tmClo, p);
     else if (wide)
         e = launch_kernel(chained, assign_tc_kernel<false, false, false, true>, g, b, tc::Fmt<false, true>::SMEM_BYTES,
                           stream, tmX, tmChi, tmClo, p);

@@ -161,6 +161,7 @@ struct AssignLayout {
     int64_t split_elem_bytes;  // 2: bf16 hi / lo of C; 4: fp32 (3xTF32) hi / lo
     int64_t off_kacc;    // K-split tiles: kKSplitSlots x kKSplitSlotBytes parked accumulators (0: none)
     int64_t off_ksync;   // K-split tiles: kKSplitSlots x kKSplitSyncWords tickets and ready tags
+    int64_t off_park;    // chunked wide units: kChunkParkCtas x kChunkParkCtaBytes running sums (0: none)
     int64_t bytes;
 };
 
@@ -178,12 +179,23 @@ constexpr int64_t kKSplitMinTiles = 64;
 constexpr int64_t kKSplitSlotBytes = 2 * 128 * 256 * 4;  // both CTAs of a pair
 constexpr int kKSplitSyncWords = 2 * 8 * 2;              // CTA x epilogue warp x (ticket, tag)
 
+// Above kWideChunkD features the bf16x3 wide units (256 samples x 512
+// centroids, one accumulator per 256-column tile) run K in chunks of at most
+// kWideChunkD features, so that each accumulator's truncation error stays
+// that of d = kWideChunkD.  Between chunks every CTA adds its raw accumulator
+// (128 rows x 512 columns of float32) into a running sum of its own in the
+// workspace; the persistent grid has at most kChunkParkCtas CTAs.
+constexpr int64_t kWideChunkD = 8192;
+constexpr int kChunkParkCtas = 160;
+constexpr int64_t kChunkParkCtaBytes = 128 * 512 * 4;
+
 inline int64_t assign_tiles(int64_t n, int64_t k) { return ((n + 255) / 256) * ((k + 255) / 256); }
 
-// `tail_split`: reserve the K-split parking area (tensor-core paths that may
-// split their last round; not the built-in scratch or the fused update).
+// `park`: reserve the parking areas of the K-split tiles and of the chunked
+// wide units (tensor-core paths that may use them; not the built-in scratch
+// or the fused update).
 inline AssignLayout assign_layout(int64_t n, int64_t k, int64_t d, bool split, int split_elem_bytes = 2,
-                                  bool tail_split = true) {
+                                  bool park = true) {
     AssignLayout L{};
     L.d_pad = align_up(d, 64);
     L.split_elem_bytes = split ? split_elem_bytes : 0;
@@ -198,10 +210,13 @@ inline AssignLayout assign_layout(int64_t n, int64_t k, int64_t d, bool split, i
         L.off_chi = L.off_clo = 0;
     }
     o = align_up(o, 1024); L.off_partial = o; o += kMaxReduceBlocks * 8;
-    L.off_kacc = L.off_ksync = 0;
-    if (split && tail_split && assign_tiles(n, k) > kKSplitMinTiles) {
+    L.off_kacc = L.off_ksync = L.off_park = 0;
+    if (split && park && assign_tiles(n, k) > kKSplitMinTiles) {
         o = align_up(o, 1024); L.off_kacc = o; o += kKSplitSlots * kKSplitSlotBytes;
         o = align_up(o, 1024); L.off_ksync = o; o += kKSplitSlots * kKSplitSyncWords * 4;
+    }
+    if (split && park && split_elem_bytes == 2 && d > kWideChunkD && k > 256) {
+        o = align_up(o, 1024); L.off_park = o; o += kChunkParkCtas * kChunkParkCtaBytes;
     }
     L.bytes = align_up(o, 1024);
     return L;

@@ -31,12 +31,18 @@
  *  - Precision: inputs must be finite.  The assignment contraction runs on the
  *    tensor cores as three bf16 products of an error-compensated split of
  *    each float32 operand (hi = bf16(v), lo = bf16(v - hi)) with float32
- *    accumulation (up to d = 8192 the three products share one accumulator
- *    per tile; above, the two correction products keep their own, which is
- *    about three times more accurate); the reported distance is within
- *    1e-4 * (||x||^2 + ||c||^2) of the exact one for d up to about 16384 (the
+ *    accumulation.  The three products share one accumulator per tile, over
+ *    chunks of at most 8192 features whose sums are added in float32 (the
  *    error of the float32 tensor-core accumulation grows about linearly with
- *    d).  Ties between centroids go to the lowest index.
+ *    the features an accumulator covers).  Where that does not apply (above
+ *    4096 features with k <= 256, above 8192 in the built-in scratch of
+ *    kmeans_assign_noalloc, and the 3xTF32 comparator above 2048) the two
+ *    correction products keep an accumulator of their own, about three times
+ *    more accurate than one shared over the same features.  The reported
+ *    distance is within 1e-4 * (||x||^2 + ||c||^2) of the exact one (tested
+ *    up to d = 24576 in chunks, whose error stays that of one 8192-feature
+ *    chunk; up to about 16384 with separate accumulators).  Ties between
+ *    centroids go to the lowest index.
  *  - Workspace: `ws` is a device buffer of at least
  *    kmeans_workspace_bytes(op, n, k, d) bytes, 256-byte aligned, owned by the
  *    caller.  Its size has no n*k term: no (n, k) buffer exists anywhere.
@@ -121,13 +127,15 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d);
  * Extra requirement of this tensor-core path: d % 4 == 0 and X, C 16-byte
  * aligned (KMEANS_ERR_UNSUPPORTED otherwise; kmeans_assign_ffma has none).
  * Schedule: pairs of SMs work through 256 x 256 tiles of (samples,
- * centroids), or 256 x 512 units of two such tiles for 2048 <= d <= 8192
- * with k > 256, in rounds; when the last round of single tiles is at most
- * half full (d <= 4096), each of its tiles is computed as two halves of the
- * features on two pairs and the halves' sums are added at the end.  Those tiles' distances
- * carry a different (no larger) float32 accumulation error than a single
- * pass would, within the accuracy stated above; the results are the same
- * from run to run on a given GPU.
+ * centroids), or 256 x 512 units of two such tiles for d >= 2048 with
+ * k > 256, in rounds; above 8192 features a unit runs its features in
+ * chunks of at most 8192, adding each chunk's sums into a running sum kept
+ * in the workspace.  When the last round of single tiles is at most half
+ * full (d <= 4096), each of its tiles is computed as two halves of the
+ * features on two pairs and the halves' sums are added at the end.  Those
+ * tiles' distances carry a different (no larger) float32 accumulation error
+ * than a single pass would, within the accuracy stated above; the results
+ * are the same from run to run on a given GPU.
  * seed: unused (kept for a uniform signature). */
 int kmeans_assign(const float *X, const float *C, int64_t n, int64_t k, int64_t d,
                   int64_t *labels, float *best_dist, double *inertia,

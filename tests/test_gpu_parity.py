@@ -353,11 +353,14 @@ def test_large_workload_one_iteration(gpu_lib, name, record_property):
     assert np.isfinite(bd).all() and (bd >= 0).all()
 
 
-@pytest.mark.parametrize("shape", [(3000, 300, 2048), (5000, 700, 4100), (2600, 257, 8192), (9000, 1100, 2052)],
+@pytest.mark.parametrize("shape", [(3000, 300, 2048), (5000, 700, 4100), (2600, 257, 8192), (9000, 1100, 2052),
+                                   (2600, 300, 8196), (3000, 700, 16384), (700, 300, 24576)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_wide_units_with_ragged_centroid_columns(gpu_lib, shape):
     # wide units (two 256-column tiles per CTA pair) where the second tile
-    # is partly or, in the last unit column, entirely past k; ragged rows
+    # is partly or, in the last unit column, entirely past k; ragged rows.
+    # Above 8192 features the units run K in chunks (8196: two uneven
+    # chunks, 16384: two, 24576: three) with a running sum per CTA.
     n, k, d = shape
     X, _, _ = synth.planted_blobs(n, d, max(1, k // 3), seed=n + d)
     C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=k)])
@@ -371,13 +374,16 @@ def test_wide_units_with_ragged_centroid_columns(gpu_lib, shape):
     assert np.array_equal(host(counts).astype(np.int64), o_cnt)
 
 
-@pytest.mark.parametrize("impl,d", [("tc", 4096), ("tc", 4100), ("tf32", 2048), ("tf32", 2052), ("tf32", 8192)])
-def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d, impl):
-    # up to 4096 features (bf16x3; 2048 for 3xTF32) the three split products
-    # share one double-buffered accumulator per tile; above, the corrections
-    # keep their own.  Several tiles per CTA pair, ragged sample and centroid
-    # tiles.
-    n, k = 20000, 700
+@pytest.mark.parametrize("impl,d,k", [("tc", 4096, 250), ("tc", 4100, 250), ("tc", 8192, 700), ("tc", 8196, 700),
+                                     ("tf32", 2048, 700), ("tf32", 2052, 700), ("tf32", 8192, 700)])
+def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d, k, impl):
+    # bf16x3 with one centroid tile (k <= 256): one double-buffered
+    # accumulator per tile up to 4096 features, separate accumulators for the
+    # corrections above.  bf16x3 with more (k > 256): wide units, one
+    # accumulator per tile, over K chunks above 8192 features.  3xTF32: one
+    # double-buffered accumulator up to 2048, separate ones above.  Several
+    # tiles per CTA pair, ragged sample and centroid tiles.
+    n = 20000
     X, _, _ = synth.planted_blobs(n, d, 64, seed=91)
     C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=92)])
     labels, best, inertia = getattr(gpu_lib, ASSIGN_IMPLS[impl])(dev_tensor(X), dev_tensor(C))
@@ -385,7 +391,7 @@ def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d, impl):
     o_l, o_b, o_s, _ = oracle.assign(X[rows], C)
     flips, worst = check_assign(X[rows], C, host(labels), host(best), o_l, o_b, o_s, rows=rows,
                                 what=f"{impl} d={d}")
-    print(f"{impl} d={d}: worst relative distance error {worst:.3e}, near-tie flips {flips} of {len(rows)}")
+    print(f"{impl} d={d} k={k}: worst relative distance error {worst:.3e}, near-tie flips {flips} of {len(rows)}")
 
 
 @pytest.mark.slow
