@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kmeanspp", action="store_true")
+    ap.add_argument("--e2e-slices", type=int, default=16,
+                    help="row slices of kmeans_lloyd_iter_host in the end-to-end leg")
     return ap.parse_args()
 
 
@@ -570,47 +572,56 @@ def run_gb300(args):
     if not args.no_e2e:
         Xh = torch.from_numpy(X).pin_memory()
         Ch = torch.from_numpy(C0).pin_memory()
-        C_out_h = torch.empty((k, d), dtype=torch.float32).pin_memory()
-        lab_h = torch.empty(n, dtype=torch.int64).pin_memory()
-        in_h = torch.empty(1, dtype=torch.float64).pin_memory()
-        # two sets of device buffers, alternated, so that a step's copies may
-        # overlap the previous step's update and read-back
+        C_out_h = [torch.empty((k, d), dtype=torch.float32).pin_memory() for _ in range(2)]
+        lab_h = [torch.empty(n, dtype=torch.int64).pin_memory() for _ in range(2)]
+        in_h = [torch.empty(1, dtype=torch.float64).pin_memory() for _ in range(2)]
+        # two sets of device buffers (inputs and outputs) and two copy
+        # streams, alternated: a step's copies in overlap the previous step's
+        # assignment, and its read-back (on its copy stream) the next step's
         Xe = [torch.empty_like(Xd), torch.empty_like(Xd)]
         Ce = [torch.empty_like(C0d), torch.empty_like(C0d)]
-        Cn = torch.empty_like(C0d)
+        Cn = [torch.empty_like(C0d), torch.empty_like(C0d)]
+        labels_e = [torch.empty_like(labels), torch.empty_like(labels)]
+        inertia_e = [torch.empty(1, dtype=torch.float64, device=dev) for _ in range(2)]
         e2e_steps = max(1, min(steps, 50))
 
-        slices = 16  # measured per step: 2 -> 3.00 ms, 4 -> 2.91, 8 -> 2.86, 16 -> 2.84 (no overlap)
-        copy_stream = torch.cuda.Stream(dev)
-        inertia_d = torch.empty(1, dtype=torch.float64, device=dev)
-        done = [None, None]  # per buffer set: the event after the last step that used it
+        slices = args.e2e_slices  # lloyd10, per step: 2 -> 3.00 ms, 4 -> 2.91, 8 -> 2.86, 16 -> 2.84 (no overlap)
+        copy_streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
 
         def e2e_step(j):
+            # a set is reused only by the copies of the step after next, which
+            # its copy stream orders after that set's read-back, itself after
+            # the step's update
             slot = j % 2
-            if done[slot] is not None:
-                copy_stream.wait_event(done[slot])  # that step's compute no longer reads the set
-            done[slot] = km.kmeans_lloyd_iter_host(Xh, Ch, Xe[slot], Ce[slot], Cn, labels, best, counts, C_out_h,
-                                                   lab_h, in_h, slices=slices, ws=ws, inertia=inertia_d,
-                                                   copy_stream=copy_stream, stream=stream, overlap_previous=True)
+            km.kmeans_lloyd_iter_host(Xh, Ch, Xe[slot], Ce[slot], Cn[slot], labels_e[slot], best, counts,
+                                      C_out_h[slot], lab_h[slot], in_h[slot], slices=slices, ws=ws,
+                                      inertia=inertia_e[slot],
+                                      copy_stream=copy_streams[slot], stream=stream, overlap_previous=True,
+                                      readback_on_copy_stream=True)
 
         for j in range(min(warm, 3)):
             e2e_step(j)
+        for cs in copy_streams:
+            stream.wait_stream(cs)
         barrier()
         ev0.record(stream)
-        copy_stream.wait_event(ev0)  # the first timed step's copies start inside the timed region
+        for cs in copy_streams:
+            cs.wait_event(ev0)  # the first timed steps' copies start inside the timed region
         for j in range(e2e_steps):
             e2e_step(j)
+        for cs in copy_streams:
+            stream.wait_stream(cs)  # the last read-backs end inside it
         ev1.record(stream)
         barrier()
         t_e2e = ev0.elapsed_time(ev1) / 1e3 / e2e_steps
         e2e = {"value": flop / t_e2e / 1e12, "unit": "TFLOP/s", "ms_per_step": 1e3 * t_e2e,
-               "steps": e2e_steps, "pipeline": f"kmeans_lloyd_iter_host: {slices} row slices copied on a second "
+               "steps": e2e_steps, "pipeline": f"kmeans_lloyd_iter_host: {slices} row slices copied on a copy "
                                                "stream, each assigned as it lands; finalize and update; C_new, "
-                                               "labels and inertia copied back; two device buffer sets "
-                                               "alternate so each step's copies overlap the previous step's "
-                                               "update",
+                                               "labels and inertia copied back on the copy stream; two device "
+                                               "buffer sets and two copy streams alternate, so each step's copies "
+                                               "in and out overlap the neighbouring steps' compute",
                "h2d_bytes_per_step": int(Xh.numel() * 4 + Ch.numel() * 4),
-               "d2h_bytes_per_step": int(C_out_h.numel() * 4 + lab_h.numel() * 8 + in_h.numel() * 8)}
+               "d2h_bytes_per_step": int(C_out_h[0].numel() * 4 + lab_h[0].numel() * 8 + in_h[0].numel() * 8)}
 
     # max over ranks
     t_lloyd, t_assign, t_update, t_e2e_max = max_over_ranks(

@@ -58,6 +58,7 @@ KERNEL_KMEANSPP_DIST = 2
 TRACE_MAX_CAPACITY = 65536
 HOST_MAX_SLICES = 64
 HOST_OVERLAP_PREVIOUS = 1
+HOST_READBACK_ON_COPY_STREAM = 2
 # Features per slice of the k-means++ distance pass: each pass writes one
 # float2 partial sum per (slice, trial, sample), ceil(d / 4096) slices.
 KPP_SLICE_FEATURES = 4096
@@ -460,7 +461,7 @@ def kmeans_trace_stop() -> None:
 
 def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_out_h, labels_h, inertia_h,
                            slices: int = 16, ws=None, inertia=None, copy_stream=None, stream=None,
-                           overlap_previous: bool = False):
+                           overlap_previous: bool = False, readback_on_copy_stream: bool = False):
     """One Lloyd iteration on inputs that live in pinned host memory.
 
     The library copies the samples to ``Xd`` in ``slices`` row slices on
@@ -470,9 +471,13 @@ def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_o
     device outputs are kmeans_lloyd_iter's: bit for bit with one slice; with
     more, the distances and inertia within the distance tolerance (each
     slice's pass may split other tiles along K).  Returns an event
-    recorded on ``stream`` after the last copy.  ``overlap_previous``: the
-    copies may overlap earlier work on ``stream`` (the caller guarantees that
-    ``Xd`` and ``Cd`` are not in use, e.g. by alternating two sets).
+    recorded after the last copy.  ``overlap_previous``: the copies may
+    overlap earlier work on ``stream`` (the caller guarantees that ``Xd`` and
+    ``Cd`` are not in use, e.g. by alternating two sets).
+    ``readback_on_copy_stream``: the copies back to the host run on
+    ``copy_stream`` after the update (the event is recorded there), so that
+    ``stream`` can start the next iteration; the caller leaves ``C_new``,
+    ``labels`` and ``inertia`` unchanged until the event.
     Xh, Ch, C_out_h, labels_h, inertia_h: pinned host tensors.
     Xd, Cd, C_new, labels, best_dist, counts: device tensors (preallocated).
     """
@@ -500,11 +505,12 @@ def kmeans_lloyd_iter_host(Xh, Ch, Xd, Cd, C_new, labels, best_dist, counts, C_o
     st = load().kmeans_lloyd_iter_host(Xh.data_ptr(), Ch.data_ptr(), _ptr(Xd), _ptr(Cd), _ptr(C_new), _ptr(labels),
                                        _ptr(best_dist), _ptr(inertia), _ptr(counts), C_out_h.data_ptr(),
                                        labels_h.data_ptr(), inertia_h.data_ptr(), n, k, d, int(slices),
-                                       HOST_OVERLAP_PREVIOUS if overlap_previous else 0, _ptr(ws),
+                                       (HOST_OVERLAP_PREVIOUS if overlap_previous else 0) |
+                                       (HOST_READBACK_ON_COPY_STREAM if readback_on_copy_stream else 0), _ptr(ws),
                                        ws.numel(), _stream_handle(stream), _stream_handle(copy_stream))
     _raise(st, "kmeans_lloyd_iter_host")
     done = torch.cuda.Event()
-    done.record(stream)
+    done.record(copy_stream if readback_on_copy_stream else stream)
     return done
 
 

@@ -280,7 +280,7 @@ int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, f
     if (!X_host || !C_host || !X || !C_old || !C_new || !labels || !best_dist) return KMEANS_ERR_INVALID_ARG;
     if (!sizes_ok(n, k, d)) return KMEANS_ERR_INVALID_ARG;
     if (slices < 1 || slices > KMEANS_HOST_MAX_SLICES) return KMEANS_ERR_INVALID_ARG;
-    if (flags & ~KMEANS_HOST_OVERLAP_PREVIOUS) return KMEANS_ERR_INVALID_ARG;
+    if (flags & ~(KMEANS_HOST_OVERLAP_PREVIOUS | KMEANS_HOST_READBACK_ON_COPY_STREAM)) return KMEANS_ERR_INVALID_ARG;
     if (stream == copy_stream || (inertia_host && !inertia)) return KMEANS_ERR_INVALID_ARG;
     if (!aligned4(C_new) || (reinterpret_cast<uintptr_t>(labels) & 7u)) return KMEANS_ERR_INVALID_ARG;
     const int st = tc_path_ok(X, C_old, d);
@@ -295,11 +295,12 @@ int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, f
     const int64_t per = ((n + slices - 1) / slices + 255) / 256 * 256;
     const int used = (int)((n + per - 1) / per);
     // ev[0 .. used-1]: slice i has landed; ev[used]: the entry point on
-    // `stream`; ev[used + 1]: the centroids have landed
-    cudaEvent_t ev[KMEANS_HOST_MAX_SLICES + 2];
+    // `stream`; ev[used + 1]: the centroids have landed; ev[used + 2]: the
+    // update is done (read-back on the copy stream)
+    cudaEvent_t ev[KMEANS_HOST_MAX_SLICES + 3];
     int made = 0;
     cudaError_t e = cudaSuccess;
-    for (; made < used + 2 && e == cudaSuccess; ++made) e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+    for (; made < used + 3 && e == cudaSuccess; ++made) e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
     if (e != cudaSuccess) --made;  // the failed one was not created
     // the copies wait for everything enqueued on `stream` before this call,
     // unless the caller vouches that X and C_old are free (then they may
@@ -331,11 +332,19 @@ int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, f
         if (e == cudaSuccess) e = launch_assign_tc(X + r0 * d, rows, k, d, Ai, w, s, false);
     }
     if (e == cudaSuccess) e = lloyd_finish(X, C_old, C_new, labels, best_dist, inertia, counts, n, k, d, A, w, s);
+    // the read-backs: on `stream`, or on the copy stream once the update is done
+    cudaStream_t rs = s;
+    if (flags & KMEANS_HOST_READBACK_ON_COPY_STREAM) {
+        rs = cs;
+        if (e == cudaSuccess) e = cudaEventRecord(ev[used + 2], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[used + 2], 0);
+    }
     if (e == cudaSuccess && C_new_host)
-        e = cudaMemcpyAsync(C_new_host, C_new, (size_t)(k * d) * sizeof(float), cudaMemcpyDeviceToHost, s);
+        e = cudaMemcpyAsync(C_new_host, C_new, (size_t)(k * d) * sizeof(float), cudaMemcpyDeviceToHost, rs);
     if (e == cudaSuccess && labels_host)
-        e = cudaMemcpyAsync(labels_host, labels, (size_t)n * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess && inertia_host) e = cudaMemcpyAsync(inertia_host, inertia, sizeof(double), cudaMemcpyDeviceToHost, s);
+        e = cudaMemcpyAsync(labels_host, labels, (size_t)n * sizeof(int64_t), cudaMemcpyDeviceToHost, rs);
+    if (e == cudaSuccess && inertia_host)
+        e = cudaMemcpyAsync(inertia_host, inertia, sizeof(double), cudaMemcpyDeviceToHost, rs);
     // released by the runtime once the work that uses them has completed
     for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
     return cuda_status(e);

@@ -216,6 +216,15 @@ int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, in
  * of device buffers between successive calls. */
 #define KMEANS_HOST_OVERLAP_PREVIOUS 1
 
+/* kmeans_lloyd_iter_host flag: the copies to C_new_host, labels_host and
+ * *inertia_host run on `copy_stream` once the update is done, instead of on
+ * `stream`, so that `stream` can go on to the next iteration while they run.
+ * The call's work is then complete when `copy_stream` (not `stream`) reaches
+ * the point after it.  The caller leaves C_new, labels and inertia unchanged
+ * until then, for example by alternating two sets of device buffers and two
+ * copy streams between successive calls. */
+#define KMEANS_HOST_READBACK_ON_COPY_STREAM 2
+
 /* One Lloyd iteration [U] on inputs that live in host memory (the pages have
  * no counterpart: it serves callers whose data is not resident on the GPU).
  * X_host (n, d) and C_host (k, d) are host arrays, page-locked for the copies
@@ -234,9 +243,10 @@ int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, in
  * C_new, the labels and *inertia are copied to C_new_host, labels_host and
  * *inertia_host (each may be NULL; inertia_host needs inertia).
  * The copies into X wait for the work enqueued on `stream` before the call
- * (flags = 0) or not (flags = KMEANS_HOST_OVERLAP_PREVIOUS, see there);
- * everything the call enqueues is complete when `stream` reaches the point
- * after it (the copy stream's part is joined back into `stream`).
+ * (without KMEANS_HOST_OVERLAP_PREVIOUS in flags) or not (with it, see
+ * there); everything the call enqueues is complete when `stream` reaches the
+ * point after it (the copy stream's part is joined back into `stream`),
+ * unless flags has KMEANS_HOST_READBACK_ON_COPY_STREAM (see there).
  * copy_stream must differ from stream.  Same requirements as
  * kmeans_lloyd_iter; the workspace is the KMEANS_OP_LLOYD one. */
 int kmeans_lloyd_iter_host(const float *X_host, const float *C_host, float *X, float *C_old, float *C_new,

@@ -36,6 +36,16 @@ def test_library_exports_every_declared_symbol(km):
     assert set(km.EXPORTS) == set(declared)
 
 
+def test_binding_constants_match_the_header(km):
+    # every integer #define of the header that the binding mirrors
+    text = open(HEADER).read()
+    defines = dict(re.findall(r"^#define KMEANS_(\w+) (\d+)\s*$", text, flags=re.M))
+    assert {"HOST_MAX_SLICES", "HOST_OVERLAP_PREVIOUS", "HOST_READBACK_ON_COPY_STREAM"} <= set(defines)
+    for name, value in defines.items():
+        if hasattr(km, name):
+            assert getattr(km, name) == int(value), name
+
+
 def test_status_strings(km):
     for st in range(8):
         s = km.kmeans_status_string(st)

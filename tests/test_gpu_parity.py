@@ -543,6 +543,41 @@ def test_back_to_back_host_iterations_overlapping_their_copies(gpu_lib):
         assert abs(float(in_h[0]) - float(ref[3].item())) <= DIST_RTOL * total  # four slices: see above
 
 
+def test_host_iterations_reading_back_on_alternating_copy_streams(gpu_lib):
+    # the read-backs on the copy stream: two alternating sets of device
+    # buffers (inputs and outputs) and two copy streams, so each call's
+    # read-back runs beside the next call's assignment; every call must give
+    # the device call's results, visible once its copy stream is done
+    w = synth.Workload("t", 20000, 300, 64, 300, 1, 55, 56, "")
+    X, C0, _ = synth.workload_inputs(w)
+    n, k, d = w.n, w.k, w.d
+    ref = gpu_lib.kmeans_lloyd_iter(dev_tensor(X), dev_tensor(C0))
+    Xh, Ch = torch.from_numpy(X).pin_memory(), torch.from_numpy(C0).pin_memory()
+    Xd = [torch.empty((n, d), device="cuda") for _ in range(2)]
+    Cd = [torch.empty((k, d), device="cuda") for _ in range(2)]
+    C_new = [torch.empty((k, d), device="cuda") for _ in range(2)]
+    labels = [torch.empty(n, dtype=torch.int64, device="cuda") for _ in range(2)]
+    inertia = [torch.empty(1, dtype=torch.float64, device="cuda") for _ in range(2)]
+    best = torch.empty(n, device="cuda")
+    counts = torch.empty(k, dtype=torch.int32, device="cuda")
+    outs = [(torch.empty((k, d)).pin_memory(), torch.empty(n, dtype=torch.int64).pin_memory(),
+             torch.empty(1, dtype=torch.float64).pin_memory()) for _ in range(5)]
+    cs = [torch.cuda.Stream(), torch.cuda.Stream()]
+    done = []
+    for j in range(5):
+        slot = j % 2
+        C_h, lab_h, in_h = outs[j]
+        done.append(gpu_lib.kmeans_lloyd_iter_host(Xh, Ch, Xd[slot], Cd[slot], C_new[slot], labels[slot], best,
+                                                   counts, C_h, lab_h, in_h, slices=1, inertia=inertia[slot],
+                                                   copy_stream=cs[slot], overlap_previous=True,
+                                                   readback_on_copy_stream=True))
+    for (C_h, lab_h, in_h), ev in zip(outs, done):
+        ev.synchronize()
+        np.testing.assert_array_equal(lab_h.numpy(), host(ref[1]))
+        assert C_h.numpy().tobytes() == host(ref[0]).tobytes()
+        assert float(in_h[0]) == float(ref[3].item())  # one slice: bit for bit
+
+
 def test_lloyd_iteration_from_host_buffers_rejects_bad_arguments(gpu_lib):
     lib = gpu_lib.load()
     fake = ctypes.c_void_p(0x10000)  # validation fails before any pointer is used
@@ -552,4 +587,4 @@ def test_lloyd_iteration_from_host_buffers_rejects_bad_arguments(gpu_lib):
     assert lib.kmeans_lloyd_iter_host(*args(0, None)) == gpu_lib.KMEANS_ERR_INVALID_ARG
     assert lib.kmeans_lloyd_iter_host(*args(gpu_lib.HOST_MAX_SLICES + 1, None)) == gpu_lib.KMEANS_ERR_INVALID_ARG
     assert lib.kmeans_lloyd_iter_host(*args(4, s)) == gpu_lib.KMEANS_ERR_INVALID_ARG  # copy stream == stream
-    assert lib.kmeans_lloyd_iter_host(*args(4, None, 2)) == gpu_lib.KMEANS_ERR_INVALID_ARG  # unknown flag
+    assert lib.kmeans_lloyd_iter_host(*args(4, None, 4)) == gpu_lib.KMEANS_ERR_INVALID_ARG  # unknown flag
