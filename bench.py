@@ -613,6 +613,16 @@ def run_gb300(args):
             stream.wait_stream(cs)  # the last read-backs end inside it
         ev1.record(stream)
         barrier()
+        # the host link's rate for one whole copy of X, after the timed
+        # region: what the copies in could take at most (the link is shared
+        # with the rest of the machine, so it differs from run to run)
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0.record(copy_streams[0])
+        with torch.cuda.stream(copy_streams[0]):
+            Xe[0].copy_(Xh, non_blocking=True)
+        h1.record(copy_streams[0])
+        h1.synchronize()
+        link_gbs = Xh.numel() * 4 / (h0.elapsed_time(h1) / 1e3) / 1e9
         t_e2e = ev0.elapsed_time(ev1) / 1e3 / e2e_steps
         e2e = {"value": flop / t_e2e / 1e12, "unit": "TFLOP/s", "ms_per_step": 1e3 * t_e2e,
                "steps": e2e_steps, "pipeline": f"kmeans_lloyd_iter_host: {slices} row slices copied on a copy "
@@ -621,6 +631,7 @@ def run_gb300(args):
                                                "buffer sets and two copy streams alternate, so each step's copies "
                                                "in and out overlap the neighbouring steps' compute",
                "h2d_bytes_per_step": int(Xh.numel() * 4 + Ch.numel() * 4),
+               "host_link_gbs": round(link_gbs, 1),
                "d2h_bytes_per_step": int(C_out_h[0].numel() * 4 + lab_h[0].numel() * 8 + in_h[0].numel() * 8)}
 
     # max over ranks
