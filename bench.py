@@ -356,23 +356,35 @@ def time_kmeanspp(km, synth, dev, stream, barrier):
 
     t = seed_once(False)
     first = idx.clone()
+    rows = km.kmeanspp_rows_read(ws, stream)
     match = kmeanspp_matches_stored_oracle(X, w, T, first.cpu().numpy())
     t_traced = seed_once(True)
     dist_ms, dist_timed, dist_seen = km.kmeans_trace_read(km.KERNEL_KMEANSPP_DIST)
     km.kmeans_trace_stop()
     assert torch.equal(first, idx)
-    moved = 4.0 * w.n * w.d * w.k  # one read of X per center
-    # one distance pass: X once, plus its (slice, trial, sample) float2 partial sums
+    # one distance pass over every row: X once, plus its (slice, trial,
+    # sample) float2 partial sums; rows that every trial provably leaves at
+    # their D^2 are skipped, so the passes read `rows` rows in all
+    passes = w.k * ((T + 7) // 8)
+    if rows <= 0:
+        rows = w.n * passes  # no pruning: every pass reads every row
     slices = (w.d + km.KPP_SLICE_FEATURES - 1) // km.KPP_SLICE_FEATURES
-    pass_bytes = 4.0 * w.n * w.d + 8.0 * slices * T * w.n
+    row_bytes = 4.0 * w.d + 8.0 * slices * T
+    full_pass = row_bytes * w.n
+    read = row_bytes * rows  # over the whole seeding
     t_pass = dist_ms / 1e3 / max(dist_timed, 1)
-    return {"workload": f"n={w.n} d={w.d} k={w.k} trials={T}", "ms": 1e3 * t, "gbs": moved / t / 1e9,
+    return {"workload": f"n={w.n} d={w.d} k={w.k} trials={T}", "ms": 1e3 * t, "gbs": read / t / 1e9,
             "ms_per_center": 1e3 * t / w.k, "indices_match_oracle": match,
+            "rows_read_fraction": rows / (w.n * passes),
+            "unpruned_hbm_floor_ms": 1e3 * full_pass * passes / (load_peaks()[0]["hbm_gbs"] * 1e9),
             "distance_pass": {"kernel": "kpp_dist_part_kernel", "launches": dist_seen, "us": 1e6 * t_pass,
-                              "bytes_per_launch": pass_bytes, "gbs": pass_bytes / t_pass / 1e9,
+                              "bytes_per_launch": read / passes, "gbs": read / passes / t_pass / 1e9,
+                              "bytes_per_launch_unpruned": full_pass,
                               "share_of_call": dist_ms / 1e3 / t_traced,
                               "timed": "a second seeding with CUDA events around each distance pass "
-                                       f"({1e3 * t_traced:.1f} ms with them)"}}
+                                       f"({1e3 * t_traced:.1f} ms with them)"},
+            "pruning": "each round reads only the rows some trial can bring below their D^2 (triangle "
+                       "inequality through the nearest chosen center); gbs and frac_of_hbm count the bytes read"}
 
 
 def run_gb300(args):

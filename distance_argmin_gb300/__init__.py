@@ -71,7 +71,7 @@ EXPORTS = (
     "kmeans_trace_stop", "kmeans_lloyd_iter_host", "kmeans_fit", "kmeans_assign_3xtf32",
     "kmeans_lloyd_iter_fused", "kmeans_relocate_empty", "kmeans_update_partial", "kmeans_lloyd_iter_partial",
     "kmeans_reduce_partials", "kmeanspp_shard_exchange_bytes", "kmeanspp_shard_first", "kmeanspp_shard_pick",
-    "kmeanspp_shard_dist", "kmeanspp_shard_commit",
+    "kmeanspp_shard_dist", "kmeanspp_shard_commit", "kmeanspp_rows_read",
 )
 
 _lock = threading.Lock()
@@ -118,6 +118,8 @@ def load(path: str | None = None):
         lib.kmeanspp_init.restype = INT
         lib.kmeans_device_status.argtypes = [P, P]
         lib.kmeans_device_status.restype = INT
+        lib.kmeanspp_rows_read.argtypes = [P, P, ctypes.POINTER(I64)]
+        lib.kmeanspp_rows_read.restype = INT
         lib.kmeans_status_string.argtypes = [INT]
         lib.kmeans_status_string.restype = ctypes.c_char_p
         lib.kmeans_build_info.argtypes = []
@@ -369,6 +371,14 @@ def kmeanspp_init(X, k: int, seed: int, n_trials: int = 0, centers=None, indices
                               _ptr(ws), ws.numel(), _stream_handle(stream))
     _raise(st, "kmeanspp_init")
     return indices, centers
+
+
+def kmeanspp_rows_read(ws, stream=None) -> int:
+    """Rows of X the last seeding on ``ws`` read over its distance passes
+    (0: it read every row); synchronises the stream."""
+    v = ctypes.c_int64(0)
+    _raise(load().kmeanspp_rows_read(_ptr(ws), _stream_handle(stream), ctypes.byref(v)), "kmeanspp_rows_read")
+    return int(v.value)
 
 
 def kmeans_device_status(ws, stream=None) -> int:

@@ -96,7 +96,7 @@ FitLayout fit_layout(int64_t n, int64_t k, int64_t d) {
     FitLayout F{};
     const int64_t a = assign_layout(n, k, d, true).bytes;
     const int64_t u = update_layout(n, k, d).bytes;
-    const int64_t p = kpp_layout(n, d, default_trials(k)).bytes;
+    const int64_t p = kpp_layout(n, d, default_trials(k), k).bytes;
     F.shared = a > u ? a : u;
     if (p > F.shared) F.shared = p;
     int64_t o = align_up(F.shared, 1024);
@@ -177,7 +177,7 @@ size_t kmeans_workspace_bytes(int op, int64_t n, int64_t k, int64_t d) {
         case KMEANS_OP_LLOYD:
             return (size_t)lloyd_ws_bytes(n, k, d);
         case KMEANS_OP_KMEANSPP:
-            return (size_t)kpp_layout(n, d, kKppMaxTrials).bytes;
+            return (size_t)kpp_layout(n, d, kKppMaxTrials, k).bytes;
         case KMEANS_OP_FIT:
             return (size_t)fit_layout(n, k, d).bytes;
         case KMEANS_OP_LLOYD_FUSED:
@@ -377,7 +377,7 @@ int kmeans_fit(const float *X, float *C, int64_t *labels, float *best_dist, int3
         const int T = default_trials(k);
         if (T > kKppMaxTrials) return KMEANS_ERR_UNSUPPORTED;
         e = launch_kmeanspp(X, n, d, k, T, seed, C, reinterpret_cast<int64_t *>(w + F.off_indices),
-                            kpp_layout(n, d, T), w, s);
+                            kpp_layout(n, d, T, k), w, s);
     }
     const AssignLayout A = assign_layout(n, k, d, true);
     const UpdateLayout U = update_layout(n, k, d);
@@ -571,11 +571,22 @@ int kmeanspp_init(const float *X, int64_t n, int64_t d, int64_t k, int n_trials,
         return KMEANS_ERR_INVALID_ARG;
     const int T = n_trials > 0 ? n_trials : default_trials(k);
     if (T > kKppMaxTrials) return KMEANS_ERR_UNSUPPORTED;
-    const KppLayout L = kpp_layout(n, d, T);
+    const KppLayout L = kpp_layout(n, d, T, k);
     const int wst = check_ws(ws, ws_bytes, (size_t)L.bytes);
     if (wst != KMEANS_OK) return wst;
     return cuda_status(launch_kmeanspp(X, n, d, k, T, seed, centers, indices, L, static_cast<uint8_t *>(ws),
                                        static_cast<cudaStream_t>(stream)));
+}
+
+int kmeanspp_rows_read(const void *ws, void *stream, int64_t *rows) {
+    if (ws == nullptr || rows == nullptr) return KMEANS_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KMEANS_ERR_CUDA;
+    unsigned long long v = 0;
+    if (cudaMemcpy(&v, static_cast<const uint8_t *>(ws) + offsetof(WsHeader, kpp_rows), sizeof(v),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KMEANS_ERR_CUDA;
+    *rows = (int64_t)v;
+    return KMEANS_OK;
 }
 
 int kmeans_device_status(const void *ws, void *stream) {

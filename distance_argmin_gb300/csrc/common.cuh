@@ -95,7 +95,8 @@ struct WsHeader {
     uint32_t done_blocks;     // "last block" counter of the inertia reduction
     double fit_inertia;       // kmeans_fit: the last iteration's inertia
     uint32_t fit_nempty;      // kmeans_fit: clusters left empty by the last update
-    uint32_t pad[59];
+    unsigned long long kpp_rows;  // k-means++ with row pruning: sample rows its distance passes read
+    uint32_t pad[56];
 };
 // kmeans_fit reads the status word, the inertia and the empty count back in
 // one copy of the header's first bytes.
@@ -103,6 +104,7 @@ constexpr size_t kFitRecordBytes = 20;
 static_assert(offsetof(WsHeader, fit_inertia) == 8 && offsetof(WsHeader, fit_nempty) + 4 == kFitRecordBytes,
               "the fit's record is the header's first bytes");
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+static_assert(offsetof(WsHeader, kpp_rows) == 24, "8-byte aligned");
 
 // Wall-clock limit of one pipeline wait.  A wait that legitimately takes this
 // long does not exist (the slowest stage waits for one k-block of a tile).
@@ -317,10 +319,23 @@ struct KppLayout {
     int64_t off_bpot;     // T x n_blocks x f64 block potentials
     int64_t off_cand;     // T x i64 candidates of the current center
     int64_t off_chosen;   // spare
+    // Rows that no trial can change (see kmeanspp.cu); 0 offsets: not reserved
+    int64_t k;            // row pitch of the center-candidate table
+    int64_t off_near;     // n x i32 each sample's nearest committed center (its position in the indices)
+    int64_t off_dcc;      // T x k x f32 squared distances between the trial candidates and the committed centers
+    int64_t off_rows;     // n_blocks x kKppScanBlock x i32 rows each block of samples has to read, ascending
+    int64_t off_rcount;   // n_blocks x i32 rows listed per block
+    int64_t off_flag;     // n x u8 1: the distance pass reads the row this round
     int64_t bytes;
 };
 
-inline KppLayout kpp_layout(int64_t n, int64_t d, int T) {
+// The distance pass keeps the prefix of the per-block row counts in shared
+// memory beside the candidates; past this many sample blocks (16.7 M
+// samples) the seeding reads every row.
+constexpr int64_t kKppPruneMaxBlocks = 16384;
+
+// k > 0: also the regions of the row pruning (the single-GPU seeding).
+inline KppLayout kpp_layout(int64_t n, int64_t d, int T, int64_t k = 0) {
     KppLayout L{};
     L.T = T;
     L.n_blocks = (n + kKppScanBlock - 1) / kKppScanBlock;
@@ -334,6 +349,16 @@ inline KppLayout kpp_layout(int64_t n, int64_t d, int T) {
     o = align_up(o, 1024); L.off_bpot = o; o += (int64_t)T * L.n_blocks * 8;
     o = align_up(o, 1024); L.off_cand = o; o += (int64_t)T * 8;
     o = align_up(o, 1024); L.off_chosen = o; o += 8;
+    L.k = 0;
+    L.off_near = L.off_dcc = L.off_rows = L.off_rcount = L.off_flag = 0;
+    if (k > 0 && L.n_blocks <= kKppPruneMaxBlocks) {
+        L.k = k;
+        o = align_up(o, 1024); L.off_near = o; o += n * 4;
+        o = align_up(o, 1024); L.off_dcc = o; o += (int64_t)T * k * 4;
+        o = align_up(o, 1024); L.off_rows = o; o += L.n_blocks * kKppScanBlock * 4;
+        o = align_up(o, 1024); L.off_rcount = o; o += L.n_blocks * 4;
+        o = align_up(o, 1024); L.off_flag = o; o += n;
+    }
     L.bytes = align_up(o, 1024);
     return L;
 }

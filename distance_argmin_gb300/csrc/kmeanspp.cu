@@ -57,9 +57,11 @@ __device__ double philox_uniform(uint64_t seed, uint64_t draw) {
 }
 
 // -------------------------------------------------------------- first center
-__global__ void kpp_first_kernel(int64_t n, uint64_t seed, int64_t *cand, int64_t *indices, WsHeader *hdr) {
+__global__ void kpp_first_kernel(int64_t n, uint64_t seed, int64_t *cand, int64_t *indices, WsHeader *hdr,
+                                 int count_rows) {
     hdr->status = 0u;
     hdr->done_blocks = 0u;
+    hdr->kpp_rows = count_rows ? (unsigned long long)n : 0ull;  // the first pass reads every row
     const double u = philox_uniform(seed, 0);
     int64_t idx = static_cast<int64_t>(u * static_cast<double>(n));  // u >= 0: truncation is floor
     if (idx > n - 1) idx = n - 1;
@@ -247,19 +249,61 @@ __device__ __forceinline__ void load4x2(const float *__restrict__ p, int avail, 
 // a lane's 8 features of a step is added to a per-lane sum, the two rows'
 // sums paired in one packed add.  A lane adds at most W / 256 runs (16 for a
 // 4096-feature slice); lanes and slices are combined in double-float.
+// With `rows` the pass reads only the listed rows: block b of samples lists
+// rcount[b] of them, ascending, at rows[b * kKppScanBlock ...] (the others
+// cannot change this round, see kpp_select_rows_kernel); the list is walked
+// in sample order.  A row's sums do not depend on which rows share its warp.
 template <bool VEC>
 __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     kpp_dist_part_kernel(const float *__restrict__ X, int64_t n, int d, const int64_t *__restrict__ cand,
-                         const float *__restrict__ crows, int T, int t0, int W, int rev, float2 *__restrict__ dpart) {
-    extern __shared__ __align__(16) float cs[];  // [KT][W], negated
+                         const float *__restrict__ crows, int T, int t0, int W, int rev,
+                         const int32_t *__restrict__ rows, const int32_t *__restrict__ rcount, int nb,
+                         float2 *__restrict__ dpart) {
+    extern __shared__ __align__(16) float cs[];  // [KT][W], negated; with rows, then nb + 1 ints
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nt = min(kd::KT, T - t0);
     const int slice = blockIdx.y;
     const int fb = slice * W;
     const int width = min(W, d - fb);
-    const int64_t n_groups = (n + kd::GROUP - 1) / kd::GROUP;
     static_assert(kd::ROWS == 2, "the two rows' sums are paired in float2");
+    // entries of the list of rows to read: every row, or the listed ones
+    // (their count is known after the wait, from the block counts' prefix)
+    int *pref = reinterpret_cast<int *>(cs + kd::KT * W);
+    int64_t count = n;
+    if (rows) {
+        griddep_wait();
+        if (warp == 0) {
+            int run = 0;
+            for (int b0 = 0; b0 < nb; b0 += 32) {
+                const int v = b0 + lane < nb ? rcount[b0 + lane] : 0;
+                int incl = v;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                if (b0 + lane < nb) pref[b0 + lane] = run + incl - v;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) pref[nb] = run;
+        }
+        __syncthreads();
+        count = pref[nb];
+    }
+    const int64_t n_groups = (count + kd::GROUP - 1) / kd::GROUP;
+    // the sample of list entry e, or n past the list
+    auto row_of = [&](int64_t e) -> int64_t {
+        if (e >= count) return n;
+        if (!rows) return e;
+        int lo = 0, hi = nb;  // pref[lo] <= e < pref[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pref[mid] <= e) lo = mid;
+            else hi = mid;
+        }
+        return rows[(int64_t)lo * kKppScanBlock + (e - pref[lo])];
+    };
 
     // A lane owns features f .. f+3 and f+128 .. f+131 of each 256-feature
     // step, so every 16-byte load of the warp (global and shared) covers 512
@@ -274,13 +318,15 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     // pass then starts on the rows the previous pass read last, which are
     // still in L2.  The i-th group a block visits is group(i) either way.
     float2 x[kd::ROWS][4], xn[kd::ROWS][4];
+    int64_t rn[kd::ROWS];  // the rows whose first step is in xn
     auto group = [&](int64_t i) { return rev ? n_groups - 1 - i : i; };
     auto load_first_step = [&](int64_t i) {
-        const int64_t rr = (i < n_groups ? group(i) : n_groups) * kd::GROUP + warp * kd::ROWS;
+        const int64_t e0 = (i < n_groups ? group(i) : n_groups) * kd::GROUP + warp * kd::ROWS;
 #pragma unroll
         for (int r = 0; r < kd::ROWS; ++r) {
-            if (rr + r < n) {  // past the last group every row is past n
-                load4x2<VEC>(X + (rr + r) * (int64_t)d + fb + lane * 4, width - lane * 4, xn[r]);
+            rn[r] = row_of(e0 + r);
+            if (rn[r] < n) {  // past the last group every row is past n
+                load4x2<VEC>(X + rn[r] * (int64_t)d + fb + lane * 4, width - lane * 4, xn[r]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) xn[r][e] = make_float2(0.f, 0.f);
@@ -288,10 +334,10 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
         }
     };
     // X is an input of the whole entry point, never written by a kernel of
-    // the chain, so its first rows are requested before the wait for the
-    // kernel that chose the candidates
+    // the chain, so without a row list its first rows are requested before
+    // the wait for the kernel that chose the candidates
     load_first_step(blockIdx.x);
-    griddep_wait();
+    if (!rows) griddep_wait();
     // the candidates are rows of X, or (a shard) rows of the exchange buffer
     if (VEC) {
         // W and width are multiples of 4: a 16-byte group never straddles a
@@ -318,7 +364,9 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
     __syncthreads();
 
     for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x) {
-        const int64_t r0 = group(g) * kd::GROUP + warp * kd::ROWS;
+        int64_t rw[kd::ROWS];
+#pragma unroll
+        for (int r = 0; r < kd::ROWS; ++r) rw[r] = rn[r];
         float2 s2[kd::KT];  // .x row 0, .y row 1
 #pragma unroll
         for (int t = 0; t < kd::KT; ++t) s2[t] = make_float2(0.f, 0.f);
@@ -331,7 +379,7 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
             if (f0 + 256 < width) {
 #pragma unroll
                 for (int r = 0; r < kd::ROWS; ++r) {
-                    if (r0 + r < n) load4x2<VEC>(X + (r0 + r) * (int64_t)d + fb + f + 256, width - f - 256, xn[r]);
+                    if (rw[r] < n) load4x2<VEC>(X + rw[r] * (int64_t)d + fb + f + 256, width - f - 256, xn[r]);
                 }
             } else {
                 load_first_step(g + gridDim.x);
@@ -389,7 +437,7 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
         // sums, held by both lanes of a pair)
         const int v = NS == 32 ? lane : lane >> 1;
         const int t = v % kd::KT;
-        const int64_t row = r0 + v / kd::KT;
+        const int64_t row = v < kd::KT ? rw[0] : rw[1];
         if ((NS == 32 || (lane & 1) == 0) && t < nt && row < n)
             dpart[((int64_t)slice * kd::KT + t) * n + row] = make_float2(hi[0], lo[0]);
     }
@@ -398,9 +446,12 @@ __global__ void __launch_bounds__(kd::THREADS, kd::MIN_BLOCKS)
 // dist[t0 + t][i] = sum of the S slice partials (slice order, double-float); with D2, the
 // block potentials bpot[t0 + t][block] = sum over the block's samples of
 // min(D2_i, dist) in a fixed order.  Grid: (sample blocks, trials).
+// With `flag`, a row the pass did not read (flag 0) is at distance +inf from
+// every trial: no trial can lower its D^2 this round.
 __global__ void __launch_bounds__(kBsThreads)
     kpp_combine_kernel(const float2 *__restrict__ dpart, int S, int64_t n, int t0, const double *__restrict__ D2,
-                       double *__restrict__ dist, double *__restrict__ bpot, int64_t n_blocks) {
+                       const uint8_t *__restrict__ flag, double *__restrict__ dist, double *__restrict__ bpot,
+                       int64_t n_blocks) {
     griddep_wait();
     __shared__ double red[kBsThreads];
     const int t = blockIdx.y;
@@ -412,13 +463,17 @@ __global__ void __launch_bounds__(kBsThreads)
         if (i < n) {
             // slice partials added as double-float values, one conversion at the end
             float hi = 0.f, lo = 0.f;
-            for (int sl = 0; sl < S; ++sl) {
-                const float2 pv = dpart[((int64_t)sl * kd::KT + t) * n + i];
-                float s2, e;
-                two_sum(hi, pv.x, s2, e);
-                e += lo + pv.y;
-                hi = s2 + e;
-                lo = e - (hi - s2);
+            if (flag && !flag[i]) {
+                hi = __int_as_float(0x7f800000);  // +inf
+            } else {
+                for (int sl = 0; sl < S; ++sl) {
+                    const float2 pv = dpart[((int64_t)sl * kd::KT + t) * n + i];
+                    float s2, e;
+                    two_sum(hi, pv.x, s2, e);
+                    e += lo + pv.y;
+                    hi = s2 + e;
+                    lo = e - (hi - s2);
+                }
             }
             const double v = static_cast<double>(hi) + static_cast<double>(lo);
             dist[(int64_t)(t0 + t) * n + i] = v;
@@ -470,12 +525,22 @@ __device__ int select_best_trial(const double *__restrict__ bpot, int T, int64_t
 
 // K1 of center c: choose the winner of center c-1 (from c = 2 on), lower D^2
 // by its distances, and the per-block sums of D^2 for the draws of center c.
+// With `near`, a sample whose D^2 the winner lowers records center c-1 as
+// its nearest (every sample records center 0 at c = 1), and the rows of the
+// center-candidate table for centers 0 .. c-1 are cleared for this round.
 __global__ void __launch_bounds__(kBsThreads)
     kpp_update_kernel(const double *__restrict__ dist, const double *__restrict__ bpot, int T, int64_t n,
                       int64_t n_blocks, const int64_t *__restrict__ cand, int64_t *__restrict__ indices,
-                      int64_t prev, int init, double *__restrict__ D2, double *__restrict__ bsum) {
+                      int64_t prev, int init, double *__restrict__ D2, double *__restrict__ bsum,
+                      int32_t *__restrict__ near, float *__restrict__ dcc, int64_t kst) {
     griddep_wait();
     __shared__ double red[kBsThreads];
+    if (dcc) {
+        const int64_t cells = (int64_t)T * (prev + 1);
+        for (int64_t e = (int64_t)blockIdx.x * kBsThreads + threadIdx.x; e < cells;
+             e += (int64_t)gridDim.x * kBsThreads)
+            dcc[(e / (prev + 1)) * kst + e % (prev + 1)] = 0.f;
+    }
     int best = 0;
     if (!init) {
         best = select_best_trial(bpot, T, n_blocks);
@@ -489,8 +554,10 @@ __global__ void __launch_bounds__(kBsThreads)
         const int64_t i = base + threadIdx.x + (int64_t)q * kBsThreads;
         if (i < n) {
             const double v = db[i];
-            const double nd = init ? v : fmin(D2[i], v);
+            const double old = init ? 0.0 : D2[i];
+            const double nd = init ? v : fmin(old, v);
             D2[i] = nd;
+            if (near && (init || v < old)) near[i] = (int32_t)prev;
             s += nd;
         }
     }
@@ -501,6 +568,131 @@ __global__ void __launch_bounds__(kBsThreads)
         __syncthreads();
     }
     if (threadIdx.x == 0) bsum[blockIdx.x] = red[0];
+}
+
+// ------------------------------------------------------- row pruning
+// A sample x whose nearest committed center is c_j (D(x) = ||x - c_j||, so
+// D^2(x) is its current D^2) is at least ||c_j - y|| - D(x) from a trial
+// candidate y (triangle inequality).  When ||c_j - y|| >= 2.001 D(x), y is
+// more than 1.0009 D(x) from x, and min(D^2(x), ||x - y||^2) is D^2(x)
+// whatever rounding either distance carries (float32 sums are good to about
+// 1e-6 relative, far inside the 0.2% margin on the squares).  A row that
+// this clears for every trial of the round cannot change D^2, a potential or
+// a draw: the distance pass skips it and the combine puts it at +inf.  The
+// seeding's indices are therefore the same as without pruning.
+constexpr double kKppPruneSq = 4.004;  // (2 + 0.001)^2, rounded up
+constexpr int kDccChunk = 1024;        // features of one block of the center-candidate distances
+
+// dcc[t][j] += sum over features [f0, f0 + 1024) of (X[indices[j]] - X[cand[t]])^2
+// for the committed centers j < c, in float32, onto zeros the update kernel
+// left (the feature chunks of a (t, j) pair add in any order: the table only
+// decides which rows are read, never a value).  Grid (centers / 8, chunks):
+// warp w takes center 8 * blockIdx.x + w; the block stages the chunk of every
+// candidate.  Needs d % 4 == 0 and 16-byte aligned rows.
+__global__ void __launch_bounds__(kBsThreads)
+    kpp_dcc_kernel(const float *__restrict__ X, int d, const int64_t *__restrict__ indices, int64_t c,
+                   const int64_t *__restrict__ cand, int T, int64_t kst, float *__restrict__ dcc) {
+    constexpr int V = kDccChunk / 4;  // float4 per chunk of a row
+    static_assert(V == kBsThreads, "one float4 of every candidate per thread");
+    extern __shared__ float4 ys[];    // [T][V]
+    griddep_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t j = (int64_t)blockIdx.x * (kBsThreads / 32) + (threadIdx.x >> 5);
+    const int f0 = blockIdx.y * kDccChunk;
+    const int w4 = min(kDccChunk, d - f0) / 4;
+    // every candidate's chunk: one float4 each per thread, all in flight
+#pragma unroll
+    for (int t = 0; t < kKppMaxTrials; ++t) {
+        if (t < T) {
+            const float4 *src = reinterpret_cast<const float4 *>(X + cand[t] * (int64_t)d + f0);
+            ys[t * V + threadIdx.x] = threadIdx.x < w4 ? __ldg(src + threadIdx.x) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    __syncthreads();
+    if (j >= c) return;
+    const float4 *cj = reinterpret_cast<const float4 *>(X + indices[j] * (int64_t)d + f0);
+    float4 xv[V / 32];
+#pragma unroll
+    for (int m = 0; m < V / 32; ++m) {
+        const int q = lane + 32 * m;
+        xv[m] = q < w4 ? __ldg(cj + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < V / 32; ++m) {
+            const float4 y = ys[t * V + lane + 32 * m];
+            const float dx = xv[m].x - y.x, dy = xv[m].y - y.y, dz = xv[m].z - y.z, dw = xv[m].w - y.w;
+            acc = fmaf(dx, dx, acc);
+            acc = fmaf(dy, dy, acc);
+            acc = fmaf(dz, dz, acc);
+            acc = fmaf(dw, dw, acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) atomicAdd(dcc + (int64_t)t * kst + j, acc);
+    }
+}
+
+// Per block of kKppScanBlock samples: flag[i] = 1 when some trial is closer
+// than 2.001 D(x) to the sample's nearest center (the pass must read the
+// row), and the flagged rows listed in ascending order at rows[block * 1024
+// ...], their number in rcount[block].  Four consecutive samples a thread,
+// every load issued before the first comparison.
+__global__ void __launch_bounds__(kBsThreads)
+    kpp_select_rows_kernel(int64_t n, const int32_t *__restrict__ near, const double *__restrict__ D2,
+                           const float *__restrict__ dcc, int T, int64_t kst, uint8_t *__restrict__ flag,
+                           int32_t *__restrict__ rows, int32_t *__restrict__ rcount, int passes, WsHeader *hdr) {
+    static_assert(kKppScanBlock == 4 * kBsThreads, "four samples a thread");
+    __shared__ int wsum[kBsThreads / 32];
+    griddep_wait();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t i0 = (int64_t)blockIdx.x * kKppScanBlock + 4 * threadIdx.x;
+    double lim[4];
+    int jn[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const bool in = i0 + r < n;
+        lim[r] = in ? kKppPruneSq * D2[i0 + r] : 0.0;
+        jn[r] = in ? near[i0 + r] : 0;
+    }
+    bool need[4];
+    int cnt = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        need[r] = false;
+#pragma unroll
+        for (int t = 0; t < kKppMaxTrials; ++t)
+            if (t < T) need[r] |= (double)dcc[(int64_t)t * kst + jn[r]] < lim[r];
+        if (i0 + r >= n) need[r] = false;
+        else flag[i0 + r] = need[r] ? 1 : 0;
+        cnt += need[r] ? 1 : 0;
+    }
+    // exclusive prefix of the counts over the block, in thread order
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int q = 0; q < kBsThreads / 32; ++q) {
+        if (q < w) before += wsum[q];
+        total += wsum[q];
+    }
+    int pos = before + incl - cnt;
+    int32_t *out = rows + (int64_t)blockIdx.x * kKppScanBlock;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+        if (need[r]) out[pos++] = (int32_t)(i0 + r);
+    if (threadIdx.x == 0) {
+        rcount[blockIdx.x] = total;
+        atomicAdd(&hdr->kpp_rows, (unsigned long long)total * (unsigned long long)passes);
+    }
 }
 
 // Winner of the last center.
@@ -523,21 +715,26 @@ __global__ void gather_rows_kernel(const float *__restrict__ X, const int64_t *_
 // One pass over X for the candidates of trials [0, Tn): the per-slice
 // partial distances, then their combination (with D2: and the block
 // potentials).  Candidates: rows cand[] of X, or the rows of `crows`.
+// `prune`: read only the rows kpp_select_rows_kernel listed (the layout has
+// the pruning regions).
 static cudaError_t kpp_dist_pass(const float *X, int64_t n, int64_t d, const KppLayout &L, uint8_t *ws, int Tn,
                                  const int64_t *cand, const float *crows, const double *d2, bool chained_first,
-                                 bool rev, cudaStream_t s) {
+                                 bool rev, bool prune, cudaStream_t s) {
     double *dist = reinterpret_cast<double *>(ws + L.off_dist);
     float2 *dpart = reinterpret_cast<float2 *>(ws + L.off_dpart);
     double *bpot = reinterpret_cast<double *>(ws + L.off_bpot);
+    const int32_t *rows = prune ? reinterpret_cast<const int32_t *>(ws + L.off_rows) : nullptr;
+    const int32_t *rcount = prune ? reinterpret_cast<const int32_t *>(ws + L.off_rcount) : nullptr;
+    const uint8_t *flag = prune ? ws + L.off_flag : nullptr;
     const bool vec = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(crows)) & 15) == 0;
-    const size_t smem = (size_t)kd::KT * L.W * sizeof(float);
+    // the candidates' slice, then (row list) the prefix of the block counts
+    const size_t smem = (size_t)kd::KT * L.W * sizeof(float) + (prune ? (size_t)(L.n_blocks + 1) * sizeof(int) : 0);
     {
         static std::once_flag attr_once[kMaxDevices];
         once_per_device(attr_once, [] {
-            cudaFuncSetAttribute(kpp_dist_part_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(kd::KT * kKppSliceFloats * sizeof(float)));
-            cudaFuncSetAttribute(kpp_dist_part_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(kd::KT * kKppSliceFloats * sizeof(float)));
+            const int most = (int)(kd::KT * kKppSliceFloats * sizeof(float) + (kKppPruneMaxBlocks + 1) * sizeof(int));
+            cudaFuncSetAttribute(kpp_dist_part_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+            cudaFuncSetAttribute(kpp_dist_part_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
         });
     }
     static std::atomic<int> sm_cache[kMaxDevices];
@@ -557,14 +754,14 @@ static cudaError_t kpp_dist_pass(const float *X, int64_t n, int64_t d, const Kpp
         const bool chained = chained_first || t0 > 0;
         trace_mark(kTraceKppDist, false, s);
         e = vec ? launch_kernel(chained, kpp_dist_part_kernel<true>, dgrid, dim3(kd::THREADS), smem, s, X, n, (int)d,
-                                cand, crows, Tn, t0, L.W, (int)rev, dpart)
+                                cand, crows, Tn, t0, L.W, (int)rev, rows, rcount, (int)L.n_blocks, dpart)
                 : launch_kernel(chained, kpp_dist_part_kernel<false>, dgrid, dim3(kd::THREADS), smem, s, X, n, (int)d,
-                                cand, crows, Tn, t0, L.W, (int)rev, dpart);
+                                cand, crows, Tn, t0, L.W, (int)rev, rows, rcount, (int)L.n_blocks, dpart);
         trace_mark(kTraceKppDist, true, s);
         const int nt = Tn - t0 < kd::KT ? Tn - t0 : kd::KT;
         if (e == cudaSuccess)
             e = launch_kernel(true, kpp_combine_kernel, dim3((unsigned)L.n_blocks, (unsigned)nt), dim3(kBsThreads), 0,
-                              s, (const float2 *)dpart, L.S, n, t0, d2, dist, bpot, L.n_blocks);
+                              s, (const float2 *)dpart, L.S, n, t0, d2, flag, dist, bpot, L.n_blocks);
     }
     return e;
 }
@@ -585,18 +782,43 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
         if (e == cudaSuccess) e = r;
     };
 
-    kpp_first_kernel<<<1, 1, 0, s>>>(n, seed, cand, indices, hdr);
+    // row pruning (see kpp_select_rows_kernel) where the layout reserves it
+    // and the rows are whole 16-byte groups
+    const bool prune = L.off_near != 0 && L.k >= k && d % 4 == 0 && (reinterpret_cast<uintptr_t>(X) & 15) == 0;
+    int32_t *near = prune ? reinterpret_cast<int32_t *>(ws + L.off_near) : nullptr;
+    float *dcc = prune ? reinterpret_cast<float *>(ws + L.off_dcc) : nullptr;
+    const size_t dcc_smem = (size_t)T * kDccChunk * sizeof(float);
+    const unsigned dcc_chunks = (unsigned)((d + kDccChunk - 1) / kDccChunk);
+    if (prune) {
+        static std::once_flag attr_once[kMaxDevices];
+        once_per_device(attr_once, [] {
+            cudaFuncSetAttribute(kpp_dcc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(kKppMaxTrials * kDccChunk * sizeof(float)));
+        });
+    }
+
+    kpp_first_kernel<<<1, 1, 0, s>>>(n, seed, cand, indices, hdr, prune ? 1 : 0);
     chain(cudaGetLastError());
     // distances to the first center
-    if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, 1, cand, nullptr, nullptr, true, false, s));
+    if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, 1, cand, nullptr, nullptr, true, false, false, s));
     for (int64_t c = 1; c < k && e == cudaSuccess; ++c) {
         chain(launch_kernel(true, kpp_update_kernel, dim3((unsigned)L.n_blocks), dim3(kBsThreads), 0, s,
                             (const double *)dist, (const double *)bpot, T, n, L.n_blocks, (const int64_t *)cand, indices,
-                            c - 1, c == 1 ? 1 : 0, D2, bsum));
+                            c - 1, c == 1 ? 1 : 0, D2, bsum, near, dcc, L.k));
         chain(launch_kernel(true, kpp_pick_kernel, dim3((unsigned)T), dim3(32), 0, s, (const double *)bsum, L.n_blocks,
                             (const double *)D2, n, seed, 1 + (uint64_t)(c - 1) * (uint64_t)T, T, cand));
+        if (prune) {
+            // the trials' distances to the c committed centers, then the rows to read
+            const unsigned dblocks = (unsigned)((c + kBsThreads / 32 - 1) / (kBsThreads / 32));
+            chain(launch_kernel(true, kpp_dcc_kernel, dim3(dblocks, dcc_chunks), dim3(kBsThreads), dcc_smem, s, X, (int)d,
+                                (const int64_t *)indices, c, (const int64_t *)cand, T, L.k, dcc));
+            chain(launch_kernel(true, kpp_select_rows_kernel, dim3((unsigned)L.n_blocks), dim3(kBsThreads), 0, s, n,
+                                (const int32_t *)near, (const double *)D2, (const float *)dcc, T, L.k,
+                                ws + L.off_flag, reinterpret_cast<int32_t *>(ws + L.off_rows),
+                                reinterpret_cast<int32_t *>(ws + L.off_rcount), (T + kd::KT - 1) / kd::KT, hdr));
+        }
         // successive passes run in opposite directions over X (see the kernel)
-        if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, T, cand, nullptr, D2, true, (c & 1) != 0, s));
+        if (e == cudaSuccess) chain(kpp_dist_pass(X, n, d, L, ws, T, cand, nullptr, D2, true, (c & 1) != 0, prune, s));
     }
     if (k > 1)
         chain(launch_kernel(true, kpp_select_last_kernel, dim3(1), dim3(256), 0, s, (const double *)bpot, T,
@@ -799,7 +1021,7 @@ cudaError_t launch_kpp_shard_dist(const float *X, int64_t n_local, int64_t d, in
                                                (int)d, crow, cglob, &hdr->status);
     cudaError_t e = cudaGetLastError();
     const double *D2 = first ? nullptr : reinterpret_cast<const double *>(ws + L.K.off_d2);
-    if (e == cudaSuccess) e = kpp_dist_pass(X, n_local, d, L.K, ws, Tn, nullptr, crow, D2, true, false, s);
+    if (e == cudaSuccess) e = kpp_dist_pass(X, n_local, d, L.K, ws, Tn, nullptr, crow, D2, true, false, false, s);
     if (e == cudaSuccess && !first)
         e = launch_kernel(true, kpp_shard_potentials_kernel, dim3(1), dim3(256), 0, s,
                           (const double *)(ws + L.K.off_bpot), T, L.K.n_blocks, pot_out);

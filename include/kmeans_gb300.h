@@ -393,10 +393,23 @@ int kmeans_relocate_empty(int64_t *labels, const float *best_dist, int64_t n, in
  * sum_i min(D^2_i, ||x_i - cand||^2) wins (lowest trial on ties).
  * Distances are float32 differences, squared and summed in float32 over
  * runs of at most 8 x 16 features per thread, the runs combined in
- * double-float; running sums and potentials are float64. */
+ * double-float; running sums and potentials are float64.
+ * Rows that cannot change: each round skips the samples that every trial
+ * provably leaves at their D^2 (by the triangle inequality through the
+ * sample's nearest chosen center, with a 0.1% margin on the distance), so
+ * the indices are those of the unpruned seeding while fewer rows of X are
+ * read.  The workspace holds the bookkeeping for n <= 16,777,216; beyond
+ * that every round reads every row. */
 int kmeanspp_init(const float *X, int64_t n, int64_t d, int64_t k, int n_trials,
                   uint64_t seed, float *centers, int64_t *indices,
                   void *ws, size_t ws_bytes, void *stream);
+
+/* Rows of X that the distance passes of the last kmeanspp_init (or
+ * kmeans_fit's seeding) on `ws` read, summed over its passes: n for the
+ * first center, then the rows each round could not skip, times the passes
+ * of a round (ceil(n_trials / 8)).  0 when that seeding read every row (no
+ * pruning).  Synchronises `stream` first; *rows is host memory. */
+int kmeanspp_rows_read(const void *ws, void *stream, int64_t *rows);
 
 /* A full fit: Lloyd iterations [U] until the inertia stops improving (the
  * pages fix no stopping rule; this is the plain one).  With

@@ -243,6 +243,32 @@ def test_kmeanspp_indices_match_oracle(gpu_lib, case, record_property):
     assert host(centers).tobytes() == np.ascontiguousarray(X[o_idx]).tobytes()
 
 
+@pytest.mark.parametrize("T,aligned", [(8, True), (12, True), (8, False)], ids=["T8", "T12-two-passes", "unaligned"])
+def test_kmeanspp_row_pruning_keeps_the_oracle_indices(gpu_lib, T, aligned):
+    # well-separated blobs (the planted ones: center spread 1, within 0.5),
+    # more centers than blobs: once a blob has a center its rows can no
+    # longer change and are skipped, so the passes read fewer rows than
+    # n per pass; the picks stay the oracle's.  Rows that are not 16-byte
+    # groups (X offset by one float) are never pruned.
+    n, d, k, seed = 6000, 512, 96, 77
+    X, _, _ = synth.planted_blobs(n, d, 48, seed=n + d)
+    Xd = dev_tensor(X)
+    if not aligned:
+        buf = torch.empty(n * d + 1, dtype=torch.float32, device="cuda")
+        buf[1:].copy_(Xd.reshape(-1))
+        Xd = buf[1:].view(n, d)
+    ws = gpu_lib.workspace(gpu_lib.OP_KMEANSPP, n, k, d)
+    idx, _ = gpu_lib.kmeanspp_init(Xd, k, seed, n_trials=T, ws=ws)
+    rows = gpu_lib.kmeanspp_rows_read(ws)
+    o_idx, _, _ = oracle.kmeanspp(X, k, seed, n_trials=T)
+    assert np.array_equal(host(idx), o_idx), f"first mismatch at {np.argmax(host(idx) != o_idx)}"
+    passes = k * ((T + 7) // 8)
+    if aligned:
+        assert n <= rows < 0.9 * n * passes, rows
+    else:
+        assert rows == 0
+
+
 def test_kmeanspp_identical_points(gpu_lib):
     X = np.ones((100, 8), np.float32)
     idx, _ = gpu_lib.kmeanspp_init(dev_tensor(X), 5, 3, n_trials=2)
