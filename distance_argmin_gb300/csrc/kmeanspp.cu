@@ -617,78 +617,78 @@ __global__ void __launch_bounds__(kBsThreads)
         const int q = lane + 32 * m;
         xv[m] = q < w4 ? __ldg(cj + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // eight trials at a time, their butterflies interleaved
+    constexpr int G = kKppGroupTrials;
 #pragma unroll 1
-    for (int t = 0; t < T; ++t) {
-        float acc = 0.f;
+    for (int t0 = 0; t0 < T; t0 += G) {
+        float acc[G];
+#pragma unroll
+        for (int q = 0; q < G; ++q) acc[q] = 0.f;
 #pragma unroll
         for (int m = 0; m < V / 32; ++m) {
-            const float4 y = ys[t * V + lane + 32 * m];
-            const float dx = xv[m].x - y.x, dy = xv[m].y - y.y, dz = xv[m].z - y.z, dw = xv[m].w - y.w;
-            acc = fmaf(dx, dx, acc);
-            acc = fmaf(dy, dy, acc);
-            acc = fmaf(dz, dz, acc);
-            acc = fmaf(dw, dw, acc);
+#pragma unroll
+            for (int q = 0; q < G; ++q) {
+                if (t0 + q < T) {
+                    const float4 y = ys[(t0 + q) * V + lane + 32 * m];
+                    const float dx = xv[m].x - y.x, dy = xv[m].y - y.y, dz = xv[m].z - y.z, dw = xv[m].w - y.w;
+                    acc[q] = fmaf(dx, dx, acc[q]);
+                    acc[q] = fmaf(dy, dy, acc[q]);
+                    acc[q] = fmaf(dz, dz, acc[q]);
+                    acc[q] = fmaf(dw, dw, acc[q]);
+                }
+            }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) atomicAdd(dcc + (int64_t)t * kst + j, acc);
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int q = 0; q < G; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+        if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < G; ++q)
+                if (t0 + q < T) atomicAdd(dcc + (int64_t)(t0 + q) * kst + j, acc[q]);
+        }
     }
 }
 
-// Per block of kKppScanBlock samples: flag[i] = 1 when some trial is closer
-// than 2.001 D(x) to the sample's nearest center (the pass must read the
-// row), and the flagged rows listed in ascending order at rows[block * 1024
-// ...], their number in rcount[block].  Four consecutive samples a thread,
-// every load issued before the first comparison.
-__global__ void __launch_bounds__(kBsThreads)
+// Per block of kKppScanBlock samples, one a thread: flag[i] = 1 when some
+// trial is closer than 2.001 D(x) to the sample's nearest center (the pass
+// must read the row), and the flagged rows listed in ascending order at
+// rows[block * 1024 ...], their number in rcount[block].  The table entries
+// of eight trials are loaded before any is compared.
+__global__ void __launch_bounds__(kKppScanBlock)
     kpp_select_rows_kernel(int64_t n, const int32_t *__restrict__ near, const double *__restrict__ D2,
                            const float *__restrict__ dcc, int T, int64_t kst, uint8_t *__restrict__ flag,
                            int32_t *__restrict__ rows, int32_t *__restrict__ rcount, int passes, WsHeader *hdr) {
-    static_assert(kKppScanBlock == 4 * kBsThreads, "four samples a thread");
-    __shared__ int wsum[kBsThreads / 32];
+    constexpr int WARPS = kKppScanBlock / 32;
+    constexpr int G = kKppGroupTrials;
+    __shared__ int wsum[WARPS];
     griddep_wait();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t i0 = (int64_t)blockIdx.x * kKppScanBlock + 4 * threadIdx.x;
-    double lim[4];
-    int jn[4];
+    const int64_t i = (int64_t)blockIdx.x * kKppScanBlock + threadIdx.x;
+    bool need = false;
+    if (i < n) {
+        const double lim = kKppPruneSq * D2[i];
+        const float *dj = dcc + near[i];
+        for (int t0 = 0; t0 < T; t0 += G) {
+            float v[G];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const bool in = i0 + r < n;
-        lim[r] = in ? kKppPruneSq * D2[i0 + r] : 0.0;
-        jn[r] = in ? near[i0 + r] : 0;
+            for (int q = 0; q < G; ++q) v[q] = t0 + q < T ? dj[(int64_t)(t0 + q) * kst] : __int_as_float(0x7f800000);
+#pragma unroll
+            for (int q = 0; q < G; ++q) need |= (double)v[q] < lim;
+        }
+        flag[i] = need ? 1 : 0;
     }
-    bool need[4];
-    int cnt = 0;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        need[r] = false;
-#pragma unroll
-        for (int t = 0; t < kKppMaxTrials; ++t)
-            if (t < T) need[r] |= (double)dcc[(int64_t)t * kst + jn[r]] < lim[r];
-        if (i0 + r >= n) need[r] = false;
-        else flag[i0 + r] = need[r] ? 1 : 0;
-        cnt += need[r] ? 1 : 0;
-    }
-    // exclusive prefix of the counts over the block, in thread order
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) wsum[w] = incl;
+    // ascending positions: a ballot per warp, the warps' counts before it
+    const unsigned m = __ballot_sync(0xffffffffu, need);
+    if (lane == 0) wsum[w] = __popc(m);
     __syncthreads();
     int before = 0, total = 0;
 #pragma unroll
-    for (int q = 0; q < kBsThreads / 32; ++q) {
+    for (int q = 0; q < WARPS; ++q) {
         if (q < w) before += wsum[q];
         total += wsum[q];
     }
-    int pos = before + incl - cnt;
-    int32_t *out = rows + (int64_t)blockIdx.x * kKppScanBlock;
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-        if (need[r]) out[pos++] = (int32_t)(i0 + r);
+    if (need) rows[(int64_t)blockIdx.x * kKppScanBlock + before + __popc(m & ((1u << lane) - 1u))] = (int32_t)i;
     if (threadIdx.x == 0) {
         rcount[blockIdx.x] = total;
         atomicAdd(&hdr->kpp_rows, (unsigned long long)total * (unsigned long long)passes);
@@ -812,7 +812,7 @@ cudaError_t launch_kmeanspp(const float *X, int64_t n, int64_t d, int64_t k, int
             const unsigned dblocks = (unsigned)((c + kBsThreads / 32 - 1) / (kBsThreads / 32));
             chain(launch_kernel(true, kpp_dcc_kernel, dim3(dblocks, dcc_chunks), dim3(kBsThreads), dcc_smem, s, X, (int)d,
                                 (const int64_t *)indices, c, (const int64_t *)cand, T, L.k, dcc));
-            chain(launch_kernel(true, kpp_select_rows_kernel, dim3((unsigned)L.n_blocks), dim3(kBsThreads), 0, s, n,
+            chain(launch_kernel(true, kpp_select_rows_kernel, dim3((unsigned)L.n_blocks), dim3(kKppScanBlock), 0, s, n,
                                 (const int32_t *)near, (const double *)D2, (const float *)dcc, T, L.k,
                                 ws + L.off_flag, reinterpret_cast<int32_t *>(ws + L.off_rows),
                                 reinterpret_cast<int32_t *>(ws + L.off_rcount), (T + kd::KT - 1) / kd::KT, hdr));
