@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         hdr->status = 0u;
         hdr->done_blocks = 0u;
+        hdr->round_arrivals = 0u;
     }
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int j = blockIdx.x; j < k; j += gridDim.x) {

@@ -136,6 +136,21 @@ constexpr int WIDE_MAX_D = 8192;
 // halving the split; with fewer features the epilogue's share grows, and the
 // double-buffered tiles (with their K split of a short last round) stay.
 constexpr int WIDE_MIN_D = 2048;
+// Pairs that read the same X block or centroid columns in a round share its
+// k-blocks in L2 only while they read them within about the time L2 holds
+// them; over a long launch the pairs drift apart and re-read from DRAM (35
+// to 68 GB a launch on the sample-heavy shape against 25 GB in step).  So
+// from this many rounds on, each CTA's producer waits at the start of a round
+// until the round's CTAs have all started it, for at most
+// ROUND_SYNC_WAIT_NS: a scheduling hint, never an error, so a CTA that is
+// not resident yet (another kernel on the GPU) costs at most that wait.
+// Measured back to back under the power cap: the sample-heavy shape 1.0 and
+// 1.3% faster on two boxes, centroid-heavy +0.3 and -1.0%, feature-heavy
+// +0.3% (a barrier without the time limit: -2.4% and -1.8%); with it on
+// every launch, lloyd10 (7 rounds) was 3.5% slower, hence the lower bound.
+// Longer limits (100 and 300 us) measured no better.
+constexpr int ROUND_SYNC_MIN_ROUNDS = 16;
+constexpr uint64_t ROUND_SYNC_WAIT_NS = 20000;
 constexpr int GROUP_M = 8;                     // pair sample blocks per raster band
 constexpr uint16_t PAIR_MASK = 0x3;
 static_assert(SPLIT_WARPS % 4 == 0 && WARP_EPI % 4 == 0, "epilogue warps start on a lane-quarter boundary");
@@ -205,6 +220,10 @@ struct TcParams {
     // per CTA, indexed by blockIdx.x).
     int kb_chunk;
     float *park;
+    // Soft round barrier of the wide units (null: off): every CTA's producer
+    // counts itself in when it starts a round and waits, at most
+    // ROUND_SYNC_WAIT_NS, for the round's other CTAs
+    uint32_t *rsync;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb) {
@@ -693,6 +712,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
                 tile_coords(un.tile, p.num_m, p.num_n, mb, nb);
                 const int m0 = mb * (2 * tc::BM) + (int)rank * tc::BM;
                 const int c0 = nb * UNIT_N + (int)rank * tc::BN_CTA;
+                if (WIDE && p.rsync) {
+                    // both CTAs of every pair with a unit in this round
+                    const int r = (unit - pair) / num_pairs;
+                    const uint32_t target =
+                        2u * (uint32_t)(num_pairs * r + min(num_pairs, p.num_units - r * num_pairs));
+                    atomicAdd(p.rsync, 1u);
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_acquire_gpu(p.rsync) < target && globaltimer_ns() - t0 < tc::ROUND_SYNC_WAIT_NS)
+                        __nanosleep(64);
+                }
                 for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
                     const int s = it % F::SXB;
                     if (!mbar_wait(bar(F::XB_EMPTY + s), ((it / F::SXB) & 1) ^ 1, p.status)) {
@@ -1032,6 +1061,11 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
     // K chunks of at most WIDE_MAX_D features, balanced
     p.kb_chunk = p.num_kb;
     p.park = nullptr;
+    // the soft round barrier of long wide launches (its counter is cleared
+    // by the prep kernel before each call's first launch)
+    p.rsync = nullptr;
+    if (wide && (p.num_units + pairs - 1) / pairs >= tc::ROUND_SYNC_MIN_ROUNDS)
+        p.rsync = &reinterpret_cast<WsHeader *>(ws)->round_arrivals;
     if (chunked) {
         const int max_kb = tc::WIDE_MAX_D / tc::BK;
         const int chunks = (p.num_kb + max_kb - 1) / max_kb;

@@ -96,7 +96,8 @@ struct WsHeader {
     double fit_inertia;       // kmeans_fit: the last iteration's inertia
     uint32_t fit_nempty;      // kmeans_fit: clusters left empty by the last update
     unsigned long long kpp_rows;  // k-means++ with row pruning: sample rows its distance passes read
-    uint32_t pad[56];
+    uint32_t round_arrivals;      // tensor-core assignment: CTAs that have started each round (soft barrier)
+    uint32_t pad[55];
 };
 // kmeans_fit reads the status word, the inertia and the empty count back in
 // one copy of the header's first bytes.

@@ -400,6 +400,24 @@ def test_wide_units_with_ragged_centroid_columns(gpu_lib, shape):
     assert np.array_equal(host(counts).astype(np.int64), o_cnt)
 
 
+def test_wide_units_in_step_over_many_rounds(gpu_lib):
+    # 1256 wide units over 76 CTA pairs: 17 rounds, so the producers hold
+    # each other at the round starts (a soft barrier, a last round of 40
+    # units); sampled rows against the oracle, and a second call on the same
+    # workspace gives the same bits
+    n, k, d = 40000, 4000, 2048
+    X, _, _ = synth.planted_blobs(n, d, 500, seed=95)
+    C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=96)])
+    Xd, Cd = dev_tensor(X), dev_tensor(C)
+    ws = gpu_lib.workspace(gpu_lib.OP_ASSIGN, n, k, d)
+    labels, best, inertia = gpu_lib.kmeans_assign(Xd, Cd, ws=ws)
+    rows = _sample_rows(n, 512, 97)
+    o_l, o_b, o_s, _ = oracle.assign(X[rows], C)
+    check_assign(X[rows], C, host(labels), host(best), o_l, o_b, o_s, rows=rows, what="many rounds")
+    labels2, best2, _ = gpu_lib.kmeans_assign(Xd, Cd, ws=ws)
+    assert torch.equal(labels, labels2) and torch.equal(best, best2)
+
+
 @pytest.mark.parametrize("impl,d,k", [("tc", 4096, 250), ("tc", 4100, 250), ("tc", 8192, 700), ("tc", 8196, 700),
                                      ("tf32", 2048, 700), ("tf32", 2052, 700), ("tf32", 8192, 700)])
 def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d, k, impl):
