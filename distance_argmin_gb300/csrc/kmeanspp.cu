@@ -4,14 +4,18 @@
 //
 //   update   the winner of the previous round is the trial with the lowest
 //            potential (lowest trial on ties); D^2 <- min(D^2, its distances);
-//            per-block sums of D^2 (fixed order)
+//            per-block sums of D^2 (fixed order); each sample's nearest center
 //   pick     per trial: uniform from Philox4x32-10, target = u * sum D^2,
 //            candidate = first sample whose running sum exceeds the target
-//   dist     one pass over X per 8 trials: each block keeps one feature slice
-//            of the candidates in shared memory and streams its samples once,
-//            writing per-slice partial squared distances
-//   combine  distances = slice partials added in slice order; per-block
-//            potentials sum_i min(D^2_i, dist_ti)
+//   dcc      the trials' squared distances to the chosen centers
+//   select   the rows some trial may bring below their D^2 (the others
+//            provably keep it: see the row pruning below)
+//   dist     one pass over the selected rows of X per 8 trials: each block
+//            keeps one feature slice of the candidates in shared memory and
+//            streams its samples once, writing per-slice partial squared
+//            distances
+//   combine  distances = slice partials added in slice order (+inf for rows
+//            not read); per-block potentials sum_i min(D^2_i, dist_ti)
 //
 // Distances: float32 differences, squared and summed in runs of 8 features,
 // a lane's runs added in float32, lanes and slices combined in double-float,
