@@ -38,6 +38,12 @@ cudaError_t launch_assign_tc(const float *X, int64_t n, int64_t k, int64_t d, co
                              uint8_t *ws, cudaStream_t s, bool chained = true, bool tf32 = false,
                              const FusedUpdate *fused = nullptr);
 
+// Sample rows whose wide units (bf16x3, d >= 2048, k > 256) fill whole
+// rounds of the persistent schedule: a multiple of this many rows is
+// assigned without a part-filled last round.  256 (one sample pair-block)
+// where the tiles are not wide units.
+int64_t assign_round_rows(int64_t k, int64_t d);
+
 // launch_prep_split for the 3xTF32 path: C's hi (low 13 mantissa bits
 // cleared) and lo (C - hi, low 13 bits cleared) as fp32, row pitch L.d_pad.
 cudaError_t launch_prep_split_tf32(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,

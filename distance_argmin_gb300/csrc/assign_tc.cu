@@ -947,6 +947,18 @@ static int resident_pairs() {
     });
 }
 
+int64_t assign_round_rows(int64_t k, int64_t d) {
+    if (d < tc::WIDE_MIN_D || k <= tc::BN) return 2 * tc::BM;
+    int64_t a = resident_pairs(), b = (k + 2 * tc::BN - 1) / (2 * tc::BN);  // pairs, unit columns
+    const int64_t pairs = a;
+    while (b) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return 2 * tc::BM * (pairs / a);  // pair blocks * unit columns a multiple of the pairs
+}
+
 // Ready tags of K-split tiles: one per launch, never 0 (the value the prologue
 // leaves), so a tag from an earlier launch on the same workspace never reads
 // as ready.

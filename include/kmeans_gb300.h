@@ -230,8 +230,9 @@ int kmeans_lloyd_iter_fused(const float *X, const float *C_old, float *C_new, in
  * X_host (n, d) and C_host (k, d) are host arrays, page-locked for the copies
  * to overlap; X and C_old are the device arrays they are copied into (and
  * then hold).  The samples travel in `slices` row slices (1 <= slices <=
- * KMEANS_HOST_MAX_SLICES, each a whole number of 256-sample blocks) on
- * `copy_stream`; on `stream` the centroids are copied and split once, and
+ * KMEANS_HOST_MAX_SLICES, each a whole number of 256-sample blocks; where
+ * the assignment runs wide units, of whole rounds of its schedule when that
+ * keeps at least half as many slices) on `copy_stream`; on `stream` the centroids are copied and split once, and
  * each slice's tensor-core pass starts as soon as its rows have landed, so
  * the copies and the assignment overlap.  Finalize and the mean update then
  * run on `stream` exactly as in kmeans_lloyd_iter.  With slices = 1 the
