@@ -626,12 +626,14 @@ const char *kmeans_status_string(int status) {
 }
 
 const char *kmeans_build_info(void) {
-    return "kmeans_gb300 sm_103a: assign = tcgen05 cta_group::2 CTA pairs, 256x256 tile, bf16x3 split "
-           "(one double-buffered f32 accumulator up to d = 4096, separate hi.hi and correction accumulators "
-           "above), BK 32, X/C ring 4, split ring 6, 8 split warps; comparator = FFMA 128x128; update = "
-           "counting-scatter member list (k <= 32768; LSD radix above) + compensated segmented mean; "
-           "sharded update = per-rank sums reduced in rank order; k-means++ = Philox4x32-10 greedy D^2 "
-           "(single GPU or sharded steps)";
+    return "kmeans_gb300 sm_103a: assign = tcgen05 cta_group::2 CTA pairs, bf16x3 split, BK 32, 8 split warps; "
+           "d >= 2048 with k > 256: 256x512 wide units (one f32 accumulator per 256-column tile, X/C ring 3, "
+           "split ring 5), K chunks of <= 8192 features above d = 8192, a soft barrier at each round start "
+           "from 16 rounds; otherwise 256x256 tiles (one double-buffered accumulator up to d = 4096, separate "
+           "hi.hi and correction accumulators above; X/C ring 4, split ring 6); comparator = FFMA 128x128; "
+           "update = counting-scatter member list (k <= 32768; LSD radix above) + compensated segmented mean; "
+           "sharded update = per-rank sums reduced in rank order; k-means++ = Philox4x32-10 greedy D^2 with "
+           "triangle-inequality row pruning (single GPU; sharded steps without)";
 }
 
 }  // extern "C"
