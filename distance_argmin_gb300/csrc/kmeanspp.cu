@@ -604,7 +604,15 @@ __global__ void __launch_bounds__(kBsThreads)
     const int64_t j = (int64_t)blockIdx.x * (kBsThreads / 32) + (threadIdx.x >> 5);
     const int f0 = blockIdx.y * kDccChunk;
     const int w4 = min(kDccChunk, d - f0) / 4;
-    // every candidate's chunk: one float4 each per thread, all in flight
+    // this warp's center chunk and every candidate's chunk, all in flight
+    // together (the centers come from DRAM, the candidates mostly from L2)
+    float4 xv[V / 32];
+    const float4 *cj = j < c ? reinterpret_cast<const float4 *>(X + indices[j] * (int64_t)d + f0) : nullptr;
+#pragma unroll
+    for (int m = 0; m < V / 32; ++m) {
+        const int q = lane + 32 * m;
+        xv[m] = cj && q < w4 ? __ldg(cj + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
     for (int t = 0; t < kKppMaxTrials; ++t) {
         if (t < T) {
@@ -614,13 +622,6 @@ __global__ void __launch_bounds__(kBsThreads)
     }
     __syncthreads();
     if (j >= c) return;
-    const float4 *cj = reinterpret_cast<const float4 *>(X + indices[j] * (int64_t)d + f0);
-    float4 xv[V / 32];
-#pragma unroll
-    for (int m = 0; m < V / 32; ++m) {
-        const int q = lane + 32 * m;
-        xv[m] = q < w4 ? __ldg(cj + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
     // eight trials at a time, their butterflies interleaved
     constexpr int G = kKppGroupTrials;
 #pragma unroll 1
