@@ -405,11 +405,14 @@ int kmeanspp_init(const float *X, int64_t n, int64_t d, int64_t k, int n_trials,
                   uint64_t seed, float *centers, int64_t *indices,
                   void *ws, size_t ws_bytes, void *stream);
 
-/* Rows of X that the distance passes of the last kmeanspp_init (or
- * kmeans_fit's seeding) on `ws` read, summed over its passes: n for the
- * first center, then the rows each round could not skip, times the passes
- * of a round (ceil(n_trials / 8)).  0 when that seeding read every row (no
- * pruning).  Synchronises `stream` first; *rows is host memory. */
+/* Support for measurement (the pages have no counterpart): the rows of X
+ * that the distance passes of the last kmeanspp_init (or kmeans_fit's
+ * seeding) on `ws` read, summed over its passes: n for the first center,
+ * then the rows each round could not skip, times the passes of a round
+ * (ceil(n_trials / 8)).  0 when that seeding read every row (no pruning).
+ * Synchronises `stream` first; *rows is host memory.  Returns
+ * KMEANS_ERR_INVALID_ARG for a null ws or rows, KMEANS_ERR_CUDA when the
+ * synchronisation or the copy fails. */
 int kmeanspp_rows_read(const void *ws, void *stream, int64_t *rows);
 
 /* A full fit: Lloyd iterations [U] until the inertia stops improving (the
