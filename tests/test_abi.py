@@ -46,6 +46,13 @@ def test_binding_constants_match_the_header(km):
             assert getattr(km, name) == int(value), name
 
 
+def test_kmeanspp_rows_read_rejects_null_pointers(km):
+    lib = _lib(km)
+    out = ctypes.c_int64(0)
+    assert lib.kmeanspp_rows_read(None, None, ctypes.byref(out)) == km.KMEANS_ERR_INVALID_ARG
+    assert lib.kmeanspp_rows_read(ctypes.c_void_p(0x10000), None, None) == km.KMEANS_ERR_INVALID_ARG
+
+
 def test_status_strings(km):
     for st in range(8):
         s = km.kmeans_status_string(st)
