@@ -418,6 +418,26 @@ def test_wide_units_in_step_over_many_rounds(gpu_lib):
     assert torch.equal(labels, labels2) and torch.equal(best, best2)
 
 
+def test_two_long_assignments_at_once_on_two_streams(gpu_lib):
+    # two launches of 17 rounds each on two streams: while one holds the SMs
+    # the other's CTAs are not all resident, so its round barrier runs out of
+    # its short wait; both must finish cleanly with the bits of a call alone
+    n, k, d = 40000, 4000, 2048
+    X, _, _ = synth.planted_blobs(n, d, 500, seed=98)
+    C = np.ascontiguousarray(X[synth.init_rows(n, k, seed=99)])
+    Xd, Cd = dev_tensor(X), dev_tensor(C)
+    ref = gpu_lib.kmeans_assign(Xd, Cd)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wss = [gpu_lib.workspace(gpu_lib.OP_ASSIGN, n, k, d) for _ in range(2)]
+    torch.cuda.synchronize()
+    outs = [gpu_lib.kmeans_assign(Xd, Cd, ws=wss[i], stream=streams[i]) for i in range(2)]
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert gpu_lib.kmeans_device_status(wss[i], streams[i]) == gpu_lib.KMEANS_OK
+        assert torch.equal(outs[i][0], ref[0]) and torch.equal(outs[i][1], ref[1])
+
+
 @pytest.mark.parametrize("impl,d,k", [("tc", 4096, 250), ("tc", 4100, 250), ("tc", 8192, 700), ("tc", 8196, 700),
                                      ("tf32", 2048, 700), ("tf32", 2052, 700), ("tf32", 8192, 700)])
 def test_accumulator_modes_either_side_of_their_feature_limit(gpu_lib, d, k, impl):
