@@ -257,26 +257,24 @@ static int prep_grid(int64_t k, int64_t n) {
 cudaError_t launch_prep_split(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
                               uint8_t *ws, cudaStream_t s) {
     const bool ks = L.off_ksync != 0;
-    prep_split_kernel<<<prep_grid(k, n), kPrepThreads, 0, s>>>(
-        C, (int)k, (int)d, (int)L.d_pad, reinterpret_cast<__nv_bfloat16 *>(ws + L.off_chi),
-        reinterpret_cast<__nv_bfloat16 *>(ws + L.off_clo), reinterpret_cast<float *>(ws + L.off_cnorm),
-        reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws),
-        ks ? reinterpret_cast<float *>(ws + L.off_xnorm) : nullptr,
+    return launch_kernel(
+        true, prep_split_kernel, dim3(prep_grid(k, n)), dim3(kPrepThreads), 0, s, C, (int)k, (int)d, (int)L.d_pad,
+        reinterpret_cast<__nv_bfloat16 *>(ws + L.off_chi), reinterpret_cast<__nv_bfloat16 *>(ws + L.off_clo),
+        reinterpret_cast<float *>(ws + L.off_cnorm), reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n,
+        reinterpret_cast<WsHeader *>(ws), ks ? reinterpret_cast<float *>(ws + L.off_xnorm) : nullptr,
         ks ? reinterpret_cast<uint32_t *>(ws + L.off_ksync) : nullptr, ks ? kKSplitSlots * kKSplitSyncWords : 0);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_prep_split_tf32(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,
                                    uint8_t *ws, cudaStream_t s) {
     if (L.split_elem_bytes != 4) return cudaErrorInvalidValue;
     const bool ks = L.off_ksync != 0;
-    prep_split_tf32_kernel<<<prep_grid(k, n), kPrepThreads, 0, s>>>(
-        C, (int)k, (int)d, (int)L.d_pad, reinterpret_cast<float *>(ws + L.off_chi),
-        reinterpret_cast<float *>(ws + L.off_clo), reinterpret_cast<float *>(ws + L.off_cnorm),
-        reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n, reinterpret_cast<WsHeader *>(ws),
-        ks ? reinterpret_cast<float *>(ws + L.off_xnorm) : nullptr,
+    return launch_kernel(
+        true, prep_split_tf32_kernel, dim3(prep_grid(k, n)), dim3(kPrepThreads), 0, s, C, (int)k, (int)d,
+        (int)L.d_pad, reinterpret_cast<float *>(ws + L.off_chi), reinterpret_cast<float *>(ws + L.off_clo),
+        reinterpret_cast<float *>(ws + L.off_cnorm), reinterpret_cast<unsigned long long *>(ws + L.off_keys), (int)n,
+        reinterpret_cast<WsHeader *>(ws), ks ? reinterpret_cast<float *>(ws + L.off_xnorm) : nullptr,
         ks ? reinterpret_cast<uint32_t *>(ws + L.off_ksync) : nullptr, ks ? kKSplitSlots * kKSplitSyncWords : 0);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_prep_norms(const float *C, int64_t n, int64_t k, int64_t d, const AssignLayout &L,

@@ -47,6 +47,7 @@ __device__ __forceinline__ uint32_t clamp_label(int64_t lab, int k, uint32_t *st
 
 // counts[] = 0 (and header cleared when this call owns it)
 __global__ void update_clear_kernel(int32_t *counts, int k, WsHeader *hdr, int clear_header) {
+    griddep_wait();
     if (clear_header && blockIdx.x == 0 && threadIdx.x == 0) {
         hdr->status = 0u;
         hdr->done_blocks = 0u;
@@ -817,9 +818,8 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
         const size_t csmem = (size_t)k * 4;
         set_counting_smem_limits(k);
         cudaError_t e = cudaSuccess;
-        // the first kernel of a standalone update starts the ordinary way
         if (!tile_counts_ready)
-            e = launch_kernel(!clear_header, upd_tile_count_kernel, dim3(ut), dim3(256), csmem, s, labels, (int)n,
+            e = launch_kernel(true, upd_tile_count_kernel, dim3(ut), dim3(256), csmem, s, labels, (int)n,
                               (int)k, (int)L.utile, table, status, hdr, clear_header ? 1 : 0);
         if (e == cudaSuccess)
             e = launch_kernel(true, upd_col_prefix_kernel, dim3((unsigned)((k + kPrefixCols - 1) / kPrefixCols)),
@@ -842,8 +842,10 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
         return e;
     }
 
-    update_clear_kernel<<<(int)((k + 255) / 256 < 1024 ? (k + 255) / 256 : 1024), 256, 0, s>>>(
-        counts, (int)k, hdr, clear_header ? 1 : 0);
+    const unsigned clear_grid = (unsigned)((k + 255) / 256 < 1024 ? (k + 255) / 256 : 1024);
+    cudaError_t ce = launch_kernel(true, update_clear_kernel, dim3(clear_grid), dim3(256), 0, s, counts, (int)k, hdr,
+                                   clear_header ? 1 : 0);
+    if (ce != cudaSuccess) return ce;
     const int passes = radix_passes(k);
     uint32_t *kin = nullptr, *kout = ka;
     int32_t *vin = nullptr, *vout = va;
