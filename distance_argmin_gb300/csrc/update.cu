@@ -287,14 +287,11 @@ __global__ void __launch_bounds__(kFinCountThreads)
 // Per cluster: table[t][j] <- members of j in tiles before t; totals[j].
 // One block covers kPrefixCols clusters; thread t holds tile t (the tile
 // count equals the block size) and the tiles are scanned across the block.
-// The last block to finish turns the totals into the exclusive offsets
-// (k + 1 entries, the member total last).
+// The exclusive offsets over the clusters are left to the scatter.
 constexpr int kPrefixCols = 8;
 __global__ void __launch_bounds__(kCountingTiles)
-    upd_col_prefix_kernel(int32_t *__restrict__ table, int k, int32_t *__restrict__ totals,
-                          int32_t *__restrict__ offsets, WsHeader *hdr) {
+    upd_col_prefix_kernel(int32_t *__restrict__ table, int k, int32_t *__restrict__ totals) {
     __shared__ int32_t wsum[kCountingTiles / 32][kPrefixCols];
-    __shared__ int is_last;
     griddep_wait();
     const int t = threadIdx.x;
     const int lane = t & 31, wid = t >> 5;
@@ -328,22 +325,39 @@ __global__ void __launch_bounds__(kCountingTiles)
             if (t == kCountingTiles - 1) totals[j0 + u] = total;
         }
     }
-    __threadfence();
-    __syncthreads();
-    if (t == 0) is_last = atomicAdd(&hdr->done_blocks, 1u) == gridDim.x - 1u;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    // exclusive scan of totals[0..k) in rounds of kCountingTiles x 8 values,
-    // thread t holding 8 consecutive ones; `carry` is the sum of the rounds
-    // before
-    __shared__ int32_t carry;
-    if (t == 0) carry = 0;
-    for (int base = 0; base < k; base += kCountingTiles * 8) {
-        const int j = base + t * 8;
-        int32_t q[8];
+}
+
+// Every block first scans the cluster totals (the exclusive offsets, which
+// block 0 also writes out, k + 1 entries with the member total last) and adds
+// its tile's column prefixes: the cursor of each cluster, in shared memory.
+// One warp then walks the tile in index order, 32 samples at a time, the
+// cursors giving the member-list positions; the whole block stages the tile's
+// labels in shared memory first.
+constexpr int kMaxCountingTile = 2048;  // samples per tile staged at once
+constexpr int kScatterThreads = 256;
+
+__global__ void __launch_bounds__(kScatterThreads)
+    upd_tile_scatter_kernel(const int64_t *__restrict__ labels, int n, int k, int tile,
+                            const int32_t *__restrict__ table, const int32_t *__restrict__ totals,
+                            int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+                            uint32_t *__restrict__ sorted_labels, uint32_t *status) {
+    extern __shared__ int32_t cur[];
+    __shared__ uint32_t lab_s[kMaxCountingTile];
+    __shared__ int32_t wsum[kScatterThreads / 32];
+    griddep_wait();
+    const int32_t *row = table + (size_t)blockIdx.x * k;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    // rounds of kScatterThreads x 8 clusters, thread t holding 8 consecutive
+    // ones; `carry` is the member total of the rounds before
+    int32_t carry = 0;
+    for (int base = 0; base < k; base += kScatterThreads * 8) {
+        const int j = base + threadIdx.x * 8;
+        int32_t q[8], r[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[e] = j + e < k ? __ldcg(totals + j + e) : 0;
+        for (int e = 0; e < 8; ++e) {
+            q[e] = j + e < k ? totals[j + e] : 0;
+            r[e] = j + e < k ? row[j + e] : 0;
+        }
         int32_t run = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) run += q[e];
@@ -353,47 +367,27 @@ __global__ void __launch_bounds__(kCountingTiles)
             const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
             if (lane >= o) x += y;
         }
-        __syncthreads();  // carry and wsum of the previous round are read
-        if (lane == 31) wsum[wid][0] = x;
+        if (lane == 31) wsum[wid] = x;
         __syncthreads();
-        int32_t before = carry + x - run;
-        int32_t round_total = 0;
+        int32_t before = carry + x - run, round_total = 0;
 #pragma unroll
-        for (int w = 0; w < kCountingTiles / 32; ++w) {
-            const int32_t ws = wsum[w][0];
+        for (int w = 0; w < kScatterThreads / 32; ++w) {
+            const int32_t ws = wsum[w];
             if (w < wid) before += ws;
             round_total += ws;
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            if (j + e < k) offsets[j + e] = before;
+            if (j + e < k) {
+                if (blockIdx.x == 0) offsets[j + e] = before;
+                cur[j + e] = before + r[e];
+            }
             before += q[e];
         }
-        __syncthreads();
-        if (t == 0) carry += round_total;
+        carry += round_total;
+        __syncthreads();  // wsum is rewritten by the next round
     }
-    __syncthreads();
-    if (t == 0) {
-        offsets[k] = carry;
-        hdr->done_blocks = 0u;
-    }
-}
-
-// One warp walks its tile in index order, 32 samples at a time; the cursor of
-// each cluster (in shared memory) gives the member-list position.  The whole
-// block first stages the tile's labels in shared memory.
-constexpr int kMaxCountingTile = 2048;  // samples per tile staged at once
-
-__global__ void __launch_bounds__(256)
-    upd_tile_scatter_kernel(const int64_t *__restrict__ labels, int n, int k, int tile,
-                            const int32_t *__restrict__ table, const int32_t *__restrict__ offsets,
-                            int32_t *__restrict__ perm, uint32_t *__restrict__ sorted_labels, uint32_t *status) {
-    extern __shared__ int32_t cur[];
-    __shared__ uint32_t lab_s[kMaxCountingTile];
-    griddep_wait();
-    const int32_t *row = table + (size_t)blockIdx.x * k;
-    for (int j = threadIdx.x; j < k; j += blockDim.x) cur[j] = offsets[j] + row[j];
-    const int lane = threadIdx.x & 31;
+    if (blockIdx.x == 0 && threadIdx.x == 0) offsets[k] = carry;
     const int i0 = blockIdx.x * tile;
     const int i1 = min(n, i0 + tile);
     for (int c0 = i0; c0 < i1; c0 += kMaxCountingTile) {
@@ -823,10 +817,11 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
                               (int)k, (int)L.utile, table, status, hdr, clear_header ? 1 : 0);
         if (e == cudaSuccess)
             e = launch_kernel(true, upd_col_prefix_kernel, dim3((unsigned)((k + kPrefixCols - 1) / kPrefixCols)),
-                              dim3(kCountingTiles), 0, s, table, (int)k, counts, offsets, hdr);
+                              dim3(kCountingTiles), 0, s, table, (int)k, counts);
         if (e == cudaSuccess)
-            e = launch_kernel(true, upd_tile_scatter_kernel, dim3(ut), dim3(256), csmem, s, labels, (int)n, (int)k,
-                              (int)L.utile, (const int32_t *)table, (const int32_t *)offsets, perm, slab, status);
+            e = launch_kernel(true, upd_tile_scatter_kernel, dim3(ut), dim3(kScatterThreads), csmem, s, labels,
+                              (int)n, (int)k, (int)L.utile, (const int32_t *)table, (const int32_t *)counts, offsets,
+                              perm, slab, status);
         trace_mark(kTraceUpdateMean, false, s);
         if (e == cudaSuccess)
             e = launch_kernel(true, mean_k, mgrid, dim3(kMeanThreads), msmem, s, X, (const int32_t *)perm,
