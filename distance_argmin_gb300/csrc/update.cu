@@ -332,7 +332,10 @@ __global__ void __launch_bounds__(kCountingTiles)
 // its tile's column prefixes: the cursor of each cluster, in shared memory.
 // One warp then walks the tile in index order, 32 samples at a time, the
 // cursors giving the member-list positions; the whole block stages the tile's
-// labels in shared memory first.
+// labels in shared memory first (the first round's labels are requested
+// before the scan).  Meanwhile the other warps write the counts of the block's
+// share of the clusters (j = block + i x blocks) and the rows of its empty
+// clusters: the old row, or zeros with `mean` 0 (sums mode).
 constexpr int kMaxCountingTile = 2048;  // samples per tile staged at once
 constexpr int kScatterThreads = 256;
 
@@ -340,13 +343,23 @@ __global__ void __launch_bounds__(kScatterThreads)
     upd_tile_scatter_kernel(const int64_t *__restrict__ labels, int n, int k, int tile,
                             const int32_t *__restrict__ table, const int32_t *__restrict__ totals,
                             int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
-                            uint32_t *__restrict__ sorted_labels, uint32_t *status) {
+                            uint32_t *__restrict__ sorted_labels, uint32_t *status, const float *__restrict__ C_old,
+                            float *__restrict__ C_new, int32_t *__restrict__ counts_out, int d, int mean) {
+    constexpr int kPre = kMaxCountingTile / kScatterThreads;
     extern __shared__ int32_t cur[];
     __shared__ uint32_t lab_s[kMaxCountingTile];
     __shared__ int32_t wsum[kScatterThreads / 32];
     griddep_wait();
     const int32_t *row = table + (size_t)blockIdx.x * k;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int i0 = blockIdx.x * tile;
+    const int i1 = min(n, i0 + tile);
+    int64_t pre[kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const int i = i0 + threadIdx.x + u * kScatterThreads;
+        pre[u] = i < min(i1, i0 + kMaxCountingTile) ? labels[i] : 0;
+    }
     // rounds of kScatterThreads x 8 clusters, thread t holding 8 consecutive
     // ones; `carry` is the member total of the rounds before
     int32_t carry = 0;
@@ -388,12 +401,18 @@ __global__ void __launch_bounds__(kScatterThreads)
         __syncthreads();  // wsum is rewritten by the next round
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) offsets[k] = carry;
-    const int i0 = blockIdx.x * tile;
-    const int i1 = min(n, i0 + tile);
     for (int c0 = i0; c0 < i1; c0 += kMaxCountingTile) {
         const int c1 = min(i1, c0 + kMaxCountingTile);
         __syncthreads();
-        for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) lab_s[i - c0] = clamp_label(labels[i], k, status);
+        if (c0 == i0) {
+#pragma unroll
+            for (int u = 0; u < kPre; ++u) {
+                const int i = c0 + threadIdx.x + u * kScatterThreads;
+                if (i < c1) lab_s[i - c0] = clamp_label(pre[u], k, status);
+            }
+        } else {
+            for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) lab_s[i - c0] = clamp_label(labels[i], k, status);
+        }
         __syncthreads();
         if (threadIdx.x < 32) {
             for (int b = c0; b < c1; b += 32) {
@@ -412,6 +431,26 @@ __global__ void __launch_bounds__(kScatterThreads)
                     sorted_labels[pos] = lab;
                 }
             }
+        }
+    }
+    if (wid == 0) return;
+    for (int sh = (wid - 1) * 32 + lane;; sh += (kScatterThreads / 32 - 1) * 32) {
+        const int64_t jl = blockIdx.x + (int64_t)sh * gridDim.x;
+        const bool has = jl < k;
+        if (!__any_sync(0xffffffffu, has)) break;
+        const int j = has ? (int)jl : 0;
+        int32_t cnt = 1;
+        if (has) {
+            cnt = totals[j];
+            if (counts_out) counts_out[j] = cnt;
+        }
+        for (uint32_t empty = __ballot_sync(0xffffffffu, has && cnt == 0); empty; empty &= empty - 1u) {
+            const int je = __shfl_sync(0xffffffffu, j, __ffs(empty) - 1);
+            float *dst = C_new + (size_t)je * d;
+            if (!mean)
+                for (int f = lane; f < d; f += 32) dst[f] = 0.f;
+            else if (C_new != C_old)
+                for (int f = lane; f < d; f += 32) dst[f] = C_old[(size_t)je * d + f];
         }
     }
 }
@@ -570,18 +609,17 @@ __global__ void __launch_bounds__(kMeanThreads)
 
 // Fix-up of the counting path: block c finishes the cluster that leaves
 // chunk c (its tail partial plus the head partials of the chunks it covers, in
-// chunk order); every block then copies the old row of empty clusters in its
-// stride and writes the counts.  A thread keeps kFixUnroll column groups (four
-// columns each when VEC) in flight at once.
+// chunk order).  A thread keeps kFixUnroll column groups (four columns each
+// when VEC) in flight at once.  (The counts and the empty clusters' rows are
+// written by the scatter.)
 constexpr int kFixThreads = 256;
 constexpr int kFixUnroll = 4;
 
 template <bool VEC, bool MEAN>
 __global__ void __launch_bounds__(kFixThreads)
-    mean_fixup_chunks_kernel(const int32_t *__restrict__ offsets, const int32_t *__restrict__ totals,
-                             const float *__restrict__ head, const float *__restrict__ tail,
-                             const int32_t *__restrict__ tailc, int n_chunks, const float *__restrict__ C_old,
-                             float *__restrict__ C_new, int32_t *__restrict__ counts_out, int k, int d, int chunk) {
+    mean_fixup_chunks_kernel(const int32_t *__restrict__ offsets, const float *__restrict__ head,
+                             const float *__restrict__ tail, const int32_t *__restrict__ tailc, int n_chunks,
+                             float *__restrict__ C_new, int d, int chunk) {
     using V = typename std::conditional<VEC, float4, float>::type;
     griddep_wait();
     constexpr int W = VEC ? 4 : 1;
@@ -640,14 +678,6 @@ __global__ void __launch_bounds__(kFixThreads)
                 out[g] = r;
             }
         }
-    }
-    for (int j = blockIdx.x; j < k; j += gridDim.x) {
-        const int cnt = totals[j];
-        if (counts_out && threadIdx.x == 0) counts_out[j] = cnt;
-        if (cnt == 0 && !MEAN)
-            for (int f = threadIdx.x; f < d; f += kFixThreads) C_new[(size_t)j * d + f] = 0.f;
-        else if (cnt == 0 && C_new != C_old)
-            for (int f = threadIdx.x; f < d; f += kFixThreads) C_new[(size_t)j * d + f] = C_old[(size_t)j * d + f];
     }
 }
 
@@ -821,19 +851,17 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
         if (e == cudaSuccess)
             e = launch_kernel(true, upd_tile_scatter_kernel, dim3(ut), dim3(kScatterThreads), csmem, s, labels,
                               (int)n, (int)k, (int)L.utile, (const int32_t *)table, (const int32_t *)counts, offsets,
-                              perm, slab, status);
+                              perm, slab, status, C_old, C_new, counts_out, (int)d, mean ? 1 : 0);
         trace_mark(kTraceUpdateMean, false, s);
         if (e == cudaSuccess)
             e = launch_kernel(true, mean_k, mgrid, dim3(kMeanThreads), msmem, s, X, (const int32_t *)perm,
                               (const uint32_t *)slab, (const int32_t *)offsets, (int)n, (int)d, (int)L.chunk, C_new,
                               head, tail, tailc);
         trace_mark(kTraceUpdateMean, true, s);
-        const int fgrid = (int)(L.n_chunks > 256 ? L.n_chunks : 256);
         if (e == cudaSuccess)
-            e = launch_kernel(true, fix_k, dim3(fgrid), dim3(kFixThreads), 0, s, (const int32_t *)offsets,
-                              (const int32_t *)counts, (const float *)head, (const float *)tail,
-                              (const int32_t *)tailc, (int)L.n_chunks, C_old, C_new, counts_out, (int)k, (int)d,
-                              (int)L.chunk);
+            e = launch_kernel(true, fix_k, dim3((unsigned)L.n_chunks), dim3(kFixThreads), 0, s,
+                              (const int32_t *)offsets, (const float *)head, (const float *)tail,
+                              (const int32_t *)tailc, (int)L.n_chunks, C_new, (int)d, (int)L.chunk);
         return e;
     }
 
