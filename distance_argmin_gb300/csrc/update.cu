@@ -6,10 +6,11 @@
 // The member list, for k <= 32768 (the counting path):
 //   1. per-cluster member counts of 256 fixed sample tiles (in a Lloyd
 //      iteration the finalize of the assignment does this)
-//   2. per-cluster prefixes over the tiles and the exclusive scan of the
-//      totals -> segment offsets
-//   3. one warp per tile scatters its samples in index order -> a stable
-//      member list ordered by (label, sample index)
+//   2. per-cluster prefixes over the tiles, and the totals
+//   3. each tile's block scans the totals (-> segment offsets), then one warp
+//      scatters the tile's samples in index order -> a stable member list
+//      ordered by (label, sample index); the other warps write the counts
+//      and the rows of empty clusters
 // For larger k: a stable LSD radix sort of (label, sample index) with 8-bit
 // digits (ceil(bits(k-1) / 8) passes: hist -> scan -> stable scatter), then
 // the exclusive scan of the counts.
@@ -18,12 +19,13 @@
 //      chunk x one 512-column slice, sums each segment in member order with
 //      compensated float32 additions and writes the mean when the segment is
 //      inside its chunk, or a partial sum when it crosses the chunk boundary
-//   5. fix-up: segments that crossed chunks add their partials in chunk order;
-//      empty clusters keep their old row bit for bit
+//   5. fix-up: segments that crossed chunks add their partials in chunk order
+// An empty cluster keeps its old row bit for bit (written by step 3 on the
+// counting path, by step 5 on the radix path).
 // Every step has a fixed order, so C_new is bitwise reproducible.
 //
 // The same kernels also serve a shard of the samples (the sample-sharded
-// iteration): in sums mode steps 4 and 5 write each cluster's unnormalised
+// iteration): in sums mode the steps write each cluster's unnormalised
 // sum, and zeros for an empty cluster, and reduce_partials_kernel later adds
 // the shards' sums in rank order and divides.
 #include <cuda_runtime.h>
