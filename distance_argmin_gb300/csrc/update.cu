@@ -340,6 +340,9 @@ __global__ void __launch_bounds__(kCountingTiles)
 // clusters: the old row, or zeros with `mean` 0 (sums mode).
 constexpr int kMaxCountingTile = 2048;  // samples per tile staged at once
 constexpr int kScatterThreads = 256;
+constexpr int kEmptyThreads = kScatterThreads - 32;
+constexpr int kEmptyList = (int)((kCountingMaxK + kCountingTiles - 1) / kCountingTiles);  // clusters a block owns
+constexpr int kEmptyUnroll = 8;
 
 __global__ void __launch_bounds__(kScatterThreads)
     upd_tile_scatter_kernel(const int64_t *__restrict__ labels, int n, int k, int tile,
@@ -351,6 +354,8 @@ __global__ void __launch_bounds__(kScatterThreads)
     extern __shared__ int32_t cur[];
     __shared__ uint32_t lab_s[kMaxCountingTile];
     __shared__ int32_t wsum[kScatterThreads / 32];
+    __shared__ int32_t empty_s[kEmptyList];
+    __shared__ int n_empty;
     griddep_wait();
     const int32_t *row = table + (size_t)blockIdx.x * k;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -436,23 +441,42 @@ __global__ void __launch_bounds__(kScatterThreads)
         }
     }
     if (wid == 0) return;
-    for (int sh = (wid - 1) * 32 + lane;; sh += (kScatterThreads / 32 - 1) * 32) {
-        const int64_t jl = blockIdx.x + (int64_t)sh * gridDim.x;
-        const bool has = jl < k;
-        if (!__any_sync(0xffffffffu, has)) break;
-        const int j = has ? (int)jl : 0;
-        int32_t cnt = 1;
-        if (has) {
-            cnt = totals[j];
-            if (counts_out) counts_out[j] = cnt;
+    // warps 1.. (kEmptyThreads threads) meet on named barrier 1; warp 0 is
+    // still walking
+    const int te = threadIdx.x - 32;
+    if (te == 0) n_empty = 0;
+    asm volatile("bar.sync 1, %0;" ::"n"(kEmptyThreads) : "memory");
+    for (int64_t jl = blockIdx.x + (int64_t)te * gridDim.x; jl < k; jl += (int64_t)kEmptyThreads * gridDim.x) {
+        const int j = (int)jl;
+        const int32_t cnt = totals[j];
+        if (counts_out) counts_out[j] = cnt;
+        if (cnt == 0) {
+            const int slot = atomicAdd(&n_empty, 1);
+            if (slot < kEmptyList) {
+                empty_s[slot] = j;
+            } else {  // not reached with k <= kCountingMaxK over kCountingTiles blocks
+                for (int f = 0; f < d; ++f) C_new[(size_t)j * d + f] = mean ? C_old[(size_t)j * d + f] : 0.f;
+            }
         }
-        for (uint32_t empty = __ballot_sync(0xffffffffu, has && cnt == 0); empty; empty &= empty - 1u) {
-            const int je = __shfl_sync(0xffffffffu, j, __ffs(empty) - 1);
-            float *dst = C_new + (size_t)je * d;
-            if (!mean)
-                for (int f = lane; f < d; f += 32) dst[f] = 0.f;
-            else if (C_new != C_old)
-                for (int f = lane; f < d; f += 32) dst[f] = C_old[(size_t)je * d + f];
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kEmptyThreads) : "memory");
+    const int ne = min(n_empty, kEmptyList);
+    if (ne == 0 || (mean && C_new == C_old)) return;
+    // the listed rows as one flat range of ne x d floats, kEmptyUnroll loads
+    // in flight per thread
+    const int64_t total = (int64_t)ne * d;
+    for (int64_t g0 = te; g0 < total; g0 += (int64_t)kEmptyThreads * kEmptyUnroll) {
+        float v[kEmptyUnroll];
+#pragma unroll
+        for (int u = 0; u < kEmptyUnroll; ++u) {
+            const int64_t g = g0 + (int64_t)u * kEmptyThreads;
+            v[u] = 0.f;
+            if (mean && g < total) v[u] = C_old[(size_t)empty_s[g / d] * d + g % d];
+        }
+#pragma unroll
+        for (int u = 0; u < kEmptyUnroll; ++u) {
+            const int64_t g = g0 + (int64_t)u * kEmptyThreads;
+            if (g < total) C_new[(size_t)empty_s[g / d] * d + g % d] = v[u];
         }
     }
 }
