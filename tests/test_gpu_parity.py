@@ -141,6 +141,25 @@ def test_update_one_cluster_across_many_small_chunks(gpu_lib):
     check_centroids(host(C_new), o_C, what="one cluster over many chunks")
 
 
+@pytest.mark.parametrize("shape", [(1, 1, 4), (5, 3, 8), (100, 7, 9), (255, 40, 516)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_update_fewer_samples_than_count_tiles(gpu_lib, shape):
+    # n below the 256 counting tiles: some tiles hold no sample, and their
+    # blocks only scan the totals and write their share of the counts and
+    # empty rows; the last cluster is left empty
+    n, k, d = shape
+    X = synth.gaussian((n, d), seed=n + 11, scale=1.5)
+    C_old = synth.gaussian((k, d), seed=k + 12)
+    labels = (np.arange(n) % max(1, k - 1)).astype(np.int64)
+    C_new, counts = gpu_lib.kmeans_update(dev_tensor(X), dev_tensor(labels), dev_tensor(C_old))
+    o_C, o_cnt = oracle.update(X, labels, C_old)
+    assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+    got = host(C_new)
+    check_centroids(got, o_C, what=str(shape))
+    empty = o_cnt == 0
+    assert got[empty].tobytes() == C_old[empty].tobytes()
+
+
 def test_update_in_place(gpu_lib):
     n, k, d = 3000, 50, 64
     X = synth.gaussian((n, d), seed=8)
