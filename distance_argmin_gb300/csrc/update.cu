@@ -359,6 +359,12 @@ __global__ void __launch_bounds__(kScatterThreads)
     griddep_wait();
     const int32_t *row = table + (size_t)blockIdx.x * k;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    // warps 1.. take the block's share of the clusters for the counts and
+    // empty rows, one each (a block owns at most kEmptyList <= kEmptyThreads
+    // of them); their counts are requested now and used after the scan
+    const int te = threadIdx.x - 32;
+    const int64_t jl0 = blockIdx.x + (int64_t)(te < 0 ? 0 : te) * gridDim.x;
+    const int32_t cnt0 = (te >= 0 && jl0 < k) ? totals[jl0] : -1;
     const int i0 = blockIdx.x * tile;
     const int i1 = min(n, i0 + tile);
     int64_t pre[kPre];
@@ -443,12 +449,11 @@ __global__ void __launch_bounds__(kScatterThreads)
     if (wid == 0) return;
     // warps 1.. (kEmptyThreads threads) meet on named barrier 1; warp 0 is
     // still walking
-    const int te = threadIdx.x - 32;
     if (te == 0) n_empty = 0;
     asm volatile("bar.sync 1, %0;" ::"n"(kEmptyThreads) : "memory");
-    for (int64_t jl = blockIdx.x + (int64_t)te * gridDim.x; jl < k; jl += (int64_t)kEmptyThreads * gridDim.x) {
+    for (int64_t jl = jl0; jl < k; jl += (int64_t)kEmptyThreads * gridDim.x) {
         const int j = (int)jl;
-        const int32_t cnt = totals[j];
+        const int32_t cnt = jl == jl0 ? cnt0 : totals[j];
         if (counts_out) counts_out[j] = cnt;
         if (cnt == 0) {
             const int slot = atomicAdd(&n_empty, 1);
@@ -462,8 +467,29 @@ __global__ void __launch_bounds__(kScatterThreads)
     asm volatile("bar.sync 1, %0;" ::"n"(kEmptyThreads) : "memory");
     const int ne = min(n_empty, kEmptyList);
     if (ne == 0 || (mean && C_new == C_old)) return;
-    // the listed rows as one flat range of ne x d floats, kEmptyUnroll loads
-    // in flight per thread
+    // the listed rows as one flat range of ne x d floats (four at a time
+    // where rows are whole aligned float4s), kEmptyUnroll loads in flight per
+    // thread
+    if ((d & 3) == 0 && ((reinterpret_cast<uintptr_t>(C_new) | reinterpret_cast<uintptr_t>(C_old)) & 15) == 0) {
+        const int d4 = d >> 2;
+        const int64_t total4 = (int64_t)ne * d4;
+        for (int64_t g0 = te; g0 < total4; g0 += (int64_t)kEmptyThreads * kEmptyUnroll) {
+            float4 v[kEmptyUnroll];
+#pragma unroll
+            for (int u = 0; u < kEmptyUnroll; ++u) {
+                const int64_t g = g0 + (int64_t)u * kEmptyThreads;
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (mean && g < total4)
+                    v[u] = reinterpret_cast<const float4 *>(C_old + (size_t)empty_s[g / d4] * d)[g % d4];
+            }
+#pragma unroll
+            for (int u = 0; u < kEmptyUnroll; ++u) {
+                const int64_t g = g0 + (int64_t)u * kEmptyThreads;
+                if (g < total4) reinterpret_cast<float4 *>(C_new + (size_t)empty_s[g / d4] * d)[g % d4] = v[u];
+            }
+        }
+        return;
+    }
     const int64_t total = (int64_t)ne * d;
     for (int64_t g0 = te; g0 < total; g0 += (int64_t)kEmptyThreads * kEmptyUnroll) {
         float v[kEmptyUnroll];
