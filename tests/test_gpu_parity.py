@@ -671,3 +671,48 @@ def test_lloyd_iteration_from_host_buffers_rejects_bad_arguments(gpu_lib):
     assert lib.kmeans_lloyd_iter_host(*args(gpu_lib.HOST_MAX_SLICES + 1, None)) == gpu_lib.KMEANS_ERR_INVALID_ARG
     assert lib.kmeans_lloyd_iter_host(*args(4, s)) == gpu_lib.KMEANS_ERR_INVALID_ARG  # copy stream == stream
     assert lib.kmeans_lloyd_iter_host(*args(4, None, 4)) == gpu_lib.KMEANS_ERR_INVALID_ARG  # unknown flag
+
+
+def test_first_kernel_waits_for_the_callers_kernel(gpu_lib):
+    # Each call's first kernel is launched so that it may be scheduled while
+    # the kernel before it on the stream drains.  Here that kernel is the
+    # caller's own (a torch multiply writing X and C, then the labels, right
+    # before the call, with no synchronisation): the library must read what
+    # it wrote, not the zeros underneath.
+    n, k, d = 65536, 256, 512
+    X = synth.gaussian((n, d), seed=71)
+    Xs = dev_tensor(X)
+    Cs = dev_tensor(X[:: n // k][:k])
+    ref_lab, ref_best, ref_in = gpu_lib.kmeans_assign(Xs, Cs)
+    ref_C, ref_cnt = gpu_lib.kmeans_update(Xs, ref_lab, Cs)
+    ref_l = gpu_lib.kmeans_lloyd_iter(Xs, Cs)
+    torch.cuda.synchronize()
+    Xd, Cd = torch.empty_like(Xs), torch.empty_like(Cs)
+    lab, best, inertia = torch.empty_like(ref_lab), torch.empty_like(ref_best), torch.empty_like(ref_in)
+    labd = torch.empty_like(ref_lab)
+    C_new, counts = torch.empty_like(Cs), torch.empty_like(ref_cnt)
+    ws_a = gpu_lib.workspace(gpu_lib.OP_ASSIGN, n, k, d)
+    ws_u = gpu_lib.workspace(gpu_lib.OP_UPDATE, n, k, d)
+    ws_l = gpu_lib.workspace(gpu_lib.OP_LLOYD, n, k, d)
+    for _ in range(3):
+        Xd.zero_()
+        Cd.zero_()
+        labd.zero_()
+        torch.cuda.synchronize()
+        torch.mul(Xs, 1.0, out=Xd)
+        torch.mul(Cs, 1.0, out=Cd)
+        gpu_lib.kmeans_assign(Xd, Cd, lab, best, inertia, ws=ws_a)
+        torch.mul(ref_lab, 1, out=labd)
+        gpu_lib.kmeans_update(Xd, labd, Cd, C_new, counts, ws=ws_u)
+        torch.cuda.synchronize()
+        assert torch.equal(lab, ref_lab) and torch.equal(best, ref_best) and torch.equal(inertia, ref_in)
+        assert torch.equal(C_new, ref_C) and torch.equal(counts, ref_cnt)
+        Xd.zero_()
+        Cd.zero_()
+        torch.cuda.synchronize()
+        torch.mul(Xs, 1.0, out=Xd)
+        torch.mul(Cs, 1.0, out=Cd)
+        got = gpu_lib.kmeans_lloyd_iter(Xd, Cd, ws=ws_l)
+        torch.cuda.synchronize()
+        for a, b in zip(got, ref_l):
+            assert torch.equal(a, b)
