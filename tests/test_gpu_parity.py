@@ -160,6 +160,26 @@ def test_update_fewer_samples_than_count_tiles(gpu_lib, shape):
     assert got[empty].tobytes() == C_old[empty].tobytes()
 
 
+def test_update_counting_limit_with_one_block_all_empty(gpu_lib):
+    # k = 32768, the largest count table: 256 scatter blocks own 128 clusters
+    # each (cluster j belongs to block j mod 256).  No label is a multiple of
+    # 256, so every cluster block 0 owns is empty: its list of empty rows is
+    # full.
+    n, k, d = 40000, 32768, 8
+    X = synth.gaussian((n, d), seed=21, scale=1.5)
+    C_old = synth.gaussian((k, d), seed=22)
+    labels = np.random.default_rng(23).integers(0, k, size=n).astype(np.int64)
+    labels[labels % 256 == 0] += 1
+    C_new, counts = gpu_lib.kmeans_update(dev_tensor(X), dev_tensor(labels), dev_tensor(C_old))
+    o_C, o_cnt = oracle.update(X, labels, C_old)
+    assert np.array_equal(host(counts).astype(np.int64), o_cnt)
+    got = host(C_new)
+    check_centroids(got, o_C, what="k = 32768")
+    empty = o_cnt == 0
+    assert empty[::256].all()
+    assert got[empty].tobytes() == C_old[empty].tobytes()
+
+
 def test_update_in_place(gpu_lib):
     n, k, d = 3000, 50, 64
     X = synth.gaussian((n, d), seed=8)
