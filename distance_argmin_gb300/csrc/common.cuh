@@ -247,7 +247,7 @@ struct UpdateLayout {
     int64_t off_vals_b;  // n x i32 (pong)
     int64_t off_head;    // n_chunks x d f32 partial sums, cluster entering a chunk
     int64_t off_tail;    // n_chunks x d f32 partial sums, cluster leaving a chunk
-    int64_t off_tailc;   // n_chunks x i32 cluster that leaves each chunk (-1: none)
+    int64_t off_tailc;   // n_chunks x int4 {cluster leaving the chunk (-1: none), its segment's bounds}
     int64_t n_utiles;    // tiles of the counting scatter (a constant cap, not n-proportional)
     int64_t utile;       // samples per counting tile
     int64_t off_table;   // n_utiles x k x i32 per-tile cluster counts, then column prefixes
@@ -289,7 +289,7 @@ inline UpdateLayout update_layout(int64_t n, int64_t k, int64_t d) {
     o = align_up(o, 1024); L.off_vals_b = o; o += n * 4;
     o = align_up(o, 1024); L.off_head = o; o += L.n_chunks * d * 4;
     o = align_up(o, 1024); L.off_tail = o; o += L.n_chunks * d * 4;
-    o = align_up(o, 1024); L.off_tailc = o; o += L.n_chunks * 4;
+    o = align_up(o, 1024); L.off_tailc = o; o += L.n_chunks * 16;
     L.counting = k <= kCountingMaxK;
     L.n_utiles = kCountingTiles;  // fixed, so the table is O(k) for every n
     L.utile = (n + L.n_utiles - 1) / L.n_utiles;

@@ -525,13 +525,13 @@ __global__ void __launch_bounds__(kMeanThreads)
     segmented_mean_kernel(const float *__restrict__ X, const int32_t *__restrict__ perm,
                           const uint32_t *__restrict__ sorted_labels, const int32_t *__restrict__ offsets,
                           int n, int d, int chunk, float *__restrict__ C_new, float *__restrict__ head,
-                          float *__restrict__ tail, int32_t *__restrict__ tailc) {
+                          float *__restrict__ tail, int4 *__restrict__ tailc) {
     extern __shared__ int32_t s_members[];  // [chunk] sample indices, then [chunk] labels
     griddep_wait();
     int32_t *s_perm = s_members;
     uint32_t *s_lab = reinterpret_cast<uint32_t *>(s_members + chunk);
     const int c = blockIdx.x;
-    if (tailc && blockIdx.y == 0 && threadIdx.x == 0) tailc[c] = -1;
+    if (tailc && blockIdx.y == 0 && threadIdx.x == 0) tailc[c] = make_int4(-1, 0, 0, 0);
     const int p0 = c * chunk;
     const int p1 = min(n, p0 + chunk);
     for (int p = p0 + threadIdx.x; p < p1; p += kMeanThreads) {
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(kMeanThreads)
             dst = head + (size_t)c * d + col;
         } else {
             dst = tail + (size_t)c * d + col;
-            if (tailc && blockIdx.y == 0 && threadIdx.x == 0) tailc[c] = (int32_t)j;
+            if (tailc && blockIdx.y == 0 && threadIdx.x == 0) tailc[c] = make_int4((int)j, seg0, seg1, 0);
         }
         if (MEAN && mean) {
             const float cnt = (float)(seg1 - seg0);
@@ -669,18 +669,19 @@ constexpr int kFixUnroll = 4;
 
 template <bool VEC, bool MEAN>
 __global__ void __launch_bounds__(kFixThreads)
-    mean_fixup_chunks_kernel(const int32_t *__restrict__ offsets, const float *__restrict__ head,
-                             const float *__restrict__ tail, const int32_t *__restrict__ tailc, int n_chunks,
-                             float *__restrict__ C_new, int d, int chunk) {
+    mean_fixup_chunks_kernel(const float *__restrict__ head, const float *__restrict__ tail,
+                             const int4 *__restrict__ tailc, int n_chunks, float *__restrict__ C_new, int d,
+                             int chunk) {
     using V = typename std::conditional<VEC, float4, float>::type;
     griddep_wait();
     constexpr int W = VEC ? 4 : 1;
     const int dv = d / W;  // VEC: d % 4 == 0
     for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
-        const int j = tailc[c];
+        const int4 tc = tailc[c];  // {cluster, its first member, one past its last}
+        const int j = tc.x;
         if (j < 0) continue;
-        const int seg0 = offsets[j];
-        const int seg1 = offsets[j + 1];
+        const int seg0 = tc.y;
+        const int seg1 = tc.z;
         const int ce = (seg1 - 1) / chunk;
         const float cnt = (float)(seg1 - seg0);
         const V *tl = reinterpret_cast<const V *>(tail + (size_t)c * d);
@@ -889,7 +890,7 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
         int32_t *table = reinterpret_cast<int32_t *>(ws + L.off_table);
         int32_t *perm = va;
         uint32_t *slab = ka;
-        int32_t *tailc = reinterpret_cast<int32_t *>(ws + L.off_tailc);
+        int4 *tailc = reinterpret_cast<int4 *>(ws + L.off_tailc);
         const int ut = (int)L.n_utiles;
         const size_t csmem = (size_t)k * 4;
         set_counting_smem_limits(k);
@@ -912,8 +913,8 @@ cudaError_t launch_update(const float *X, const int64_t *labels, const float *C_
         trace_mark(kTraceUpdateMean, true, s);
         if (e == cudaSuccess)
             e = launch_kernel(true, fix_k, dim3((unsigned)L.n_chunks), dim3(kFixThreads), 0, s,
-                              (const int32_t *)offsets, (const float *)head, (const float *)tail,
-                              (const int32_t *)tailc, (int)L.n_chunks, C_new, (int)d, (int)L.chunk);
+                              (const float *)head, (const float *)tail,
+                              (const int4 *)tailc, (int)L.n_chunks, C_new, (int)d, (int)L.chunk);
         return e;
     }
 
